@@ -1,0 +1,196 @@
+"""fp64 CPU oracle for the packed variable-length gated-delta layer.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by ``__graft_entry__.smoke()``
+and by the cpu_baseline / reference legs of ``bench.py``; never by the
+product package.  The arithmetic lives in ``gdn_oracle.c`` (plain fp64 C);
+this module marshals numpy arrays into it and adds the brute-force unrolled
+product form of the recurrence used as an independent pin.
+
+Sources restated (by page title and item):
+  * paged_ssm.rs (onnxruntime-ep-mlx 0.31.1): CONV, DELTA_PREPARE and DELTA
+    kernel sources, and the ``conv`` / ``delta`` operator handlers (scale 0
+    means 1/sqrt(K); key width at most 256).
+  * gated_delta_rate_activation.rs (mlx-c-rust): the decay chain
+    exp(-exp(f32(A_log)) * logaddexp(a + dt_bias, 0)) and sigmoid rates.
+
+Every function here is pinned by tests in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        i = ctypes.c_int
+        lib.oracle_round_bf16.restype = ctypes.c_double
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_conv1d_varlen.argtypes = [dp, dp, dp, ip, dp, dp, dp] + [i] * 7
+        lib.oracle_prepare.argtypes = [dp] * 7 + [i] * 5
+        lib.oracle_delta_varlen.argtypes = [dp, dp, dp, ip, dp, dp, dp] + [i] * 6 + [ctypes.c_double]
+        lib.oracle_layer_varlen.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [i] * 9
+                                            + [ctypes.c_double, i])
+        lib.oracle_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x):
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _p(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _pi(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise OracleError(f"{what}: oracle status {rc}")
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return _load().oracle_threads()
+
+
+def round_bf16(x):
+    """Round every element to the nearest bfloat16 value (ties to even), as fp64."""
+    lib = _load()
+    arr = _f64(x)
+    out = np.empty_like(arr)
+    flat_in, flat_out = arr.reshape(-1), out.reshape(-1)
+    for j in range(flat_in.size):
+        flat_out[j] = lib.oracle_round_bf16(float(flat_in[j]))
+    return out
+
+
+_ROUND = {None: 0, "f64": 0, "bf16": 1, "f32": 2}
+
+
+def conv1d_varlen(x, w, bias, offsets, init, Kc, D, silu=True, round_to=None):
+    """Varlen causal depthwise conv1d with state; returns (y [N,C], fin [B,C,L])."""
+    x, w, init = _f64(x), _f64(w), _f64(init)
+    bias = _f64(bias)
+    offsets = _i32(offsets)
+    N, C = x.shape
+    B = offsets.size - 1
+    L = (Kc - 1) * D
+    y = np.zeros((N, C))
+    fin = np.zeros((B, C, L))
+    rc = _load().oracle_conv1d_varlen(_p(x), _p(w), _p(bias), _pi(offsets), _p(init),
+                                      _p(y), _p(fin), B, N, C, Kc, D, int(bool(silu)),
+                                      _ROUND[round_to])
+    _check(rc, "conv1d_varlen")
+    return y, fin
+
+
+def prepare(y, a, b, A_log, dt_bias, H, HQ, K, V):
+    """L2-normalised q/k ([2,N,HQ,K]) and (g, beta) ([2,N,H])."""
+    y, a, b, A_log, dt_bias = map(_f64, (y, a, b, A_log, dt_bias))
+    N = y.shape[0]
+    qk = np.zeros((2, N, HQ, K))
+    gb = np.zeros((2, N, H))
+    rc = _load().oracle_prepare(_p(y), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(qk), _p(gb),
+                                N, H, HQ, K, V)
+    _check(rc, "prepare")
+    return qk, gb
+
+
+def delta_varlen(y, qk, gb, offsets, state_init, H, HQ, K, V, scale=0.0):
+    """Gated delta recurrence; returns (out [N,H,V], state_fin [B,H,V,K])."""
+    y, qk, gb, state_init = map(_f64, (y, qk, gb, state_init))
+    offsets = _i32(offsets)
+    N = y.shape[0]
+    B = offsets.size - 1
+    out = np.zeros((N, H, V))
+    fin = np.zeros((B, H, V, K))
+    rc = _load().oracle_delta_varlen(_p(y), _p(qk), _p(gb), _pi(offsets), _p(state_init),
+                                     _p(out), _p(fin), B, N, H, HQ, K, V, float(scale))
+    _check(rc, "delta_varlen")
+    return out, fin
+
+
+def layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init,
+                 H, HQ, K, V, Kc, D, silu=True, scale=0.0, act_dtype="bf16"):
+    """conv -> prepare -> recurrence.  Returns (out, conv_fin, state_fin), fp64."""
+    qkv, w, a, b, A_log, dt_bias, conv_init, state_init = map(
+        _f64, (qkv, w, a, b, A_log, dt_bias, conv_init, state_init))
+    bias = _f64(bias)
+    offsets = _i32(offsets)
+    N = qkv.shape[0]
+    B = offsets.size - 1
+    C = 2 * HQ * K + H * V
+    L = (Kc - 1) * D
+    out = np.zeros((N, H, V))
+    conv_fin = np.zeros((B, C, L))
+    state_fin = np.zeros((B, H, V, K))
+    rc = _load().oracle_layer_varlen(
+        _p(qkv), _p(w), _p(bias), _p(a), _p(b), _p(A_log), _p(dt_bias), _pi(offsets),
+        _p(conv_init), _p(conv_fin), _p(state_init), _p(out), _p(state_fin),
+        B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype])
+    _check(rc, "layer_varlen")
+    return out, conv_fin, state_fin
+
+
+def delta_unrolled(q, k, v, g, beta, S0, scale):
+    """Explicit product form of the recurrence for ONE sequence and ONE head.
+
+    With A_t = g_t (I - beta_t k_t k_t^T) (a K x K matrix), the state after t
+    tokens is  S_t = S_0 A_1 ... A_t + sum_{i<=t} beta_i v_i k_i^T A_{i+1} ... A_t,
+    and o_t = scale * S_t q_t.  Every S_t is rebuilt from scratch from these
+    matrix products (cubic cost; tiny inputs only).  q, k: [T,K] (already
+    normalised), v: [T,V], g, beta: [T], S0: [V,K].  Returns (o [T,V], S_T).
+    """
+    q, k, v, S0 = (np.asarray(x, dtype=np.float64) for x in (q, k, v, S0))
+    g = np.asarray(g, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    T, Kd = k.shape
+    eye = np.eye(Kd)
+    A = [g[t] * (eye - beta[t] * np.outer(k[t], k[t])) for t in range(T)]
+
+    def chain(lo, hi):
+        m = eye.copy()
+        for s in range(lo, hi):
+            m = m @ A[s]
+        return m
+
+    outs = []
+    S = S0.copy()
+    for tt in range(1, T + 1):
+        S = S0 @ chain(0, tt)
+        for i in range(tt):
+            S = S + beta[i] * np.outer(v[i], k[i]) @ chain(i + 1, tt)
+        outs.append(scale * (S @ q[tt - 1]))
+    return np.array(outs).reshape(T, -1), S

@@ -1,0 +1,278 @@
+/*
+ * gdn_oracle.c - plain fp64 CPU oracle for the packed variable-length
+ * gated-delta layer (causal depthwise conv1d -> prepare -> gated delta rule).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file: it is used by tests/, by __graft_entry__.smoke() and by
+ * the cpu_baseline / reference legs of bench.py.  It shares no code, header,
+ * table or helper with the CUDA library.
+ *
+ * Every function restates the method as the source pages define it, in the
+ * pages' order, in double precision, with no blocking, fusion or reordering:
+ *
+ *   [paged_ssm.rs, onnxruntime-ep-mlx 0.31.1, CONV kernel]
+ *       varlen causal depthwise conv with per-sequence initial state,
+ *       optional bias, optional SiLU, and the emitted final conv state.
+ *   [paged_ssm.rs, DELTA_PREPARE kernel]
+ *       q/k L2 normalisation x*rsqrt(sum x^2 + 1e-12), decay
+ *       g = exp(-exp(A_log) * softplus(a + dt_bias)), rate beta = sigmoid(b).
+ *   [gated_delta_rate_activation.rs (mlx-c-rust), decay chain]
+ *       softplus as logaddexp(x, 0), A_log taken in float32 before exp.
+ *   [paged_ssm.rs, DELTA kernel]
+ *       per (sequence, value head, state row): decay the state, retrieve
+ *       with the decayed state, beta-scaled delta, rank-1 update, read out
+ *       the updated state with q, multiply by scale; key head kh = h/(H/HQ).
+ *
+ * Readings where the pages leave a step open are listed at each function.
+ * Status codes: 0 ok, 2 bad shape, 4 malformed offsets.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_SHAPE 2
+#define ORACLE_ERR_OFFSETS 4
+
+int oracle_version(void) { return 1; }
+
+/* Round a double to the nearest bfloat16 value, ties to even, returned as a
+ * double.  bfloat16 keeps 8 significant bits and float32's exponent range
+ * (normal exponents down to 2^-126, subnormal quantum 2^-133, largest finite
+ * value (2 - 2^-7) * 2^127).  The rounding mode is round-to-nearest-even
+ * [rlx-cpu thunk/types.rs, CastF32ToBf16 note]. */
+double oracle_round_bf16(double x) {
+    if (isnan(x) || isinf(x) || x == 0.0) return x;
+    int e;
+    (void)frexp(x, &e);              /* x = m * 2^e with 0.5 <= |m| < 1 */
+    int q = e - 8;                   /* quantum of an 8-significant-bit value */
+    if (q < -133) q = -133;          /* subnormal range of the float32 exponent */
+    double scaled = ldexp(x, -q);    /* exact: a power-of-two scaling */
+    double r = nearbyint(scaled);    /* default rounding mode: ties to even */
+    double y = ldexp(r, q);
+    const double max_bf16 = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+    if (fabs(y) > max_bf16) return x > 0 ? INFINITY : -INFINITY;
+    return y;
+}
+
+/* Round a double to the nearest float32 value (ties to even). */
+static double round_f32(double x) { return (double)(float)x; }
+
+static int check_offsets(const int32_t *offsets, int B, int N) {
+    if (offsets[0] != 0 || offsets[B] != N) return ORACLE_ERR_OFFSETS;
+    for (int b = 0; b < B; ++b)
+        if (offsets[b + 1] < offsets[b]) return ORACLE_ERR_OFFSETS;
+    return ORACLE_OK;
+}
+
+/*
+ * Varlen causal depthwise conv1d  [paged_ssm.rs, CONV kernel].
+ *
+ *   x     [N, C]      packed inputs (one row per token)
+ *   w     [C, Kc]     weight of shape [C, 1, Kc]; tap j multiplies the input
+ *                     (Kc-1-j)*D steps back, tap Kc-1 is the current token
+ *   bias  [C] or NULL
+ *   init  [B, C, L]   initial conv state, L = (Kc-1)*D, index L-1 = newest
+ *   y     [N, C]      output;  fin [B, C, L] final conv state
+ *   out_round: 0 keep fp64, 1 round outputs to bfloat16, 2 round to float32
+ *
+ * For token t of sequence b (start s, end e) and channel c:
+ *   y[t,c] = act(bias[c] + sum_j w[c,j] * x~(t - s - (Kc-1-j)*D)),
+ * with x~(i) = x[s+i, c] for i >= 0 and init[b, c, L+i] for i < 0.
+ * act is SiLU z/(1+exp(-z)) when silu != 0.
+ * fin[b,c,j] = x~(e - s - L + j): the last L raw inputs of init || sequence.
+ */
+int oracle_conv1d_varlen(const double *x, const double *w, const double *bias,
+                         const int32_t *offsets, const double *init,
+                         double *y, double *fin, int B, int N, int C, int Kc,
+                         int D, int silu, int out_round) {
+    if (B < 1 || N < 0 || C < 1 || Kc < 1 || D < 1) return ORACLE_ERR_SHAPE;
+    if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
+    const int L = (Kc - 1) * D;
+    for (int b = 0; b < B; ++b) {
+        const int s = offsets[b], e = offsets[b + 1];
+#pragma omp parallel for schedule(static)
+        for (int c = 0; c < C; ++c) {
+            for (int t = s; t < e; ++t) {
+                double sum = bias ? bias[c] : 0.0;
+                for (int j = 0; j < Kc; ++j) {
+                    int local = t - s - (Kc - 1 - j) * D;
+                    double xv = local >= 0
+                                    ? x[(size_t)(s + local) * C + c]
+                                    : init[((size_t)b * C + c) * L + L + local];
+                    sum += xv * w[(size_t)c * Kc + j];
+                }
+                if (silu) sum = sum / (1.0 + exp(-sum));
+                if (out_round == 1) sum = oracle_round_bf16(sum);
+                else if (out_round == 2) sum = round_f32(sum);
+                y[(size_t)t * C + c] = sum;
+            }
+            for (int j = 0; j < L; ++j) {
+                int local = e - s - L + j;
+                fin[((size_t)b * C + c) * L + j] =
+                    local >= 0 ? x[(size_t)(s + local) * C + c]
+                               : init[((size_t)b * C + c) * L + L + local];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Prepare  [paged_ssm.rs, DELTA_PREPARE kernel; gated_delta_rate_activation.rs].
+ *
+ *   y        [N, W]   conv output, W = 2*HQ*K + H*V: q heads in columns
+ *                     [0, HQ*K), k heads in [HQ*K, 2*HQ*K), v heads after
+ *   a, bl    [N, H]   decay logits and rate logits
+ *   A_log, dt_bias [H]
+ *   qk       [2, N, HQ, K]   plane 0 = q/|q|, plane 1 = k/|k| (unscaled)
+ *   gb       [2, N, H]       plane 0 = g, plane 1 = beta
+ *
+ * Readings: the epsilon 1e-12 is added to the sum of squares inside the
+ * root; softplus(x) = max(x,0) + log(1 + exp(-|x|)) (= logaddexp(x, 0));
+ * A_log is rounded to float32 before exp (the rate-activation graph casts it).
+ */
+int oracle_prepare(const double *y, const double *a, const double *bl,
+                   const double *A_log, const double *dt_bias, double *qk,
+                   double *gb, int N, int H, int HQ, int K, int V) {
+    if (N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
+    const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < N; ++t) {
+        for (int kh = 0; kh < HQ; ++kh) {
+            const double *q = y + (size_t)t * W + (size_t)kh * K;
+            const double *k = y + (size_t)t * W + (size_t)HQ * K + (size_t)kh * K;
+            double nq = 0.0, nk = 0.0;
+            for (int i = 0; i < K; ++i) {
+                nq += q[i] * q[i];
+                nk += k[i] * k[i];
+            }
+            double rq = 1.0 / sqrt(nq + 1e-12);
+            double rk = 1.0 / sqrt(nk + 1e-12);
+            for (int i = 0; i < K; ++i) {
+                qk[((size_t)t * HQ + kh) * K + i] = q[i] * rq;
+                qk[(((size_t)N + t) * HQ + kh) * K + i] = k[i] * rk;
+            }
+        }
+        for (int h = 0; h < H; ++h) {
+            double x = a[(size_t)t * H + h] + dt_bias[h];
+            double softplus = fmax(x, 0.0) + log1p(exp(-fabs(x)));
+            double alog = round_f32(A_log[h]);
+            double g = exp(-exp(alog) * softplus);
+            double beta = 1.0 / (1.0 + exp(-bl[(size_t)t * H + h]));
+            gb[(size_t)t * H + h] = g;
+            gb[((size_t)N + t) * H + h] = beta;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Gated delta recurrence over packed sequences  [paged_ssm.rs, DELTA kernel].
+ *
+ *   y      [N, W]          conv output; v of value head h is columns
+ *                          2*HQ*K + h*V + [0, V)
+ *   qk     [2, N, HQ, K]   normalised q and k (from oracle_prepare)
+ *   gb     [2, N, H]       g and beta
+ *   init   [B, H, V, K]    initial state (row vi of head h is S[vi, :])
+ *   out    [N, H, V]       o_t = scale * S_t q_t
+ *   fin    [B, H, V, K]    final state
+ *   scale  0 means 1/sqrt(K)
+ *
+ * For every state row, per token in order:  S *= g;  r = S . k;
+ * delta = beta * (v - r);  S += delta * k;  o = scale * (S . q).
+ * That is S_t = g_t S_{t-1} + beta_t (v_t - g_t S_{t-1} k_t) k_t^T and
+ * o_t = S_t (scale q_t), with value head h reading key head h / (H/HQ).
+ */
+int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
+                        const int32_t *offsets, const double *init, double *out,
+                        double *fin, int B, int N, int H, int HQ, int K, int V,
+                        double scale) {
+    if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ)
+        return ORACLE_ERR_SHAPE;
+    if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
+    if (scale == 0.0) scale = 1.0 / sqrt((double)K);
+    const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
+    const int G = H / HQ;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const int kh = h / G;
+            const int s = offsets[b], e = offsets[b + 1];
+            double *S = (double *)malloc(sizeof(double) * (size_t)V * K);
+            memcpy(S, init + ((size_t)b * H + h) * V * K, sizeof(double) * (size_t)V * K);
+            for (int t = s; t < e; ++t) {
+                const double *q = qk + ((size_t)t * HQ + kh) * K;
+                const double *k = qk + (((size_t)N + t) * HQ + kh) * K;
+                const double g = gb[(size_t)t * H + h];
+                const double beta = gb[((size_t)N + t) * H + h];
+                for (int vi = 0; vi < V; ++vi) {
+                    double *row = S + (size_t)vi * K;
+                    double retrieval = 0.0;
+                    for (int i = 0; i < K; ++i) {
+                        row[i] *= g;
+                        retrieval += k[i] * row[i];
+                    }
+                    double delta = y[(size_t)t * W + (size_t)2 * HQ * K + (size_t)h * V + vi];
+                    delta -= retrieval;
+                    delta *= beta;
+                    double readout = 0.0;
+                    for (int i = 0; i < K; ++i) {
+                        row[i] += k[i] * delta;
+                        readout += q[i] * row[i];
+                    }
+                    out[((size_t)t * H + h) * V + vi] = readout * scale;
+                }
+            }
+            memcpy(fin + ((size_t)b * H + h) * V * K, S, sizeof(double) * (size_t)V * K);
+            free(S);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * The whole layer: conv -> prepare -> recurrence, composed from the three
+ * functions above exactly as the two separate operators of the pages chain
+ * (VarlenCausalConvWithState feeds GatedDeltaNet).  When act_dtype is
+ * bfloat16 (1) the conv output is rounded to bfloat16 before the later
+ * stages, because the conv operator writes its output in the activation
+ * dtype and the delta operator reads it back from there; act_dtype 2 rounds
+ * to float32, 0 keeps fp64.  Outputs of the recurrence stay in fp64.
+ * Readings: scale 0 means 1/sqrt(K); work buffers are owned here.
+ */
+int oracle_layer_varlen(const double *qkv, const double *w, const double *bias,
+                        const double *a, const double *bl, const double *A_log,
+                        const double *dt_bias, const int32_t *offsets,
+                        const double *conv_init, double *conv_fin,
+                        const double *state_init, double *out, double *state_fin,
+                        int B, int N, int H, int HQ, int K, int V, int Kc, int D,
+                        int silu, double scale, int act_dtype) {
+    if (H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
+    const int C = 2 * HQ * K + H * V;
+    double *y = (double *)malloc(sizeof(double) * ((size_t)N * C + 1));
+    double *qk = (double *)malloc(sizeof(double) * ((size_t)2 * N * HQ * K + 1));
+    double *gb = (double *)malloc(sizeof(double) * ((size_t)2 * N * H + 1));
+    int rc = oracle_conv1d_varlen(qkv, w, bias, offsets, conv_init, y, conv_fin, B, N,
+                                  C, Kc, D, silu, act_dtype);
+    if (!rc) rc = oracle_prepare(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V);
+    if (!rc) rc = oracle_delta_varlen(y, qk, gb, offsets, state_init, out, state_fin,
+                                      B, N, H, HQ, K, V, scale);
+    free(y);
+    free(qk);
+    free(gb);
+    return rc;
+}
+
+/* Number of OpenMP threads the oracle's parallel loops use (1 without OpenMP). */
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
