@@ -1,0 +1,399 @@
+"""Benchmark of the packed variable-length gated-delta layer on GB300.
+
+One step = one gdn_layer_varlen call (conv -> prepare -> recurrence) over one
+batch of the workload, inputs resident in HBM.  Default workload: the decode
+step (64 sequences x 1 token, HQ=16, H=32, K=V=128, bf16, fp32 state
+[64,32,128,128] carried in place).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the fp64 CPU oracle, timed on host cores)
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own batch of
+the workload (independent sequences: no data-path collective), so scaling is
+weak; value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "ragged", "long", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_bytes_delta(wl, N, B):
+    """Bytes the token-serial recurrence kernel must move per launch."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    state = 2 * B * wl.H * wl.V * wl.K * 4            # read + write fp32 state
+    qk = N * wl.HQ * 2 * wl.K * 4                     # normalised q and k (fp32)
+    gb = N * wl.H * 2 * 4                             # g and beta
+    v = N * wl.H * wl.V * esz                         # v columns of the conv output
+    out = N * wl.H * wl.V * esz
+    return state + qk + gb + v + out
+
+
+def algorithmic_bytes_layer(wl, N, B):
+    """Bytes the whole layer must move per step (inputs read once, outputs written once)."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    W = wl.width
+    return (N * W * esz                               # qkv
+            + W * wl.Kc * esz + W * esz               # conv weight, bias
+            + 2 * B * W * wl.L * esz                  # conv state in / out
+            + 2 * N * wl.H * 4 + 2 * wl.H * 4         # a, b, A_log, dt_bias
+            + 2 * B * wl.H * wl.V * wl.K * 4          # delta state in / out
+            + N * wl.H * wl.V * esz)                  # out
+
+
+def _profile_traffic(kernel, workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    info = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                info[k.strip()] = v.strip()
+    src = info.get("source_file")
+    sha = info.get("source_sha256")
+    tb = info.get("traffic_bytes_per_launch")
+    if not (src and sha and tb):
+        return None
+    with open(os.path.join(ROOT, src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != sha:
+            return None
+    return int(float(tb))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_reference(args, wl):
+    """The fp64 CPU oracle, timed as it stands on this host's cores."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from varlen_gated_delta_gb300 import workloads as W
+
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    sample_wl, sample = _oracle_sample(wl)
+    d = W.make_inputs(sample_wl, "cpu")
+    c = lambda t: None if t is None else t.double().numpy()
+    inputs = [c(d[k]) for k in ("qkv", "w", "bias", "a", "b", "A_log", "dt_bias")]
+    offs = np.asarray(d["offsets_list"], np.int32)
+    ci, si = c(d["conv_init"]), c(d["state_init"])
+    act = "bf16" if sample_wl.dtype == "bf16" else "f32"
+
+    def step():
+        oracle.layer_varlen(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ, sample_wl.K,
+                            sample_wl.V, sample_wl.Kc, sample_wl.D, silu=sample_wl.silu,
+                            scale=d["scale"], act_dtype=act)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    toks = sample_wl.N * args.steps
+    value = toks / dt
+    line = {
+        "impl": "reference", "metric": "gated-delta layer tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _oracle_sample(wl):
+    """A bounded slice of the workload for the CPU oracle (about a second a step)."""
+    from varlen_gated_delta_gb300 import workloads as W
+    if wl.name == "decode":
+        return wl, "the whole decode batch (64 sequences x 1 token, all 32 heads)"
+    if wl.name == "tiny":
+        return wl, "the whole tiny batch"
+    # prefill-like workloads: one 256-token sequence with the workload's head geometry
+    s = W.scaled(wl, (256,), name=wl.name + "-sample")
+    return s, f"one 256-token sequence of the {wl.name} geometry (HQ={wl.HQ}, H={wl.H}, K={wl.K}, V={wl.V})"
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    import numpy as np
+
+    import oracle
+    from varlen_gated_delta_gb300 import workloads as W
+    sample_wl, sample = _oracle_sample(wl)
+    d = W.make_inputs(sample_wl, "cpu")
+    c = lambda t: None if t is None else t.double().numpy()
+    inputs = [c(d[k]) for k in ("qkv", "w", "bias", "a", "b", "A_log", "dt_bias")]
+    offs = np.asarray(d["offsets_list"], np.int32)
+    ci, si = c(d["conv_init"]), c(d["state_init"])
+    act = "bf16" if sample_wl.dtype == "bf16" else "f32"
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer_varlen(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ, sample_wl.K,
+                            sample_wl.V, sample_wl.Kc, sample_wl.D, silu=sample_wl.silu,
+                            scale=d["scale"], act_dtype=act)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or reps >= 200:
+            break
+    return {"value": sample_wl.N * reps / dt, "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle", "sample": f"{sample}; {reps} repetitions in {dt:.1f} s"}
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import varlen_gated_delta_gb300 as gdn
+    from varlen_gated_delta_gb300 import build as gdn_build
+    from varlen_gated_delta_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        gdn_build.build()
+    if world > 1:
+        dist.barrier()
+    gdn.load_library()
+
+    d = W.make_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    offs = d["offsets_list"]
+    N, B = offs[-1], len(offs) - 1
+    act = gdn.GDN_ACT_SILU if wl.silu else gdn.GDN_ACT_NONE
+    ws = torch.empty(gdn.gdn_workspace_bytes(B, N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D,
+                                             gdn.GDN_BF16 if wl.dtype == "bf16" else gdn.GDN_F32),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((N, wl.H, wl.V), dtype=wl.torch_dtype, device=dev)
+    conv_state, state = d["conv_init"], d["state_init"]
+
+    def step():
+        # decode-style carry: the final states overwrite the initial ones in place
+        gdn.gdn_layer_varlen(d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"],
+                             d["dt_bias"], d["offsets"], conv_state, state, H=wl.H, HQ=wl.HQ,
+                             K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act, scale=d["scale"],
+                             offsets_host=offs, out=out, conv_fin=conv_state, state_fin=state,
+                             workspace=ws)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    gdn.gdn_workspace_status(ws)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = gdn.gdn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = gdn.gdn_launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+
+    # dominant kernel alone: the token-serial recurrence, same inputs, CUDA events
+    # on the launching stream around every launch
+    y, _ = gdn.gdn_conv1d_varlen(d["qkv"], d["w"], d["bias"], d["offsets"], conv_state,
+                                 Kc=wl.Kc, D=wl.D, act=act)
+    qk, gb = gdn.gdn_prepare(y, d["a"], d["b"], d["A_log"], d["dt_bias"], H=wl.H, HQ=wl.HQ,
+                             K=wl.K, V=wl.V)
+    kern_ms = []
+    for i in range(max(3, args.warmup) + args.steps):
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        gdn.gdn_delta_varlen(y, qk, gb, d["offsets"], state, H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V,
+                             scale=d["scale"], out=out, state_fin=state)
+        k1.record(stream)
+        if i >= max(3, args.warmup):
+            kern_ms.append((k0, k1))
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in kern_ms]
+    clocks = sampler.stop()
+
+    # end to end through the public API with host buffers
+    host = {k: d[k].cpu().pin_memory() for k in ("qkv", "a", "b")}
+    host_offs = d["offsets"].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(d[k]) for k in ("qkv", "a", "b")}
+    dev_offs = torch.empty_like(d["offsets"])
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_offs.numel() * 4
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        dev_offs.copy_(host_offs, non_blocking=True)
+        gdn.gdn_layer_varlen(dev_in["qkv"], d["w"], d["bias"], dev_in["a"], dev_in["b"],
+                             d["A_log"], d["dt_bias"], dev_offs, conv_state, state, H=wl.H,
+                             HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act,
+                             scale=d["scale"], offsets_host=offs, out=out, conv_fin=conv_state,
+                             state_fin=state, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1)
+
+    t = torch.tensor([ms, e2e_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = t.tolist()
+    if rank == 0:
+        hbm, tf, tf_s, peak_src = _peaks()
+        kavg = statistics.mean(kern_ms)
+        kbytes = algorithmic_bytes_delta(wl, N, B)
+        achieved = kbytes / (kavg * 1e-3) / 1e9
+        traffic = _profile_traffic("delta_serial", wl.name)
+        value = world * N * args.steps / (ms * 1e-3)
+        line = {
+            "metric": "gated-delta layer tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "N": N, "HQ": wl.HQ, "H": wl.H, "K": wl.K,
+                       "V": wl.V, "Kc": wl.Kc, "D": wl.D, "state_carry": "in place",
+                       "l2": f"inputs larger than L2 (fp32 state {2 * B * wl.H * wl.V * wl.K * 4 / 2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
+            "roofline": {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": traffic, "algorithmic_bytes": kbytes,
+                         "kernel_ms": kavg, "peak_source": f"hbm_gbs of {peak_src}"},
+            "e2e": {"value": world * N * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    from varlen_gated_delta_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * gdn.h - C ABI of libgdn.so, a GB300 (sm_103a) implementation of the packed
+ * variable-length gated-delta-rule layer:
+ *
+ *   causal depthwise conv1d (+bias, +SiLU) with per-sequence conv state
+ *     -> prepare: L2-normalised q/k, decay g and update rate beta
+ *     -> gated delta recurrence with a per-sequence fp32 state.
+ *
+ * The operations follow the two operators of paged_ssm.rs
+ * (onnxruntime-ep-mlx 0.31.1): VarlenCausalConvWithState (CONV kernel and
+ * the `conv` handler) and GatedDeltaNet (DELTA_PREPARE and DELTA kernels and
+ * the `delta` handler), with the decay formula of
+ * gated_delta_rate_activation.rs (mlx-c-rust).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Sizes: B sequences packed into N tokens; offsets[B+1] (int32) delimit
+ *   them: sequence b is tokens [offsets[b], offsets[b+1]).  offsets[0] must
+ *   be 0, offsets[B] must be N, and offsets must be nondecreasing.  Empty
+ *   sequences are allowed (their states pass through unchanged).
+ * - Heads: HQ key heads of width K, H value heads of width V, G = H/HQ
+ *   (H % HQ == 0); value head h reads key head kh = h / G.
+ * - Packed qkv / conv output rows have WIDTH = 2*HQ*K + H*V channels: q heads
+ *   in [0, HQ*K), k heads in [HQ*K, 2*HQ*K), v heads in [2*HQ*K, WIDTH).
+ * - dtype (gdn_dtype) is the activation type T of qkv, the conv weight, bias,
+ *   conv states, conv output and layer output.  Decay/rate logits a, b,
+ *   A_log, dt_bias and the recurrent state are always float32.
+ * - Every tensor is dense, row-major (last index fastest).  Pointers are
+ *   DEVICE pointers unless the name ends in _host.  `stream` is a
+ *   cudaStream_t passed as void* (NULL = legacy default stream).
+ * - Calls are asynchronous on `stream`; they validate arguments on the host
+ *   and return a gdn_status.  On error nothing is launched and
+ *   gdn_last_error() returns a message (thread-local, valid until the next
+ *   call on the same thread).
+ * - The caller owns all memory.  No call allocates device memory; the layer
+ *   call takes a caller-provided workspace sized by gdn_workspace_bytes().
+ * - In-place carry: a *_fin pointer may equal the matching *_init pointer
+ *   (the final state overwrites the initial state).  No other output may
+ *   alias any input or another output.
+ * - Offsets are also checked on the device: a sequence whose bounds are
+ *   malformed is skipped (its outputs are not written) and, for the layer
+ *   call, GDN_ERR_OFFSETS is recorded in the workspace status word
+ *   (gdn_workspace_status).  Pass offsets_host to the layer call to get the
+ *   error synchronously instead.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Symbols of this header are the library's only exported symbols. */
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* inconsistent or out-of-range geometry */
+    GDN_ERR_OVERFLOW = 3,    /* a size or launch grid exceeds its integer range */
+    GDN_ERR_OFFSETS = 4,     /* offsets[0] != 0, offsets[B] != N or decreasing */
+    GDN_ERR_UNSUPPORTED = 5, /* valid request this build does not implement */
+    GDN_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has detail) */
+    GDN_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
+    GDN_ERR_WORKSPACE = 8    /* workspace missing, misaligned or too small */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Conv activation: "none" or "silu" ("swish" is the same function). */
+typedef enum gdn_activation { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1 } gdn_activation;
+
+/* ABI version (GDN_ABI_VERSION of the built library). */
+GDN_API int gdn_version(void);
+
+/* Message of the last failing call on this thread ("" if none). */
+GDN_API const char *gdn_last_error(void);
+
+/*
+ * gdn_conv1d_varlen - varlen causal depthwise conv1d with state
+ * [paged_ssm.rs, CONV kernel and `conv` handler].
+ *
+ *   x         [N, C] T       packed inputs
+ *   w         [C, Kc] T      weight of shape [C, 1, Kc]; tap j multiplies the
+ *                            input (Kc-1-j)*D tokens back (tap Kc-1 = now)
+ *   bias      [C] T or NULL
+ *   offsets   [B+1] int32
+ *   conv_init [B, C, L] T    L = (Kc-1)*D; index L-1 is the newest token
+ *   y         [N, C] T       y[t,c] = act(bias[c] + sum_j w[c,j] x~(t-s-(Kc-1-j)D)),
+ *                            x~(i) = x[s+i,c] for i >= 0, conv_init[b,c,L+i] else;
+ *                            accumulated in fp32 and rounded to T (nearest even)
+ *   conv_fin  [B, C, L] T    last L raw inputs of (conv_init || sequence),
+ *                            copied bit-exactly; may equal conv_init
+ *   act       gdn_activation
+ * Requires B >= 1, N >= 0, C >= 1, Kc >= 1, D >= 1, (Kc-1)*D < 2^31.
+ * When L == 0, conv_init and conv_fin may be NULL.
+ */
+GDN_API int gdn_conv1d_varlen(const void *x, const void *w, const void *bias,
+                      const int32_t *offsets, const void *conv_init, void *y,
+                      void *conv_fin, int B, int N, int C, int Kc, int D, int act,
+                      int dtype, void *stream);
+
+/*
+ * gdn_prepare - per-token coefficients [paged_ssm.rs, DELTA_PREPARE kernel;
+ * gated_delta_rate_activation.rs, decay chain].
+ *
+ *   y        [N, WIDTH] T   conv output (q and k heads are read)
+ *   a, b     [N, H] f32     decay logits and rate logits
+ *   A_log    [H] f32, dt_bias [H] f32
+ *   qk_norm  [2, N, HQ, K] f32   plane 0: q/sqrt(|q|^2 + 1e-12),
+ *                                plane 1: k/sqrt(|k|^2 + 1e-12)
+ *   g_beta   [2, N, H] f32       plane 0: g = exp(-exp(A_log) softplus(a + dt_bias)),
+ *                                plane 1: beta = sigmoid(b)
+ * Requires N >= 0, 1 <= K <= 256, V >= 1, H % HQ == 0.
+ */
+GDN_API int gdn_prepare(const void *y, const float *a, const float *b, const float *A_log,
+                const float *dt_bias, float *qk_norm, float *g_beta, int N, int H,
+                int HQ, int K, int V, int dtype, void *stream);
+
+/*
+ * gdn_delta_varlen - the gated delta recurrence over packed sequences
+ * [paged_ssm.rs, DELTA kernel and `delta` handler].
+ *
+ *   y          [N, WIDTH] T      v of head h is columns 2*HQ*K + h*V + [0, V)
+ *   qk_norm    [2, N, HQ, K] f32 g_beta [2, N, H] f32 (from gdn_prepare)
+ *   offsets    [B+1] int32
+ *   state_init [B, H, V, K] f32  row vi of head h is S[vi, :]
+ *   out        [N, H, V] T       o_t = scale * S_t q_t
+ *   state_fin  [B, H, V, K] f32  final state; may equal state_init
+ *   scale      0 means 1/sqrt(K)
+ * Per token: S_t = g_t S_{t-1} + beta_t (v_t - g_t S_{t-1} k_t) k_t^T.
+ * This call always runs the token-serial kernel.
+ * Requires 1 <= K <= 256, 1 <= V, H % HQ == 0.
+ */
+GDN_API int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
+                     const int32_t *offsets, const float *state_init, void *out,
+                     float *state_fin, int B, int N, int H, int HQ, int K, int V,
+                     float scale, int dtype, void *stream);
+
+/*
+ * gdn_layer_varlen - the whole layer, conv -> prepare -> recurrence, fused
+ * where the hardware path allows; results equal the three calls above run
+ * in sequence (conv output rounded to T before the later stages).
+ *
+ *   qkv [N, WIDTH] T; w [WIDTH, Kc] T; bias [WIDTH] T or NULL;
+ *   a, b [N, H] f32; A_log, dt_bias [H] f32; offsets [B+1] int32 (device);
+ *   offsets_host [B+1] int32 host copy of offsets, or NULL (then the
+ *     schedule is built on the device and offsets errors are reported
+ *     through gdn_workspace_status);
+ *   conv_init / conv_fin [B, WIDTH, L] T; state_init / state_fin [B, H, V, K] f32;
+ *   out [N, H, V] T; act, scale as above;
+ *   workspace: device buffer of at least gdn_workspace_bytes(...) bytes,
+ *     256-byte aligned, not shared with a concurrently running call.
+ * Sequences of at least gdn_chunk_min_len() tokens run on the chunkwise
+ * tensor-core kernel when the geometry allows it (bf16, K == 128,
+ * V % 128 == 0); the rest run on the token-serial kernel.
+ */
+GDN_API int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const float *a,
+                     const float *b, const float *A_log, const float *dt_bias,
+                     const int32_t *offsets, const int32_t *offsets_host,
+                     const void *conv_init, void *conv_fin, const float *state_init,
+                     void *out, float *state_fin, int B, int N, int H, int HQ, int K,
+                     int V, int Kc, int D, int act, float scale, int dtype,
+                     void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes gdn_layer_varlen needs for this geometry (0 on bad input). */
+GDN_API size_t gdn_workspace_bytes(int B, int N, int H, int HQ, int K, int V, int Kc, int D,
+                           int dtype);
+
+/*
+ * Synchronises `stream`, then reads the status the last layer call wrote into
+ * `workspace`: returns GDN_OK or GDN_ERR_OFFSETS / GDN_ERR_TIMEOUT.  When
+ * `counts` is not NULL it receives {sequences on the token-serial kernel,
+ * sequences on the chunked kernel, chunked work units}.
+ */
+GDN_API int gdn_workspace_status(const void *workspace, int *counts, void *stream);
+
+/*
+ * Length threshold (tokens) from which a sequence takes the chunked kernel.
+ * gdn_set_chunk_min_len(n): n > 0 sets it, n == 0 restores the default
+ * (environment variable GDN_CHUNK_MIN_LEN if set, else 64); a very large n
+ * keeps every sequence on the token-serial kernel.  Process-wide setting.
+ */
+GDN_API int gdn_set_chunk_min_len(int n);
+GDN_API int gdn_chunk_min_len(void);
+
+/* Number of kernels this library has launched in this process. */
+GDN_API uint64_t gdn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,1 +1,268 @@
-"""GB300-native packed variable-length gated-delta layer (placeholder; binding lands next)."""
+"""GB300-native packed variable-length gated-delta layer.
+
+Thin Python binding over the C ABI of ``libgdn.so`` (include/gdn.h).  Each
+function has the C call's name and only marshals arguments: it checks device,
+dtype, shape and contiguity of torch tensors, passes their data pointers and
+the current CUDA stream, and raises :class:`GdnError` on a non-zero status.
+All arithmetic runs in the library's CUDA kernels; there is no CPU fallback.
+If the library is missing, every call raises.
+
+Operations follow paged_ssm.rs (onnxruntime-ep-mlx 0.31.1): the
+VarlenCausalConvWithState operator (``gdn_conv1d_varlen``) and the
+GatedDeltaNet operator (``gdn_prepare`` + ``gdn_delta_varlen``), plus the
+fused layer ``gdn_layer_varlen``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "GdnError", "load_library", "library_path", "gdn_version", "gdn_conv1d_varlen",
+    "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen", "gdn_workspace_bytes",
+    "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_chunk_min_len",
+    "gdn_launch_count", "GDN_F32", "GDN_BF16", "GDN_ACT_NONE", "GDN_ACT_SILU",
+    "STATUS_NAMES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+GDN_F32, GDN_BF16 = 0, 1
+GDN_ACT_NONE, GDN_ACT_SILU = 0, 1
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_OVERFLOW",
+                4: "GDN_ERR_OFFSETS", 5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA",
+                7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_WORKSPACE"}
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libgdn.so")
+
+
+def load_library():
+    """Load libgdn.so (built by ``varlen_gated_delta_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise GdnError(6, f"{path} is missing: build it with "
+                          "`python -m varlen_gated_delta_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.gdn_version.restype = i
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_conv1d_varlen.argtypes = [vp] * 7 + [i] * 7 + [vp]
+    lib.gdn_prepare.argtypes = [vp] * 7 + [i] * 6 + [vp]
+    lib.gdn_delta_varlen.argtypes = [vp] * 7 + [i] * 6 + [f, i, vp]
+    lib.gdn_layer_varlen.argtypes = [vp] * 14 + [i] * 9 + [f, i, vp, sz, vp]
+    lib.gdn_workspace_bytes.restype = sz
+    lib.gdn_workspace_bytes.argtypes = [i] * 9
+    lib.gdn_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
+    lib.gdn_set_chunk_min_len.argtypes = [i]
+    lib.gdn_chunk_min_len.restype = i
+    lib.gdn_launch_count.restype = ctypes.c_uint64
+    for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
+                 "gdn_workspace_status", "gdn_set_chunk_min_len"):
+        getattr(lib, name).restype = i
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise GdnError(rc, load_library().gdn_last_error().decode(errors="replace"))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise GdnError(5, f"activation dtype {t.dtype} not supported (bf16 or fp32)")
+
+
+def _ptr(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise GdnError(6, f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise GdnError(6, f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise GdnError(2, f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise GdnError(2, f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise GdnError(2, f"{name} must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _host_offsets(offsets_host):
+    if offsets_host is None:
+        return None, None
+    arr = (ctypes.c_int32 * len(offsets_host))(*[int(v) for v in offsets_host])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def gdn_version() -> int:
+    return load_library().gdn_version()
+
+
+def gdn_launch_count() -> int:
+    return load_library().gdn_launch_count()
+
+
+def gdn_set_chunk_min_len(n: int) -> None:
+    _check(load_library().gdn_set_chunk_min_len(int(n)))
+
+
+def gdn_chunk_min_len() -> int:
+    return load_library().gdn_chunk_min_len()
+
+
+def gdn_conv1d_varlen(x, w, bias, offsets, conv_init, y=None, conv_fin=None, *, Kc, D=1,
+                      act=GDN_ACT_SILU):
+    """Varlen causal depthwise conv1d with state.  Returns (y, conv_fin)."""
+    lib = load_library()
+    N, C = x.shape
+    B = offsets.numel() - 1
+    L = (Kc - 1) * D
+    T = x.dtype
+    dev = x.device
+    if y is None:
+        y = torch.empty((N, C), dtype=T, device=dev)
+    if conv_fin is None:
+        conv_fin = torch.empty((B, C, L), dtype=T, device=dev)
+    args = [_ptr(x, "x", T, (N, C), dev), _ptr(w, "w", T, (C, Kc), dev),
+            _ptr(bias, "bias", T, (C,), dev), _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
+            _ptr(conv_init, "conv_init", T, (B, C, L), dev), _ptr(y, "y", T, (N, C), dev),
+            _ptr(conv_fin, "conv_fin", T, (B, C, L), dev)]
+    _check(lib.gdn_conv1d_varlen(*args, B, N, C, Kc, D, act, _dtype_code(x), _stream(dev)))
+    return y, conv_fin
+
+
+def gdn_prepare(y, a, b, A_log, dt_bias, *, H, HQ, K, V, qk_norm=None, g_beta=None):
+    """q/k L2 norms ([2,N,HQ,K] f32) and g/beta ([2,N,H] f32).  Returns (qk_norm, g_beta)."""
+    lib = load_library()
+    N = y.shape[0]
+    dev = y.device
+    f32 = torch.float32
+    if qk_norm is None:
+        qk_norm = torch.empty((2, N, HQ, K), dtype=f32, device=dev)
+    if g_beta is None:
+        g_beta = torch.empty((2, N, H), dtype=f32, device=dev)
+    W = 2 * HQ * K + H * V
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
+            _ptr(dt_bias, "dt_bias", f32, (H,), dev),
+            _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
+            _ptr(g_beta, "g_beta", f32, (2, N, H), dev)]
+    _check(lib.gdn_prepare(*args, N, H, HQ, K, V, _dtype_code(y), _stream(dev)))
+    return qk_norm, g_beta
+
+
+def gdn_delta_varlen(y, qk_norm, g_beta, offsets, state_init, *, H, HQ, K, V, scale=0.0,
+                     out=None, state_fin=None):
+    """Token-serial gated delta recurrence.  Returns (out [N,H,V], state_fin)."""
+    lib = load_library()
+    N = y.shape[0]
+    B = offsets.numel() - 1
+    dev = y.device
+    f32 = torch.float32
+    if out is None:
+        out = torch.empty((N, H, V), dtype=y.dtype, device=dev)
+    if state_fin is None:
+        state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev)
+    W = 2 * HQ * K + H * V
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
+            _ptr(g_beta, "g_beta", f32, (2, N, H), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", y.dtype, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev)]
+    _check(lib.gdn_delta_varlen(*args, B, N, H, HQ, K, V, float(scale), _dtype_code(y),
+                                _stream(dev)))
+    return out, state_fin
+
+
+def gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dtype=GDN_BF16) -> int:
+    return int(load_library().gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dtype))
+
+
+def gdn_workspace_status(workspace: torch.Tensor):
+    """Synchronise and read the device status of the last layer call.
+
+    Returns (status, counts) with counts = (serial sequences, chunked
+    sequences, chunked units); raises GdnError on a non-zero status."""
+    lib = load_library()
+    counts = (ctypes.c_int * 3)()
+    rc = lib.gdn_workspace_status(_ptr(workspace, "workspace"), counts,
+                                  _stream(workspace.device))
+    _check(rc)
+    return rc, tuple(counts)
+
+
+def gdn_layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init, *,
+                     H, HQ, K, V, Kc=4, D=1, act=GDN_ACT_SILU, scale=0.0, offsets_host=None,
+                     out=None, conv_fin=None, state_fin=None, workspace=None):
+    """The whole layer (conv -> prepare -> recurrence).
+
+    Returns (out [N,H,V] T, conv_fin [B,WIDTH,L] T, state_fin [B,H,V,K] f32).
+    ``conv_fin`` / ``state_fin`` may be the ``conv_init`` / ``state_init``
+    tensors themselves (in-place carry).  ``offsets_host`` is an optional
+    host list of the offsets (lets the library validate and schedule on the
+    host).  ``workspace`` is an optional uint8 CUDA tensor of at least
+    ``gdn_workspace_bytes`` bytes (allocated here when omitted).
+    """
+    lib = load_library()
+    N, W = qkv.shape
+    B = offsets.numel() - 1
+    L = (Kc - 1) * D
+    T = qkv.dtype
+    dev = qkv.device
+    f32 = torch.float32
+    dcode = _dtype_code(qkv)
+    if W != 2 * HQ * K + H * V:
+        raise GdnError(2, f"qkv width {W} != 2*HQ*K + H*V = {2 * HQ * K + H * V}")
+    if out is None:
+        out = torch.empty((N, H, V), dtype=T, device=dev)
+    if conv_fin is None:
+        conv_fin = torch.empty((B, W, L), dtype=T, device=dev)
+    if state_fin is None:
+        state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev)
+    need = gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dcode)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    hp, keep = _host_offsets(offsets_host)
+    args = [_ptr(qkv, "qkv", T, (N, W), dev), _ptr(w, "w", T, (W, Kc), dev),
+            _ptr(bias, "bias", T, (W,), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
+            _ptr(dt_bias, "dt_bias", f32, (H,), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev), hp,
+            _ptr(conv_init, "conv_init", T, (B, W, L), dev),
+            _ptr(conv_fin, "conv_fin", T, (B, W, L), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", T, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev)]
+    rc = lib.gdn_layer_varlen(*args, B, N, H, HQ, K, V, Kc, D, act, float(scale), dcode,
+                              _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                              _stream(dev))
+    del keep
+    _check(rc)
+    return out, conv_fin, state_fin

@@ -1,0 +1,288 @@
+// api.cpp - the C ABI of libgdn.so (declared in include/gdn.h): argument
+// validation, workspace carving, path selection and kernel dispatch.
+//
+// The checks restate the operator contracts of paged_ssm.rs
+// (onnxruntime-ep-mlx 0.31.1): the `conv` / `delta` handlers (shapes,
+// receptive-field and dispatch-size overflow, key width <= 256, grouped-head
+// divisibility, scale 0 -> 1/sqrt(K)) and the claim predicates (dtype and
+// activation rules).  Where the pages' kernels silently skip malformed
+// offsets, this library reports GDN_ERR_OFFSETS.
+#include "../../include/gdn.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+namespace gdn {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+static thread_local char g_err[512] = "";
+static std::atomic<int> g_chunk_min_len{0};
+
+static int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static int cuda_fail(cudaError_t e, const char *what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static int default_chunk_min_len() {
+    const char *env = getenv("GDN_CHUNK_MIN_LEN");
+    if (env && *env) {
+        long v = strtol(env, nullptr, 10);
+        if (v > 0 && v <= INT_MAX) return (int)v;
+    }
+    return 64;
+}
+
+static int chunk_min_len() {
+    int v = g_chunk_min_len.load(std::memory_order_relaxed);
+    return v > 0 ? v : default_chunk_min_len();
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool dtype_ok(int dtype) { return dtype == GDN_F32 || dtype == GDN_BF16; }
+static size_t dsize(int dtype) { return dtype == GDN_BF16 ? 2 : 4; }
+
+// Geometry of the recurrence: mirrors the `delta` handler's rules.
+static int check_heads(int H, int HQ, int K, int V, long *width) {
+    if (H < 1 || HQ < 1 || K < 1 || V < 1)
+        return fail(GDN_ERR_SHAPE, "head geometry must be positive (H=%d HQ=%d K=%d V=%d)", H, HQ, K, V);
+    if (K > 256) return fail(GDN_ERR_SHAPE, "key width K=%d exceeds 256", K);
+    if (H % HQ != 0) return fail(GDN_ERR_SHAPE, "value heads H=%d not a multiple of key heads HQ=%d", H, HQ);
+    long w = 2L * HQ * K + (long)H * V;
+    if (w > INT_MAX) return fail(GDN_ERR_OVERFLOW, "packed width 2*HQ*K+H*V exceeds int32");
+    *width = w;
+    return GDN_OK;
+}
+
+static int check_offsets_host(const int32_t *offsets_host, int B, int N) {
+    if (offsets_host[0] != 0) return fail(GDN_ERR_OFFSETS, "offsets[0]=%d, expected 0", offsets_host[0]);
+    if (offsets_host[B] != N) return fail(GDN_ERR_OFFSETS, "offsets[B]=%d, expected N=%d", offsets_host[B], N);
+    for (int b = 0; b < B; ++b)
+        if (offsets_host[b + 1] < offsets_host[b])
+            return fail(GDN_ERR_OFFSETS, "offsets decrease at b=%d (%d > %d)", b, offsets_host[b], offsets_host[b + 1]);
+    return GDN_OK;
+}
+
+struct WsLayout {
+    size_t header, y, qk, gb, total;
+};
+
+static WsLayout ws_layout(int N, int H, int HQ, int K, int V, int dtype) {
+    WsLayout l;
+    const size_t W = 2 * (size_t)HQ * K + (size_t)H * V;
+    size_t off = 0;
+    l.header = off;
+    off += align256(sizeof(WsHeader));
+    l.y = off;
+    off += align256((size_t)N * W * dsize(dtype));
+    l.qk = off;
+    off += align256((size_t)2 * N * HQ * K * 4);
+    l.gb = off;
+    off += align256((size_t)2 * N * H * 4);
+    l.total = off;
+    return l;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_version(void) { return GDN_ABI_VERSION; }
+
+const char *gdn_last_error(void) { return g_err; }
+
+uint64_t gdn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int gdn_set_chunk_min_len(int n) {
+    if (n < 0) return fail(GDN_ERR_SHAPE, "chunk threshold must be >= 0");
+    g_chunk_min_len.store(n, std::memory_order_relaxed);
+    return GDN_OK;
+}
+
+int gdn_chunk_min_len(void) { return chunk_min_len(); }
+
+int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int32_t *offsets,
+                      const void *conv_init, void *y, void *conv_fin, int B, int N, int C, int Kc,
+                      int D, int act, int dtype, void *stream) {
+    g_err[0] = 0;
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
+    if (B < 1 || N < 0 || C < 1 || Kc < 1 || D < 1)
+        return fail(GDN_ERR_SHAPE, "need B>=1, N>=0, C>=1, Kc>=1, D>=1 (B=%d N=%d C=%d Kc=%d D=%d)", B, N, C, Kc, D);
+    const long L = (long)(Kc - 1) * D;
+    if (L >= INT_MAX) return fail(GDN_ERR_OVERFLOW, "receptive field (Kc-1)*D exceeds int32");
+    if (!w || !offsets || !y || (N > 0 && !x) || (L > 0 && (!conv_init || !conv_fin)))
+        return fail(GDN_ERR_NULL, "conv1d: a required pointer is NULL");
+    if ((long)B * C > INT_MAX) return fail(GDN_ERR_OVERFLOW, "conv dispatch B*C exceeds int32");
+    if (L > 4096) return fail(GDN_ERR_UNSUPPORTED, "receptive field L=%ld above 4096", L);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ConvParams p{};
+    p.x = x; p.w = w; p.bias = bias; p.offsets = offsets; p.init = conv_init; p.y = y;
+    p.B = B; p.N = N; p.C = C; p.Kc = Kc; p.D = D; p.L = (int)L; p.silu = act == GDN_ACT_SILU;
+    p.prep = 0;
+    cudaError_t e = launch_conv(p, dtype, s, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
+    e = launch_conv_final(x, offsets, conv_init, conv_fin, B, N, C, (int)L, dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "conv final-state kernel launch");
+    return GDN_OK;
+}
+
+int gdn_prepare(const void *y, const float *a, const float *b, const float *A_log,
+                const float *dt_bias, float *qk_norm, float *g_beta, int N, int H, int HQ, int K,
+                int V, int dtype, void *stream) {
+    g_err[0] = 0;
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    long width;
+    int rc = check_heads(H, HQ, K, V, &width);
+    if (rc) return rc;
+    if (N < 0) return fail(GDN_ERR_SHAPE, "N=%d < 0", N);
+    if (N > 0 && (!y || !a || !b || !qk_norm || !g_beta)) return fail(GDN_ERR_NULL, "prepare: a required pointer is NULL");
+    if (!A_log || !dt_bias) return fail(GDN_ERR_NULL, "prepare: A_log / dt_bias is NULL");
+    if ((long)N * H > INT_MAX / 2 || (long)N * HQ * 32 > INT_MAX) return fail(GDN_ERR_OVERFLOW, "prepare dispatch exceeds int32");
+    PrepParams p{};
+    p.y = y; p.a = a; p.bl = b; p.A_log = A_log; p.dt_bias = dt_bias; p.qk = qk_norm; p.gb = g_beta;
+    p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
+    cudaError_t e = launch_prepare(p, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
+    return GDN_OK;
+}
+
+int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
+                     const int32_t *offsets, const float *state_init, void *out, float *state_fin,
+                     int B, int N, int H, int HQ, int K, int V, float scale, int dtype,
+                     void *stream) {
+    g_err[0] = 0;
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    long width;
+    int rc = check_heads(H, HQ, K, V, &width);
+    if (rc) return rc;
+    if (B < 1 || N < 0) return fail(GDN_ERR_SHAPE, "need B>=1 and N>=0 (B=%d N=%d)", B, N);
+    if (!offsets || !state_init || !state_fin || (N > 0 && (!y || !qk_norm || !g_beta || !out)))
+        return fail(GDN_ERR_NULL, "delta: a required pointer is NULL");
+    if ((long)B * H * V * 32 > INT_MAX) return fail(GDN_ERR_OVERFLOW, "delta dispatch B*H*V*32 exceeds int32");
+    if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
+    DeltaParams p{};
+    p.y = y; p.qk = qk_norm; p.gb = g_beta; p.offsets = offsets; p.state_init = state_init;
+    p.out = out; p.state_fin = state_fin; p.B = B; p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
+    p.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
+    p.serial_max_len = INT_MAX;
+    cudaError_t e = launch_delta_serial(p, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
+    return GDN_OK;
+}
+
+size_t gdn_workspace_bytes(int B, int N, int H, int HQ, int K, int V, int Kc, int D, int dtype) {
+    if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || Kc < 1 || D < 1) return 0;
+    if (!dtype_ok(dtype) || H % HQ != 0 || K > 256) return 0;
+    return ws_layout(N, H, HQ, K, V, dtype).total;
+}
+
+int gdn_workspace_status(const void *workspace, int *counts, void *stream) {
+    g_err[0] = 0;
+    if (!workspace) return fail(GDN_ERR_NULL, "workspace is NULL");
+    WsHeader h;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+    if (counts) {
+        counts[0] = h.n_serial;
+        counts[1] = h.n_chunked;
+        counts[2] = h.n_units;
+    }
+    if (h.status == GDN_ERR_OFFSETS) return fail(GDN_ERR_OFFSETS, "device check: malformed offsets");
+    if (h.status == GDN_ERR_TIMEOUT) return fail(GDN_ERR_TIMEOUT, "device check: a bounded wait gave up");
+    return h.status;
+}
+
+int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const float *a,
+                     const float *b, const float *A_log, const float *dt_bias,
+                     const int32_t *offsets, const int32_t *offsets_host, const void *conv_init,
+                     void *conv_fin, const float *state_init, void *out, float *state_fin, int B,
+                     int N, int H, int HQ, int K, int V, int Kc, int D, int act, float scale,
+                     int dtype, void *workspace, size_t ws_bytes, void *stream) {
+    g_err[0] = 0;
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
+    long width;
+    int rc = check_heads(H, HQ, K, V, &width);
+    if (rc) return rc;
+    if (B < 1 || N < 0 || Kc < 1 || D < 1)
+        return fail(GDN_ERR_SHAPE, "need B>=1, N>=0, Kc>=1, D>=1 (B=%d N=%d Kc=%d D=%d)", B, N, Kc, D);
+    const long L = (long)(Kc - 1) * D;
+    if (L >= INT_MAX) return fail(GDN_ERR_OVERFLOW, "receptive field (Kc-1)*D exceeds int32");
+    if (L > 4096) return fail(GDN_ERR_UNSUPPORTED, "receptive field L=%ld above 4096", L);
+    if (!w || !A_log || !dt_bias || !offsets || !state_init || !state_fin ||
+        (N > 0 && (!qkv || !a || !b || !out)) || (L > 0 && (!conv_init || !conv_fin)))
+        return fail(GDN_ERR_NULL, "layer: a required pointer is NULL");
+    if ((long)B * H * V * 32 > INT_MAX || (long)B * width > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "layer dispatch size exceeds int32");
+    if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
+    const WsLayout lay = ws_layout(N, H, HQ, K, V, dtype);
+    if (!workspace || ((uintptr_t)workspace & 255) != 0)
+        return fail(GDN_ERR_WORKSPACE, "workspace must be a non-NULL 256-byte aligned device pointer");
+    if (ws_bytes < lay.total)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, lay.total);
+    if (offsets_host) {
+        rc = check_offsets_host(offsets_host, B, N);
+        if (rc) return rc;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws + lay.header);
+    void *y = ws + lay.y;
+    float *qk = reinterpret_cast<float *>(ws + lay.qk);
+    float *gb = reinterpret_cast<float *>(ws + lay.gb);
+    const int serial_max = INT_MAX;  // every sequence on the token-serial kernel
+
+    ConvParams cp{};
+    cp.x = qkv; cp.w = w; cp.bias = bias; cp.offsets = offsets; cp.init = conv_init; cp.y = y;
+    cp.B = B; cp.N = N; cp.C = (int)width; cp.Kc = Kc; cp.D = D; cp.L = (int)L;
+    cp.silu = act == GDN_ACT_SILU;
+    cp.prep = 1; cp.qk = qk; cp.gb = gb; cp.a = a; cp.bl = b; cp.A_log = A_log; cp.dt_bias = dt_bias;
+    cp.H = H; cp.HQ = HQ; cp.K = K; cp.V = V; cp.prep_max_len = serial_max;
+    cp.header = hdr; cp.chunk_min_len = serial_max;
+    bool fused = false;
+    cudaError_t e = launch_conv(cp, dtype, s, &fused);
+    if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
+    if (!fused && N > 0) {
+        PrepParams pp{};
+        pp.y = y; pp.a = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias; pp.qk = qk; pp.gb = gb;
+        pp.N = N; pp.H = H; pp.HQ = HQ; pp.K = K; pp.V = V;
+        e = launch_prepare(pp, dtype, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
+    }
+    e = launch_conv_final(qkv, offsets, conv_init, conv_fin, B, N, (int)width, (int)L, dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "conv final-state kernel launch");
+
+    DeltaParams dp{};
+    dp.y = y; dp.qk = qk; dp.gb = gb; dp.offsets = offsets; dp.state_init = state_init;
+    dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;
+    dp.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
+    dp.serial_max_len = serial_max;
+    e = launch_delta_serial(dp, dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// common.cuh - small device helpers shared by the libgdn kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace gdn {
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);  // round to nearest even
+}
+
+// Round an fp32 value to T and back (what a store of T followed by a load sees).
+template <typename T>
+__device__ __forceinline__ float round_through(float x) { return to_f32(from_f32<T>(x)); }
+
+// 16-byte vector of T: 8 bf16 or 4 fp32 values.
+template <typename T>
+struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    union {
+        uint4 u;
+        T v[N];
+    };
+};
+
+// Full-warp xor reduction over groups of `W` consecutive lanes (W a power of 2).
+template <int W>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int off = W / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// True when offsets are globally consistent and sequence b is well formed
+// (offsets[0] == 0, offsets[B] == N, 0 <= start <= end <= N).
+__device__ __forceinline__ bool seq_bounds(const int32_t *offsets, int B, int N, int b,
+                                           int &start, int &end) {
+    start = __ldg(offsets + b);
+    end = __ldg(offsets + b + 1);
+    return __ldg(offsets) == 0 && __ldg(offsets + B) == N && start >= 0 && end >= start &&
+           end <= N;
+}
+
+// Index of the sequence holding token t (0 <= t < offsets[B]): the largest b
+// in [0, B) with offsets[b] <= t.  For nondecreasing offsets that sequence is
+// not empty and offsets[b] <= t < offsets[b+1].
+__device__ __forceinline__ int seq_of_token(const int32_t *offsets, int B, int t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(offsets + mid) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Decay and update rate of one (token, value head) [paged_ssm.rs,
+// DELTA_PREPARE; gated_delta_rate_activation.rs, decay chain]:
+//   g = exp(-exp(A_log) * softplus(a + dt_bias)),  beta = sigmoid(b),
+// softplus(x) = max(x, 0) + log1p(exp(-|x|)).  Shared by every kernel that
+// computes them so the fused and standalone routes give identical bits.
+__device__ __forceinline__ void decay_and_rate(float a, float dt_bias, float A_log, float b,
+                                               float &g, float &beta) {
+    const float x = a + dt_bias;
+    const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+    g = expf(-expf(A_log) * softplus);
+    beta = 1.f / (1.f + expf(-b));
+}
+
+// log(g) for the same (token, value head), kept in the log domain.
+__device__ __forceinline__ float log_decay(float a, float dt_bias, float A_log) {
+    const float x = a + dt_bias;
+    const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+    return -expf(A_log) * softplus;
+}
+
+}  // namespace gdn

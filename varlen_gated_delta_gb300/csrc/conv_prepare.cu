@@ -1,0 +1,434 @@
+// conv_prepare.cu - varlen causal depthwise conv1d with state, fused with the
+// prepare step (q/k L2 norms, decay g, rate beta).
+//
+// Operations: paged_ssm.rs (onnxruntime-ep-mlx 0.31.1), CONV kernel (conv,
+// SiLU, final conv state) and DELTA_PREPARE kernel (norms, g, beta);
+// gated_delta_rate_activation.rs (mlx-c-rust), decay chain.
+//
+// GB300 design: one CTA owns a tile of TT tokens x CT channels, CT = 32 lanes
+// x one 16-byte vector per lane (256 bf16 / 128 fp32 channels).  The tile's
+// input rows plus the L-row causal halo are staged once in shared memory with
+// 128-bit loads, so every x element is read from HBM once; weights are
+// transposed to [Kc][CT] fp32 in shared memory.  Each warp then produces
+// whole token rows, so a head's K channels sit in K/VEC consecutive lanes and
+// its sum of squares is a segmented xor-shuffle: the prepare step is fused
+// into the conv pass without another read of the conv output.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kConvThreads = 256;
+
+template <typename T, int VEC>
+__device__ __forceinline__ void load_f(const T *p, float (&f)[VEC]) {
+    if constexpr (sizeof(T) * VEC == 16) {
+        Vec16<T> v;
+        v.u = *reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = to_f32(v.v[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = to_f32(p[e]);
+    }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void store_f(T *p, const float (&f)[VEC]) {
+    if constexpr (sizeof(T) * VEC == 16) {
+        Vec16<T> v;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v.v[e] = from_f32<T>(f[e]);
+        *reinterpret_cast<uint4 *>(p) = v.u;
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) p[e] = from_f32<T>(f[e]);
+    }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void copy_raw(T *dst, const T *src) {
+    if constexpr (sizeof(T) * VEC == 16) {
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dst[e] = src[e];
+    }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void zero_raw(T *dst) {
+    if constexpr (sizeof(T) * VEC == 16) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dst[e] = from_f32<T>(0.f);
+    }
+}
+
+__device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, float &g,
+                                           float &beta) {
+    decay_and_rate(__ldg(p.a + (size_t)t * p.H + h), __ldg(p.dt_bias + h), __ldg(p.A_log + h),
+                   __ldg(p.bl + (size_t)t * p.H + h), g, beta);
+}
+
+// Block 0 of the conv launch checks the whole offsets array and records the
+// status and the serial / chunked sequence counts in the workspace header.
+__device__ void validate_offsets_block(const ConvParams &p) {
+    __shared__ int s_bad, s_serial, s_chunked;
+    if (threadIdx.x == 0) {
+        s_bad = (__ldg(p.offsets) != 0 || __ldg(p.offsets + p.B) != p.N);
+        s_serial = 0;
+        s_chunked = 0;
+    }
+    __syncthreads();
+    int bad = 0, ns = 0, nc = 0;
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        const int len = __ldg(p.offsets + b + 1) - __ldg(p.offsets + b);
+        if (len < 0) bad = 1;
+        else if (len >= p.chunk_min_len) ++nc;
+        else ++ns;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    atomicAdd(&s_serial, ns);
+    atomicAdd(&s_chunked, nc);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        p.header->status = s_bad ? 4 /* GDN_ERR_OFFSETS */ : 0;
+        p.header->n_serial = s_bad ? 0 : s_serial;
+        p.header->n_chunked = s_bad ? 0 : s_chunked;
+        p.header->n_units = 0;
+    }
+}
+
+// Dynamic shared memory: [Kc][CT] f32 weights | [TT+L][CT] T window |
+// 3 x [TT] int token info.
+template <typename T, int VEC, bool PREP>
+__global__ void __launch_bounds__(kConvThreads)
+    conv_prepare_kernel(const ConvParams p, const int TT, const int n_ctiles) {
+    constexpr int CT = 32 * VEC;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tile_c = blockIdx.x % n_ctiles;
+    const int tile_t = blockIdx.x / n_ctiles;
+    const int c0 = tile_c * CT;
+    const int t0 = tile_t * TT;
+    const int L = p.L, Kc = p.Kc, D = p.D, C = p.C, N = p.N, B = p.B;
+
+    float *sw = reinterpret_cast<float *>(smem);
+    T *sx = reinterpret_cast<T *>(smem + (((size_t)Kc * CT * 4 + 15) & ~size_t(15)));
+    int *s_seq = reinterpret_cast<int *>(sx + (size_t)(TT + L) * CT);
+    int *s_start = s_seq + TT;
+    int *s_len = s_start + TT;
+
+    if (p.header != nullptr && blockIdx.x == 0) validate_offsets_block(p);
+
+    // 1. token -> sequence (or -1 when the token's sequence is malformed)
+    for (int i = threadIdx.x; i < TT; i += blockDim.x) {
+        const int t = t0 + i;
+        int b = -1, st = 0, en = 0;
+        if (t < N) {
+            const int bb = seq_of_token(p.offsets, B, t);
+            if (seq_bounds(p.offsets, B, N, bb, st, en) && t >= st && t < en) b = bb;
+        }
+        s_seq[i] = b;
+        s_start[i] = st;
+        s_len[i] = en - st;
+    }
+    // 2. weights, transposed to [Kc][CT]
+    const T *w = static_cast<const T *>(p.w);
+    for (int i = threadIdx.x; i < Kc * CT; i += blockDim.x) {
+        const int j = i / CT, c = c0 + i % CT;
+        sw[i] = c < C ? to_f32(w[(size_t)c * Kc + j]) : 0.f;
+    }
+    // 3. input window rows [t0 - L, t0 + TT), 128-bit loads
+    const T *x = static_cast<const T *>(p.x);
+    const int rows = TT + L;
+    for (int i = threadIdx.x; i < rows * 32; i += blockDim.x) {
+        const int r = i >> 5, v = i & 31;
+        const long t = (long)t0 - L + r;
+        const int c = c0 + v * VEC;
+        T *dst = sx + (size_t)r * CT + v * VEC;
+        if (t >= 0 && t < N && c < C) copy_raw<T, VEC>(dst, x + (size_t)t * C + c);
+        else zero_raw<T, VEC>(dst);
+    }
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int c = c0 + lane * VEC;
+    const bool cvalid = c < C;
+    float bias[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) bias[e] = 0.f;
+    if (p.bias != nullptr && cvalid) load_f<T, VEC>(static_cast<const T *>(p.bias) + c, bias);
+    const T *init = static_cast<const T *>(p.init);
+    T *y = static_cast<T *>(p.y);
+    const int qk_width = PREP ? 2 * p.HQ * p.K : 0;
+    const int lanes_per_head = PREP ? p.K / VEC : 1;
+
+    for (int i = warp; i < TT; i += nwarps) {
+        const int b = s_seq[i];
+        if (b < 0) continue;  // warp-uniform
+        const int t = t0 + i, s = s_start[i];
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = bias[e];
+        for (int j = 0; j < Kc; ++j) {
+            const int src = t - (Kc - 1 - j) * D;
+            float xv[VEC];
+            if (src >= s) {
+                load_f<T, VEC>(sx + (size_t)(src - t0 + L) * CT + lane * VEC, xv);
+            } else {
+                const int local = src - s;  // in [-L, -1]: read the initial conv state
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    xv[e] = cvalid ? to_f32(init[((size_t)b * C + c + e) * L + L + local]) : 0.f;
+            }
+            const float *wj = sw + j * CT + lane * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] = fmaf(xv[e], wj[e], acc[e]);
+        }
+        float yv[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            float z = acc[e];
+            if (p.silu) z = z / (1.f + expf(-z));
+            yv[e] = round_through<T>(z);  // the conv output is stored in T
+        }
+        if (cvalid) store_f<T, VEC>(y + (size_t)t * C + c, yv);
+
+        if constexpr (PREP) {
+            if (c0 < qk_width) {  // warp-uniform
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) ss = fmaf(yv[e], yv[e], ss);
+                for (int off = lanes_per_head >> 1; off > 0; off >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (cvalid && c < qk_width && s_len[i] < p.prep_max_len) {
+                    const float r = rsqrtf(ss + 1e-12f);
+                    const int plane = c >= p.HQ * p.K;
+                    const int cc = c - plane * p.HQ * p.K;
+                    float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) dst[e] = yv[e] * r;
+                }
+            }
+        }
+    }
+
+    if constexpr (PREP) {
+        if (tile_c == 0) {
+            for (int i = threadIdx.x; i < TT * p.H; i += blockDim.x) {
+                const int ti = i / p.H, h = i % p.H;
+                if (s_seq[ti] < 0 || s_len[ti] >= p.prep_max_len) continue;
+                const int t = t0 + ti;
+                float g, beta;
+                decay_rate(p, t, h, g, beta);
+                p.gb[(size_t)t * p.H + h] = g;
+                p.gb[((size_t)N + t) * p.H + h] = beta;
+            }
+        }
+    }
+}
+
+// Final conv state: fin[b,c,j] = x~(len - L + j).  One thread per (b, c) walks
+// j upward; it reads init index len + j >= j before writing index j, so
+// fin may alias init.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    conv_final_kernel(const T *__restrict__ x, const int32_t *__restrict__ offsets,
+                      const T *init, T *fin, int B, int N, int C, int L) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)B * C) return;
+    const int b = (int)(i / C), c = (int)(i % C);
+    int s, e;
+    if (!seq_bounds(offsets, B, N, b, s, e)) return;
+    const int len = e - s;
+    const T *irow = init + ((size_t)b * C + c) * L;
+    T *frow = fin + ((size_t)b * C + c) * L;
+    for (int j = 0; j < L; ++j) {
+        const int local = len - L + j;
+        const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
+        frow[j] = v;
+    }
+}
+
+// Standalone prepare: one warp per (token, key head) for the norms, then one
+// thread per (token, value head) for g and beta.  With VEC > 1 lane l holds
+// the VEC consecutive channels [l*VEC, (l+1)*VEC) of the head and the sum of
+// squares is reduced over K/VEC lanes in the same order as the fused conv
+// kernel, so both routes give identical bits.  VEC == 1 covers any K <= 256
+// with a strided layout.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const int nb_norm) {
+    const int W = 2 * p.HQ * p.K + p.H * p.V;
+    if ((int)blockIdx.x < nb_norm) {
+        const int lane = threadIdx.x & 31;
+        const long pair = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+        if (pair >= (long)p.N * p.HQ) return;  // warp-uniform
+        const int t = (int)(pair / p.HQ), kh = (int)(pair % p.HQ);
+        const T *y = static_cast<const T *>(p.y) + (size_t)t * W;
+        float *qdst = p.qk + ((size_t)t * p.HQ + kh) * p.K;
+        float *kdst = p.qk + (((size_t)p.N + t) * p.HQ + kh) * p.K;
+        if constexpr (VEC > 1) {
+            const int lph = p.K / VEC;
+            const bool act = lane < lph;
+            float q[VEC], k[VEC], nq = 0.f, nk = 0.f;
+            if (act) {
+                load_f<T, VEC>(y + kh * p.K + lane * VEC, q);
+                load_f<T, VEC>(y + p.HQ * p.K + kh * p.K + lane * VEC, k);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) q[e] = k[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                nq = fmaf(q[e], q[e], nq);
+                nk = fmaf(k[e], k[e], nk);
+            }
+            for (int off = lph >> 1; off > 0; off >>= 1) {
+                nq += __shfl_xor_sync(0xffffffffu, nq, off);
+                nk += __shfl_xor_sync(0xffffffffu, nk, off);
+            }
+            if (act) {
+                const float rq = rsqrtf(nq + 1e-12f), rk = rsqrtf(nk + 1e-12f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    qdst[lane * VEC + e] = q[e] * rq;
+                    kdst[lane * VEC + e] = k[e] * rk;
+                }
+            }
+        } else {
+            float q[8], k[8], nq = 0.f, nk = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = lane + 32 * j;
+                q[j] = i < p.K ? to_f32(y[kh * p.K + i]) : 0.f;
+                k[j] = i < p.K ? to_f32(y[p.HQ * p.K + kh * p.K + i]) : 0.f;
+                nq = fmaf(q[j], q[j], nq);
+                nk = fmaf(k[j], k[j], nk);
+            }
+            nq = group_sum<32>(nq);
+            nk = group_sum<32>(nk);
+            const float rq = rsqrtf(nq + 1e-12f), rk = rsqrtf(nk + 1e-12f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = lane + 32 * j;
+                if (i < p.K) {
+                    qdst[i] = q[j] * rq;
+                    kdst[i] = k[j] * rk;
+                }
+            }
+        }
+    } else {
+        const long i = (long)(blockIdx.x - nb_norm) * blockDim.x + threadIdx.x;
+        if (i >= (long)p.N * p.H) return;
+        const int h = (int)(i % p.H);
+        float g, beta;
+        decay_and_rate(__ldg(p.a + i), __ldg(p.dt_bias + h), __ldg(p.A_log + h), __ldg(p.bl + i),
+                       g, beta);
+        p.gb[i] = g;
+        p.gb[(size_t)p.N * p.H + i] = beta;
+    }
+}
+
+template <typename T, int VEC, bool PREP>
+cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
+    constexpr int CT = 32 * VEC;
+    const int n_ctiles = (p.C + CT - 1) / CT;
+    // tokens per CTA: small batches (decode) use short tiles for parallelism
+    int TT = p.N >= 4096 ? 64 : (p.N >= 512 ? 32 : 8);
+    const long n_ttiles = p.N > 0 ? (p.N + TT - 1) / TT : 1;  // >= 1 block for block 0 duties
+    const long blocks = n_ttiles * n_ctiles;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    const size_t smem = (((size_t)p.Kc * CT * 4 + 15) & ~size_t(15)) +
+                        (size_t)(TT + p.L) * CT * sizeof(T) + 3 * sizeof(int) * TT;
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    auto kern = conv_prepare_kernel<T, VEC, PREP>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<(unsigned)blocks, kConvThreads, smem, s>>>(p, TT, n_ctiles);
+    note_launch();
+    return cudaGetLastError();
+}
+
+bool aligned16(const void *ptr) { return ptr == nullptr || (((uintptr_t)ptr) & 15) == 0; }
+
+}  // namespace
+
+bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int nptrs) {
+    const int vec = dtype == 1 ? 8 : 4;
+    for (int i = 0; i < nptrs; ++i)
+        if (!aligned16(ptrs[i])) return false;
+    if (C % vec != 0) return false;
+    if (K % vec != 0) return false;
+    const int lph = K / vec;
+    return lph >= 1 && lph <= 32 && (lph & (lph - 1)) == 0;
+}
+
+cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t s, bool *fused_prep) {
+    const void *ptrs[] = {p.x, p.y, p.bias};
+    const bool vec_ok = dtype == 1 ? (p.C % 8 == 0) : (p.C % 4 == 0);
+    const bool aligned = vec_ok && aligned16(p.x) && aligned16(p.y) && aligned16(p.bias);
+    const bool fuse = p.prep && conv_can_fuse_prepare(dtype, p.C, p.K, ptrs, 3);
+    if (fused_prep) *fused_prep = fuse;
+    ConvParams q = p;
+    q.prep = fuse;
+    if (dtype == 1) {
+        using T = __nv_bfloat16;
+        if (aligned) return fuse ? launch_conv_t<T, 8, true>(q, s) : launch_conv_t<T, 8, false>(q, s);
+        return launch_conv_t<T, 1, false>(q, s);
+    }
+    if (aligned) return fuse ? launch_conv_t<float, 4, true>(q, s) : launch_conv_t<float, 4, false>(q, s);
+    return launch_conv_t<float, 1, false>(q, s);
+}
+
+cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void *init,
+                              void *fin, int B, int N, int C, int L, int dtype,
+                              cudaStream_t s) {
+    if (L == 0) return cudaSuccess;
+    const long total = (long)B * C;
+    const long blocks = (total + 255) / 256;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    if (dtype == 1) {
+        using T = __nv_bfloat16;
+        conv_final_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
+            static_cast<const T *>(x), offsets, static_cast<const T *>(init),
+            static_cast<T *>(fin), B, N, C, L);
+    } else {
+        conv_final_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+            static_cast<const float *>(x), offsets, static_cast<const float *>(init),
+            static_cast<float *>(fin), B, N, C, L);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s) {
+    const long nb_norm = ((long)p.N * p.HQ + 7) / 8;
+    const long nb_gb = ((long)p.N * p.H + 255) / 256;
+    const long blocks = nb_norm + nb_gb;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    const int W = 2 * p.HQ * p.K + p.H * p.V;
+    const void *ptrs[] = {p.y};
+    const bool chunked = conv_can_fuse_prepare(dtype, W, p.K, ptrs, 1);
+    if (dtype == 1) {
+        using T = __nv_bfloat16;
+        if (chunked) prepare_kernel<T, 8><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+        else prepare_kernel<T, 1><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+    } else {
+        if (chunked) prepare_kernel<float, 4><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+        else prepare_kernel<float, 1><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

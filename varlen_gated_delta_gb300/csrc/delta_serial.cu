@@ -1,0 +1,212 @@
+// delta_serial.cu - token-serial gated delta recurrence (decode and short
+// sequences).
+//
+// Operation: paged_ssm.rs (onnxruntime-ep-mlx 0.31.1), DELTA kernel: per state
+// row S[vi,:] of (sequence b, value head h) and per token t in order,
+//   S <- g S;  r = S.k;  delta = beta (v - r);  S <- S + delta k;  o = scale S.q
+// with k, q the normalised key/query of key head kh = h / (H/HQ).
+//
+// GB300 design.  The state is streamed through HBM exactly once per call: a
+// warp owns a set of state rows and keeps them in registers for the whole
+// sequence.  Each row is split over LPR = KP/16 lanes holding 16 fp32 values
+// (four 16-byte loads), so the two dot products a row needs per token,
+// S_old.k and S_old.q, are reduced with log2(LPR) xor-shuffles for LPR rows at
+// once.  Using S_old.q instead of S_new.q, the read-out is
+//   o = scale (g (S_old.q) + delta (k.q)),
+// which is the same quantity (S_new = g S_old + delta k^T) with one shuffle
+// tree per token instead of two dependent ones; k.q is shared by all rows.
+// The next token's q/k/g/beta/v are prefetched while the current one is
+// applied.
+#include "common.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kSerialThreads = 128;
+
+template <typename T, int KP, int RG, bool VEC4>
+__global__ void __launch_bounds__(kSerialThreads)
+    delta_serial_kernel(const DeltaParams p) {
+    constexpr int EPL = 16;          // state values per lane per row
+    constexpr int LPR = KP / EPL;    // lanes per row
+    constexpr int RPI = 32 / LPR;    // rows per warp per row group
+    constexpr int ROWS_W = RPI * RG; // rows per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane % LPR, rlane = lane / LPR;
+    const int rows_cta = (blockDim.x >> 5) * ROWS_W;
+    const int nrb = (p.V + rows_cta - 1) / rows_cta;
+    const int K = p.K, V = p.V, H = p.H, HQ = p.HQ, N = p.N;
+
+    long blk = blockIdx.x;
+    const int rb = (int)(blk % nrb);
+    blk /= nrb;
+    const int h = (int)(blk % H);
+    const int b = (int)(blk / H);
+    int s, e;
+    if (!seq_bounds(p.offsets, p.B, N, b, s, e)) return;
+    if (e - s >= p.serial_max_len) return;  // owned by the chunked kernel
+    const int kh = h / (H / HQ);
+    const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
+
+    // this lane's K columns: float4 blocks (sub + LPR*m), m = 0..3
+    int kidx[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) kidx[m] = 4 * (sub + LPR * m);
+
+    int vi[RG];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) vi[r] = rb * rows_cta + warp * ROWS_W + r * RPI + rlane;
+
+    auto load4 = [&](const float *base, int k0, float *dst) {
+        if constexpr (VEC4) {
+            if (k0 < K) {
+                const float4 v = *reinterpret_cast<const float4 *>(base + k0);
+                dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+            } else {
+                dst[0] = dst[1] = dst[2] = dst[3] = 0.f;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dst[u] = (k0 + u < K) ? base[k0 + u] : 0.f;
+        }
+    };
+    auto store4 = [&](float *base, int k0, const float *src) {
+        if constexpr (VEC4) {
+            if (k0 < K) *reinterpret_cast<float4 *>(base + k0) = make_float4(src[0], src[1], src[2], src[3]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (k0 + u < K) base[k0 + u] = src[u];
+        }
+    };
+
+    float S[RG][EPL];
+    const size_t head_base = ((size_t)b * H + h) * V;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+        if (vi[r] < V) {
+            const float *row = p.state_init + (head_base + vi[r]) * K;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) load4(row, kidx[m], &S[r][4 * m]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) S[r][u] = 0.f;
+        }
+    }
+
+    const T *y = static_cast<const T *>(p.y);
+    T *out = static_cast<T *>(p.out);
+    const float scale = p.scale;
+
+    float qc[EPL], kc[EPL], vc[RG], gc = 1.f, bc = 0.f;
+    auto fetch = [&](int t, float *q, float *k, float *v, float &g, float &beta) {
+        const float *qrow = p.qk + ((size_t)t * HQ + kh) * K;
+        const float *krow = p.qk + (((size_t)N + t) * HQ + kh) * K;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            load4(qrow, kidx[m], &q[4 * m]);
+            load4(krow, kidx[m], &k[4 * m]);
+        }
+        g = __ldg(p.gb + (size_t)t * H + h);
+        beta = __ldg(p.gb + ((size_t)N + t) * H + h);
+        const T *vrow = y + (size_t)t * W + (size_t)2 * HQ * K + (size_t)h * V;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) v[r] = vi[r] < V ? to_f32(vrow[vi[r]]) : 0.f;
+    };
+    if (s < e) fetch(s, qc, kc, vc, gc, bc);
+
+    for (int t = s; t < e; ++t) {
+        float qn[EPL], kn[EPL], vn[RG], gn = 1.f, bn = 0.f;
+        if (t + 1 < e) fetch(t + 1, qn, kn, vn, gn, bn);
+
+        float kq = 0.f;
+#pragma unroll
+        for (int u = 0; u < EPL; ++u) kq = fmaf(kc[u], qc[u], kq);
+        kq = group_sum<LPR>(kq);
+
+        float sk[RG], sq[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) {
+                a0 = fmaf(S[r][u], kc[u], a0);
+                a1 = fmaf(S[r][u], qc[u], a1);
+            }
+            sk[r] = a0;
+            sq[r] = a1;
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) {
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+                sk[r] += __shfl_xor_sync(0xffffffffu, sk[r], off);
+                sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], off);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            const float delta = bc * (vc[r] - gc * sk[r]);
+            const float o = gc * sq[r] + delta * kq;
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) S[r][u] = fmaf(gc, S[r][u], delta * kc[u]);
+            if (sub == 0 && vi[r] < V)
+                out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
+        }
+        if (t + 1 < e) {
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) {
+                qc[u] = qn[u];
+                kc[u] = kn[u];
+            }
+#pragma unroll
+            for (int r = 0; r < RG; ++r) vc[r] = vn[r];
+            gc = gn;
+            bc = bn;
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+        if (vi[r] < V) {
+            float *row = p.state_fin + (head_base + vi[r]) * K;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) store4(row, kidx[m], &S[r][4 * m]);
+        }
+    }
+}
+
+template <typename T, int KP, int RG>
+cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s) {
+    constexpr int ROWS_W = (32 / (KP / 16)) * RG;
+    const int rows_cta = (kSerialThreads / 32) * ROWS_W;
+    const long nrb = (p.V + rows_cta - 1) / rows_cta;
+    const long blocks = (long)p.B * p.H * nrb;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    if (vec4) delta_serial_kernel<T, KP, RG, true><<<(unsigned)blocks, kSerialThreads, 0, s>>>(p);
+    else delta_serial_kernel<T, KP, RG, false><<<(unsigned)blocks, kSerialThreads, 0, s>>>(p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_serial_t(const DeltaParams &p, cudaStream_t s) {
+    const bool vec4 = (p.K % 4 == 0) && ((uintptr_t)p.qk % 16 == 0) &&
+                      ((uintptr_t)p.state_init % 16 == 0) && ((uintptr_t)p.state_fin % 16 == 0);
+    if (p.K <= 16) return launch_serial_kp<T, 16, 1>(p, vec4, s);
+    if (p.K <= 32) return launch_serial_kp<T, 32, 1>(p, vec4, s);
+    if (p.K <= 64) return launch_serial_kp<T, 64, 1>(p, vec4, s);
+    if (p.K <= 128) return launch_serial_kp<T, 128, 2>(p, vec4, s);
+    return launch_serial_kp<T, 256, 4>(p, vec4, s);
+}
+
+}  // namespace
+
+cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s) {
+    if (dtype == 1) return launch_serial_t<__nv_bfloat16>(p, s);
+    return launch_serial_t<float>(p, s);
+}
+
+}  // namespace gdn

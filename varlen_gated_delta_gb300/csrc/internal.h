@@ -1,0 +1,71 @@
+// internal.h - host-side interface between the C ABI (api.cpp) and the
+// kernel launchers (*.cu).  Not installed; the public ABI is include/gdn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Workspace header written by the device (first 256 bytes of a workspace).
+struct WsHeader {
+    int status;          // gdn_status of the device-side checks
+    int n_serial;        // sequences run by the token-serial kernel
+    int n_chunked;       // sequences run by the chunked kernel
+    int n_units;         // chunked work units
+    unsigned int next_unit;  // work counter of the persistent chunked kernel
+    int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+struct ConvParams {
+    const void *x, *w, *bias;
+    const int32_t *offsets;
+    const void *init;
+    void *y;
+    int B, N, C, Kc, D, L, silu;
+    // fused prepare (prep != 0): q/k norms and g/beta for tokens of sequences
+    // shorter than prep_max_len.
+    int prep;
+    float *qk, *gb;
+    const float *a, *bl, *A_log, *dt_bias;
+    int H, HQ, K, V, prep_max_len;
+    // block 0 validates offsets and writes counts when header != nullptr
+    WsHeader *header;
+    int chunk_min_len;
+};
+
+struct PrepParams {
+    const void *y;
+    const float *a, *bl, *A_log, *dt_bias;
+    float *qk, *gb;
+    int N, H, HQ, K, V;
+};
+
+struct DeltaParams {
+    const void *y;
+    const float *qk, *gb;
+    const int32_t *offsets;
+    const float *state_init;
+    void *out;
+    float *state_fin;
+    int B, N, H, HQ, K, V;
+    float scale;
+    int serial_max_len;  // sequences with len >= this are skipped (chunked path)
+};
+
+// Kernel launchers (return the launch error, counted in gdn_launch_count()).
+cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t s, bool *fused_prep);
+cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void *init,
+                              void *fin, int B, int N, int C, int L, int dtype,
+                              cudaStream_t s);
+cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s);
+
+// Whether launch_conv can fuse the prepare step for this geometry.
+bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int nptrs);
+
+void note_launch(unsigned n = 1);
+
+}  // namespace gdn
