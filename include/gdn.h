@@ -101,7 +101,7 @@ GDN_API const char *gdn_last_error(void);
  *   conv_fin  [B, C, L] T    last L raw inputs of (conv_init || sequence),
  *                            copied bit-exactly; may equal conv_init
  *   act       gdn_activation
- * Requires B >= 1, N >= 0, C >= 1, Kc >= 1, D >= 1, (Kc-1)*D < 2^31.
+ * Requires B >= 1, N >= 0, C >= 1, 1 <= Kc <= 64, D >= 1, (Kc-1)*D <= 4096.
  * When L == 0, conv_init and conv_fin may be NULL.
  */
 GDN_API int gdn_conv1d_varlen(const void *x, const void *w, const void *bias,

@@ -72,6 +72,7 @@ GEOMS = [
     ("bf16-k256-v64", "bf16", 1, 2, 256, 64, 4, 1, True, True, (12, 3)),
     ("f32-kc1", "f32", 1, 1, 16, 16, 1, 1, True, True, (6, 2)),
     ("bf16-kc2-d3", "bf16", 1, 2, 64, 32, 2, 3, True, True, (1, 2, 3, 20)),
+    ("bf16-d100-unstaged", "bf16", 1, 2, 32, 16, 4, 100, True, True, (150, 0, 420)),
 ]
 
 

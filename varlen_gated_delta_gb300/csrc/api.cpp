@@ -135,6 +135,7 @@ int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int3
         return fail(GDN_ERR_NULL, "conv1d: a required pointer is NULL");
     if ((long)B * C > INT_MAX) return fail(GDN_ERR_OVERFLOW, "conv dispatch B*C exceeds int32");
     if (L > 4096) return fail(GDN_ERR_UNSUPPORTED, "receptive field L=%ld above 4096", L);
+    if (Kc > 64) return fail(GDN_ERR_UNSUPPORTED, "conv width Kc=%d above 64", Kc);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ConvParams p{};
     p.x = x; p.w = w; p.bias = bias; p.offsets = offsets; p.init = conv_init; p.y = y;
@@ -232,6 +233,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     const long L = (long)(Kc - 1) * D;
     if (L >= INT_MAX) return fail(GDN_ERR_OVERFLOW, "receptive field (Kc-1)*D exceeds int32");
     if (L > 4096) return fail(GDN_ERR_UNSUPPORTED, "receptive field L=%ld above 4096", L);
+    if (Kc > 64) return fail(GDN_ERR_UNSUPPORTED, "conv width Kc=%d above 64", Kc);
     if (!w || !A_log || !dt_bias || !offsets || !state_init || !state_fin ||
         (N > 0 && (!qkv || !a || !b || !out)) || (L > 0 && (!conv_init || !conv_fin)))
         return fail(GDN_ERR_NULL, "layer: a required pointer is NULL");

@@ -104,9 +104,10 @@ __device__ void validate_offsets_block(const ConvParams &p) {
     }
 }
 
-// Dynamic shared memory: [Kc][CT] f32 weights | [TT+L][CT] T window |
-// 3 x [TT] int token info.
-template <typename T, int VEC, bool PREP>
+// Dynamic shared memory: [Kc][CT] f32 weights | [TT+L][CT] T window (only
+// when STAGE) | 3 x [TT] int token info.  Without STAGE (very long receptive
+// fields) the taps are read from global memory directly.
+template <typename T, int VEC, bool PREP, bool STAGE>
 __global__ void __launch_bounds__(kConvThreads)
     conv_prepare_kernel(const ConvParams p, const int TT, const int n_ctiles) {
     constexpr int CT = 32 * VEC;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kConvThreads)
 
     float *sw = reinterpret_cast<float *>(smem);
     T *sx = reinterpret_cast<T *>(smem + (((size_t)Kc * CT * 4 + 15) & ~size_t(15)));
-    int *s_seq = reinterpret_cast<int *>(sx + (size_t)(TT + L) * CT);
+    int *s_seq = reinterpret_cast<int *>(sx + (STAGE ? (size_t)(TT + L) * CT : 0));
     int *s_start = s_seq + TT;
     int *s_len = s_start + TT;
 
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kConvThreads)
     }
     // 3. input window rows [t0 - L, t0 + TT), 128-bit loads
     const T *x = static_cast<const T *>(p.x);
-    const int rows = TT + L;
+    const int rows = STAGE ? TT + L : 0;
     for (int i = threadIdx.x; i < rows * 32; i += blockDim.x) {
         const int r = i >> 5, v = i & 31;
         const long t = (long)t0 - L + r;
@@ -180,7 +181,14 @@ __global__ void __launch_bounds__(kConvThreads)
             const int src = t - (Kc - 1 - j) * D;
             float xv[VEC];
             if (src >= s) {
-                load_f<T, VEC>(sx + (size_t)(src - t0 + L) * CT + lane * VEC, xv);
+                if constexpr (STAGE) {
+                    load_f<T, VEC>(sx + (size_t)(src - t0 + L) * CT + lane * VEC, xv);
+                } else if (cvalid) {
+                    load_f<T, VEC>(x + (size_t)src * C + c, xv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) xv[e] = 0.f;
+                }
             } else {
                 const int local = src - s;  // in [-L, -1]: read the initial conv state
 #pragma unroll
@@ -344,10 +352,12 @@ cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
     const long n_ttiles = p.N > 0 ? (p.N + TT - 1) / TT : 1;  // >= 1 block for block 0 duties
     const long blocks = n_ttiles * n_ctiles;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    const size_t smem = (((size_t)p.Kc * CT * 4 + 15) & ~size_t(15)) +
-                        (size_t)(TT + p.L) * CT * sizeof(T) + 3 * sizeof(int) * TT;
+    const size_t wbytes = ((size_t)p.Kc * CT * 4 + 15) & ~size_t(15);
+    const size_t window = (size_t)(TT + p.L) * CT * sizeof(T);
+    const bool stage = window <= 64 * 1024;
+    const size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    auto kern = conv_prepare_kernel<T, VEC, PREP>;
+    auto kern = stage ? conv_prepare_kernel<T, VEC, PREP, true> : conv_prepare_kernel<T, VEC, PREP, false>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
