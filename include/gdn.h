@@ -196,6 +196,46 @@ GDN_API int gdn_chunk_min_len(void);
 /* Number of kernels this library has launched in this process. */
 GDN_API uint64_t gdn_launch_count(void);
 
+/* Size of the static device scratch used by gdn_layer_varlen_noalloc. */
+#define GDN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * gdn_layer_varlen_noalloc - gdn_layer_varlen for callers that cannot
+ * allocate device memory (no counterpart on the source pages; this is an
+ * interface convenience, not part of the method).
+ *
+ * Some callers cannot call cudaMalloc for a workspace: a plain-C host runtime
+ * without a device allocator, an inference plugin whose host framework owns
+ * all device memory, or a latency-critical loop that cannot accept
+ * cudaMalloc's implicit device synchronisation.  This call takes the same
+ * inputs and outputs as gdn_layer_varlen (the caller still provides them)
+ * but uses a fixed device array of GDN_NOALLOC_SCRATCH_BYTES (16 MiB) inside
+ * the library as its workspace; it allocates nothing.
+ *
+ * - Every GPU that loads the library holds the 16 MiB array until exit.
+ * - The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress (the device must be current); make that first call
+ *   before any stream capture.
+ * - Geometries whose gdn_workspace_bytes() exceeds the array are rejected
+ *   with GDN_ERR_WORKSPACE and a message naming both sizes (for the
+ *   HQ=16, H=32, K=V=128 bf16 geometry that is about 500 tokens per call).
+ * - All calls share the array and it keeps the last call's contents; the
+ *   part that must start cleared is cleared on `stream` before use.  Calls
+ *   that overlap on the GPU (for example on two streams) race on the array:
+ *   serialise them.
+ * - gdn_workspace_status() can read the status of the last call only through
+ *   the regular entry point's workspace; here errors in host-provided
+ *   offsets are reported synchronously when offsets_host is given.
+ */
+GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void *bias,
+                                     const float *a, const float *b, const float *A_log,
+                                     const float *dt_bias, const int32_t *offsets,
+                                     const int32_t *offsets_host, const void *conv_init,
+                                     void *conv_fin, const float *state_init, void *out,
+                                     float *state_fin, int B, int N, int H, int HQ, int K,
+                                     int V, int Kc, int D, int act, float scale, int dtype,
+                                     void *stream);
+
 #ifdef __cplusplus
 }
 #endif

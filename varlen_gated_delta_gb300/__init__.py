@@ -65,6 +65,8 @@ def load_library():
     lib.gdn_prepare.argtypes = [vp] * 7 + [i] * 6 + [vp]
     lib.gdn_delta_varlen.argtypes = [vp] * 7 + [i] * 6 + [f, i, vp]
     lib.gdn_layer_varlen.argtypes = [vp] * 14 + [i] * 9 + [f, i, vp, sz, vp]
+    lib.gdn_layer_varlen_noalloc.argtypes = [vp] * 14 + [i] * 9 + [f, i, vp]
+    lib.gdn_layer_varlen_noalloc.restype = i
     lib.gdn_workspace_bytes.restype = sz
     lib.gdn_workspace_bytes.argtypes = [i] * 9
     lib.gdn_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]

@@ -68,4 +68,7 @@ bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int
 
 void note_launch(unsigned n = 1);
 
+// Record a message for gdn_last_error() on this thread and return `code`.
+int set_error(int code, const char *fmt, ...);
+
 }  // namespace gdn
