@@ -280,22 +280,46 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     gdn.gdn_workspace_status(ws)
 
+    # eager steps (one library call per step from Python)
+    eager0, eager1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eager0.record(stream)
+    for _ in range(args.steps):
+        step()
+    eager1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = eager0.elapsed_time(eager1)
+
+    # the same step captured once in a CUDA graph (launch-bound decode), replayed
+    launches_per_step0 = gdn.gdn_launch_count()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    launches_per_step = gdn.gdn_launch_count() - launches_per_step0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    launches0 = gdn.gdn_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    launches = gdn.gdn_launch_count() - launches0
+    launches = launches_per_step * args.steps
     ms = e0.elapsed_time(e1)
 
     # dominant kernel alone: the token-serial recurrence, same inputs, CUDA events
@@ -376,6 +400,8 @@ def run_ours(args, wl):
             "e2e": {"value": world * N * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "timing": "CUDA graph replay of one gdn_layer_varlen call per step",
+            "ms_per_step_eager": eager_ms / args.steps,
             "clocks": clocks,
         }
         if not args.no_cpu_baseline:

@@ -171,7 +171,7 @@ int gdn_prepare(const void *y, const float *a, const float *b, const float *A_lo
     PrepParams p{};
     p.y = y; p.a = a; p.bl = b; p.A_log = A_log; p.dt_bias = dt_bias; p.qk = qk_norm; p.gb = g_beta;
     p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
-    cudaError_t e = launch_prepare(p, dtype, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_prepare(p, dtype, static_cast<cudaStream_t>(stream), false);
     if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     return GDN_OK;
 }
@@ -195,7 +195,8 @@ int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
     p.out = out; p.state_fin = state_fin; p.B = B; p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
     p.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
     p.serial_max_len = INT_MAX;
-    cudaError_t e = launch_delta_serial(p, dtype, static_cast<cudaStream_t>(stream));
+    p.conv_fin = nullptr;
+    cudaError_t e = launch_delta_serial(p, dtype, static_cast<cudaStream_t>(stream), false);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
     return GDN_OK;
 }
@@ -279,18 +280,20 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         PrepParams pp{};
         pp.y = y; pp.a = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias; pp.qk = qk; pp.gb = gb;
         pp.N = N; pp.H = H; pp.HQ = HQ; pp.K = K; pp.V = V;
-        e = launch_prepare(pp, dtype, s);
+        e = launch_prepare(pp, dtype, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
-    e = launch_conv_final(qkv, offsets, conv_init, conv_fin, B, N, (int)width, (int)L, dtype, s);
-    if (e != cudaSuccess) return cuda_fail(e, "conv final-state kernel launch");
-
     DeltaParams dp{};
     dp.y = y; dp.qk = qk; dp.gb = gb; dp.offsets = offsets; dp.state_init = state_init;
     dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;
     dp.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
     dp.serial_max_len = serial_max;
-    e = launch_delta_serial(dp, dtype, s);
+    // the recurrence kernel also writes the final conv state (after the conv
+    // kernel has finished reading the initial one) and overlaps, through
+    // programmatic dependent launch, its state loads with the conv kernel
+    dp.conv_x = qkv; dp.conv_init = conv_init; dp.conv_fin = L > 0 ? conv_fin : nullptr;
+    dp.conv_L = (int)L;
+    e = launch_delta_serial(dp, dtype, s, /*pdl=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
     return GDN_OK;
 }

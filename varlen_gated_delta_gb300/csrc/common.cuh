@@ -35,6 +35,16 @@ struct Vec16 {
     };
 };
 
+// Programmatic dependent launch: a primary grid lets its dependent grid start
+// early; the dependent waits for the primary's completion (and memory) only
+// where it consumes the primary's outputs.  Both are no-ops without PDL.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Full-warp xor reduction over groups of `W` consecutive lanes (W a power of 2).
 template <int W>
 __device__ __forceinline__ float group_sum(float x) {

@@ -124,6 +124,9 @@ __global__ void __launch_bounds__(kConvThreads)
     int *s_start = s_seq + TT;
     int *s_len = s_start + TT;
 
+    // The dependent kernel (recurrence / final state) may start streaming its
+    // own inputs now; it waits for this grid before reading what it writes.
+    pdl_launch_dependents();
     if (p.header != nullptr && blockIdx.x == 0) validate_offsets_block(p);
 
     // 1. token -> sequence (or -1 when the token's sequence is malformed)
@@ -249,6 +252,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     conv_final_kernel(const T *__restrict__ x, const int32_t *__restrict__ offsets,
                       const T *init, T *fin, int B, int N, int C, int L) {
+    pdl_wait_primary();  // the conv kernel reads init before fin may overwrite it
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)B * C) return;
     const int b = (int)(i / C), c = (int)(i % C);
@@ -272,6 +276,8 @@ __global__ void __launch_bounds__(256)
 // with a strided layout.
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const int nb_norm) {
+    pdl_launch_dependents();
+    pdl_wait_primary();  // reads the conv output when launched as a PDL dependent
     const int W = 2 * p.HQ * p.K + p.H * p.V;
     if ((int)blockIdx.x < nb_norm) {
         const int lane = threadIdx.x & 31;
@@ -406,21 +412,23 @@ cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void 
     const long total = (long)B * C;
     const long blocks = (total + 255) / 256;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    cudaError_t e;
     if (dtype == 1) {
         using T = __nv_bfloat16;
-        conv_final_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(
-            static_cast<const T *>(x), offsets, static_cast<const T *>(init),
-            static_cast<T *>(fin), B, N, C, L);
+        e = launch_kernel(conv_final_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                          static_cast<const T *>(x), offsets, static_cast<const T *>(init),
+                          static_cast<T *>(fin), B, N, C, L);
     } else {
-        conv_final_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
-            static_cast<const float *>(x), offsets, static_cast<const float *>(init),
-            static_cast<float *>(fin), B, N, C, L);
+        e = launch_kernel(conv_final_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                          static_cast<const float *>(x), offsets,
+                          static_cast<const float *>(init), static_cast<float *>(fin), B, N, C,
+                          L);
     }
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
-cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s) {
+cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s, bool pdl) {
     const long nb_norm = ((long)p.N * p.HQ + 7) / 8;
     const long nb_gb = ((long)p.N * p.H + 255) / 256;
     const long blocks = nb_norm + nb_gb;
@@ -429,16 +437,19 @@ cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s) {
     const int W = 2 * p.HQ * p.K + p.H * p.V;
     const void *ptrs[] = {p.y};
     const bool chunked = conv_can_fuse_prepare(dtype, W, p.K, ptrs, 1);
+    const dim3 grid((unsigned)blocks), block(256);
+    const int nb = (int)nb_norm;
+    cudaError_t e;
     if (dtype == 1) {
         using T = __nv_bfloat16;
-        if (chunked) prepare_kernel<T, 8><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
-        else prepare_kernel<T, 1><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+        e = chunked ? launch_kernel(prepare_kernel<T, 8>, grid, block, 0, s, pdl, p, nb)
+                    : launch_kernel(prepare_kernel<T, 1>, grid, block, 0, s, pdl, p, nb);
     } else {
-        if (chunked) prepare_kernel<float, 4><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
-        else prepare_kernel<float, 1><<<(unsigned)blocks, 256, 0, s>>>(p, (int)nb_norm);
+        e = chunked ? launch_kernel(prepare_kernel<float, 4>, grid, block, 0, s, pdl, p, nb)
+                    : launch_kernel(prepare_kernel<float, 1>, grid, block, 0, s, pdl, p, nb);
     }
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gdn

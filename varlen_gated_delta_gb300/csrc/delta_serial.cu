@@ -25,6 +25,32 @@ namespace {
 
 constexpr int kSerialThreads = 128;
 
+// Final conv state of sequence b for the channel slice `slice` of `nslices`:
+// fin[b,c,j] = x~(len - L + j).  One thread per channel walks j upward and
+// reads index len + j >= j of its own row before writing index j, so the
+// final state may alias the initial one.
+template <typename T>
+__device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int slice,
+                                 int nslices, size_t C) {
+    const int L = p.conv_L;
+    const int len = e - s;
+    const size_t cs = (C + nslices - 1) / nslices;
+    const size_t c0 = (size_t)slice * cs;
+    const size_t c1 = c0 + cs < C ? c0 + cs : C;
+    const T *x = static_cast<const T *>(p.conv_x);
+    const T *init = static_cast<const T *>(p.conv_init);
+    T *fin = static_cast<T *>(p.conv_fin);
+    for (size_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+        const T *irow = init + ((size_t)b * C + c) * L;
+        T *frow = fin + ((size_t)b * C + c) * L;
+        for (int j = 0; j < L; ++j) {
+            const int local = len - L + j;
+            const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
+            frow[j] = v;
+        }
+    }
+}
+
 template <typename T, int KP, int RG, bool VEC4>
 __global__ void __launch_bounds__(kSerialThreads)
     delta_serial_kernel(const DeltaParams p) {
@@ -45,7 +71,7 @@ __global__ void __launch_bounds__(kSerialThreads)
     const int b = (int)(blk / H);
     int s, e;
     if (!seq_bounds(p.offsets, p.B, N, b, s, e)) return;
-    if (e - s >= p.serial_max_len) return;  // owned by the chunked kernel
+    const bool own = e - s < p.serial_max_len;  // else owned by the chunked kernel
     const int kh = h / (H / HQ);
     const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
 
@@ -85,7 +111,7 @@ __global__ void __launch_bounds__(kSerialThreads)
     const size_t head_base = ((size_t)b * H + h) * V;
 #pragma unroll
     for (int r = 0; r < RG; ++r) {
-        if (vi[r] < V) {
+        if (own && vi[r] < V) {
             const float *row = p.state_init + (head_base + vi[r]) * K;
 #pragma unroll
             for (int m = 0; m < 4; ++m) load4(row, kidx[m], &S[r][4 * m]);
@@ -94,6 +120,12 @@ __global__ void __launch_bounds__(kSerialThreads)
             for (int u = 0; u < EPL; ++u) S[r][u] = 0.f;
         }
     }
+
+    // The state loads above are in flight; everything below reads what the
+    // conv/prepare kernel wrote (when launched as its PDL dependent).
+    pdl_wait_primary();
+    if (p.conv_fin != nullptr) conv_final_slice<T>(p, b, s, e, h * nrb + rb, H * nrb, W);
+    if (!own) return;
 
     const T *y = static_cast<const T *>(p.y);
     T *out = static_cast<T *>(p.out);
@@ -178,35 +210,40 @@ __global__ void __launch_bounds__(kSerialThreads)
 }
 
 template <typename T, int KP, int RG>
-cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s) {
+cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s, bool pdl) {
     constexpr int ROWS_W = (32 / (KP / 16)) * RG;
     const int rows_cta = (kSerialThreads / 32) * ROWS_W;
     const long nrb = (p.V + rows_cta - 1) / rows_cta;
     const long blocks = (long)p.B * p.H * nrb;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    if (vec4) delta_serial_kernel<T, KP, RG, true><<<(unsigned)blocks, kSerialThreads, 0, s>>>(p);
-    else delta_serial_kernel<T, KP, RG, false><<<(unsigned)blocks, kSerialThreads, 0, s>>>(p);
+    cudaError_t e;
+    if (vec4)
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true>, dim3((unsigned)blocks),
+                          dim3(kSerialThreads), 0, s, pdl, p);
+    else
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, false>, dim3((unsigned)blocks),
+                          dim3(kSerialThreads), 0, s, pdl, p);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <typename T>
-cudaError_t launch_serial_t(const DeltaParams &p, cudaStream_t s) {
+cudaError_t launch_serial_t(const DeltaParams &p, cudaStream_t s, bool pdl) {
     const bool vec4 = (p.K % 4 == 0) && ((uintptr_t)p.qk % 16 == 0) &&
                       ((uintptr_t)p.state_init % 16 == 0) && ((uintptr_t)p.state_fin % 16 == 0);
-    if (p.K <= 16) return launch_serial_kp<T, 16, 1>(p, vec4, s);
-    if (p.K <= 32) return launch_serial_kp<T, 32, 1>(p, vec4, s);
-    if (p.K <= 64) return launch_serial_kp<T, 64, 1>(p, vec4, s);
-    if (p.K <= 128) return launch_serial_kp<T, 128, 2>(p, vec4, s);
-    return launch_serial_kp<T, 256, 4>(p, vec4, s);
+    if (p.K <= 16) return launch_serial_kp<T, 16, 1>(p, vec4, s, pdl);
+    if (p.K <= 32) return launch_serial_kp<T, 32, 1>(p, vec4, s, pdl);
+    if (p.K <= 64) return launch_serial_kp<T, 64, 1>(p, vec4, s, pdl);
+    if (p.K <= 128) return launch_serial_kp<T, 128, 2>(p, vec4, s, pdl);
+    return launch_serial_kp<T, 256, 4>(p, vec4, s, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s) {
-    if (dtype == 1) return launch_serial_t<__nv_bfloat16>(p, s);
-    return launch_serial_t<float>(p, s);
+cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s, bool pdl) {
+    if (dtype == 1) return launch_serial_t<__nv_bfloat16>(p, s, pdl);
+    return launch_serial_t<float>(p, s, pdl);
 }
 
 }  // namespace gdn

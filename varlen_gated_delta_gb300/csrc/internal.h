@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace gdn {
 
 // Workspace header written by the device (first 256 bytes of a workspace).
@@ -53,15 +55,39 @@ struct DeltaParams {
     int B, N, H, HQ, K, V;
     float scale;
     int serial_max_len;  // sequences with len >= this are skipped (chunked path)
+    // optional fused conv final-state copy (layer path): conv_fin[b,c,:] =
+    // last L raw inputs of (conv_init || sequence) for every sequence
+    const void *conv_x;
+    const void *conv_init;
+    void *conv_fin;
+    int conv_L;
 };
+
+// Launch `kernel` on `s`; with pdl the launch may overlap the previous kernel
+// on the stream (the kernel must call pdl_wait_primary() before consuming it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel launchers (return the launch error, counted in gdn_launch_count()).
 cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t s, bool *fused_prep);
 cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void *init,
                               void *fin, int B, int N, int C, int L, int dtype,
                               cudaStream_t s);
-cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s, bool pdl);
+cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s, bool pdl);
 
 // Whether launch_conv can fuse the prepare step for this geometry.
 bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int nptrs);
