@@ -1,0 +1,131 @@
+"""GPU parity of the chunked tensor-core recurrence (tcgen05 + TMA).
+
+Sequences of at least gdn_chunk_min_len() tokens take the chunked kernel when
+the geometry allows (bf16, K = 128, V a multiple of 128).  These tests force
+that path (threshold 1) or mix both paths, and compare with the fp64 oracle
+(bf16 tolerance: 2e-2 relative L2) and with the token-serial kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import varlen_gated_delta_gb300 as gdn
+from varlen_gated_delta_gb300 import workloads as W
+from gdn_testlib import cpu64, max_abs, oracle_layer, rel_l2
+from test_gpu_parity import DEV, SERIAL_ONLY, chunk_threshold, run_layer
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def _case(lens, **over):
+    wl = W.scaled(W.WORKLOADS["decode"], lens, name="chunked", **over)
+    return wl, W.make_inputs(wl, DEV)
+
+
+def _check(wl, d, out, cfin, sfin):
+    o_ref, c_ref, s_ref = oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cpu64(cfin), c_ref)
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL and es <= TOL, (f"out {eo:.3e} (max-abs {max_abs(cpu64(out), o_ref):.3e}) "
+                                     f"state {es:.3e} (max-abs {max_abs(cpu64(sfin), s_ref):.3e})")
+    return eo, es
+
+
+def _counts(wl, d, **kw):
+    ws = torch.zeros(gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D),
+                     dtype=torch.uint8, device=DEV)
+    res = run_layer(wl, d, workspace=ws, **kw)
+    return res, gdn.gdn_workspace_status(ws)[1]
+
+
+@pytest.mark.parametrize("lens", [(64,), (1,), (65,), (5, 63, 64, 127, 128, 200), (300, 7, 1000)])
+def test_chunked_matches_oracle(lens):
+    wl, d = _case(lens, HQ=2, H=4)
+    with chunk_threshold(1):
+        (out, cfin, sfin), counts = _counts(wl, d)
+    assert counts[1] == sum(1 for n in lens if n > 0) and counts[2] == counts[1] * wl.H
+    _check(wl, d, out, cfin, sfin)
+
+
+@pytest.mark.parametrize("geom", [dict(HQ=1, H=1), dict(HQ=2, H=2), dict(HQ=1, H=3),
+                                  dict(HQ=2, H=4, V=256), dict(HQ=1, H=2, V=384)])
+def test_chunked_head_geometries(geom):
+    wl, d = _case((150, 40), **geom)
+    with chunk_threshold(1):
+        out, cfin, sfin = run_layer(wl, d)
+    _check(wl, d, out, cfin, sfin)
+
+
+def test_chunked_strong_decay_and_zero_states():
+    wl, d = _case((257, 90), HQ=2, H=4, a_mean=-1.0, b_std=2.0, conv_init_std=None,
+                  state_std=None)
+    d["A_log"].fill_(2.7)              # exp(A_log) ~ 15: near-complete forgetting per chunk
+    with chunk_threshold(1):
+        out, cfin, sfin = run_layer(wl, d)
+    _check(wl, d, out, cfin, sfin)
+
+
+def test_chunked_and_serial_paths_agree():
+    wl, d = _case((3, 90, 64, 200, 1, 130), HQ=2, H=4)
+    with chunk_threshold(1):
+        o1, c1, s1 = run_layer(wl, d)
+    with chunk_threshold(SERIAL_ONLY):
+        o2, c2, s2 = run_layer(wl, d)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    assert rel_l2(cpu64(o1), cpu64(o2)) <= TOL and rel_l2(cpu64(s1), cpu64(s2)) <= TOL
+
+
+def test_mixed_batch_uses_both_kernels():
+    wl, d = _case((3, 17, 0, 64, 1, 90, 500), HQ=2, H=4)
+    (out, cfin, sfin), counts = _counts(wl, d)          # default threshold
+    thr = gdn.gdn_chunk_min_len()
+    n_long = sum(1 for n in wl.lengths() if n >= thr)
+    assert counts[1] == n_long and counts[0] == wl.B - n_long and counts[1] > 0 and counts[0] > 0
+    _check(wl, d, out, cfin, sfin)
+
+
+def test_chunked_device_schedule_without_host_offsets():
+    wl, d = _case((700, 2, 129, 64, 300), HQ=2, H=4)
+    (o1, c1, s1), _ = _counts(wl, d, offsets_host=d["offsets_list"])
+    (o2, c2, s2), counts = _counts(wl, d)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2) and torch.equal(c1, c2)
+
+
+def test_chunked_packed_equals_each_sequence_alone_bitwise():
+    wl, d = _case((70, 130, 64, 1), HQ=2, H=4)
+    with chunk_threshold(1):
+        out, cfin, sfin = run_layer(wl, d)
+        offs = d["offsets_list"]
+        for b in range(wl.B):
+            s, e = offs[b], offs[b + 1]
+            d1 = dict(d, qkv=d["qkv"][s:e].contiguous(), a=d["a"][s:e].contiguous(),
+                      b=d["b"][s:e].contiguous(),
+                      offsets=torch.tensor([0, e - s], dtype=torch.int32, device=DEV),
+                      conv_init=d["conv_init"][b:b + 1].contiguous(),
+                      state_init=d["state_init"][b:b + 1].contiguous())
+            o1, c1, s1 = run_layer(wl, d1)
+            assert torch.equal(o1, out[s:e]) and torch.equal(s1[0], sfin[b])
+
+
+def test_chunked_resume_across_calls():
+    wl, d = _case((300,), HQ=2, H=4)
+    with chunk_threshold(1):
+        out, cfin, sfin = run_layer(wl, d)
+        cut = 100
+        part = lambda t, a, b: t[a:b].contiguous()
+        d1 = dict(d, qkv=part(d["qkv"], 0, cut), a=part(d["a"], 0, cut), b=part(d["b"], 0, cut),
+                  offsets=torch.tensor([0, cut], dtype=torch.int32, device=DEV))
+        o1, c1, s1 = run_layer(wl, d1)
+        d2 = dict(d, qkv=part(d["qkv"], cut, 300), a=part(d["a"], cut, 300),
+                  b=part(d["b"], cut, 300),
+                  offsets=torch.tensor([0, 300 - cut], dtype=torch.int32, device=DEV),
+                  conv_init=c1, state_init=s1)
+        o2, c2, s2 = run_layer(wl, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(c2, cfin)
+    assert rel_l2(cpu64(torch.cat([o1, o2])), cpu64(out)) <= 5e-3
+    assert rel_l2(cpu64(s2), cpu64(sfin)) <= 5e-3

@@ -153,6 +153,23 @@ def test_delta_standalone(dt):
 
 # ------------------------------------------------------------------ structural properties
 
+class chunk_threshold:
+    """Temporarily set the length from which sequences take the chunked kernel."""
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        self.old = gdn.gdn_chunk_min_len()
+        gdn.gdn_set_chunk_min_len(self.n)
+
+    def __exit__(self, *exc):
+        gdn.gdn_set_chunk_min_len(0)
+
+
+SERIAL_ONLY = 1 << 30
+
+
 def _bf16_case(lens=(3, 17, 0, 64, 1, 90), **over):
     wl = W.scaled(W.WORKLOADS["decode"], lens, name="props", **over)
     return wl, W.make_inputs(wl, DEV)
@@ -160,7 +177,8 @@ def _bf16_case(lens=(3, 17, 0, 64, 1, 90), **over):
 
 def test_fused_layer_equals_composed_calls_bitwise():
     wl, d = _bf16_case()
-    out, cfin, sfin = run_layer(wl, d)
+    with chunk_threshold(SERIAL_ONLY):   # the composed route is the token-serial kernel
+        out, cfin, sfin = run_layer(wl, d)
     y, c2 = gdn.gdn_conv1d_varlen(d["qkv"], d["w"], d["bias"], d["offsets"], d["conv_init"],
                                   Kc=wl.Kc, D=wl.D)
     qk, gb = gdn.gdn_prepare(y, d["a"], d["b"], d["A_log"], d["dt_bias"], H=wl.H, HQ=wl.HQ,

@@ -90,15 +90,17 @@ static int check_offsets_host(const int32_t *offsets_host, int B, int N) {
 }
 
 struct WsLayout {
-    size_t header, y, qk, gb, total;
+    size_t header, order, y, qk, gb, total;
 };
 
-static WsLayout ws_layout(int N, int H, int HQ, int K, int V, int dtype) {
+static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) {
     WsLayout l;
     const size_t W = 2 * (size_t)HQ * K + (size_t)H * V;
     size_t off = 0;
     l.header = off;
     off += align256(sizeof(WsHeader));
+    l.order = off;
+    off += align256((size_t)B * 4);
     l.y = off;
     off += align256((size_t)N * W * dsize(dtype));
     l.qk = off;
@@ -204,7 +206,7 @@ int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
 size_t gdn_workspace_bytes(int B, int N, int H, int HQ, int K, int V, int Kc, int D, int dtype) {
     if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || Kc < 1 || D < 1) return 0;
     if (!dtype_ok(dtype) || H % HQ != 0 || K > 256) return 0;
-    return ws_layout(N, H, HQ, K, V, dtype).total;
+    return ws_layout(B, N, H, HQ, K, V, dtype).total;
 }
 
 int gdn_workspace_status(const void *workspace, int *counts, void *stream) {
@@ -249,7 +251,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     if ((long)B * H * V * 32 > INT_MAX || (long)B * width > INT_MAX)
         return fail(GDN_ERR_OVERFLOW, "layer dispatch size exceeds int32");
     if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
-    const WsLayout lay = ws_layout(N, H, HQ, K, V, dtype);
+    const WsLayout lay = ws_layout(B, N, H, HQ, K, V, dtype);
     if (!workspace || ((uintptr_t)workspace & 255) != 0)
         return fail(GDN_ERR_WORKSPACE, "workspace must be a non-NULL 256-byte aligned device pointer");
     if (ws_bytes < lay.total)
@@ -258,13 +260,25 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         rc = check_offsets_host(offsets_host, B, N);
         if (rc) return rc;
     }
+    // path choice per sequence: at least `thr` tokens -> chunked kernel
+    const bool chunk_ok = chunked_supported(dtype, K, V, (int)width);
+    const int thr = chunk_min_len();
+    const int serial_max = chunk_ok ? thr : INT_MAX;
+    bool run_chunked = chunk_ok && N >= thr;
+    long max_units = run_chunked ? (long)(B < N / thr ? B : N / thr) * H * (V / 128) : 0;
+    if (run_chunked && offsets_host) {
+        long n = 0;
+        for (int i = 0; i < B; ++i) n += (offsets_host[i + 1] - offsets_host[i]) >= thr;
+        run_chunked = n > 0;
+        max_units = n * H * (V / 128);
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws + lay.header);
     void *y = ws + lay.y;
     float *qk = reinterpret_cast<float *>(ws + lay.qk);
     float *gb = reinterpret_cast<float *>(ws + lay.gb);
-    const int serial_max = INT_MAX;  // every sequence on the token-serial kernel
+    int32_t *order = reinterpret_cast<int32_t *>(ws + lay.order);
 
     ConvParams cp{};
     cp.x = qkv; cp.w = w; cp.bias = bias; cp.offsets = offsets; cp.init = conv_init; cp.y = y;
@@ -273,6 +287,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     cp.prep = 1; cp.qk = qk; cp.gb = gb; cp.a = a; cp.bl = b; cp.A_log = A_log; cp.dt_bias = dt_bias;
     cp.H = H; cp.HQ = HQ; cp.K = K; cp.V = V; cp.prep_max_len = serial_max;
     cp.header = hdr; cp.chunk_min_len = serial_max;
+    cp.seq_order = run_chunked ? order : nullptr; cp.VT = V / 128;
     bool fused = false;
     cudaError_t e = launch_conv(cp, dtype, s, &fused);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
@@ -283,6 +298,18 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         e = launch_prepare(pp, dtype, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
+    const float eff_scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
+    if (run_chunked) {
+        ChunkLaunch cl{};
+        cl.y = y; cl.a = a; cl.bl = b; cl.A_log = A_log; cl.dt_bias = dt_bias;
+        cl.offsets = offsets; cl.seq_order = order; cl.header = hdr;
+        cl.state_init = state_init; cl.state_fin = state_fin; cl.out = out;
+        cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
+        cl.scale = eff_scale; cl.max_units = max_units;
+        e = launch_delta_chunked(cl, s);
+        if (e != cudaSuccess) return cuda_fail(e, "chunked kernel launch");
+    }
+
     DeltaParams dp{};
     dp.y = y; dp.qk = qk; dp.gb = gb; dp.offsets = offsets; dp.state_init = state_init;
     dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;

@@ -22,6 +22,7 @@ namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 256;
+constexpr int kOffsetsCache = 4096;  // offsets entries cached in shared memory
 
 template <typename T, int VEC>
 __device__ __forceinline__ void load_f(const T *p, float (&f)[VEC]) {
@@ -75,32 +76,73 @@ __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, fl
                    __ldg(p.bl + (size_t)t * p.H + h), g, beta);
 }
 
-// Block 0 of the conv launch checks the whole offsets array and records the
-// status and the serial / chunked sequence counts in the workspace header.
-__device__ void validate_offsets_block(const ConvParams &p) {
-    __shared__ int s_bad, s_serial, s_chunked;
+// Block 0 of the conv launch checks the whole offsets array, records the
+// status and the serial / chunked sequence counts in the workspace header
+// and, when asked, schedules the chunked work: the sequences of at least
+// chunk_min_len tokens are listed longest first (by rank, for up to 1024
+// sequences; in index order beyond that) and the work counter is reset.
+__device__ void schedule_block(const ConvParams &p) {
+    __shared__ int s_bad, s_serial, s_chunked, s_base;
+    __shared__ int s_lens[1024];
+    __shared__ int s_warp[kConvThreads / 32];
+    const int B = p.B;
     if (threadIdx.x == 0) {
-        s_bad = (__ldg(p.offsets) != 0 || __ldg(p.offsets + p.B) != p.N);
+        s_bad = (__ldg(p.offsets) != 0 || __ldg(p.offsets + B) != p.N);
         s_serial = 0;
         s_chunked = 0;
+        s_base = 0;
     }
     __syncthreads();
     int bad = 0, ns = 0, nc = 0;
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int len = __ldg(p.offsets + b + 1) - __ldg(p.offsets + b);
         if (len < 0) bad = 1;
         else if (len >= p.chunk_min_len) ++nc;
         else ++ns;
+        if (B <= 1024) s_lens[b] = len;
     }
     if (bad) atomicOr(&s_bad, 1);
     atomicAdd(&s_serial, ns);
     atomicAdd(&s_chunked, nc);
     __syncthreads();
+    const bool ok = !s_bad;
+    if (p.seq_order != nullptr && ok) {
+        const int thr = p.chunk_min_len;
+        if (B <= 1024) {
+            for (int b = threadIdx.x; b < B; b += blockDim.x) {
+                const int len = s_lens[b];
+                if (len < thr) continue;
+                int rank = 0;
+                for (int o = 0; o < B; ++o) {
+                    const int lo = s_lens[o];
+                    rank += (lo >= thr) && (lo > len || (lo == len && o < b));
+                }
+                p.seq_order[rank] = b;
+            }
+        } else {
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+                const int b = b0 + threadIdx.x;
+                const bool take = b < B && (__ldg(p.offsets + b + 1) - __ldg(p.offsets + b)) >= thr;
+                const unsigned m = __ballot_sync(0xffffffffu, take);
+                if (lane == 0) s_warp[warp] = __popc(m);
+                __syncthreads();
+                int before = s_base;
+                for (int w = 0; w < warp; ++w) before += s_warp[w];
+                if (take) p.seq_order[before + __popc(m & ((1u << lane) - 1u))] = b;
+                __syncthreads();
+                if (threadIdx.x == 0)
+                    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s_base += s_warp[w];
+                __syncthreads();
+            }
+        }
+    }
     if (threadIdx.x == 0) {
-        p.header->status = s_bad ? 4 /* GDN_ERR_OFFSETS */ : 0;
-        p.header->n_serial = s_bad ? 0 : s_serial;
-        p.header->n_chunked = s_bad ? 0 : s_chunked;
-        p.header->n_units = 0;
+        p.header->status = ok ? 0 : 4 /* GDN_ERR_OFFSETS */;
+        p.header->n_serial = ok ? s_serial : 0;
+        p.header->n_chunked = ok ? s_chunked : 0;
+        p.header->n_units = (ok && p.seq_order != nullptr) ? s_chunked * p.H * p.VT : 0;
+        p.header->next_unit = 0;
     }
 }
 
@@ -123,19 +165,40 @@ __global__ void __launch_bounds__(kConvThreads)
     int *s_seq = reinterpret_cast<int *>(sx + (STAGE ? (size_t)(TT + L) * CT : 0));
     int *s_start = s_seq + TT;
     int *s_len = s_start + TT;
+    int *s_offs = s_len + TT;  // offsets[0..B] when B + 1 <= kOffsetsCache
+    const bool cache_offs = B + 1 <= kOffsetsCache;
 
     // The dependent kernel (recurrence / final state) may start streaming its
     // own inputs now; it waits for this grid before reading what it writes.
     pdl_launch_dependents();
-    if (p.header != nullptr && blockIdx.x == 0) validate_offsets_block(p);
+    if (p.header != nullptr && blockIdx.x == 0) schedule_block(p);
 
-    // 1. token -> sequence (or -1 when the token's sequence is malformed)
+    // 1. token -> sequence (or -1 when the token's sequence is malformed); the
+    //    search runs in shared memory when the offsets fit there
+    if (cache_offs) {
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) s_offs[i] = __ldg(p.offsets + i);
+        __syncthreads();
+    }
     for (int i = threadIdx.x; i < TT; i += blockDim.x) {
         const int t = t0 + i;
         int b = -1, st = 0, en = 0;
         if (t < N) {
-            const int bb = seq_of_token(p.offsets, B, t);
-            if (seq_bounds(p.offsets, B, N, bb, st, en) && t >= st && t < en) b = bb;
+            if (cache_offs) {
+                int lo = 0, hi = B - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_offs[mid] <= t) lo = mid;
+                    else hi = mid - 1;
+                }
+                st = s_offs[lo];
+                en = s_offs[lo + 1];
+                if (s_offs[0] == 0 && s_offs[B] == N && st >= 0 && en >= st && en <= N && t >= st &&
+                    t < en)
+                    b = lo;
+            } else {
+                const int bb = seq_of_token(p.offsets, B, t);
+                if (seq_bounds(p.offsets, B, N, bb, st, en) && t >= st && t < en) b = bb;
+            }
         }
         s_seq[i] = b;
         s_start[i] = st;
@@ -361,7 +424,8 @@ cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
     const size_t wbytes = ((size_t)p.Kc * CT * 4 + 15) & ~size_t(15);
     const size_t window = (size_t)(TT + p.L) * CT * sizeof(T);
     const bool stage = window <= 64 * 1024;
-    const size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT;
+    const size_t offs_bytes = p.B + 1 <= kOffsetsCache ? sizeof(int) * (p.B + 1) : 0;
+    const size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT + offs_bytes;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     auto kern = stage ? conv_prepare_kernel<T, VEC, PREP, true> : conv_prepare_kernel<T, VEC, PREP, false>;
     if (smem > 48 * 1024) {

@@ -33,9 +33,13 @@ struct ConvParams {
     float *qk, *gb;
     const float *a, *bl, *A_log, *dt_bias;
     int H, HQ, K, V, prep_max_len;
-    // block 0 validates offsets and writes counts when header != nullptr
+    // block 0 validates offsets and writes counts when header != nullptr;
+    // with seq_order != nullptr it also lists the sequences of at least
+    // chunk_min_len tokens, longest first, and sets n_units = count * H * VT
     WsHeader *header;
     int chunk_min_len;
+    int32_t *seq_order;
+    int VT;
 };
 
 struct PrepParams {
@@ -88,6 +92,22 @@ cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void 
                               cudaStream_t s);
 cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s, bool pdl);
+
+// Chunked (tensor-core) recurrence for sequences listed in seq_order.
+struct ChunkLaunch {
+    const void *y;  // conv output [N, W] bf16
+    const float *a, *bl, *A_log, *dt_bias;
+    const int32_t *offsets, *seq_order;
+    WsHeader *header;
+    const float *state_init;
+    float *state_fin;
+    void *out;
+    int B, N, H, HQ, V, W;
+    float scale;
+    long max_units;  // upper bound on work units (grid sizing)
+};
+bool chunked_supported(int dtype, int K, int V, int W);
+cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
 
 // Whether launch_conv can fuse the prepare step for this geometry.
 bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int nptrs);
