@@ -41,7 +41,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = 64;            // chunk length
-constexpr int kThreads = 128;     // 4 warps: all epilogue work; thread 0 issues TMA and MMA
+constexpr int kThreads = 256;     // 8 warps; thread 0 issues TMA and MMA
 constexpr int kAStride = 68;      // fp32 row stride of the A / T scratch (bank-conflict free)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -54,7 +54,7 @@ constexpr uint32_t kOffTb = kOffTw + 8192;             // 8 KB
 constexpr uint32_t kOffP = kOffTb + 8192;              // 8 KB  [64 t][64 i]  K-major
 constexpr uint32_t kOffWt = kOffP + 8192;              // 16 KB [128 kk][64 t] MN-major
 constexpr uint32_t kOffS0 = kOffWt + 16384;            // 32 KB [128 vi][128 kk] K-major
-constexpr uint32_t kOffScratch = kOffS0 + 32768;       // 32 KB: A,T fp32 | Delta^T, Delta'^T bf16
+constexpr uint32_t kOffScratch = kOffS0 + 32768;       // 34 KB: A,T fp32 | Delta^T, Delta'^T bf16
 constexpr uint32_t kOffDt = kOffScratch;               // 16 KB [128 vi][64 t] K-major
 constexpr uint32_t kOffDt2 = kOffScratch + 16384;      // 16 KB
 constexpr uint32_t kOffVec = kOffScratch + 2 * 64 * kAStride * 4;  // per-token vectors
@@ -63,8 +63,10 @@ constexpr uint32_t kOffBar = kOffVec + kVecFloats * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + alignment slack
 static_assert(2 * 64 * kAStride * 4 >= 32768, "A/T scratch must cover the Delta buffers");
 
-// TMEM columns
-constexpr uint32_t kColD1 = 0, kColD2 = 64, kColD3 = 128, kColD4 = 192, kColD5 = 256, kColS = 320;
+// TMEM columns (512 allocated): D1 is [Kr;Qr][Kr;Qr]^T (128 columns: K K^T,
+// Q K^T and, on its diagonal, |q|^2), then one 64-column accumulator each.
+constexpr uint32_t kColD1 = 0, kColD2 = 128, kColD3 = 192, kColD4 = 256, kColD5 = 320,
+                   kColS = 384;
 
 struct ChunkParams {
     const float *a, *bl, *A_log, *dt_bias;
@@ -94,8 +96,35 @@ __device__ __forceinline__ void st_sw128_8(unsigned char *tile, int row, int c8,
     *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = q;
 }
 
-__device__ __forceinline__ float ld_sw128(const unsigned char *tile, int row, int col) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(row, col)));
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// One warp: C[16 x 8] tile at (m0, n0) of sgn * (a[:, 0:kd] * b[0:kd, :]) with
+// warp-level m16n8k8 TF32 tensor-core MMAs; a, b, dst are fp32 row-major
+// with row stride kAStride.  Used for the merges of the triangular inverse.
+__device__ __forceinline__ void warp_tile_product(const float *a, const float *b, float *dst,
+                                                  int m0, int n0, int kd, float sgn, int lane) {
+    const int g = lane >> 2, tg = lane & 3;
+    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+    for (int k0 = 0; k0 < kd; k0 += 8) {
+        const uint32_t a0 = to_tf32(a[(m0 + g) * kAStride + k0 + tg]);
+        const uint32_t a1 = to_tf32(a[(m0 + g + 8) * kAStride + k0 + tg]);
+        const uint32_t a2 = to_tf32(a[(m0 + g) * kAStride + k0 + tg + 4]);
+        const uint32_t a3 = to_tf32(a[(m0 + g + 8) * kAStride + k0 + tg + 4]);
+        const uint32_t b0 = to_tf32(b[(k0 + tg) * kAStride + n0 + g]);
+        const uint32_t b1 = to_tf32(b[(k0 + tg + 4) * kAStride + n0 + g]);
+        asm volatile(
+            "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    *reinterpret_cast<float2 *>(dst + (m0 + g) * kAStride + n0 + 2 * tg) = make_float2(sgn * c0, sgn * c1);
+    *reinterpret_cast<float2 *>(dst + (m0 + g + 8) * kAStride + n0 + 2 * tg) =
+        make_float2(sgn * c2, sgn * c3);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -115,6 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sT = sA + 64 * kAStride;                                    // [64][kAStride]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // TMEM access: warp w reads lane quadrant (w & 3); warps w and w + 4 split
+    // the columns of an accumulator into halves hc = w >> 2.
+    const int quad = warp & 3, hc = warp >> 2;
+    const int row = quad * 32 + lane;  // this thread's TMEM lane (accumulator row)
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -132,17 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
 
     // everything below reads what the conv kernel wrote
     pdl_wait_primary();
 
-    const int H = p.H, HQ = p.HQ, V = p.V, N = p.N;
+    const int H = p.H, HQ = p.HQ, V = p.V;
     const int G = H / HQ;
     const int n_units = p.header->n_units;
     uint32_t gchunk = 0;      // chunks issued by this CTA (stage = gchunk & 1)
     uint32_t mma_phase = 0;   // completed MMA commits
-    bool aborted = false;
 
     auto wait_mma = [&]() {
         const bool ok = mbar_wait(bar_mma, mma_phase & 1, kWaitLimitNs);
@@ -154,6 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+    };
+    auto ld32f = [&](uint32_t col, float (&f)[32]) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + col, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
     };
 
     while (true) {
@@ -170,22 +209,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qcol = kh * 128, kcol = HQ * 128 + kh * 128;
         const int vcol = 2 * HQ * 128 + h * V + vt * 128;
         const float A_log = __ldg(p.A_log + h), dtb = __ldg(p.dt_bias + h);
+        const size_t state_row = ((size_t)seq * H + h) * V + vt * 128 + row;
 
-        // state rows -> TMEM (thread tid owns state row vt*128 + tid)
+        // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
         {
-            const float *row = p.state_init + (((size_t)seq * H + h) * V + vt * 128 + tid) * 128;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            const float *src = p.state_init + state_row * 128 + hc * 64;
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(row + c0 + j);
+                    const float4 f = *reinterpret_cast<const float4 *>(src + c0 + j);
                     r[j] = __float_as_uint(f.x);
                     r[j + 1] = __float_as_uint(f.y);
                     r[j + 2] = __float_as_uint(f.z);
                     r[j + 3] = __float_as_uint(f.w);
                 }
-                tmem_st32(tmem + lane_base + kColS + c0, r);
+                tmem_st32(lane_base + kColS + hc * 64 + c0, r);
             }
             tmem_wait_st();
         }
@@ -203,6 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(base + 40960, &ymap, &bar_full[st], vcol + 64, t0);
         };
         if (tid == 0) issue_tma(0);
+        // gate logits of the current chunk, loaded one chunk ahead
+        float ga = 0.f, gbl = 0.f;
+        if (tid < 64 && tid < e - s) {
+            ga = __ldg(p.a + (size_t)(s + tid) * H + h);
+            gbl = __ldg(p.bl + (size_t)(s + tid) * H + h);
+        }
 
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
@@ -218,21 +264,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid < 64) {
                 float lg = 0.f, beta = 0.f;
                 if (tid < Cn) {
-                    const size_t i = (size_t)(t0 + tid) * H + h;
-                    lg = log_decay(__ldg(p.a + i), dtb, A_log);
-                    beta = 1.f / (1.f + expf(-__ldg(p.bl + i)));
+                    lg = log_decay(ga, dtb, A_log);
+                    beta = 1.f / (1.f + expf(-gbl));
                 }
                 v_lg[tid] = lg;
                 v_beta[tid] = beta;
+                ga = gbl = 0.f;
+                if (t0 + kC + tid < e) {
+                    ga = __ldg(p.a + (size_t)(t0 + kC + tid) * H + h);
+                    gbl = __ldg(p.bl + (size_t)(t0 + kC + tid) * H + h);
+                }
             }
             if (!mbar_wait(&bar_full[st], full_parity, kWaitLimitNs)) atomicExch(s_abort, 1);
             __syncthreads();
             if (*s_abort) break;
 
-            // ---- D1 = [Kr; Qr] Kr^T
+            // ---- D1 = [Kr; Qr] [Kr; Qr]^T  (K K^T | Q K^T, Q Q^T)
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16(128, 64, false, false);
+                const uint32_t idesc = idesc_bf16(128, 128, false, false);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -241,9 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar_mma);
             }
-            // cumulative log decay b_t (warp 0) and |q_t|^2 (threads 64..127)
-            if (warp == 0) {
-                float x0 = v_lg[2 * lane], x1 = v_lg[2 * lane + 1];
+            // cumulative log decay b_t (warp 1)
+            if (warp == 1) {
+                const float x0 = v_lg[2 * lane], x1 = v_lg[2 * lane + 1];
                 float sum = x0 + x1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -253,126 +303,142 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float b1 = sum, b0 = sum - x1;
                 v_b[2 * lane] = b0;
                 v_b[2 * lane + 1] = b1;
-                v_gam[2 * lane] = expf(b0);
-                v_gam[2 * lane + 1] = expf(b1);
-            } else if (tid >= 64) {
-                const int t = tid - 64;
-                const unsigned char *qt = stage + 8192;
-                float ss = 0.f;
-#pragma unroll 4
-                for (int c = 0; c < 64; ++c) {
-                    const float q0 = ld_sw128(qt, t, c), q1 = ld_sw128(qt + 16384, t, c);
-                    ss = fmaf(q0, q0, ss);
-                    ss = fmaf(q1, q1, ss);
-                }
-                v_rq[t] = rsqrtf(ss + 1e-12f);
+                v_gam[2 * lane] = __expf(b0);
+                v_gam[2 * lane + 1] = __expf(b1);
             }
             wait_mma();
 
-            // ---- E1: norms of k (diagonal of K K^T), A, P, decay vector c
-            float row[64];
-            {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColD1, r);
-                tmem_wait_ld();
+            // ---- E1: norms (diagonals), A (rows 0..63), P (rows 64..127)
+            float d1[32];
+            ld32f(kColD1 + hc * 32, d1);  // columns [32 hc, 32 hc + 32) of K K^T / Q K^T
+            auto pick = [&](const float (&f)[32]) {  // f[lane] without dynamic indexing
+                float d = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) row[j] = __uint_as_float(r[j]);
-                tmem_ld32(tmem + lane_base + kColD1 + 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) row[32 + j] = __uint_as_float(r[j]);
-            }
-            if (tid < 64) {
-                float diag = 0.f;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) diag = (j == tid) ? row[j] : diag;
-                v_rk[tid] = rsqrtf(diag + 1e-12f);
+                for (int j = 0; j < 32; ++j) d = (j == lane) ? f[j] : d;
+                return d;
+            };
+            if (row < 64) {
+                if ((row >> 5) == hc) v_rk[row] = rsqrtf(pick(d1) + 1e-12f);
+            } else {
+                float dq[32];  // Q Q^T columns; the warp's load stays convergent
+                ld32f(kColD1 + 64 + hc * 32, dq);
+                if (((row - 64) >> 5) == hc) v_rq[row - 64] = rsqrtf(pick(dq) + 1e-12f);
             }
             __syncthreads();
             const float bC = v_b[63];
-            if (tid < 64) {
-                const int t = tid;
+            if (row < 64) {
+                const int t = row;
                 const float bt = v_b[t], f = v_beta[t] * v_rk[t];
-                float *arow = sA + t * kAStride;
+                float *arow = sA + t * kAStride + hc * 32;
 #pragma unroll
-                for (int i = 0; i < 64; i += 4) {
-                    float4 o;
-                    o.x = (i + 0 < t) ? f * v_rk[i + 0] * expf(bt - v_b[i + 0]) * row[i + 0] : 0.f;
-                    o.y = (i + 1 < t) ? f * v_rk[i + 1] * expf(bt - v_b[i + 1]) * row[i + 1] : 0.f;
-                    o.z = (i + 2 < t) ? f * v_rk[i + 2] * expf(bt - v_b[i + 2]) * row[i + 2] : 0.f;
-                    o.w = (i + 3 < t) ? f * v_rk[i + 3] * expf(bt - v_b[i + 3]) * row[i + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(arow + i) = o;
+                for (int j = 0; j < 32; j += 4) {
+                    float o[4];
+#pragma unroll
+                    for (int u2 = 0; u2 < 4; ++u2) {
+                        const int i = hc * 32 + j + u2;
+                        o[u2] = (i < t) ? f * v_rk[i] * __expf(bt - v_b[i]) * d1[j + u2] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(arow + j) = make_float4(o[0], o[1], o[2], o[3]);
                 }
-                v_c[t] = expf(bC - bt) * v_rk[t];
+                if (hc == 0) v_c[t] = __expf(bC - bt) * v_rk[t];
             } else {
-                const int t = tid - 64;
+                const int t = row - 64;
                 const float bt = v_b[t], f = v_rq[t];
-                unsigned char *ptile = sm + kOffP;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 0; c8 < 4; ++c8) {
                     float v8[8];
 #pragma unroll
                     for (int u2 = 0; u2 < 8; ++u2) {
-                        const int i = c8 * 8 + u2;
-                        v8[u2] = (i <= t) ? f * v_rk[i] * expf(bt - v_b[i]) * row[i] : 0.f;
+                        const int i = hc * 32 + c8 * 8 + u2;
+                        v8[u2] = (i <= t) ? f * v_rk[i] * __expf(bt - v_b[i]) * d1[c8 * 8 + u2] : 0.f;
                     }
-                    st_sw128_8(ptile, t, c8, v8);
+                    st_sw128_8(sm + kOffP, t, hc * 4 + c8, v8);
                 }
             }
             __syncthreads();
 
-            // ---- T = (I + A)^-1: diagonal 32x32 blocks, one column per lane
+            // ---- T = (I + A)^-1, lower unit-triangular, built from the bottom up:
+            // 8x8 diagonal blocks by forward substitution (one column per lane),
+            // then merges of neighbouring diagonal blocks lo, hi of growing size,
+            //   T[hi, lo] = -T[hi, hi] (A[hi, lo] T[lo, lo]),
+            // at size 8 on CUDA cores and at sizes 16 and 32 with warp-level
+            // TF32 tensor-core tiles.  The product A[hi, lo] T[lo, lo] is kept in
+            // A's (unused) upper triangle.
             if (warp < 2) {
-                const int base = warp * 32;
-                float tc[32];
+                const int blk = warp * 4 + (lane >> 3), j = lane & 7, base = blk * 8;
+                float tc[8];
 #pragma unroll
-                for (int r2 = 0; r2 < 32; ++r2) {
+                for (int r2 = 0; r2 < 8; ++r2) {
                     const float *arow = sA + (base + r2) * kAStride + base;
-                    float acc = 0.f;
+                    const float4 lo4 = *reinterpret_cast<const float4 *>(arow);
+                    const float4 hi4 = *reinterpret_cast<const float4 *>(arow + 4);
+                    const float av[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+                    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-                    for (int i = 0; i < r2; ++i) acc = fmaf(arow[i], tc[i], acc);
-                    tc[r2] = (r2 == lane) ? 1.f : (r2 > lane ? -acc : 0.f);
+                    for (int i = 0; i < r2; ++i) {
+                        if (i & 1) acc1 = fmaf(av[i], tc[i], acc1);
+                        else acc0 = fmaf(av[i], tc[i], acc0);
+                    }
+                    tc[r2] = (r2 == j) ? 1.f : (r2 > j ? -(acc0 + acc1) : 0.f);
                 }
 #pragma unroll
-                for (int r2 = 0; r2 < 32; ++r2) sT[(base + r2) * kAStride + base + lane] = tc[r2];
+                for (int r2 = 0; r2 < 8; ++r2) sT[(base + r2) * kAStride + base + j] = tc[r2];
+            } else {
+                // zero every T entry outside the 8x8 diagonal blocks (the merges
+                // fill the lower ones; the upper ones must read as zero)
+                for (int q = tid - 64; q < 4096; q += kThreads - 64) {
+                    const int r2 = q >> 6, c = q & 63;
+                    if ((r2 >> 3) != (c >> 3)) sT[r2 * kAStride + c] = 0.f;
+                }
             }
             __syncthreads();
-            // X = A[32:64, 0:32] T[0:32, 0:32]  (kept in the unused upper-right block of A)
-            {
-                const int r2 = tid >> 2, c0 = (tid & 3) * 8;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                const float *arow = sA + (32 + r2) * kAStride;
-#pragma unroll 8
-                for (int k2 = 0; k2 < 32; ++k2) {
-                    const float av = arow[k2];
-                    const float *trow = sT + k2 * kAStride + c0;
+            {   // size 8: 4 pairs, X = A[hi, lo] T[lo, lo] (8x8x8), one output per thread
+                const int pr = tid >> 6, r2 = (tid >> 3) & 7, c = tid & 7;
+                const int lo = pr * 16, hi = lo + 8;
+                float acc = 0.f;
 #pragma unroll
-                    for (int u2 = 0; u2 < 8; ++u2) acc[u2] = fmaf(av, trow[u2], acc[u2]);
-                }
-                float *xrow = sA + r2 * kAStride + 32 + c0;
-#pragma unroll
-                for (int u2 = 0; u2 < 8; ++u2) xrow[u2] = acc[u2];
+                for (int k = 0; k < 8; ++k)
+                    acc = fmaf(sA[(hi + r2) * kAStride + lo + k], sT[(lo + k) * kAStride + lo + c], acc);
+                sA[(lo + r2) * kAStride + hi + c] = acc;
             }
             __syncthreads();
-            // T[32:64, 0:32] = -T[32:64, 32:64] X
+            {   // T[hi, lo] = -T[hi, hi] X
+                const int pr = tid >> 6, r2 = (tid >> 3) & 7, c = tid & 7;
+                const int lo = pr * 16, hi = lo + 8;
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    acc = fmaf(sT[(hi + r2) * kAStride + hi + k], sA[(lo + k) * kAStride + hi + c], acc);
+                sT[(hi + r2) * kAStride + lo + c] = -acc;
+            }
+            __syncthreads();
+            // size 16: 2 pairs x (16 x 16) outputs = 4 warps x two 16x8 tiles... one tile per warp
+            if (warp < 4) {
+                const int lo = (warp >> 1) * 32, hi = lo + 16, n0 = (warp & 1) * 8;
+                warp_tile_product(sA + hi * kAStride + lo, sT + lo * kAStride + lo,
+                                  sA + lo * kAStride + hi, 0, n0, 16, 1.f, lane);
+            }
+            __syncthreads();
+            if (warp < 4) {
+                const int lo = (warp >> 1) * 32, hi = lo + 16, n0 = (warp & 1) * 8;
+                warp_tile_product(sT + hi * kAStride + hi, sA + lo * kAStride + hi,
+                                  sT + hi * kAStride + lo, 0, n0, 16, -1.f, lane);
+            }
+            __syncthreads();
+            // size 32: X2 = A[32:64, 0:32] T[0:32, 0:32] (32 x 32: 8 warps x one 16x8 tile)
             {
-                const int r2 = tid >> 2, c0 = (tid & 3) * 8;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                const float *trow = sT + (32 + r2) * kAStride + 32;
-#pragma unroll 8
-                for (int k2 = 0; k2 < 32; ++k2) {
-                    const float tv = trow[k2];
-                    const float *xrow = sA + k2 * kAStride + 32 + c0;
-#pragma unroll
-                    for (int u2 = 0; u2 < 8; ++u2) acc[u2] = fmaf(tv, xrow[u2], acc[u2]);
-                }
-                float *dst = sT + (32 + r2) * kAStride + c0;
-#pragma unroll
-                for (int u2 = 0; u2 < 8; ++u2) dst[u2] = -acc[u2];
+                const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+                warp_tile_product(sA + 32 * kAStride, sT, sA + 32, m0, n0, 32, 1.f, lane);
+            }
+            __syncthreads();
+            {   // T[32:64, 0:32] = -T[32:64, 32:64] X2
+                const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+                warp_tile_product(sT + 32 * kAStride + 32, sA + 32, sT + 32 * kAStride, m0, n0, 32,
+                                  -1.f, lane);
             }
             __syncthreads();
             // Tw = T diag(r_k beta gamma), Tb = T diag(beta), bf16 (T is lower triangular)
-#pragma unroll 1
+#pragma unroll
             for (int q = tid; q < 64 * 8; q += kThreads) {
                 const int t = q >> 3, c8 = q & 7;
                 float w8[8], b8[8];
@@ -394,52 +460,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t id = idesc_bf16(128, 64, true, false);
                 const uint32_t tw = smem_u32(sm + kOffTw), tb = smem_u32(sm + kOffTb);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColD2, sdesc_sw128(kq + ks * 2048, 16384, 1024),
                              sdesc_sw128(tw + ks * 32, 16, 1024), id, ks > 0);
-                }
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+                for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColD3, sdesc_sw128(vb + ks * 2048, 8192, 1024),
                              sdesc_sw128(tb + ks * 32, 16, 1024), id, ks > 0);
-                }
                 mma_commit(bar_mma);
             }
             wait_mma();
 
             // ---- E2: W^T -> bf16 (MN-major B operand); S -> bf16 S0; S *= gamma_C
             {
-                uint32_t r[32];
-                unsigned char *wt = sm + kOffWt;
+                float f[32];
+                ld32f(kColD2 + hc * 32, f);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + kColD2 + half * 32, r);
+                for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffWt, row, hc * 4 + c8, f + c8 * 8);
+                const float gC = __expf(bC);
+                unsigned char *s0 = sm + kOffS0 + hc * 16384;  // this half is one K-block
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + kColS + hc * 64 + c0, r);
                     tmem_wait_ld();
+                    float v[32];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float v8[8];
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 #pragma unroll
-                        for (int u2 = 0; u2 < 8; ++u2) v8[u2] = __uint_as_float(r[c8 * 8 + u2]);
-                        st_sw128_8(wt, tid, half * 4 + c8, v8);
-                    }
-                }
-                const float gC = expf(bC);
-                unsigned char *s0 = sm + kOffS0;
-#pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    tmem_ld32(tmem + lane_base + kColS + c0, r);
-                    tmem_wait_ld();
+                    for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(s0, row, (c0 >> 3) + c8, v + c8 * 8);
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float v8[8];
-#pragma unroll
-                        for (int u2 = 0; u2 < 8; ++u2) v8[u2] = __uint_as_float(r[c8 * 8 + u2]);
-                        const int col = c0 + c8 * 8;
-                        st_sw128_8(s0 + (col >> 6) * 16384, tid, (col & 63) >> 3, v8);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gC);
-                    tmem_st32(tmem + lane_base + kColS + c0, r);
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j] * gC);
+                    tmem_st32(lane_base + kColS + hc * 64 + c0, r);
                 }
                 tmem_wait_st();
             }
@@ -469,23 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- E3: Delta^T and Delta'^T = Delta^T diag(c) -> bf16 (K-major A operands)
             {
-                uint32_t r[32];
+                float f[32];
+                ld32f(kColD3 + hc * 32, f);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + kColD3 + half * 32, r);
-                    tmem_wait_ld();
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float w8[8];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float v8[8], w8[8];
-#pragma unroll
-                        for (int u2 = 0; u2 < 8; ++u2) {
-                            const int i = half * 32 + c8 * 8 + u2;
-                            v8[u2] = __uint_as_float(r[c8 * 8 + u2]);
-                            w8[u2] = v8[u2] * v_c[i];
-                        }
-                        st_sw128_8(sm + kOffDt, tid, half * 4 + c8, v8);
-                        st_sw128_8(sm + kOffDt2, tid, half * 4 + c8, w8);
-                    }
+                    for (int u2 = 0; u2 < 8; ++u2) w8[u2] = f[c8 * 8 + u2] * v_c[hc * 32 + c8 * 8 + u2];
+                    st_sw128_8(sm + kOffDt, row, hc * 4 + c8, f + c8 * 8);
+                    st_sw128_8(sm + kOffDt2, row, hc * 4 + c8, w8);
                 }
             }
             fence_async_smem();
@@ -509,42 +553,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wait_mma();
 
-            // ---- E4: o = scale (r_q gamma D4 + D5) for the valid tokens
+            // ---- E4: o = scale (r_q gamma D4 + D5), staged as a [64 t][128 vi] bf16
+            // tile in the (now free) Delta buffers, then written as 16-byte rows
             {
-                uint32_t r4[32], r5[32];
-                __nv_bfloat16 *orow = p.out + (size_t)t0 * H * V + (size_t)h * V + vt * 128 + tid;
+                float f4[32], f5[32];
+                ld32f(kColD4 + hc * 32, f4);
+                ld32f(kColD5 + hc * 32, f5);
+                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffDt);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + kColD4 + half * 32, r4);
-                    tmem_ld32(tmem + lane_base + kColD5 + half * 32, r5);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int t = half * 32 + j;
-                        if (t < Cn) {
-                            const float o = p.scale * (v_rq[t] * v_gam[t] * __uint_as_float(r4[j]) +
-                                                       __uint_as_float(r5[j]));
-                            orow[(size_t)t * H * V] = __float2bfloat16_rn(o);
-                        }
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const int t = hc * 32 + j;
+                    const float o = p.scale * (v_rq[t] * v_gam[t] * f4[j] + f5[j]);
+                    otile[t * 128 + row] = __float2bfloat16_rn(o);
+                }
+                __syncthreads();
+                __nv_bfloat16 *obase = p.out + (size_t)t0 * H * V + (size_t)h * V + vt * 128;
+                for (int q = tid; q < Cn * 16; q += kThreads) {
+                    const int t = q >> 4, c16 = q & 15;
+                    *reinterpret_cast<uint4 *>(obase + (size_t)t * H * V + c16 * 8) =
+                        *reinterpret_cast<const uint4 *>(otile + t * 128 + c16 * 8);
                 }
             }
             sync_all();
         }
         gchunk += nchunks;
-        if (*s_abort) { aborted = true; break; }
+        if (*s_abort) break;
 
-        // final state rows -> global
+        // final state row `row`, columns [64 hc, 64 hc + 64) -> global
         {
-            float *row = p.state_fin + (((size_t)seq * H + h) * V + vt * 128 + tid) * 128;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            float *dst = p.state_fin + state_row * 128 + hc * 64;
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kColS + c0, r);
+                tmem_ld32(lane_base + kColS + hc * 64 + c0, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(row + c0 + j) =
+                    *reinterpret_cast<float4 *>(dst + c0 + j) =
                         make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
                                     __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
             }
@@ -552,9 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         sync_all();
     }
 
-    if (*s_abort || aborted) {
-        // a bounded wait gave up: record it and let in-flight copies land
-        // (bounded again) before the shared memory is released
+    if (*s_abort) {
+        // a bounded wait gave up: record it and give in-flight copies time to
+        // land before the shared memory is released
         if (tid == 0) {
             atomicExch(&p.header->status, 7 /* GDN_ERR_TIMEOUT */);
             const uint64_t t0 = global_timer_ns();
