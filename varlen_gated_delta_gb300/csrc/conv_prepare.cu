@@ -60,6 +60,17 @@ __device__ __forceinline__ void copy_raw(T *dst, const T *src) {
     }
 }
 
+// 16-byte global -> shared copy that bypasses registers; `valid` false fills zeros.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, bool valid) {
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    const int bytes = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(gmem_src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 template <typename T, int VEC>
 __device__ __forceinline__ void zero_raw(T *dst) {
     if constexpr (sizeof(T) * VEC == 16) {
@@ -146,10 +157,13 @@ __device__ void schedule_block(const ConvParams &p) {
     }
 }
 
-// Dynamic shared memory: [Kc][CT] f32 weights | [TT+L][CT] T window (only
-// when STAGE) | 3 x [TT] int token info.  Without STAGE (very long receptive
-// fields) the taps are read from global memory directly.
-template <typename T, int VEC, bool PREP, bool STAGE>
+// Dynamic shared memory: [Kc][CT] f32 weights (KC == 0 only) | [TT+L][CT] T
+// window (only when STAGE) | 3 x [TT] int token info | offsets cache.  With
+// KC > 0 (conv width known at compile time) every lane keeps its VEC x KC
+// weights in registers.  Without STAGE (very long receptive fields) the taps
+// are read from global memory directly.  The window is staged with
+// asynchronous 16-byte copies so all of a thread's loads are in flight at once.
+template <typename T, int VEC, bool PREP, bool STAGE, int KC>
 __global__ void __launch_bounds__(kConvThreads)
     conv_prepare_kernel(const ConvParams p, const int TT, const int n_ctiles) {
     constexpr int CT = 32 * VEC;
@@ -161,7 +175,7 @@ __global__ void __launch_bounds__(kConvThreads)
     const int L = p.L, Kc = p.Kc, D = p.D, C = p.C, N = p.N, B = p.B;
 
     float *sw = reinterpret_cast<float *>(smem);
-    T *sx = reinterpret_cast<T *>(smem + (((size_t)Kc * CT * 4 + 15) & ~size_t(15)));
+    T *sx = reinterpret_cast<T *>(smem + (KC > 0 ? 0 : (((size_t)Kc * CT * 4 + 15) & ~size_t(15))));
     int *s_seq = reinterpret_cast<int *>(sx + (STAGE ? (size_t)(TT + L) * CT : 0));
     int *s_start = s_seq + TT;
     int *s_len = s_start + TT;
@@ -204,13 +218,7 @@ __global__ void __launch_bounds__(kConvThreads)
         s_start[i] = st;
         s_len[i] = en - st;
     }
-    // 2. weights, transposed to [Kc][CT]
-    const T *w = static_cast<const T *>(p.w);
-    for (int i = threadIdx.x; i < Kc * CT; i += blockDim.x) {
-        const int j = i / CT, c = c0 + i % CT;
-        sw[i] = c < C ? to_f32(w[(size_t)c * Kc + j]) : 0.f;
-    }
-    // 3. input window rows [t0 - L, t0 + TT), 128-bit loads
+    // 2. input window rows [t0 - L, t0 + TT), 16-byte asynchronous copies
     const T *x = static_cast<const T *>(p.x);
     const int rows = STAGE ? TT + L : 0;
     for (int i = threadIdx.x; i < rows * 32; i += blockDim.x) {
@@ -218,15 +226,52 @@ __global__ void __launch_bounds__(kConvThreads)
         const long t = (long)t0 - L + r;
         const int c = c0 + v * VEC;
         T *dst = sx + (size_t)r * CT + v * VEC;
-        if (t >= 0 && t < N && c < C) copy_raw<T, VEC>(dst, x + (size_t)t * C + c);
-        else zero_raw<T, VEC>(dst);
+        const bool valid = t >= 0 && t < N && c < C;
+        if constexpr (sizeof(T) * VEC == 16) {
+            if (valid) cp_async16(dst, x + (size_t)t * C + c, true);
+            else zero_raw<T, VEC>(dst);
+        } else {
+            if (valid) copy_raw<T, VEC>(dst, x + (size_t)t * C + c);
+            else zero_raw<T, VEC>(dst);
+        }
     }
-    __syncthreads();
-
+    // 3. weights: in registers (KC > 0) or transposed to [Kc][CT] in shared memory
+    const T *w = static_cast<const T *>(p.w);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int c = c0 + lane * VEC;
     const bool cvalid = c < C;
+    float wr[KC > 0 ? KC : 1][VEC];
+    if constexpr (KC > 0) {
+        // the lane's VEC channels hold VEC * KC consecutive weights
+        T wraw[VEC * KC];
+#pragma unroll
+        for (int q = 0; q < VEC * KC; ++q) wraw[q] = from_f32<T>(0.f);
+        if (cvalid) {
+            if constexpr ((sizeof(T) * VEC * KC) % 16 == 0) {
+#pragma unroll
+                for (int q = 0; q < VEC * KC; q += 16 / sizeof(T))
+                    *reinterpret_cast<uint4 *>(wraw + q) =
+                        *reinterpret_cast<const uint4 *>(w + (size_t)c * KC + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < VEC * KC; ++q) wraw[q] = w[(size_t)c * KC + q];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+#pragma unroll
+            for (int j = 0; j < KC; ++j) wr[j][e] = to_f32(wraw[e * KC + j]);
+    } else {
+#pragma unroll 4
+        for (int i = threadIdx.x; i < Kc * CT; i += blockDim.x) {
+            const int j = i / CT, cc = c0 + i % CT;
+            sw[i] = cc < C ? to_f32(w[(size_t)cc * Kc + j]) : 0.f;
+        }
+    }
+    if constexpr (STAGE && sizeof(T) * VEC == 16) cp_async_wait_all();
+    __syncthreads();
+
     float bias[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) bias[e] = 0.f;
@@ -243,7 +288,10 @@ __global__ void __launch_bounds__(kConvThreads)
         float acc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] = bias[e];
-        for (int j = 0; j < Kc; ++j) {
+        constexpr int kTaps = KC > 0 ? KC : 64;
+#pragma unroll
+        for (int j = 0; j < kTaps; ++j) {
+            if (KC == 0 && j >= Kc) break;
             const int src = t - (Kc - 1 - j) * D;
             float xv[VEC];
             if (src >= s) {
@@ -261,15 +309,22 @@ __global__ void __launch_bounds__(kConvThreads)
                 for (int e = 0; e < VEC; ++e)
                     xv[e] = cvalid ? to_f32(init[((size_t)b * C + c + e) * L + L + local]) : 0.f;
             }
-            const float *wj = sw + j * CT + lane * VEC;
+            if constexpr (KC > 0) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] = fmaf(xv[e], wj[e], acc[e]);
+                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(xv[e], wr[j][e], acc[e]);
+            } else {
+                const float *wj = sw + j * CT + lane * VEC;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(xv[e], wj[e], acc[e]);
+            }
         }
         float yv[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             float z = acc[e];
-            if (p.silu) z = z / (1.f + expf(-z));
+            // SiLU with the fast exponential and division: their error
+            // (a few fp32 ulp) is far below the rounding of the output to T
+            if (p.silu) z = __fdividef(z, 1.f + __expf(-z));
             yv[e] = round_through<T>(z);  // the conv output is stored in T
         }
         if (cvalid) store_f<T, VEC>(y + (size_t)t * C + c, yv);
@@ -306,6 +361,206 @@ __global__ void __launch_bounds__(kConvThreads)
             }
         }
     }
+}
+
+// Streaming variant for a compile-time conv width KC and dilation D (the
+// common Kc <= 4 cases): each warp walks a run of R consecutive tokens for
+// one tile of CT = 32 * VEC channels.  Input rows are loaded straight from
+// global memory (coalesced 16-byte vectors, prefetched kPf rows ahead) and
+// the L = (KC-1)*D previous inputs of the lane's channels live in registers,
+// so every input element is loaded and converted once.  At each sequence
+// start the window is refilled from that sequence's initial conv state.
+template <typename T, int VEC, bool PREP, int KC, int D>
+__global__ void __launch_bounds__(kConvThreads)
+    conv_stream_kernel(const ConvParams p, const int R, const int n_ctiles) {
+    constexpr int L = (KC - 1) * D;
+    constexpr int CT = 32 * VEC;
+    constexpr int kPf = 4;
+    __shared__ int s_offs[kOffsetsCache];
+
+    pdl_launch_dependents();
+    if (p.header != nullptr && blockIdx.x == 0) schedule_block(p);
+
+    const int B = p.B, N = p.N, C = p.C;
+    const bool cache_offs = B + 1 <= kOffsetsCache;
+    if (cache_offs) {
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) s_offs[i] = __ldg(p.offsets + i);
+    }
+    __syncthreads();
+    auto off = [&](int i) { return cache_offs ? s_offs[i] : __ldg(p.offsets + i); };
+    if (off(0) != 0 || off(B) != N) return;  // malformed offsets: nothing is written
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile_c = blockIdx.x % n_ctiles, tile_t = blockIdx.x / n_ctiles;
+    const int c0 = tile_c * CT, c = c0 + lane * VEC;
+    const bool cvalid = c < C;
+    const int run0 = (tile_t * (kConvThreads / 32) + warp) * R;
+    const int tend = min(run0 + R, N);
+    if (run0 >= tend) return;
+
+    const T *x = static_cast<const T *>(p.x);
+    const T *w = static_cast<const T *>(p.w);
+    const T *init = static_cast<const T *>(p.init);
+    T *y = static_cast<T *>(p.y);
+
+    // weights and bias of the lane's channels
+    float wr[KC][VEC], bias[VEC];
+    {
+        T wraw[VEC * KC];
+#pragma unroll
+        for (int q = 0; q < VEC * KC; ++q) wraw[q] = from_f32<T>(0.f);
+        if (cvalid) {
+            if constexpr ((sizeof(T) * VEC * KC) % 16 == 0) {
+#pragma unroll
+                for (int q = 0; q < VEC * KC; q += 16 / sizeof(T))
+                    *reinterpret_cast<uint4 *>(wraw + q) =
+                        *reinterpret_cast<const uint4 *>(w + (size_t)c * KC + q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < VEC * KC; ++q) wraw[q] = w[(size_t)c * KC + q];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+#pragma unroll
+            for (int j = 0; j < KC; ++j) wr[j][e] = to_f32(wraw[e * KC + j]);
+            bias[e] = 0.f;
+        }
+        if (p.bias != nullptr && cvalid) load_f<T, VEC>(static_cast<const T *>(p.bias) + c, bias);
+    }
+
+    // sequence of the first token
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off(mid) <= run0) lo = mid;
+        else hi = mid - 1;
+    }
+    int b = lo, s = off(b), e = off(b + 1);
+
+    // xw[L - m] holds the input m steps back (m = 1..L)
+    float xw[L > 0 ? L : 1][VEC];
+    auto fill_window = [&](int t) {
+#pragma unroll
+        for (int m = 1; m <= L; ++m) {
+            const int src = t - m;
+            if (src >= s) {
+                if (cvalid) load_f<T, VEC>(x + (size_t)src * C + c, xw[L - m]);
+                else
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) xw[L - m][q] = 0.f;
+            } else {
+                const int local = src - s;  // in [-L, -1]
+#pragma unroll
+                for (int q = 0; q < VEC; ++q)
+                    xw[L - m][q] = cvalid ? to_f32(init[((size_t)b * C + c + q) * L + L + local]) : 0.f;
+            }
+        }
+    };
+    const bool seq_ok0 = e >= s && s >= 0 && e <= N && run0 >= s && run0 < e;
+    if (seq_ok0) fill_window(run0);
+
+    // prefetch ring of raw input rows
+    uint4 pf[kPf];
+    static_assert(sizeof(T) * VEC == 16, "streaming conv works on 16-byte vectors");
+#pragma unroll
+    for (int q = 0; q < kPf; ++q)
+        if (run0 + q < tend && cvalid)
+            pf[q] = *reinterpret_cast<const uint4 *>(x + (size_t)(run0 + q) * C + c);
+
+    const int qk_width = PREP ? 2 * p.HQ * p.K : 0;
+    const int lanes_per_head = PREP ? p.K / VEC : 1;
+    bool seq_ok = seq_ok0;
+
+    for (int t = run0; t < tend; ++t) {
+        Vec16<T> cur;
+        cur.u = pf[0];
+#pragma unroll
+        for (int q = 0; q < kPf - 1; ++q) pf[q] = pf[q + 1];
+        if (t + kPf < tend && cvalid)
+            pf[kPf - 1] = *reinterpret_cast<const uint4 *>(x + (size_t)(t + kPf) * C + c);
+
+        if (t >= e) {  // next non-empty sequence (warp-uniform)
+            while (b + 1 < B && off(b + 1) <= t) ++b;
+            s = off(b);
+            e = off(b + 1);
+            seq_ok = e >= s && s >= 0 && e <= N && t >= s && t < e;
+            if (seq_ok) fill_window(t);
+        }
+        float xc[VEC];
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) xc[q] = cvalid ? to_f32(cur.v[q]) : 0.f;
+        if (seq_ok) {
+            float acc[VEC];
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) acc[q] = bias[q];
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                const int m = (KC - 1 - j) * D;  // steps back
+#pragma unroll
+                for (int q = 0; q < VEC; ++q)
+                    acc[q] = fmaf(m == 0 ? xc[q] : xw[L - (m > 0 ? m : 1)][q], wr[j][q], acc[q]);
+            }
+            float yv[VEC];
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) {
+                float z = acc[q];
+                if (p.silu) z = __fdividef(z, 1.f + __expf(-z));
+                yv[q] = round_through<T>(z);  // the conv output is stored in T
+            }
+            if (cvalid) store_f<T, VEC>(y + (size_t)t * C + c, yv);
+            if constexpr (PREP) {
+                if (c0 < qk_width && e - s < p.prep_max_len) {  // warp-uniform
+                    float ss = 0.f;
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) ss = fmaf(yv[q], yv[q], ss);
+                    for (int o = lanes_per_head >> 1; o > 0; o >>= 1)
+                        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                    if (cvalid && c < qk_width) {
+                        const float r = rsqrtf(ss + 1e-12f);
+                        const int plane = c >= p.HQ * p.K;
+                        const int cc = c - plane * p.HQ * p.K;
+                        float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
+#pragma unroll
+                        for (int q = 0; q < VEC; ++q) dst[q] = yv[q] * r;
+                    }
+                }
+                if (tile_c == 0 && e - s < p.prep_max_len) {
+                    for (int h = lane; h < p.H; h += 32) {
+                        float g, beta;
+                        decay_rate(p, t, h, g, beta);
+                        p.gb[(size_t)t * p.H + h] = g;
+                        p.gb[((size_t)N + t) * p.H + h] = beta;
+                    }
+                }
+            }
+        }
+        if constexpr (L > 0) {
+#pragma unroll
+            for (int m = 0; m < L - 1; ++m)
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) xw[m][q] = xw[m + 1][q];
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) xw[L - 1][q] = xc[q];
+        }
+    }
+}
+
+template <typename T, int VEC, bool PREP, int KC, int D>
+cudaError_t launch_conv_stream(const ConvParams &p, cudaStream_t s) {
+    constexpr int CT = 32 * VEC;
+    const int n_ctiles = (p.C + CT - 1) / CT;
+    // run length: enough warps for several waves, at most 32 tokens per warp
+    const long target_warps = 148L * 48;
+    long R = ((long)p.N * n_ctiles) / target_warps;
+    R = R < 1 ? 1 : (R > 32 ? 32 : R);
+    const long runs = p.N > 0 ? (p.N + R - 1) / R : 1;
+    const long ttiles = (runs + (kConvThreads / 32) - 1) / (kConvThreads / 32);
+    const long blocks = ttiles * n_ctiles;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    conv_stream_kernel<T, VEC, PREP, KC, D><<<(unsigned)blocks, kConvThreads, 0, s>>>(p, (int)R, n_ctiles);
+    note_launch();
+    return cudaGetLastError();
 }
 
 // Final conv state: fin[b,c,j] = x~(len - L + j).  One thread per (b, c) walks
@@ -412,8 +667,8 @@ __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const 
     }
 }
 
-template <typename T, int VEC, bool PREP>
-cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
+template <typename T, int VEC, bool PREP, int KC>
+cudaError_t launch_conv_kc(const ConvParams &p, cudaStream_t s) {
     constexpr int CT = 32 * VEC;
     const int n_ctiles = (p.C + CT - 1) / CT;
     // tokens per CTA: small batches (decode) use short tiles for parallelism
@@ -421,13 +676,14 @@ cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
     const long n_ttiles = p.N > 0 ? (p.N + TT - 1) / TT : 1;  // >= 1 block for block 0 duties
     const long blocks = n_ttiles * n_ctiles;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    const size_t wbytes = ((size_t)p.Kc * CT * 4 + 15) & ~size_t(15);
+    const size_t wbytes = KC > 0 ? 0 : ((size_t)p.Kc * CT * 4 + 15) & ~size_t(15);
     const size_t window = (size_t)(TT + p.L) * CT * sizeof(T);
     const bool stage = window <= 64 * 1024;
     const size_t offs_bytes = p.B + 1 <= kOffsetsCache ? sizeof(int) * (p.B + 1) : 0;
     const size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT + offs_bytes;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    auto kern = stage ? conv_prepare_kernel<T, VEC, PREP, true> : conv_prepare_kernel<T, VEC, PREP, false>;
+    auto kern = stage ? conv_prepare_kernel<T, VEC, PREP, true, KC>
+                      : conv_prepare_kernel<T, VEC, PREP, false, KC>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -436,6 +692,20 @@ cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
     kern<<<(unsigned)blocks, kConvThreads, smem, s>>>(p, TT, n_ctiles);
     note_launch();
     return cudaGetLastError();
+}
+
+template <typename T, int VEC, bool PREP>
+cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t s) {
+    if constexpr (VEC > 1) {
+        if (p.Kc == 4 && p.D == 1) return launch_conv_stream<T, VEC, PREP, 4, 1>(p, s);
+        if (p.Kc == 4 && p.D == 2) return launch_conv_stream<T, VEC, PREP, 4, 2>(p, s);
+        if (p.Kc == 3 && p.D == 1) return launch_conv_stream<T, VEC, PREP, 3, 1>(p, s);
+        if (p.Kc == 2 && p.D == 1) return launch_conv_stream<T, VEC, PREP, 2, 1>(p, s);
+    }
+    if (VEC > 1 && p.Kc == 4) return launch_conv_kc<T, VEC, PREP, 4>(p, s);
+    if (VEC > 1 && p.Kc == 3) return launch_conv_kc<T, VEC, PREP, 3>(p, s);
+    if (VEC > 1 && p.Kc == 2) return launch_conv_kc<T, VEC, PREP, 2>(p, s);
+    return launch_conv_kc<T, VEC, PREP, 0>(p, s);
 }
 
 bool aligned16(const void *ptr) { return ptr == nullptr || (((uintptr_t)ptr) & 15) == 0; }

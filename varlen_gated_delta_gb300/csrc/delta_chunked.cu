@@ -42,31 +42,42 @@ using namespace sm100;
 
 constexpr int kC = 64;            // chunk length
 constexpr int kThreads = 256;     // 8 warps; thread 0 issues TMA and MMA
+constexpr int kCtasPerSm = 2;
 constexpr int kAStride = 68;      // fp32 row stride of the A / T scratch (bank-conflict free)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 
-// Shared memory layout (offsets from a 1024-aligned base).
+// Shared memory layout (offsets from a 1024-aligned base), sized so that two
+// CTAs fit on one SM.  Buffers whose live ranges do not overlap share space:
+//   scratch: A, T (fp32, triangular inverse) -> S0 (bf16 state copy, E2..D4)
+//            -> Delta^T, Delta'^T (E3..D5/S) -> output tile (E4)
+//   Tw, Tb (until D2/D3 complete) -> W^T (E2..D3b)
 constexpr uint32_t kStageBytes = 49152;  // [Kr|Qr] x 2 K-blocks (32 KB) + V 2 blocks (16 KB)
-constexpr uint32_t kOffStage0 = 0;
-constexpr uint32_t kOffStage1 = kStageBytes;
-constexpr uint32_t kOffTw = 2 * kStageBytes;           // 8 KB  [64 t][64 t'] K-major
-constexpr uint32_t kOffTb = kOffTw + 8192;             // 8 KB
-constexpr uint32_t kOffP = kOffTb + 8192;              // 8 KB  [64 t][64 i]  K-major
-constexpr uint32_t kOffWt = kOffP + 8192;              // 16 KB [128 kk][64 t] MN-major
-constexpr uint32_t kOffS0 = kOffWt + 16384;            // 32 KB [128 vi][128 kk] K-major
-constexpr uint32_t kOffScratch = kOffS0 + 32768;       // 34 KB: A,T fp32 | Delta^T, Delta'^T bf16
-constexpr uint32_t kOffDt = kOffScratch;               // 16 KB [128 vi][64 t] K-major
-constexpr uint32_t kOffDt2 = kOffScratch + 16384;      // 16 KB
-constexpr uint32_t kOffVec = kOffScratch + 2 * 64 * kAStride * 4;  // per-token vectors
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffScratch = kStageBytes;                      // 34 KB
+constexpr uint32_t kScratchBytes = 2 * 64 * kAStride * 4;
+constexpr uint32_t kOffS0 = kOffScratch;                           // 32 KB [128 vi][128 kk] K-major
+constexpr uint32_t kOffDt = kOffScratch;                           // 16 KB [128 vi][64 t] K-major
+constexpr uint32_t kOffDt2 = kOffScratch + 16384;                  // 16 KB
+constexpr uint32_t kOffOut = kOffScratch;                          // 16 KB [64 t][128 vi] bf16
+constexpr uint32_t kOffTw = kOffScratch + ((kScratchBytes + 1023) & ~1023u);  // 8 KB [64 t][64 t']
+constexpr uint32_t kOffTb = kOffTw + 8192;                         // 8 KB
+constexpr uint32_t kOffWt = kOffTw;                                // 16 KB [128 kk][64 t] MN-major
+constexpr uint32_t kOffP = kOffTw + 16384;                         // 8 KB  [64 t][64 i] K-major
+constexpr uint32_t kOffVec = kOffP + 8192;                         // per-token vectors
 constexpr uint32_t kVecFloats = 7 * 64;
 constexpr uint32_t kOffBar = kOffVec + kVecFloats * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + alignment slack
-static_assert(2 * 64 * kAStride * 4 >= 32768, "A/T scratch must cover the Delta buffers");
+static_assert(kScratchBytes >= 32768, "the A/T scratch must hold S0 and the Delta buffers");
+static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 
-// TMEM columns (512 allocated): D1 is [Kr;Qr][Kr;Qr]^T (128 columns: K K^T,
-// Q K^T and, on its diagonal, |q|^2), then one 64-column accumulator each.
-constexpr uint32_t kColD1 = 0, kColD2 = 128, kColD3 = 192, kColD4 = 256, kColD5 = 320,
-                   kColS = 384;
+// TMEM: 256 columns per CTA (two CTAs per SM).  Accumulators share the two
+// 64-column slots X and Y by live range:  D1 (N = 128: K K^T | Q K^T and
+// Q Q^T) uses X and Y; then D2 = W^T -> Y, D3 = Delta^T -> X, D4 -> Y,
+// D5 -> X; the state S keeps columns [128, 256).
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColX = 0, kColY = 64;
+constexpr uint32_t kColD1 = kColX, kColD2 = kColY, kColD3 = kColX, kColD4 = kColY, kColD5 = kColX,
+                   kColS = 128;
 
 struct ChunkParams {
     const float *a, *bl, *A_log, *dt_bias;
@@ -127,7 +138,7 @@ __device__ __forceinline__ void warp_tile_product(const float *a, const float *b
         make_float2(sgn * c2, sgn * c3);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     chunked_delta_kernel(const __grid_constant__ CUtensorMap ymap, const ChunkParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -151,14 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
-        mbar_init(&bar_full[1], 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         tma_prefetch_desc(&ymap);
         *s_abort = 0;
     }
     if (warp == 0) {
-        tmem_alloc(s_tmem, 512);
+        tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int H = p.H, HQ = p.HQ, V = p.V;
     const int G = H / HQ;
     const int n_units = p.header->n_units;
-    uint32_t gchunk = 0;      // chunks issued by this CTA (stage = gchunk & 1)
+    uint32_t gchunk = 0;      // chunks loaded by this CTA (parity of the stage barrier)
     uint32_t mma_phase = 0;   // completed MMA commits
 
     auto wait_mma = [&]() {
@@ -231,16 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         auto issue_tma = [&](int n) {
-            const uint32_t st = (gchunk + n) & 1;
-            unsigned char *base = sm + (st ? kOffStage1 : kOffStage0);
+            unsigned char *base = sm + kOffStage;
             const int t0 = s + n * kC;
-            mbar_arrive_expect_tx(&bar_full[st], kStageBytes);
-            tma_load_2d(base + 0, &ymap, &bar_full[st], kcol, t0);
-            tma_load_2d(base + 8192, &ymap, &bar_full[st], qcol, t0);
-            tma_load_2d(base + 16384, &ymap, &bar_full[st], kcol + 64, t0);
-            tma_load_2d(base + 24576, &ymap, &bar_full[st], qcol + 64, t0);
-            tma_load_2d(base + 32768, &ymap, &bar_full[st], vcol, t0);
-            tma_load_2d(base + 40960, &ymap, &bar_full[st], vcol + 64, t0);
+            mbar_arrive_expect_tx(&bar_full[0], kStageBytes);
+            tma_load_2d(base + 0, &ymap, &bar_full[0], kcol, t0);
+            tma_load_2d(base + 8192, &ymap, &bar_full[0], qcol, t0);
+            tma_load_2d(base + 16384, &ymap, &bar_full[0], kcol + 64, t0);
+            tma_load_2d(base + 24576, &ymap, &bar_full[0], qcol + 64, t0);
+            tma_load_2d(base + 32768, &ymap, &bar_full[0], vcol, t0);
+            tma_load_2d(base + 40960, &ymap, &bar_full[0], vcol + 64, t0);
         };
         if (tid == 0) issue_tma(0);
         // gate logits of the current chunk, loaded one chunk ahead
@@ -252,13 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
-            const uint32_t st = (gchunk + n) & 1;
-            const uint32_t full_parity = ((gchunk + n) >> 1) & 1;
-            unsigned char *stage = sm + (st ? kOffStage1 : kOffStage0);
+            const uint32_t full_parity = (gchunk + n) & 1;
+            unsigned char *stage = sm + kOffStage;
             const uint32_t kq = smem_u32(stage), vb = kq + 32768;
             const int t0 = s + n * kC;
             const int Cn = min(kC, e - t0);
-            if (tid == 0 && n + 1 < nchunks) issue_tma(n + 1);
 
             // per-token gates (threads 0..63) while the tiles land
             if (tid < 64) {
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     gbl = __ldg(p.bl + (size_t)(t0 + kC + tid) * H + h);
                 }
             }
-            if (!mbar_wait(&bar_full[st], full_parity, kWaitLimitNs)) atomicExch(s_abort, 1);
+            if (!mbar_wait(&bar_full[0], full_parity, kWaitLimitNs)) atomicExch(s_abort, 1);
             __syncthreads();
             if (*s_abort) break;
 
@@ -328,31 +335,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float bC = v_b[63];
             if (row < 64) {
                 const int t = row;
-                const float bt = v_b[t], f = v_beta[t] * v_rk[t];
                 float *arow = sA + t * kAStride + hc * 32;
+                if (hc == 1 && t < 32) {  // A is strictly lower triangular: this half is zero
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float o[4];
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(arow + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    const float bt = v_b[t], f = v_beta[t] * v_rk[t];
 #pragma unroll
-                    for (int u2 = 0; u2 < 4; ++u2) {
-                        const int i = hc * 32 + j + u2;
-                        o[u2] = (i < t) ? f * v_rk[i] * __expf(bt - v_b[i]) * d1[j + u2] : 0.f;
+                    for (int j = 0; j < 32; j += 4) {
+                        const int i0 = hc * 32 + j;
+                        const float4 rk4 = *reinterpret_cast<const float4 *>(v_rk + i0);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(v_b + i0);
+                        float4 o;
+                        o.x = (i0 + 0 < t) ? f * rk4.x * __expf(bt - b4.x) * d1[j + 0] : 0.f;
+                        o.y = (i0 + 1 < t) ? f * rk4.y * __expf(bt - b4.y) * d1[j + 1] : 0.f;
+                        o.z = (i0 + 2 < t) ? f * rk4.z * __expf(bt - b4.z) * d1[j + 2] : 0.f;
+                        o.w = (i0 + 3 < t) ? f * rk4.w * __expf(bt - b4.w) * d1[j + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(arow + j) = o;
                     }
-                    *reinterpret_cast<float4 *>(arow + j) = make_float4(o[0], o[1], o[2], o[3]);
                 }
-                if (hc == 0) v_c[t] = __expf(bC - bt) * v_rk[t];
+                if (hc == 0) v_c[t] = __expf(bC - v_b[t]) * v_rk[t];
             } else {
+                // P = scale * tril(Q K^T) o Gamma with the norms folded in
                 const int t = row - 64;
-                const float bt = v_b[t], f = v_rq[t];
+                if (hc == 1 && t < 32) {
+                    const float z8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float v8[8];
+                    for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffP, t, 4 + c8, z8);
+                } else {
+                    const float bt = v_b[t], f = p.scale * v_rq[t];
 #pragma unroll
-                    for (int u2 = 0; u2 < 8; ++u2) {
-                        const int i = hc * 32 + c8 * 8 + u2;
-                        v8[u2] = (i <= t) ? f * v_rk[i] * __expf(bt - v_b[i]) * d1[c8 * 8 + u2] : 0.f;
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const int i0 = hc * 32 + c8 * 8;
+                        float rk8[8], b8[8], v8[8];
+                        *reinterpret_cast<float4 *>(rk8) = *reinterpret_cast<const float4 *>(v_rk + i0);
+                        *reinterpret_cast<float4 *>(rk8 + 4) = *reinterpret_cast<const float4 *>(v_rk + i0 + 4);
+                        *reinterpret_cast<float4 *>(b8) = *reinterpret_cast<const float4 *>(v_b + i0);
+                        *reinterpret_cast<float4 *>(b8 + 4) = *reinterpret_cast<const float4 *>(v_b + i0 + 4);
+#pragma unroll
+                        for (int u2 = 0; u2 < 8; ++u2)
+                            v8[u2] = (i0 + u2 <= t) ? f * rk8[u2] * __expf(bt - b8[u2]) * d1[c8 * 8 + u2] : 0.f;
+                        st_sw128_8(sm + kOffP, t, hc * 4 + c8, v8);
                     }
-                    st_sw128_8(sm + kOffP, t, hc * 4 + c8, v8);
                 }
             }
             __syncthreads();
@@ -384,11 +409,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r2 = 0; r2 < 8; ++r2) sT[(base + r2) * kAStride + base + j] = tc[r2];
             } else {
-                // zero every T entry outside the 8x8 diagonal blocks (the merges
-                // fill the lower ones; the upper ones must read as zero)
-                for (int q = tid - 64; q < 4096; q += kThreads - 64) {
-                    const int r2 = q >> 6, c = q & 63;
-                    if ((r2 >> 3) != (c >> 3)) sT[r2 * kAStride + c] = 0.f;
+                const int q0 = tid - 64, nq = kThreads - 64;
+                // the merges read the upper-right zero blocks of the diagonal
+                // blocks they combine: T[lo:lo+8, lo+8:lo+16] (size 8) and
+                // T[lo:lo+16, lo+16:lo+32] (size 16)
+                for (int q = q0; q < 4 * 64 + 2 * 256; q += nq) {
+                    if (q < 256) {
+                        const int lo = (q >> 6) * 16, r2 = (q >> 3) & 7, c = q & 7;
+                        sT[(lo + r2) * kAStride + lo + 8 + c] = 0.f;
+                    } else {
+                        const int q2 = q - 256, lo = (q2 >> 8) * 32, r2 = (q2 >> 4) & 15, c = q2 & 15;
+                        sT[(lo + r2) * kAStride + lo + 16 + c] = 0.f;
+                    }
+                }
+                // Q tile rows t scaled by scale * r_q(t) * gamma_t (MMA1 is done
+                // with it), so that S0 Q^T and Delta^T P^T share one accumulator
+                unsigned char *qt = stage + 8192;
+                for (int q = q0; q < 64 * 16; q += nq) {
+                    const int t = q >> 4, kb = (q >> 3) & 1, c8 = q & 7;
+                    uint4 *ptr = reinterpret_cast<uint4 *>(qt + kb * 16384 + sw128_offset(t, c8 * 8));
+                    const float f = p.scale * v_rq[t] * v_gam[t];
+                    uint4 w = *ptr;
+                    __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+                    for (int u2 = 0; u2 < 4; ++u2) {
+                        const float2 v2 = __bfloat1622float2(h2[u2]);
+                        h2[u2] = __floats2bfloat162_rn(v2.x * f, v2.y * f);
+                    }
+                    *ptr = w;
                 }
             }
             __syncthreads();
@@ -440,14 +488,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Tw = T diag(r_k beta gamma), Tb = T diag(beta), bf16 (T is lower triangular)
 #pragma unroll
             for (int q = tid; q < 64 * 8; q += kThreads) {
-                const int t = q >> 3, c8 = q & 7;
-                float w8[8], b8[8];
+                const int t = q >> 3, c8 = q & 7, i0 = c8 * 8;
+                float t8[8], be8[8], ga8[8], rk8[8], w8[8], b8[8];
+                *reinterpret_cast<float4 *>(t8) = *reinterpret_cast<const float4 *>(sT + t * kAStride + i0);
+                *reinterpret_cast<float4 *>(t8 + 4) = *reinterpret_cast<const float4 *>(sT + t * kAStride + i0 + 4);
+                *reinterpret_cast<float4 *>(be8) = *reinterpret_cast<const float4 *>(v_beta + i0);
+                *reinterpret_cast<float4 *>(be8 + 4) = *reinterpret_cast<const float4 *>(v_beta + i0 + 4);
+                *reinterpret_cast<float4 *>(ga8) = *reinterpret_cast<const float4 *>(v_gam + i0);
+                *reinterpret_cast<float4 *>(ga8 + 4) = *reinterpret_cast<const float4 *>(v_gam + i0 + 4);
+                *reinterpret_cast<float4 *>(rk8) = *reinterpret_cast<const float4 *>(v_rk + i0);
+                *reinterpret_cast<float4 *>(rk8 + 4) = *reinterpret_cast<const float4 *>(v_rk + i0 + 4);
 #pragma unroll
                 for (int u2 = 0; u2 < 8; ++u2) {
-                    const int i = c8 * 8 + u2;
-                    const float tv = (i <= t) ? sT[t * kAStride + i] : 0.f;
-                    b8[u2] = tv * v_beta[i];
-                    w8[u2] = b8[u2] * v_gam[i] * v_rk[i];
+                    const float tv = (i0 + u2 <= t) ? t8[u2] : 0.f;
+                    b8[u2] = tv * be8[u2];
+                    w8[u2] = b8[u2] * ga8[u2] * rk8[u2];
                 }
                 st_sw128_8(sm + kOffTw, t, c8, w8);
                 st_sw128_8(sm + kOffTb, t, c8, b8);
@@ -542,9 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t id5 = idesc_bf16(128, 64, false, false);
                 const uint32_t id6 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColD5, sdesc_sw128(dt + ks * 32, 16, 1024),
-                             sdesc_sw128(pp + ks * 32, 16, 1024), id5, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)  // accumulate onto S0 Q~^T
+                    mma_bf16(tmem + kColD4, sdesc_sw128(dt + ks * 32, 16, 1024),
+                             sdesc_sw128(pp + ks * 32, 16, 1024), id5, 1);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColS, sdesc_sw128(dt2 + ks * 32, 16, 1024),
@@ -552,20 +607,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar_mma);
             }
             wait_mma();
+            // the stage is free: load the next chunk while the outputs are written
+            if (tid == 0 && n + 1 < nchunks) issue_tma(n + 1);
 
-            // ---- E4: o = scale (r_q gamma D4 + D5), staged as a [64 t][128 vi] bf16
-            // tile in the (now free) Delta buffers, then written as 16-byte rows
+            // ---- E4: o = D4 (= scale (r_q gamma S0 Q^T + P Delta), the scalings
+            // being folded into Q~ and P), staged as a [64 t][128 vi] bf16 tile
+            // in the (now free) Delta buffers, then written as 16-byte rows
             {
-                float f4[32], f5[32];
+                float f4[32];
                 ld32f(kColD4 + hc * 32, f4);
-                ld32f(kColD5 + hc * 32, f5);
-                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffDt);
+                __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffOut);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = hc * 32 + j;
-                    const float o = p.scale * (v_rq[t] * v_gam[t] * f4[j] + f5[j]);
-                    otile[t * 128 + row] = __float2bfloat16_rn(o);
-                }
+                for (int j = 0; j < 32; ++j) otile[(hc * 32 + j) * 128 + row] = __float2bfloat16_rn(f4[j]);
                 __syncthreads();
                 __nv_bfloat16 *obase = p.out + (size_t)t0 * H * V + (size_t)h * V + vt * 128;
                 for (int q = tid; q < Cn * 16; q += kThreads) {
@@ -608,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     sync_all();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -669,7 +722,8 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
         attr_set = true;
     }
     const long max_units = c.max_units;
-    const int grid = (int)(max_units < sm_count() ? max_units : sm_count());
+    const long slots = (long)sm_count() * kCtasPerSm;
+    const int grid = (int)(max_units < slots ? max_units : slots);
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = launch_kernel(chunked_delta_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s,
                                   true, map, p);
