@@ -196,6 +196,24 @@ GDN_API int gdn_chunk_min_len(void);
 /* Number of kernels this library has launched in this process. */
 GDN_API uint64_t gdn_launch_count(void);
 
+/* Kernels that gdn_set_kernel_events can bracket. */
+typedef enum gdn_kernel_id {
+    GDN_KERNEL_CONV = 0,    /* conv (+ fused prepare) pass */
+    GDN_KERNEL_CHUNKED = 1, /* chunked tensor-core recurrence */
+    GDN_KERNEL_SERIAL = 2   /* token-serial recurrence */
+} gdn_kernel_id;
+
+/*
+ * Profiling aid: when `start` / `stop` are non-NULL cudaEvent_t handles, every
+ * later layer call records `start` on its stream right before launching the
+ * given kernel and `stop` right after it, so the caller can time that kernel
+ * alone with cudaEventElapsedTime.  Passing NULL for both disables it.  The
+ * records sit between dependent launches, so they also serialise the overlap
+ * those launches otherwise have.  Process-wide setting; not thread-safe.
+ * Returns GDN_ERR_SHAPE for an unknown kernel id.
+ */
+GDN_API int gdn_set_kernel_events(int kernel, void *start, void *stop);
+
 /* Size of the static device scratch used by gdn_layer_varlen_noalloc. */
 #define GDN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

@@ -158,3 +158,9 @@ def test_binding_signatures_match_header(lib):
             assert len(fn.argtypes) == n, f"{name}: binding has {len(fn.argtypes)} args, header {n}"
         else:
             assert n == 0, f"{name}: binding declares no argtypes but header has {n} params"
+
+
+def test_kernel_events_hook_validates_id(lib):
+    assert lib.gdn_set_kernel_events(3, None, None) == 2
+    assert lib.gdn_set_kernel_events(-1, None, None) == 2
+    assert lib.gdn_set_kernel_events(0, None, None) == 0

@@ -307,3 +307,20 @@ def test_full_size_sampled_rows(name):
         s, e = offs[b], offs[b + 1]
         if e - s >= L:
             assert torch.equal(cfin[b], d["qkv"][e - L:e].T.contiguous())
+
+
+
+def test_kernel_events_bracket_the_named_kernel():
+    wl, d = _bf16_case(lens=(200, 3))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    ev1.record()
+    torch.cuda.synchronize()
+    for kern in (gdn.GDN_KERNEL_CONV, gdn.GDN_KERNEL_CHUNKED, gdn.GDN_KERNEL_SERIAL):
+        gdn.gdn_set_kernel_events(kern, ev0, ev1)
+        try:
+            run_layer(wl, d)
+        finally:
+            gdn.gdn_set_kernel_events(kern, None, None)
+        torch.cuda.synchronize()
+        assert ev0.elapsed_time(ev1) > 0.0

@@ -24,7 +24,8 @@ __all__ = [
     "GdnError", "load_library", "library_path", "gdn_version", "gdn_conv1d_varlen",
     "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen", "gdn_workspace_bytes",
     "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_chunk_min_len",
-    "gdn_launch_count", "GDN_F32", "GDN_BF16", "GDN_ACT_NONE", "GDN_ACT_SILU",
+    "gdn_launch_count", "gdn_set_kernel_events", "GDN_KERNEL_CONV", "GDN_KERNEL_CHUNKED",
+    "GDN_KERNEL_SERIAL", "GDN_F32", "GDN_BF16", "GDN_ACT_NONE", "GDN_ACT_SILU",
     "STATUS_NAMES",
 ]
 
@@ -73,6 +74,8 @@ def load_library():
     lib.gdn_set_chunk_min_len.argtypes = [i]
     lib.gdn_chunk_min_len.restype = i
     lib.gdn_launch_count.restype = ctypes.c_uint64
+    lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
+    lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
                  "gdn_workspace_status", "gdn_set_chunk_min_len"):
         getattr(lib, name).restype = i
@@ -128,6 +131,16 @@ def gdn_version() -> int:
 
 def gdn_launch_count() -> int:
     return load_library().gdn_launch_count()
+
+
+GDN_KERNEL_CONV, GDN_KERNEL_CHUNKED, GDN_KERNEL_SERIAL = 0, 1, 2
+
+
+def gdn_set_kernel_events(kernel: int, start=None, stop=None) -> None:
+    """Record torch.cuda.Event `start`/`stop` around `kernel` in later layer calls
+    (None disables).  The events must have been recorded once already."""
+    h = lambda ev: None if ev is None else ctypes.c_void_p(ev.cuda_event)
+    _check(load_library().gdn_set_kernel_events(int(kernel), h(start), h(stop)))
 
 
 def gdn_set_chunk_min_len(n: int) -> None:

@@ -27,6 +27,17 @@ static std::atomic<uint64_t> g_launches{0};
 void note_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 static thread_local char g_err[512] = "";
+static cudaEvent_t g_ev_start[3] = {nullptr, nullptr, nullptr};
+static cudaEvent_t g_ev_stop[3] = {nullptr, nullptr, nullptr};
+
+// External records, so that inside a stream capture they become real event
+// record nodes of the graph (and stay ordinary records outside a capture).
+static void mark_before(int k, cudaStream_t s) {
+    if (g_ev_start[k]) cudaEventRecordWithFlags(g_ev_start[k], s, cudaEventRecordExternal);
+}
+static void mark_after(int k, cudaStream_t s) {
+    if (g_ev_stop[k]) cudaEventRecordWithFlags(g_ev_stop[k], s, cudaEventRecordExternal);
+}
 static std::atomic<int> g_chunk_min_len{0};
 
 static int fail(int code, const char *fmt, ...) {
@@ -130,6 +141,13 @@ int gdn_set_chunk_min_len(int n) {
 }
 
 int gdn_chunk_min_len(void) { return chunk_min_len(); }
+
+int gdn_set_kernel_events(int kernel, void *start, void *stop) {
+    if (kernel < 0 || kernel > 2) return fail(GDN_ERR_SHAPE, "unknown kernel id %d", kernel);
+    g_ev_start[kernel] = static_cast<cudaEvent_t>(start);
+    g_ev_stop[kernel] = static_cast<cudaEvent_t>(stop);
+    return GDN_OK;
+}
 
 int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int32_t *offsets,
                       const void *conv_init, void *y, void *conv_fin, int B, int N, int C, int Kc,
@@ -274,6 +292,8 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
+
+
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws + lay.header);
     void *y = ws + lay.y;
     float *qk = reinterpret_cast<float *>(ws + lay.qk);
@@ -289,7 +309,9 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     cp.header = hdr; cp.chunk_min_len = serial_max;
     cp.seq_order = run_chunked ? order : nullptr; cp.VT = V / 128;
     bool fused = false;
+    mark_before(GDN_KERNEL_CONV, s);
     cudaError_t e = launch_conv(cp, dtype, s, &fused);
+    mark_after(GDN_KERNEL_CONV, s);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
     if (!fused && N > 0) {
         PrepParams pp{};
@@ -306,7 +328,9 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         cl.state_init = state_init; cl.state_fin = state_fin; cl.out = out;
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
         cl.scale = eff_scale; cl.max_units = max_units;
+        mark_before(GDN_KERNEL_CHUNKED, s);
         e = launch_delta_chunked(cl, s);
+        mark_after(GDN_KERNEL_CHUNKED, s);
         if (e != cudaSuccess) return cuda_fail(e, "chunked kernel launch");
     }
 
@@ -320,7 +344,9 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     // programmatic dependent launch, its state loads with the conv kernel
     dp.conv_x = qkv; dp.conv_init = conv_init; dp.conv_fin = L > 0 ? conv_fin : nullptr;
     dp.conv_L = (int)L;
+    mark_before(GDN_KERNEL_SERIAL, s);
     e = launch_delta_serial(dp, dtype, s, /*pdl=*/true);
+    mark_after(GDN_KERNEL_SERIAL, s);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
     return GDN_OK;
 }

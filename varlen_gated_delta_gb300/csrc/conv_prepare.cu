@@ -502,13 +502,15 @@ __global__ void __launch_bounds__(kConvThreads)
                     acc[q] = fmaf(m == 0 ? xc[q] : xw[L - (m > 0 ? m : 1)][q], wr[j][q], acc[q]);
             }
             float yv[VEC];
+            Vec16<T> yo;
 #pragma unroll
             for (int q = 0; q < VEC; ++q) {
                 float z = acc[q];
                 if (p.silu) z = __fdividef(z, 1.f + __expf(-z));
-                yv[q] = round_through<T>(z);  // the conv output is stored in T
+                yo.v[q] = from_f32<T>(z);  // the conv output is stored in T
+                yv[q] = to_f32(yo.v[q]);
             }
-            if (cvalid) store_f<T, VEC>(y + (size_t)t * C + c, yv);
+            if (cvalid) *reinterpret_cast<uint4 *>(y + (size_t)t * C + c) = yo.u;
             if constexpr (PREP) {
                 if (c0 < qk_width && e - s < p.prep_max_len) {  // warp-uniform
                     float ss = 0.f;
