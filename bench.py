@@ -38,6 +38,9 @@ def _args():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "ragged", "long", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lens", default=None,
+                    help="comma-separated sequence lengths replacing the workload's "
+                         "(same head geometry and distributions; for small profiling cases)")
     return ap.parse_args()
 
 
@@ -58,14 +61,16 @@ def _peaks():
 
 
 def algorithmic_bytes_delta(wl, N, B):
-    """Bytes the token-serial recurrence kernel must move per launch."""
+    """Bytes the token-serial recurrence kernel must move per launch in the
+    layer call (it also writes the final conv state)."""
     esz = 2 if wl.dtype == "bf16" else 4
     state = 2 * B * wl.H * wl.V * wl.K * 4            # read + write fp32 state
     qk = N * wl.HQ * 2 * wl.K * 4                     # normalised q and k (fp32)
     gb = N * wl.H * 2 * 4                             # g and beta
     v = N * wl.H * wl.V * esz                         # v columns of the conv output
     out = N * wl.H * wl.V * esz
-    return state + qk + gb + v + out
+    conv_state = 2 * B * wl.width * wl.L * esz        # final conv state: read + write
+    return state + qk + gb + v + out + conv_state
 
 
 def algorithmic_bytes_layer(wl, N, B):
@@ -332,7 +337,8 @@ def run_ours(args, wl):
 
     # dominant kernel, timed inside the same layer calls with CUDA events the
     # library records on its stream right around that kernel's launch
-    dom = gdn.GDN_KERNEL_SERIAL if wl.name in ("decode", "tiny") else gdn.GDN_KERNEL_CHUNKED
+    dom = (gdn.GDN_KERNEL_SERIAL if max(wl.lengths()) < gdn.gdn_chunk_min_len()
+           else gdn.GDN_KERNEL_CHUNKED)
     k_start = torch.cuda.Event(enable_timing=True)
     k_stop = torch.cuda.Event(enable_timing=True)
     k_start.record(stream)
@@ -438,6 +444,9 @@ def main():
     args = _args()
     from varlen_gated_delta_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    if args.lens:
+        wl = W.scaled(wl, [int(x) for x in args.lens.split(",")],
+                      name=f"{wl.name}-{args.lens.replace(',', 'x')}")
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -32,11 +32,19 @@ static cudaEvent_t g_ev_stop[3] = {nullptr, nullptr, nullptr};
 
 // External records, so that inside a stream capture they become real event
 // record nodes of the graph (and stay ordinary records outside a capture).
+// Inside a stream capture the records are external, so that they become
+// real event-record nodes of the graph; outside a capture they are plain.
+static void record_event(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) st = cudaStreamCaptureStatusNone;
+    if (st == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else cudaEventRecord(ev, s);
+}
 static void mark_before(int k, cudaStream_t s) {
-    if (g_ev_start[k]) cudaEventRecordWithFlags(g_ev_start[k], s, cudaEventRecordExternal);
+    if (g_ev_start[k]) record_event(g_ev_start[k], s);
 }
 static void mark_after(int k, cudaStream_t s) {
-    if (g_ev_stop[k]) cudaEventRecordWithFlags(g_ev_stop[k], s, cudaEventRecordExternal);
+    if (g_ev_stop[k]) record_event(g_ev_stop[k], s);
 }
 static std::atomic<int> g_chunk_min_len{0};
 
@@ -215,6 +223,7 @@ int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
     p.out = out; p.state_fin = state_fin; p.B = B; p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
     p.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
     p.serial_max_len = INT_MAX;
+    p.max_len = INT_MAX;
     p.conv_fin = nullptr;
     cudaError_t e = launch_delta_serial(p, dtype, static_cast<cudaStream_t>(stream), false);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
@@ -339,6 +348,15 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;
     dp.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
     dp.serial_max_len = serial_max;
+    dp.max_len = INT_MAX;  // unknown without host offsets
+    if (offsets_host) {
+        int m = 0;
+        for (int i = 0; i < B; ++i) {
+            const int len = offsets_host[i + 1] - offsets_host[i];
+            m = len > m ? len : m;
+        }
+        dp.max_len = m;
+    }
     // the recurrence kernel also writes the final conv state (after the conv
     // kernel has finished reading the initial one) and overlaps, through
     // programmatic dependent launch, its state loads with the conv kernel

@@ -51,7 +51,10 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
     }
 }
 
-template <typename T, int KP, int RG, bool VEC4>
+// PF: prefetch the next token's operands while applying the current one
+// (sequences of several tokens); without it (one token per sequence, decode)
+// the kernel needs fewer registers and more CTAs keep state loads in flight.
+template <typename T, int KP, int RG, bool VEC4, bool PF>
 __global__ void __launch_bounds__(kSerialThreads)
     delta_serial_kernel(const DeltaParams p) {
     constexpr int EPL = 16;          // state values per lane per row
@@ -149,8 +152,10 @@ __global__ void __launch_bounds__(kSerialThreads)
     if (s < e) fetch(s, qc, kc, vc, gc, bc);
 
     for (int t = s; t < e; ++t) {
-        float qn[EPL], kn[EPL], vn[RG], gn = 1.f, bn = 0.f;
-        if (t + 1 < e) fetch(t + 1, qn, kn, vn, gn, bn);
+        float qn[PF ? EPL : 1], kn[PF ? EPL : 1], vn[RG], gn = 1.f, bn = 0.f;
+        if constexpr (PF) {
+            if (t + 1 < e) fetch(t + 1, qn, kn, vn, gn, bn);
+        }
 
         float kq = 0.f;
 #pragma unroll
@@ -187,15 +192,19 @@ __global__ void __launch_bounds__(kSerialThreads)
                 out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
         }
         if (t + 1 < e) {
+            if constexpr (PF) {
 #pragma unroll
-            for (int u = 0; u < EPL; ++u) {
-                qc[u] = qn[u];
-                kc[u] = kn[u];
+                for (int u = 0; u < EPL; ++u) {
+                    qc[u] = qn[u];
+                    kc[u] = kn[u];
+                }
+#pragma unroll
+                for (int r = 0; r < RG; ++r) vc[r] = vn[r];
+                gc = gn;
+                bc = bn;
+            } else {
+                fetch(t + 1, qc, kc, vc, gc, bc);
             }
-#pragma unroll
-            for (int r = 0; r < RG; ++r) vc[r] = vn[r];
-            gc = gn;
-            bc = bn;
         }
     }
 
@@ -218,11 +227,15 @@ cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s, bo
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     cudaError_t e;
-    if (vec4)
-        e = launch_kernel(delta_serial_kernel<T, KP, RG, true>, dim3((unsigned)blocks),
+    const bool pf = p.max_len > 1;
+    if (vec4 && pf)
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, true>, dim3((unsigned)blocks),
+                          dim3(kSerialThreads), 0, s, pdl, p);
+    else if (vec4)
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, false>, dim3((unsigned)blocks),
                           dim3(kSerialThreads), 0, s, pdl, p);
     else
-        e = launch_kernel(delta_serial_kernel<T, KP, RG, false>, dim3((unsigned)blocks),
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, false, true>, dim3((unsigned)blocks),
                           dim3(kSerialThreads), 0, s, pdl, p);
     note_launch();
     return e;

@@ -59,6 +59,7 @@ struct DeltaParams {
     int B, N, H, HQ, K, V;
     float scale;
     int serial_max_len;  // sequences with len >= this are skipped (chunked path)
+    int max_len;         // upper bound on sequence length (<= 1 selects the decode variant)
     // optional fused conv final-state copy (layer path): conv_fin[b,c,:] =
     // last L raw inputs of (conv_init || sequence) for every sequence
     const void *conv_x;
