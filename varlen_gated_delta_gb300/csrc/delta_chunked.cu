@@ -43,18 +43,19 @@ using namespace sm100;
 constexpr int kC = 64;            // chunk length
 constexpr int kThreads = 256;     // 8 warps; thread 0 issues TMA and MMA
 constexpr int kCtasPerSm = 2;
-constexpr int kAStride = 68;      // fp32 row stride of the A / T scratch (bank-conflict free)
+constexpr int kAtStride = 72;     // fp32 row stride of A^T (row = column token i)
+constexpr int kTStride = 68;      // fp32 row stride of T
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 
 // Shared memory layout (offsets from a 1024-aligned base), sized so that two
 // CTAs fit on one SM.  Buffers whose live ranges do not overlap share space:
-//   scratch: A, T (fp32, triangular inverse) -> S0 (bf16 state copy, E2..D4)
+//   scratch: A^T, T (fp32, triangular inverse) -> S0 (bf16 state copy, E2..D4)
 //            -> Delta^T, Delta'^T (E3..D5/S) -> output tile (E4)
 //   Tw, Tb (until D2/D3 complete) -> W^T (E2..D3b)
 constexpr uint32_t kStageBytes = 49152;  // [Kr|Qr] x 2 K-blocks (32 KB) + V 2 blocks (16 KB)
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffScratch = kStageBytes;                      // 34 KB
-constexpr uint32_t kScratchBytes = 2 * 64 * kAStride * 4;
+constexpr uint32_t kScratchBytes = 64 * (kAtStride + kTStride) * 4;
 constexpr uint32_t kOffS0 = kOffScratch;                           // 32 KB [128 vi][128 kk] K-major
 constexpr uint32_t kOffDt = kOffScratch;                           // 16 KB [128 vi][64 t] K-major
 constexpr uint32_t kOffDt2 = kOffScratch + 16384;                  // 16 KB
@@ -64,7 +65,7 @@ constexpr uint32_t kOffTb = kOffTw + 8192;                         // 8 KB
 constexpr uint32_t kOffWt = kOffTw;                                // 16 KB [128 kk][64 t] MN-major
 constexpr uint32_t kOffP = kOffTw + 16384;                         // 8 KB  [64 t][64 i] K-major
 constexpr uint32_t kOffVec = kOffP + 8192;                         // per-token vectors
-constexpr uint32_t kVecFloats = 7 * 64;
+constexpr uint32_t kVecFloats = 11 * 64;
 constexpr uint32_t kOffBar = kOffVec + kVecFloats * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + alignment slack
 static_assert(kScratchBytes >= 32768, "the A/T scratch must hold S0 and the Delta buffers");
@@ -89,6 +90,7 @@ struct ChunkParams {
     __nv_bfloat16 *out;
     int B, N, H, HQ, V, VT;
     float scale;
+    int tma_store;  // full output tiles leave through omap
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -113,46 +115,125 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
     return r;
 }
 
-// One warp: C[16 x 8] tile at (m0, n0) of sgn * (a[:, 0:kd] * b[0:kd, :]) with
-// warp-level m16n8k8 TF32 tensor-core MMAs; a, b, dst are fp32 row-major
-// with row stride kAStride.  Used for the merges of the triangular inverse.
-__device__ __forceinline__ void warp_tile_product(const float *a, const float *b, float *dst,
-                                                  int m0, int n0, int kd, float sgn, int lane) {
-    const int g = lane >> 2, tg = lane & 3;
-    float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-    for (int k0 = 0; k0 < kd; k0 += 8) {
-        const uint32_t a0 = to_tf32(a[(m0 + g) * kAStride + k0 + tg]);
-        const uint32_t a1 = to_tf32(a[(m0 + g + 8) * kAStride + k0 + tg]);
-        const uint32_t a2 = to_tf32(a[(m0 + g) * kAStride + k0 + tg + 4]);
-        const uint32_t a3 = to_tf32(a[(m0 + g + 8) * kAStride + k0 + tg + 4]);
-        const uint32_t b0 = to_tf32(b[(k0 + tg) * kAStride + n0 + g]);
-        const uint32_t b1 = to_tf32(b[(k0 + tg + 4) * kAStride + n0 + g]);
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// 2^x and log2(x) on the special-function unit.
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Plain non-coherent load issued where it stands (the value is consumed much later).
+__device__ __forceinline__ float ld_nc_f32(const float *ptr) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+
+// 4-byte asynchronous global -> shared copy (this thread's group)
+__device__ __forceinline__ void cp_async_4(float *smem_dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// log2 g_t and beta_t of one token from its logits (zero for padded tokens):
+// log2 g = -exp(A_log) softplus(a + dt_bias) log2(e), beta = sigmoid(b), with
+// the special-function-unit exponential and logarithm (this path computes in
+// bf16 operands; their few-ulp error is far below that rounding).
+// neg_ea_log2e = -exp(A_log) log2(e) of the head.
+__device__ __forceinline__ void chunk_gates(float a, float b, bool valid, float dt_bias,
+                                            float neg_ea_log2e, float *lg, float *beta) {
+    const float x = a + dt_bias;
+    const float softplus = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+    *lg = valid ? neg_ea_log2e * softplus : 0.f;
+    *beta = valid ? __fdividef(1.f, 1.f + __expf(-b)) : 0.f;
+}
+
+// f[lane] for a register array (a tree of selects on the lane bits, so the
+// array is never indexed dynamically).
+__device__ __forceinline__ float lane_pick(const float (&f)[32], int lane) {
+    float a16[16], a8[8], a4[4], a2[2];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) a16[m] = (lane & 1) ? f[2 * m + 1] : f[2 * m];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) a8[m] = (lane & 2) ? a16[2 * m + 1] : a16[2 * m];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a4[m] = (lane & 4) ? a8[2 * m + 1] : a8[2 * m];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) a2[m] = (lane & 8) ? a4[2 * m + 1] : a4[2 * m];
+    return (lane & 16) ? a2[1] : a2[0];
+}
+
+__device__ __forceinline__ float warp_scan_incl(float v, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
     }
-    *reinterpret_cast<float2 *>(dst + (m0 + g) * kAStride + n0 + 2 * tg) = make_float2(sgn * c0, sgn * c1);
-    *reinterpret_cast<float2 *>(dst + (m0 + g + 8) * kAStride + n0 + 2 * tg) =
-        make_float2(sgn * c2, sgn * c3);
+    return v;
+}
+
+// c += a * b on a warp-level m16n8k8 TF32 tensor-core tile: a is the 16x8
+// block with element (r, k) at ap[r * ARS + k * ACS], b the 8x8 block with
+// element (k, n) at bp[k * BRS + n] (fp32 in shared memory).
+template <int ARS, int ACS, int BRS>
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], const float *ap, const float *bp,
+                                                int g, int tg) {
+    const uint32_t a0 = to_tf32(ap[g * ARS + tg * ACS]);
+    const uint32_t a1 = to_tf32(ap[(g + 8) * ARS + tg * ACS]);
+    const uint32_t a2 = to_tf32(ap[g * ARS + (tg + 4) * ACS]);
+    const uint32_t a3 = to_tf32(ap[(g + 8) * ARS + (tg + 4) * ACS]);
+    const uint32_t b0 = to_tf32(bp[tg * BRS + g]);
+    const uint32_t b1 = to_tf32(bp[(tg + 4) * BRS + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Write rows (r0, r0 + 8), columns (c, c + 1) of Tw = T diag(ws) and
+// Tb = T diag(beta) (bf16, 128-byte swizzled, K-major) from an MMA tile.
+__device__ __forceinline__ void store_tw_tb(unsigned char *tw, unsigned char *tb, int r0, int c,
+                                            const float (&d)[4], float2 ws, float2 be) {
+    *reinterpret_cast<uint32_t *>(tw + sw128_offset(r0, c)) = pack_bf16(d[0] * ws.x, d[1] * ws.y);
+    *reinterpret_cast<uint32_t *>(tw + sw128_offset(r0 + 8, c)) = pack_bf16(d[2] * ws.x, d[3] * ws.y);
+    *reinterpret_cast<uint32_t *>(tb + sw128_offset(r0, c)) = pack_bf16(d[0] * be.x, d[1] * be.y);
+    *reinterpret_cast<uint32_t *>(tb + sw128_offset(r0 + 8, c)) = pack_bf16(d[2] * be.x, d[3] * be.y);
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    chunked_delta_kernel(const __grid_constant__ CUtensorMap ymap, const ChunkParams p) {
+    chunked_delta_kernel(const __grid_constant__ CUtensorMap ymap,
+                         const __grid_constant__ CUtensorMap omap, const ChunkParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // per-token vectors of the current chunk (log2 units for the decays):
+    //   lg: log2 g_t, beta: beta_t, lb: sum_{s<=t} log2 g_s, ck: log2 r_k(t) - lb_t,
+    //   fa: beta_t r_k(t), fp: scale r_q(t), ws: beta_t r_k(t) gamma_t,
+    //   c: Gamma[C, t] r_k(t), s: scale r_q(t) gamma_t
     float *vec = reinterpret_cast<float *>(sm + kOffVec);
-    float *v_rq = vec, *v_rk = vec + 64, *v_beta = vec + 128, *v_lg = vec + 192;
-    float *v_b = vec + 256, *v_gam = vec + 320, *v_c = vec + 384;
+    float *v_lg = vec, *v_beta = vec + 64, *v_lb = vec + 128, *v_ck = vec + 192;
+    float *v_fa = vec + 256, *v_fp = vec + 320, *v_ws = vec + 384, *v_c = vec + 448;
+    float *v_s = vec + 512;
+    float *v_na = vec + 576, *v_nb = vec + 640;  // gate logits of the next chunk (cp.async)
     uint64_t *bar_full = reinterpret_cast<uint64_t *>(sm + kOffBar);  // [2]
     uint64_t *bar_mma = bar_full + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar_full + 3);
     int *s_unit = reinterpret_cast<int *>(bar_full + 4);
     int *s_abort = s_unit + 1;
-    float *sA = reinterpret_cast<float *>(sm + kOffScratch);          // [64][kAStride]
-    float *sT = sA + 64 * kAStride;                                    // [64][kAStride]
+    float *sAt = reinterpret_cast<float *>(sm + kOffScratch);         // A^T [64 i][kAtStride]
+    float *sT = sAt + 64 * kAtStride;                                  // T [64 t][kTStride]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // TMEM access: warp w reads lane quadrant (w & 3); warps w and w + 4 split
@@ -186,6 +267,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t gchunk = 0;      // chunks loaded by this CTA (parity of the stage barrier)
     uint32_t mma_phase = 0;   // completed MMA commits
 
+    // D1 rows: lanes 0..63 hold k_t, lanes 64..127 hold q_t (t = token in chunk)
+    const bool krow = row < 64;
+    const int t_row = krow ? row : row - 64;
+    // the warp whose 32 columns contain the diagonal of its 32 rows
+    const bool diag_warp = (t_row >> 5) == hc;
+    // the warp whose columns lie right of its rows' diagonal block (A: unused, P: zero)
+    const bool upper_warp = hc == 1 && t_row < 32;
+
     auto wait_mma = [&]() {
         const bool ok = mbar_wait(bar_mma, mma_phase & 1, kWaitLimitNs);
         ++mma_phase;
@@ -218,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int kh = h / G;
         const int qcol = kh * 128, kcol = HQ * 128 + kh * 128;
         const int vcol = 2 * HQ * 128 + h * V + vt * 128;
-        const float A_log = __ldg(p.A_log + h), dtb = __ldg(p.dt_bias + h);
+        const float dtb = __ldg(p.dt_bias + h);
+        const float neg_ea = -expf(__ldg(p.A_log + h)) * 1.4426950408889634f;
         const size_t state_row = ((size_t)seq * H + h) * V + vt * 128 + row;
 
         // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
@@ -252,11 +342,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             tma_load_2d(base + 40960, &ymap, &bar_full[0], vcol + 64, t0);
         };
         if (tid == 0) issue_tma(0);
-        // gate logits of the current chunk, loaded one chunk ahead
+        // gates of chunk 0 (threads 0..63); later chunks' gates are computed
+        // during the previous chunk's state update
         float ga = 0.f, gbl = 0.f;
-        if (tid < 64 && tid < e - s) {
-            ga = __ldg(p.a + (size_t)(s + tid) * H + h);
-            gbl = __ldg(p.bl + (size_t)(s + tid) * H + h);
+        if (tid < 64) {
+            if (tid < e - s) {
+                ga = ld_nc_f32(p.a + (size_t)(s + tid) * H + h);
+                gbl = ld_nc_f32(p.bl + (size_t)(s + tid) * H + h);
+            }
+            chunk_gates(ga, gbl, tid < e - s, dtb, neg_ea, v_lg + tid, v_beta + tid);
         }
 
 #pragma unroll 1
@@ -267,26 +361,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int t0 = s + n * kC;
             const int Cn = min(kC, e - t0);
 
-            // per-token gates (threads 0..63) while the tiles land
-            if (tid < 64) {
-                float lg = 0.f, beta = 0.f;
-                if (tid < Cn) {
-                    lg = log_decay(ga, dtb, A_log);
-                    beta = 1.f / (1.f + expf(-gbl));
-                }
-                v_lg[tid] = lg;
-                v_beta[tid] = beta;
-                ga = gbl = 0.f;
-                if (t0 + kC + tid < e) {
-                    ga = __ldg(p.a + (size_t)(t0 + kC + tid) * H + h);
-                    gbl = __ldg(p.bl + (size_t)(t0 + kC + tid) * H + h);
-                }
-            }
             if (!mbar_wait(&bar_full[0], full_parity, kWaitLimitNs)) atomicExch(s_abort, 1);
             __syncthreads();
             if (*s_abort) break;
+            // the next chunk's gate logits -> shared memory, consumed by chunk_gates below
+            if (tid < 64 && t0 + kC + tid < e) {
+                cp_async_4(v_na + tid, p.a + (size_t)(t0 + kC + tid) * H + h);
+                cp_async_4(v_nb + tid, p.bl + (size_t)(t0 + kC + tid) * H + h);
+                cp_async_commit();
+            }
 
-            // ---- D1 = [Kr; Qr] [Kr; Qr]^T  (K K^T | Q K^T, Q Q^T)
+            // ---- D1 = [K; Q] [K; Q]^T  (K K^T | K Q^T over Q K^T | Q Q^T)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(128, 128, false, false);
@@ -298,219 +383,209 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 mma_commit(bar_mma);
             }
-            // cumulative log decay b_t (warp 1)
-            if (warp == 1) {
-                const float x0 = v_lg[2 * lane], x1 = v_lg[2 * lane + 1];
-                float sum = x0 + x1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, sum, off);
-                    if (lane >= off) sum += y;
-                }
-                const float b1 = sum, b0 = sum - x1;
-                v_b[2 * lane] = b0;
-                v_b[2 * lane + 1] = b1;
-                v_gam[2 * lane] = __expf(b0);
-                v_gam[2 * lane + 1] = __expf(b1);
-            }
             wait_mma();
 
-            // ---- E1: norms (diagonals), A (rows 0..63), P (rows 64..127)
-            float d1[32];
-            ld32f(kColD1 + hc * 32, d1);  // columns [32 hc, 32 hc + 32) of K K^T / Q K^T
-            auto pick = [&](const float (&f)[32]) {  // f[lane] without dynamic indexing
-                float d = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) d = (j == lane) ? f[j] : d;
-                return d;
-            };
-            if (row < 64) {
-                if ((row >> 5) == hc) v_rk[row] = rsqrtf(pick(d1) + 1e-12f);
-            } else {
-                float dq[32];  // Q Q^T columns; the warp's load stays convergent
+            // ---- E1a: norms from the diagonals, cumulative log2 decay, and the
+            // per-token vectors built from them (four diagonal warps)
+            float rq = 0.f;
+            if (diag_warp && !krow) {
+                float dq[32];
                 ld32f(kColD1 + 64 + hc * 32, dq);
-                if (((row - 64) >> 5) == hc) v_rq[row - 64] = rsqrtf(pick(dq) + 1e-12f);
+                rq = rsqrtf(lane_pick(dq, lane) + 1e-12f);
             }
+            float d1[32];  // columns [32 hc, 32 hc + 32) of K K^T (k rows) or Q K^T (q rows)
+            if (!upper_warp) ld32f(kColD1 + hc * 32, d1);
+            if (diag_warp) {
+                const float lo = warp_scan_incl(v_lg[lane], lane);
+                const float hi = warp_scan_incl(v_lg[32 + lane], lane) + __shfl_sync(0xffffffffu, lo, 31);
+                const float lbC = __shfl_sync(0xffffffffu, hi, 31);
+                const float lb = hc == 0 ? lo : hi;  // t_row = 32 hc + lane
+                if (krow) {
+                    const float rk = rsqrtf(lane_pick(d1, lane) + 1e-12f);
+                    const float ck = lg2f(rk) - lb;
+                    const float be = v_beta[t_row];
+                    v_lb[t_row] = lb;
+                    v_ck[t_row] = ck;
+                    v_fa[t_row] = be * rk;
+                    v_ws[t_row] = be * rk * ex2f(lb);
+                    v_c[t_row] = ex2f(lbC + ck);
+                } else {
+                    v_fp[t_row] = p.scale * rq;
+                    v_s[t_row] = p.scale * rq * ex2f(lb);
+                }
+            }
+            if (tid == 0) bulk_wait_read();  // the output tile (scratch) is rewritten below
             __syncthreads();
-            const float bC = v_b[63];
-            if (row < 64) {
-                const int t = row;
-                float *arow = sA + t * kAStride + hc * 32;
-                if (hc == 1 && t < 32) {  // A is strictly lower triangular: this half is zero
+
+            // ---- E1b: A[t,i] = beta_t r_k(t) r_k(i) Gamma[t,i] k_t.k_i (i < t), fp32, stored transposed;
+            //           P[t,i] = scale r_q(t) r_k(i) Gamma[t,i] q_t.k_i (i <= t), bf16;
+            // with r_k(i) Gamma[t,i] = 2^(lb_t + ck_i)
+            if (!upper_warp) {
+                const float ft = krow ? v_fa[t_row] : v_fp[t_row];
+                const float lbt = v_lb[t_row];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(arow + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-                } else {
-                    const float bt = v_b[t], f = v_beta[t] * v_rk[t];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float ck8[8], o[8];
+                    *reinterpret_cast<float4 *>(ck8) = *reinterpret_cast<const float4 *>(v_ck + hc * 32 + c8 * 8);
+                    *reinterpret_cast<float4 *>(ck8 + 4) = *reinterpret_cast<const float4 *>(v_ck + hc * 32 + c8 * 8 + 4);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const int i0 = hc * 32 + j;
-                        const float4 rk4 = *reinterpret_cast<const float4 *>(v_rk + i0);
-                        const float4 b4 = *reinterpret_cast<const float4 *>(v_b + i0);
-                        float4 o;
-                        o.x = (i0 + 0 < t) ? f * rk4.x * __expf(bt - b4.x) * d1[j + 0] : 0.f;
-                        o.y = (i0 + 1 < t) ? f * rk4.y * __expf(bt - b4.y) * d1[j + 1] : 0.f;
-                        o.z = (i0 + 2 < t) ? f * rk4.z * __expf(bt - b4.z) * d1[j + 2] : 0.f;
-                        o.w = (i0 + 3 < t) ? f * rk4.w * __expf(bt - b4.w) * d1[j + 3] : 0.f;
-                        *reinterpret_cast<float4 *>(arow + j) = o;
+                    for (int u2 = 0; u2 < 8; ++u2) {
+                        const int j = c8 * 8 + u2;  // column token 32 hc + j; the row's is 32 hc + lane
+                        o[u2] = ft * ex2f(lbt + ck8[u2]) * d1[j];
+                        if (diag_warp) o[u2] = (krow ? j < lane : j <= lane) ? o[u2] : 0.f;
+                    }
+                    if (krow) {  // A^T[i][t]: the 32 lanes write 32 consecutive words
+                        float *acol = sAt + (hc * 32 + c8 * 8) * kAtStride + t_row;
+#pragma unroll
+                        for (int u2 = 0; u2 < 8; ++u2) acol[u2 * kAtStride] = o[u2];
+                    } else {
+                        st_sw128_8(sm + kOffP, t_row, hc * 4 + c8, o);
                     }
                 }
-                if (hc == 0) v_c[t] = __expf(bC - v_b[t]) * v_rk[t];
-            } else {
-                // P = scale * tril(Q K^T) o Gamma with the norms folded in
-                const int t = row - 64;
-                if (hc == 1 && t < 32) {
-                    const float z8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            } else if (!krow) {  // P[t, i] = 0 for t < 32 <= i
+                const float z8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffP, t, 4 + c8, z8);
-                } else {
-                    const float bt = v_b[t], f = p.scale * v_rq[t];
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        const int i0 = hc * 32 + c8 * 8;
-                        float rk8[8], b8[8], v8[8];
-                        *reinterpret_cast<float4 *>(rk8) = *reinterpret_cast<const float4 *>(v_rk + i0);
-                        *reinterpret_cast<float4 *>(rk8 + 4) = *reinterpret_cast<const float4 *>(v_rk + i0 + 4);
-                        *reinterpret_cast<float4 *>(b8) = *reinterpret_cast<const float4 *>(v_b + i0);
-                        *reinterpret_cast<float4 *>(b8 + 4) = *reinterpret_cast<const float4 *>(v_b + i0 + 4);
-#pragma unroll
-                        for (int u2 = 0; u2 < 8; ++u2)
-                            v8[u2] = (i0 + u2 <= t) ? f * rk8[u2] * __expf(bt - b8[u2]) * d1[c8 * 8 + u2] : 0.f;
-                        st_sw128_8(sm + kOffP, t, hc * 4 + c8, v8);
-                    }
-                }
+                for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffP, t_row, 4 + c8, z8);
             }
             __syncthreads();
 
-            // ---- T = (I + A)^-1, lower unit-triangular, built from the bottom up:
-            // 8x8 diagonal blocks by forward substitution (one column per lane),
-            // then merges of neighbouring diagonal blocks lo, hi of growing size,
-            //   T[hi, lo] = -T[hi, hi] (A[hi, lo] T[lo, lo]),
-            // at size 8 on CUDA cores and at sizes 16 and 32 with warp-level
-            // TF32 tensor-core tiles.  The product A[hi, lo] T[lo, lo] is kept in
-            // A's (unused) upper triangle.
+            // ---- T = (I + A)^-1 (lower unit-triangular) from 16x16 blocks T_ij:
+            // step 1: diagonal blocks by right-looking forward substitution, one
+            //   column per lane (warps 0, 1); warps 6, 7 zero the upper blocks of Tw, Tb;
+            // step 2: T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22) on TF32
+            //   tensor-core tiles (warps 0..3); warps 4..7 write Tw, Tb of the diagonal blocks;
+            // step 3: T[32:64, 0:32] = -T2 (A[32:64, 0:32] T1) with T1, T2 the two 32x32
+            //   diagonal blocks (all warps).
+            // Tw = T diag(beta r_k gamma) and Tb = T diag(beta) are the bf16 MMA operands.
+            unsigned char *twp = sm + kOffTw, *tbp = sm + kOffTb;
+            const int g = lane >> 2, tg = lane & 3;
             if (warp < 2) {
-                const int blk = warp * 4 + (lane >> 3), j = lane & 7, base = blk * 8;
-                float tc[8];
+                const int blk = warp * 2 + (lane >> 4), c = lane & 15, base = blk * 16;
+                // column i of the block (A[base + r][base + i], r > i) is row i of A^T;
+                // each column is loaded one step ahead of its use
+                auto load_col = [&](int i, float (&av)[16]) {
+                    const float *acol = sAt + (base + i) * kAtStride + base;
 #pragma unroll
-                for (int r2 = 0; r2 < 8; ++r2) {
-                    const float *arow = sA + (base + r2) * kAStride + base;
-                    const float4 lo4 = *reinterpret_cast<const float4 *>(arow);
-                    const float4 hi4 = *reinterpret_cast<const float4 *>(arow + 4);
-                    const float av[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-                    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                    for (int i = 0; i < r2; ++i) {
-                        if (i & 1) acc1 = fmaf(av[i], tc[i], acc1);
-                        else acc0 = fmaf(av[i], tc[i], acc0);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        if (4 * q4 + 3 > i) {
+                            const float4 x4 = *reinterpret_cast<const float4 *>(acol + 4 * q4);
+                            av[4 * q4] = x4.x;
+                            av[4 * q4 + 1] = x4.y;
+                            av[4 * q4 + 2] = x4.z;
+                            av[4 * q4 + 3] = x4.w;
+                        }
                     }
-                    tc[r2] = (r2 == j) ? 1.f : (r2 > j ? -(acc0 + acc1) : 0.f);
+                };
+                float pr[16], tc[16], av0[16], av1[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) pr[r] = 0.f;
+                load_col(0, av0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float (&cur)[16] = (i & 1) ? av1 : av0;
+                    float (&nxt)[16] = (i & 1) ? av0 : av1;
+                    if (i + 1 < 15) load_col(i + 1, nxt);
+                    tc[i] = (i == c) ? 1.f : (i > c ? -pr[i] : 0.f);
+#pragma unroll
+                    for (int r = i + 1; r < 16; ++r) pr[r] = fmaf(cur[r], tc[i], pr[r]);
                 }
 #pragma unroll
-                for (int r2 = 0; r2 < 8; ++r2) sT[(base + r2) * kAStride + base + j] = tc[r2];
-            } else {
-                const int q0 = tid - 64, nq = kThreads - 64;
-                // the merges read the upper-right zero blocks of the diagonal
-                // blocks they combine: T[lo:lo+8, lo+8:lo+16] (size 8) and
-                // T[lo:lo+16, lo+16:lo+32] (size 16)
-                for (int q = q0; q < 4 * 64 + 2 * 256; q += nq) {
-                    if (q < 256) {
-                        const int lo = (q >> 6) * 16, r2 = (q >> 3) & 7, c = q & 7;
-                        sT[(lo + r2) * kAStride + lo + 8 + c] = 0.f;
+                for (int r = 0; r < 16; ++r) sT[(base + r) * kTStride + base + c] = tc[r];
+            } else if (warp >= 6) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int q = tid - 192; q < 2 * 192; q += 64) {
+                    const int r = q % 192;
+                    int rr, c8;
+                    if (r < 96) {
+                        rr = r / 6;
+                        c8 = 2 + r % 6;
+                    } else if (r < 160) {
+                        rr = 16 + (r - 96) / 4;
+                        c8 = 4 + (r - 96) % 4;
                     } else {
-                        const int q2 = q - 256, lo = (q2 >> 8) * 32, r2 = (q2 >> 4) & 15, c = q2 & 15;
-                        sT[(lo + r2) * kAStride + lo + 16 + c] = 0.f;
+                        rr = 32 + (r - 160) / 2;
+                        c8 = 6 + (r - 160) % 2;
                     }
-                }
-                // Q tile rows t scaled by scale * r_q(t) * gamma_t (MMA1 is done
-                // with it), so that S0 Q^T and Delta^T P^T share one accumulator
-                unsigned char *qt = stage + 8192;
-                for (int q = q0; q < 64 * 16; q += nq) {
-                    const int t = q >> 4, kb = (q >> 3) & 1, c8 = q & 7;
-                    uint4 *ptr = reinterpret_cast<uint4 *>(qt + kb * 16384 + sw128_offset(t, c8 * 8));
-                    const float f = p.scale * v_rq[t] * v_gam[t];
-                    uint4 w = *ptr;
-                    __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-                    for (int u2 = 0; u2 < 4; ++u2) {
-                        const float2 v2 = __bfloat1622float2(h2[u2]);
-                        h2[u2] = __floats2bfloat162_rn(v2.x * f, v2.y * f);
-                    }
-                    *ptr = w;
+                    *reinterpret_cast<uint4 *>((q < 192 ? twp : tbp) + sw128_offset(rr, c8 * 8)) = z;
                 }
             }
             __syncthreads();
-            {   // size 8: 4 pairs, X = A[hi, lo] T[lo, lo] (8x8x8), one output per thread
-                const int pr = tid >> 6, r2 = (tid >> 3) & 7, c = tid & 7;
-                const int lo = pr * 16, hi = lo + 8;
-                float acc = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    acc = fmaf(sA[(hi + r2) * kAStride + lo + k], sT[(lo + k) * kAStride + lo + c], acc);
-                sA[(lo + r2) * kAStride + hi + c] = acc;
-            }
-            __syncthreads();
-            {   // T[hi, lo] = -T[hi, hi] X
-                const int pr = tid >> 6, r2 = (tid >> 3) & 7, c = tid & 7;
-                const int lo = pr * 16, hi = lo + 8;
-                float acc = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    acc = fmaf(sT[(hi + r2) * kAStride + hi + k], sA[(lo + k) * kAStride + hi + c], acc);
-                sT[(hi + r2) * kAStride + lo + c] = -acc;
-            }
-            __syncthreads();
-            // size 16: 2 pairs x (16 x 16) outputs = 4 warps x two 16x8 tiles... one tile per warp
             if (warp < 4) {
-                const int lo = (warp >> 1) * 32, hi = lo + 16, n0 = (warp & 1) * 8;
-                warp_tile_product(sA + hi * kAStride + lo, sT + lo * kAStride + lo,
-                                  sA + lo * kAStride + hi, 0, n0, 16, 1.f, lane);
-            }
-            __syncthreads();
-            if (warp < 4) {
-                const int lo = (warp >> 1) * 32, hi = lo + 16, n0 = (warp & 1) * 8;
-                warp_tile_product(sT + hi * kAStride + hi, sA + lo * kAStride + hi,
-                                  sT + hi * kAStride + lo, 0, n0, 16, -1.f, lane);
-            }
-            __syncthreads();
-            // size 32: X2 = A[32:64, 0:32] T[0:32, 0:32] (32 x 32: 8 warps x one 16x8 tile)
-            {
-                const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
-                warp_tile_product(sA + 32 * kAStride, sT, sA + 32, m0, n0, 32, 1.f, lane);
-            }
-            __syncthreads();
-            {   // T[32:64, 0:32] = -T[32:64, 32:64] X2
-                const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
-                warp_tile_product(sT + 32 * kAStride + 32, sA + 32, sT + 32 * kAStride, m0, n0, 32,
-                                  -1.f, lane);
-            }
-            __syncthreads();
-            // Tw = T diag(r_k beta gamma), Tb = T diag(beta), bf16 (T is lower triangular)
+                const int lo = (warp >> 1) * 32, hi = lo + 16, n0 = lo + (warp & 1) * 8;
+                float *xs = sT + (warp >> 1) * 16 * kTStride + 32 + (warp & 1) * 8;  // unused upper block
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = tid; q < 64 * 8; q += kThreads) {
-                const int t = q >> 3, c8 = q & 7, i0 = c8 * 8;
-                float t8[8], be8[8], ga8[8], rk8[8], w8[8], b8[8];
-                *reinterpret_cast<float4 *>(t8) = *reinterpret_cast<const float4 *>(sT + t * kAStride + i0);
-                *reinterpret_cast<float4 *>(t8 + 4) = *reinterpret_cast<const float4 *>(sT + t * kAStride + i0 + 4);
-                *reinterpret_cast<float4 *>(be8) = *reinterpret_cast<const float4 *>(v_beta + i0);
-                *reinterpret_cast<float4 *>(be8 + 4) = *reinterpret_cast<const float4 *>(v_beta + i0 + 4);
-                *reinterpret_cast<float4 *>(ga8) = *reinterpret_cast<const float4 *>(v_gam + i0);
-                *reinterpret_cast<float4 *>(ga8 + 4) = *reinterpret_cast<const float4 *>(v_gam + i0 + 4);
-                *reinterpret_cast<float4 *>(rk8) = *reinterpret_cast<const float4 *>(v_rk + i0);
-                *reinterpret_cast<float4 *>(rk8 + 4) = *reinterpret_cast<const float4 *>(v_rk + i0 + 4);
+                for (int k0 = 0; k0 < 16; k0 += 8)  // X = A[hi, lo] T[lo, lo]
+                    mma_tf32_16x8x8<1, kAtStride, kTStride>(x, sAt + (lo + k0) * kAtStride + hi,
+                                                            sT + (lo + k0) * kTStride + n0, g, tg);
+                *reinterpret_cast<float2 *>(xs + g * kTStride + 2 * tg) = make_float2(x[0], x[1]);
+                *reinterpret_cast<float2 *>(xs + (g + 8) * kTStride + 2 * tg) = make_float2(x[2], x[3]);
+                __syncwarp();
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k0 = 0; k0 < 16; k0 += 8)  // T[hi, lo] = -T[hi, hi] X
+                    mma_tf32_16x8x8<kTStride, 1, kTStride>(d, sT + hi * kTStride + hi + k0,
+                                                           xs + k0 * kTStride, g, tg);
+#pragma unroll
+                for (int u2 = 0; u2 < 4; ++u2) d[u2] = -d[u2];
+                const int r0 = hi + g, cc = n0 + 2 * tg;
+                *reinterpret_cast<float2 *>(sT + r0 * kTStride + cc) = make_float2(d[0], d[1]);
+                *reinterpret_cast<float2 *>(sT + (r0 + 8) * kTStride + cc) = make_float2(d[2], d[3]);
+                store_tw_tb(twp, tbp, r0, cc, d, *reinterpret_cast<const float2 *>(v_ws + cc),
+                            *reinterpret_cast<const float2 *>(v_beta + cc));
+            } else {  // diagonal blocks: 4 blocks x 16 rows x 2 column halves, one per thread
+                const int q = tid - 128;
+                const int blk = q >> 5, rr = blk * 16 + ((q >> 1) & 15), c0 = blk * 16 + (q & 1) * 8;
+                float t8[8], ws8[8], be8[8], w8[8], b8[8];
+                *reinterpret_cast<float4 *>(t8) = *reinterpret_cast<const float4 *>(sT + rr * kTStride + c0);
+                *reinterpret_cast<float4 *>(t8 + 4) = *reinterpret_cast<const float4 *>(sT + rr * kTStride + c0 + 4);
+                *reinterpret_cast<float4 *>(ws8) = *reinterpret_cast<const float4 *>(v_ws + c0);
+                *reinterpret_cast<float4 *>(ws8 + 4) = *reinterpret_cast<const float4 *>(v_ws + c0 + 4);
+                *reinterpret_cast<float4 *>(be8) = *reinterpret_cast<const float4 *>(v_beta + c0);
+                *reinterpret_cast<float4 *>(be8 + 4) = *reinterpret_cast<const float4 *>(v_beta + c0 + 4);
 #pragma unroll
                 for (int u2 = 0; u2 < 8; ++u2) {
-                    const float tv = (i0 + u2 <= t) ? t8[u2] : 0.f;
-                    b8[u2] = tv * be8[u2];
-                    w8[u2] = b8[u2] * ga8[u2] * rk8[u2];
+                    w8[u2] = t8[u2] * ws8[u2];
+                    b8[u2] = t8[u2] * be8[u2];
                 }
-                st_sw128_8(sm + kOffTw, t, c8, w8);
-                st_sw128_8(sm + kOffTb, t, c8, b8);
+                st_sw128_8(twp, rr, c0 >> 3, w8);
+                st_sw128_8(tbp, rr, c0 >> 3, b8);
+            }
+            __syncthreads();
+            {
+                const int ni = warp & 3, mi = warp >> 2, c0 = ni * 8;
+                // X2 = A[32:64, 0:32] T1 (columns c0..c0+7; T1[k][c] = 0 for k < c0),
+                // rows 0 .. 16 mi + 15, into a scratch block T does not need any more
+                float *xs = mi ? sT + 32 + c0 : sT + 32 * kTStride + c0;
+#pragma unroll
+                for (int m2 = 0; m2 < 2; ++m2) {
+                    if (m2 > mi) break;
+                    float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int k0 = c0; k0 < 32; k0 += 8)
+                        mma_tf32_16x8x8<1, kAtStride, kTStride>(x, sAt + k0 * kAtStride + 32 + 16 * m2,
+                                                                sT + k0 * kTStride + c0, g, tg);
+                    float *xr = xs + 16 * m2 * kTStride;
+                    *reinterpret_cast<float2 *>(xr + g * kTStride + 2 * tg) = make_float2(x[0], x[1]);
+                    *reinterpret_cast<float2 *>(xr + (g + 8) * kTStride + 2 * tg) = make_float2(x[2], x[3]);
+                }
+                __syncwarp();
+                // T[32 + 16 mi + r][c0 + n] = -sum_k T2[16 mi + r][k] X2[k][n], k < 16 mi + 16
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                const float *t2 = sT + (32 + 16 * mi) * kTStride + 32;
+#pragma unroll 1
+                for (int k0 = 0; k0 < 16 * mi + 16; k0 += 8)
+                    mma_tf32_16x8x8<kTStride, 1, kTStride>(d, t2 + k0, xs + k0 * kTStride, g, tg);
+#pragma unroll
+                for (int u2 = 0; u2 < 4; ++u2) d[u2] = -d[u2];
+                const int cc = c0 + 2 * tg;
+                store_tw_tb(twp, tbp, 32 + 16 * mi + g, cc, d, *reinterpret_cast<const float2 *>(v_ws + cc),
+                            *reinterpret_cast<const float2 *>(v_beta + cc));
             }
             fence_async_smem();
             sync_all();
 
-            // ---- D2 = Kr^T Tw^T (= W^T), D3 = V^T Tb^T
+            // ---- D2 = K^T Tw^T (= W^T), D3 = V^T Tb^T
             if (tid == 0) {
                 const uint32_t id = idesc_bf16(128, 64, true, false);
                 const uint32_t tw = smem_u32(sm + kOffTw), tb = smem_u32(sm + kOffTb);
@@ -532,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 ld32f(kColD2 + hc * 32, f);
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffWt, row, hc * 4 + c8, f + c8 * 8);
-                const float gC = __expf(bC);
+                const float gC = ex2f(v_lb[63]);
                 unsigned char *s0 = sm + kOffS0 + hc * 16384;  // this half is one K-block
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -553,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             fence_async_smem();
             sync_all();
 
-            // ---- D3 -= S0 W^T ;  D4 = S0 Qr^T
+            // ---- D3 -= S0 W^T ;  D4 = S0 Q^T
             if (tid == 0) {
                 const uint32_t s0 = smem_u32(sm + kOffS0), wt = smem_u32(sm + kOffWt);
                 const uint32_t idn = idesc_bf16(128, 64, false, true, true);
@@ -571,6 +646,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                              sdesc_sw128(kq + 8192 + aoff, 16, 1024), idq, ks > 0);
                 }
                 mma_commit(bar_mma);
+            }
+            // gates of the next chunk while the MMAs run (this chunk is done with them)
+            if (tid < 64 && n + 1 < nchunks) {
+                const bool valid = t0 + kC + tid < e;
+                cp_async_wait_all();
+                chunk_gates(valid ? v_na[tid] : 0.f, valid ? v_nb[tid] : 0.f, valid, dtb, neg_ea,
+                            v_lg + tid, v_beta + tid);
             }
             wait_mma();
 
@@ -590,16 +672,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             fence_async_smem();
             sync_all();
 
-            // ---- D5 = Delta^T P^T ;  S += Delta'^T Kr
+            // ---- D5 = Delta^T P^T ;  S += Delta'^T K
             if (tid == 0) {
                 const uint32_t dt = smem_u32(sm + kOffDt), dt2 = smem_u32(sm + kOffDt2);
                 const uint32_t pp = smem_u32(sm + kOffP);
                 const uint32_t id5 = idesc_bf16(128, 64, false, false);
                 const uint32_t id6 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)  // accumulate onto S0 Q~^T
-                    mma_bf16(tmem + kColD4, sdesc_sw128(dt + ks * 32, 16, 1024),
-                             sdesc_sw128(pp + ks * 32, 16, 1024), id5, 1);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + kColD5, sdesc_sw128(dt + ks * 32, 16, 1024),
+                             sdesc_sw128(pp + ks * 32, 16, 1024), id5, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColS, sdesc_sw128(dt2 + ks * 32, 16, 1024),
@@ -610,21 +692,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // the stage is free: load the next chunk while the outputs are written
             if (tid == 0 && n + 1 < nchunks) issue_tma(n + 1);
 
-            // ---- E4: o = D4 (= scale (r_q gamma S0 Q^T + P Delta), the scalings
-            // being folded into Q~ and P), staged as a [64 t][128 vi] bf16 tile
-            // in the (now free) Delta buffers, then written as 16-byte rows
+            // ---- E4: o[vi, t] = s_t (S0 Q^T)[vi, t] + (Delta^T P^T)[vi, t], staged as a
+            // [64 t][128 vi] bf16 tile in the (now free) Delta buffers, then written
+            // as 16-byte rows
             {
-                float f4[32];
-                ld32f(kColD4 + hc * 32, f4);
                 __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffOut);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) otile[(hc * 32 + j) * 128 + row] = __float2bfloat16_rn(f4[j]);
-                __syncthreads();
-                __nv_bfloat16 *obase = p.out + (size_t)t0 * H * V + (size_t)h * V + vt * 128;
-                for (int q = tid; q < Cn * 16; q += kThreads) {
-                    const int t = q >> 4, c16 = q & 15;
-                    *reinterpret_cast<uint4 *>(obase + (size_t)t * H * V + c16 * 8) =
-                        *reinterpret_cast<const uint4 *>(otile + t * 128 + c16 * 8);
+                for (int c16 = 0; c16 < 2; ++c16) {
+                    uint32_t r4[16], r5[16];
+                    tmem_ld16(lane_base + kColD4 + hc * 32 + c16 * 16, r4);
+                    tmem_ld16(lane_base + kColD5 + hc * 32 + c16 * 16, r5);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const int tt = hc * 32 + c16 * 16 + j;
+                        const float4 s4 = *reinterpret_cast<const float4 *>(v_s + tt);
+                        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                        for (int u2 = 0; u2 < 4; ++u2)
+                            otile[(tt + u2) * 128 + row] = __float2bfloat16_rn(
+                                fmaf(sv[u2], __uint_as_float(r4[j + u2]), __uint_as_float(r5[j + u2])));
+                    }
+                }
+                if (p.tma_store && Cn == kC) {  // a full tile: one bulk store
+                    fence_async_smem();
+                    __syncthreads();
+                    if (tid == 0) {
+                        tma_store_2d(&omap, otile, h * V + vt * 128, t0);
+                        bulk_commit();
+                    }
+                } else {  // the last, ragged tile of a sequence: rows t < Cn only
+                    __syncthreads();
+                    __nv_bfloat16 *obase = p.out + (size_t)t0 * H * V + (size_t)h * V + vt * 128;
+                    for (int q = tid; q < Cn * 16; q += kThreads) {
+                        const int t = q >> 4, c16 = q & 15;
+                        *reinterpret_cast<uint4 *>(obase + (size_t)t * H * V + c16 * 8) =
+                            *reinterpret_cast<const uint4 *>(otile + t * 128 + c16 * 8);
+                    }
                 }
             }
             sync_all();
@@ -660,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
         }
     }
+    if (tid == 0) bulk_wait_all();
     sync_all();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
@@ -707,6 +812,18 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // output tiles [64 t][128 vi] of out viewed as [N, H V] (no swizzle)
+    CUtensorMap omap;
+    int tma_store = 0;
+    if ((reinterpret_cast<uintptr_t>(c.out) & 15) == 0 && c.N > 0) {
+        const cuuint64_t odims[2] = {(cuuint64_t)c.H * c.V, (cuuint64_t)c.N};
+        const cuuint64_t ostrides[1] = {(cuuint64_t)c.H * c.V * 2};
+        const cuuint32_t obox[2] = {128, 64};
+        tma_store = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.out, odims, ostrides, obox, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (!tma_store) omap = map;  // unused
     ChunkParams p{};
     p.a = c.a; p.bl = c.bl; p.A_log = c.A_log; p.dt_bias = c.dt_bias;
     p.offsets = c.offsets; p.seq_order = c.seq_order; p.header = c.header;
@@ -714,6 +831,7 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     p.out = static_cast<__nv_bfloat16 *>(c.out);
     p.B = c.B; p.N = c.N; p.H = c.H; p.HQ = c.HQ; p.V = c.V; p.VT = c.V / 128;
     p.scale = c.scale;
+    p.tma_store = tma_store;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(chunked_delta_kernel,
@@ -726,7 +844,7 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     const int grid = (int)(max_units < slots ? max_units : slots);
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = launch_kernel(chunked_delta_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s,
-                                  true, map, p);
+                                  true, map, omap, p);
     note_launch();
     return e;
 }
