@@ -299,6 +299,16 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         run_chunked = n > 0;
         max_units = n * H * (V / 128);
     }
+    // tokens of token-serial sequences need the prepare step; with host
+    // offsets a batch of chunked sequences only skips it
+    bool need_prep = true;
+    if (offsets_host) {
+        need_prep = false;
+        for (int i = 0; i < B && !need_prep; ++i) {
+            const int len = offsets_host[i + 1] - offsets_host[i];
+            need_prep = len > 0 && len < serial_max;
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
 
@@ -313,7 +323,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     cp.x = qkv; cp.w = w; cp.bias = bias; cp.offsets = offsets; cp.init = conv_init; cp.y = y;
     cp.B = B; cp.N = N; cp.C = (int)width; cp.Kc = Kc; cp.D = D; cp.L = (int)L;
     cp.silu = act == GDN_ACT_SILU;
-    cp.prep = 1; cp.qk = qk; cp.gb = gb; cp.a = a; cp.bl = b; cp.A_log = A_log; cp.dt_bias = dt_bias;
+    cp.prep = need_prep ? 1 : 0; cp.qk = qk; cp.gb = gb; cp.a = a; cp.bl = b; cp.A_log = A_log; cp.dt_bias = dt_bias;
     cp.H = H; cp.HQ = HQ; cp.K = K; cp.V = V; cp.prep_max_len = serial_max;
     cp.header = hdr; cp.chunk_min_len = serial_max;
     cp.seq_order = run_chunked ? order : nullptr; cp.VT = V / 128;
@@ -322,7 +332,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     cudaError_t e = launch_conv(cp, dtype, s, &fused);
     mark_after(GDN_KERNEL_CONV, s);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
-    if (!fused && N > 0) {
+    if (need_prep && !fused && N > 0) {
         PrepParams pp{};
         pp.y = y; pp.a = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias; pp.qk = qk; pp.gb = gb;
         pp.N = N; pp.H = H; pp.HQ = HQ; pp.K = K; pp.V = V;

@@ -15,6 +15,9 @@
 // into the conv pass without another read of the conv output.
 #include <math.h>
 
+#include <type_traits>
+#include <utility>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -70,6 +73,9 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src,
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 template <typename T, int VEC>
 __device__ __forceinline__ void zero_raw(T *dst) {
@@ -78,6 +84,20 @@ __device__ __forceinline__ void zero_raw(T *dst) {
     } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) dst[e] = from_f32<T>(0.f);
+    }
+}
+
+// Round two fp32 values to T into elements (q, q + 1) of a 16-byte vector
+// (one packed conversion for bf16).
+template <typename T>
+__device__ __forceinline__ void store_pair(Vec16<T> &v, int q, float a, float b) {
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+        v.v[q] = h2.x;
+        v.v[q + 1] = h2.y;
+    } else {
+        v.v[q] = from_f32<T>(a);
+        v.v[q + 1] = from_f32<T>(b);
     }
 }
 
@@ -364,19 +384,29 @@ __global__ void __launch_bounds__(kConvThreads)
 }
 
 // Streaming variant for a compile-time conv width KC and dilation D (the
-// common Kc <= 4 cases): each warp walks a run of R consecutive tokens for
-// one tile of CT = 32 * VEC channels.  Input rows are loaded straight from
-// global memory (coalesced 16-byte vectors, prefetched kPf rows ahead) and
-// the L = (KC-1)*D previous inputs of the lane's channels live in registers,
-// so every input element is loaded and converted once.  At each sequence
-// start the window is refilled from that sequence's initial conv state.
+// common Kc <= 4 cases).  Each warp walks a run of R tokens of one residue
+// class t = t_start + D i (for D = 1 simply R consecutive tokens) for one tile
+// of CT = 32 * VEC channels, so the conv taps of a token are the KC - 1
+// previous tokens of the same run.  Input rows stream through a per-warp
+// ring of kRing rows in shared memory filled by 16-byte cp.async copies
+// (kRing rows in flight per warp, no registers held), and the taps live in a
+// register window that rotates with the KC-fold unrolled loop, so every
+// input element is loaded, converted and moved once.  At each sequence start
+// the window is refilled from that sequence's initial conv state.
+constexpr int kRing = 8;
+constexpr int kRingBytes = (kConvThreads / 32) * kRing * 512;  // 32 lanes x 16 bytes per row
+
 template <typename T, int VEC, bool PREP, int KC, int D>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 2)
     conv_stream_kernel(const ConvParams p, const int R, const int n_ctiles) {
     constexpr int L = (KC - 1) * D;
     constexpr int CT = 32 * VEC;
-    constexpr int kPf = 4;
-    __shared__ int s_offs[kOffsetsCache];
+    static_assert(sizeof(T) * VEC == 16, "streaming conv works on 16-byte vectors");
+    // dynamic shared memory: the rows ring [warps][kRing][CT], then offsets[0..B]
+    // when B + 1 <= kOffsetsCache
+    extern __shared__ __align__(16) unsigned char conv_dsm[];
+    T *s_ring = reinterpret_cast<T *>(conv_dsm);
+    int *s_offs = reinterpret_cast<int *>(conv_dsm + kRingBytes);
 
     pdl_launch_dependents();
     if (p.header != nullptr && blockIdx.x == 0) schedule_block(p);
@@ -394,14 +424,27 @@ __global__ void __launch_bounds__(kConvThreads)
     const int tile_c = blockIdx.x % n_ctiles, tile_t = blockIdx.x / n_ctiles;
     const int c0 = tile_c * CT, c = c0 + lane * VEC;
     const bool cvalid = c < C;
-    const int run0 = (tile_t * (kConvThreads / 32) + warp) * R;
-    const int tend = min(run0 + R, N);
-    if (run0 >= tend) return;
+    // run of this warp: tokens tb + D i, i = 0 .. n - 1
+    const int gw = tile_t * (kConvThreads / 32) + warp;
+    const int span = gw / D, cls = gw % D;
+    const long tb_l = (long)span * R * D + cls;
+    if (tb_l >= N) return;
+    const int tb = (int)tb_l;
+    const int n = min(R, (N - 1 - tb) / D + 1);
 
     const T *x = static_cast<const T *>(p.x);
     const T *w = static_cast<const T *>(p.w);
     const T *init = static_cast<const T *>(p.init);
     T *y = static_cast<T *>(p.y);
+    T *ring = s_ring + (size_t)warp * kRing * CT + lane * VEC;
+
+    // the first kRing rows of the run start streaming in
+#pragma unroll
+    for (int q = 0; q < kRing; ++q) {
+        const int t = tb + D * q;
+        cp_async16(ring + q * CT, x + (size_t)(q < n ? t : tb) * C + (cvalid ? c : 0), q < n && cvalid);
+        cp_async_commit();
+    }
 
     // weights and bias of the lane's channels
     float wr[KC][VEC], bias[VEC];
@@ -433,134 +476,152 @@ __global__ void __launch_bounds__(kConvThreads)
     int lo = 0, hi = B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (off(mid) <= run0) lo = mid;
+        if (off(mid) <= tb) lo = mid;
         else hi = mid - 1;
     }
     int b = lo, s = off(b), e = off(b + 1);
+    bool seq_ok = e >= s && s >= 0 && e <= N && tb >= s && tb < e;
 
-    // xw[L - m] holds the input m steps back (m = 1..L)
-    float xw[L > 0 ? L : 1][VEC];
-    auto fill_window = [&](int t) {
+    // win[r % KC] holds run row r (as fp32); tap m of row r reads win[(r - m) % KC]
+    float win[KC][VEC];
+    // the KC - 1 rows before run row r (token t) from x or, before the sequence
+    // start, from the sequence's initial conv state
+    auto fill_window = [&](int t, auto ph_c) {
+        constexpr int ph = decltype(ph_c)::value;
 #pragma unroll
-        for (int m = 1; m <= L; ++m) {
-            const int src = t - m;
+        for (int m = 1; m < KC; ++m) {
+            float(&dst)[VEC] = win[(ph - m + KC * 4) % KC];
+            const int src = t - m * D;
             if (src >= s) {
-                if (cvalid) load_f<T, VEC>(x + (size_t)src * C + c, xw[L - m]);
+                if (cvalid) load_f<T, VEC>(x + (size_t)src * C + c, dst);
                 else
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) xw[L - m][q] = 0.f;
+                    for (int q = 0; q < VEC; ++q) dst[q] = 0.f;
             } else {
                 const int local = src - s;  // in [-L, -1]
 #pragma unroll
                 for (int q = 0; q < VEC; ++q)
-                    xw[L - m][q] = cvalid ? to_f32(init[((size_t)b * C + c + q) * L + L + local]) : 0.f;
+                    dst[q] = cvalid ? to_f32(init[((size_t)b * C + c + q) * L + L + local]) : 0.f;
             }
         }
     };
-    const bool seq_ok0 = e >= s && s >= 0 && e <= N && run0 >= s && run0 < e;
-    if (seq_ok0) fill_window(run0);
-
-    // prefetch ring of raw input rows
-    uint4 pf[kPf];
-    static_assert(sizeof(T) * VEC == 16, "streaming conv works on 16-byte vectors");
-#pragma unroll
-    for (int q = 0; q < kPf; ++q)
-        if (run0 + q < tend && cvalid)
-            pf[q] = *reinterpret_cast<const uint4 *>(x + (size_t)(run0 + q) * C + c);
 
     const int qk_width = PREP ? 2 * p.HQ * p.K : 0;
     const int lanes_per_head = PREP ? p.K / VEC : 1;
-    bool seq_ok = seq_ok0;
 
-    for (int t = run0; t < tend; ++t) {
-        Vec16<T> cur;
-        cur.u = pf[0];
+    for (int r0 = 0; r0 < n; r0 += KC) {
+        [&]<int... PH>(std::integer_sequence<int, PH...>) {
+            (
+                [&] {
+                    constexpr int ph = PH;
+                    const int r = r0 + ph;
+                    if (r >= n) return;
+                    const int t = tb + D * r;
+                    // row r has landed (one commit group per row, in order)
+                    asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+                    Vec16<T> cur;
+                    cur.u = *reinterpret_cast<const uint4 *>(ring + (r & (kRing - 1)) * CT);
+                    float(&xc)[VEC] = win[ph];
 #pragma unroll
-        for (int q = 0; q < kPf - 1; ++q) pf[q] = pf[q + 1];
-        if (t + kPf < tend && cvalid)
-            pf[kPf - 1] = *reinterpret_cast<const uint4 *>(x + (size_t)(t + kPf) * C + c);
-
-        if (t >= e) {  // next non-empty sequence (warp-uniform)
-            while (b + 1 < B && off(b + 1) <= t) ++b;
-            s = off(b);
-            e = off(b + 1);
-            seq_ok = e >= s && s >= 0 && e <= N && t >= s && t < e;
-            if (seq_ok) fill_window(t);
-        }
-        float xc[VEC];
-#pragma unroll
-        for (int q = 0; q < VEC; ++q) xc[q] = cvalid ? to_f32(cur.v[q]) : 0.f;
-        if (seq_ok) {
-            float acc[VEC];
-#pragma unroll
-            for (int q = 0; q < VEC; ++q) acc[q] = bias[q];
-#pragma unroll
-            for (int j = 0; j < KC; ++j) {
-                const int m = (KC - 1 - j) * D;  // steps back
-#pragma unroll
-                for (int q = 0; q < VEC; ++q)
-                    acc[q] = fmaf(m == 0 ? xc[q] : xw[L - (m > 0 ? m : 1)][q], wr[j][q], acc[q]);
-            }
-            float yv[VEC];
-            Vec16<T> yo;
-#pragma unroll
-            for (int q = 0; q < VEC; ++q) {
-                float z = acc[q];
-                if (p.silu) z = __fdividef(z, 1.f + __expf(-z));
-                yo.v[q] = from_f32<T>(z);  // the conv output is stored in T
-                yv[q] = to_f32(yo.v[q]);
-            }
-            if (cvalid) *reinterpret_cast<uint4 *>(y + (size_t)t * C + c) = yo.u;
-            if constexpr (PREP) {
-                if (c0 < qk_width && e - s < p.prep_max_len) {  // warp-uniform
-                    float ss = 0.f;
-#pragma unroll
-                    for (int q = 0; q < VEC; ++q) ss = fmaf(yv[q], yv[q], ss);
-                    for (int o = lanes_per_head >> 1; o > 0; o >>= 1)
-                        ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                    if (cvalid && c < qk_width) {
-                        const float r = rsqrtf(ss + 1e-12f);
-                        const int plane = c >= p.HQ * p.K;
-                        const int cc = c - plane * p.HQ * p.K;
-                        float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
-#pragma unroll
-                        for (int q = 0; q < VEC; ++q) dst[q] = yv[q] * r;
+                    for (int q = 0; q < VEC; ++q) xc[q] = cvalid ? to_f32(cur.v[q]) : 0.f;
+                    // the slot is free again: stream in row r + kRing
+                    {
+                        const int rn = r + kRing;
+                        cp_async16(ring + (r & (kRing - 1)) * CT,
+                                   x + (size_t)(rn < n ? tb + D * rn : tb) * C + (cvalid ? c : 0),
+                                   rn < n && cvalid);
+                        cp_async_commit();
                     }
-                }
-                if (tile_c == 0 && e - s < p.prep_max_len) {
-                    for (int h = lane; h < p.H; h += 32) {
-                        float g, beta;
-                        decay_rate(p, t, h, g, beta);
-                        p.gb[(size_t)t * p.H + h] = g;
-                        p.gb[((size_t)N + t) * p.H + h] = beta;
+                    if (r == 0 || t >= e) {  // run start or next sequence (warp-uniform)
+                        if (t >= e) {
+                            while (b + 1 < B && off(b + 1) <= t) ++b;
+                            s = off(b);
+                            e = off(b + 1);
+                            seq_ok = e >= s && s >= 0 && e <= N && t >= s && t < e;
+                        }
+                        if (seq_ok) fill_window(t, std::integral_constant<int, ph>{});
                     }
-                }
-            }
-        }
-        if constexpr (L > 0) {
+                    if (!seq_ok) return;
+                    float acc[VEC];
 #pragma unroll
-            for (int m = 0; m < L - 1; ++m)
+                    for (int q = 0; q < VEC; ++q) acc[q] = bias[q];
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) xw[m][q] = xw[m + 1][q];
+                    for (int j = 0; j < KC; ++j) {
+                        const float(&xs)[VEC] = win[(ph - (KC - 1 - j) + KC * 4) % KC];
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) xw[L - 1][q] = xc[q];
-        }
+                        for (int q = 0; q < VEC; ++q) acc[q] = fmaf(xs[q], wr[j][q], acc[q]);
+                    }
+                    Vec16<T> yo;
+#pragma unroll
+                    for (int q = 0; q < VEC; q += 2) {
+                        float z0 = acc[q], z1 = acc[q + 1];
+                        // SiLU with the fast exponential and division: their error
+                        // (a few fp32 ulp) is far below the rounding of the output to T
+                        if (p.silu) {
+                            z0 = __fdividef(z0, 1.f + __expf(-z0));
+                            z1 = __fdividef(z1, 1.f + __expf(-z1));
+                        }
+                        store_pair<T>(yo, q, z0, z1);  // the conv output is stored in T
+                    }
+                    if (cvalid) *reinterpret_cast<uint4 *>(y + (size_t)t * C + c) = yo.u;
+                    if constexpr (PREP) {
+                        if (c0 < qk_width && e - s < p.prep_max_len) {  // warp-uniform
+                            float yv[VEC];
+#pragma unroll
+                            for (int q = 0; q < VEC; ++q) yv[q] = to_f32(yo.v[q]);
+                            float ss = 0.f;
+#pragma unroll
+                            for (int q = 0; q < VEC; ++q) ss = fmaf(yv[q], yv[q], ss);
+                            for (int o = lanes_per_head >> 1; o > 0; o >>= 1)
+                                ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                            if (cvalid && c < qk_width) {
+                                const float rr = rsqrtf(ss + 1e-12f);
+                                const int plane = c >= p.HQ * p.K;
+                                const int cc = c - plane * p.HQ * p.K;
+                                float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
+#pragma unroll
+                                for (int q = 0; q < VEC; ++q) dst[q] = yv[q] * rr;
+                            }
+                        }
+                        if (tile_c == 0 && e - s < p.prep_max_len) {
+                            for (int h = lane; h < p.H; h += 32) {
+                                float g, beta;
+                                decay_rate(p, t, h, g, beta);
+                                p.gb[(size_t)t * p.H + h] = g;
+                                p.gb[((size_t)N + t) * p.H + h] = beta;
+                            }
+                        }
+                    }
+                }(),
+                ...);
+        }(std::make_integer_sequence<int, KC>{});
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <typename T, int VEC, bool PREP, int KC, int D>
 cudaError_t launch_conv_stream(const ConvParams &p, cudaStream_t s) {
     constexpr int CT = 32 * VEC;
     const int n_ctiles = (p.C + CT - 1) / CT;
-    // run length: enough warps for several waves, at most 32 tokens per warp
-    const long target_warps = 148L * 48;
+    // run length: enough warps for several waves, at most 64 tokens per warp
+    const long target_warps = 148L * 64;
     long R = ((long)p.N * n_ctiles) / target_warps;
-    R = R < 1 ? 1 : (R > 32 ? 32 : R);
-    const long runs = p.N > 0 ? (p.N + R - 1) / R : 1;
-    const long ttiles = (runs + (kConvThreads / 32) - 1) / (kConvThreads / 32);
+    R = R < 1 ? 1 : (R > 64 ? 64 : R);
+    const long spans = p.N > 0 ? (p.N + R * D - 1) / (R * D) : 1;
+    const long warps = spans * D;
+    const long ttiles = (warps + (kConvThreads / 32) - 1) / (kConvThreads / 32);
     const long blocks = ttiles * n_ctiles;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    conv_stream_kernel<T, VEC, PREP, KC, D><<<(unsigned)blocks, kConvThreads, 0, s>>>(p, (int)R, n_ctiles);
+    const size_t smem = kRingBytes + (p.B + 1 <= kOffsetsCache ? sizeof(int) * (p.B + 1) : 0);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(conv_stream_kernel<T, VEC, PREP, KC, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kRingBytes + sizeof(int) * kOffsetsCache));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    conv_stream_kernel<T, VEC, PREP, KC, D><<<(unsigned)blocks, kConvThreads, smem, s>>>(p, (int)R, n_ctiles);
     note_launch();
     return cudaGetLastError();
 }
