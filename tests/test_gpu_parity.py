@@ -95,6 +95,32 @@ def test_decode_full_size_matches_oracle():
     check_layer(wl, d, out, cfin, sfin)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_one_token_batches_with_empty_sequences(dt):
+    """One-token batches (the persistent bulk-copy decode path) with empty
+    sequences mixed in, out of place and carried in place over two steps."""
+    lens = (1, 0, 1, 1, 0, 0, 1, 1, 1, 0, 1)
+    wl = W.scaled(W.WORKLOADS["decode"], lens, dtype=dt, H=8, HQ=4)
+    d = W.make_inputs(wl, DEV)
+    keep = d["state_init"].clone()
+    out, cfin, sfin = run_layer(wl, d, offsets_host=d["offsets_list"])
+    check_layer(wl, d, out, cfin, sfin)
+    # empty sequences carry their state through unchanged
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.equal(sfin[b], keep[b])
+    # a second step in place from the first step's states
+    d2 = W.make_inputs(wl, DEV, seed=wl.seed + 1)
+    d2["state_init"] = sfin.clone()
+    d2["conv_init"] = cfin.clone()
+    ref = oracle_layer(wl, d2)
+    st = d2["state_init"]
+    out2, cfin2, sfin2 = run_layer(wl, d2, offsets_host=d2["offsets_list"], state_fin=st,
+                                   conv_fin=d2["conv_init"])
+    assert sfin2.data_ptr() == st.data_ptr()
+    check_layer(wl, d2, out2, cfin2, sfin2, ref=ref)
+
+
 # ------------------------------------------------------------------ standalone ops
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])

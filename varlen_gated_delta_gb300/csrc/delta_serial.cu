@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(kSerialThreads)
     };
     auto store4 = [&](float *base, int k0, const float *src) {
         if constexpr (VEC4) {
-            if (k0 < K) *reinterpret_cast<float4 *>(base + k0) = make_float4(src[0], src[1], src[2], src[3]);
+            if (k0 < K)  // streaming store: the state is not read again by this call
+                __stcs(reinterpret_cast<float4 *>(base + k0), make_float4(src[0], src[1], src[2], src[3]));
         } else {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
