@@ -561,10 +561,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int m2 = 0; m2 < 2; ++m2) {
                     if (m2 > mi) break;
                     float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int k0 = c0; k0 < 32; k0 += 8)
-                        mma_tf32_16x8x8<1, kAtStride, kTStride>(x, sAt + k0 * kAtStride + 32 + 16 * m2,
-                                                                sT + k0 * kTStride + c0, g, tg);
+#pragma unroll
+                    for (int k0 = 0; k0 < 32; k0 += 8)
+                        if (k0 >= c0)
+                            mma_tf32_16x8x8<1, kAtStride, kTStride>(x, sAt + k0 * kAtStride + 32 + 16 * m2,
+                                                                    sT + k0 * kTStride + c0, g, tg);
                     float *xr = xs + 16 * m2 * kTStride;
                     *reinterpret_cast<float2 *>(xr + g * kTStride + 2 * tg) = make_float2(x[0], x[1]);
                     *reinterpret_cast<float2 *>(xr + (g + 8) * kTStride + 2 * tg) = make_float2(x[2], x[3]);
@@ -573,9 +574,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // T[32 + 16 mi + r][c0 + n] = -sum_k T2[16 mi + r][k] X2[k][n], k < 16 mi + 16
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
                 const float *t2 = sT + (32 + 16 * mi) * kTStride + 32;
-#pragma unroll 1
-                for (int k0 = 0; k0 < 16 * mi + 16; k0 += 8)
-                    mma_tf32_16x8x8<kTStride, 1, kTStride>(d, t2 + k0, xs + k0 * kTStride, g, tg);
+#pragma unroll
+                for (int k0 = 0; k0 < 32; k0 += 8)
+                    if (k0 < 16 * mi + 16)
+                        mma_tf32_16x8x8<kTStride, 1, kTStride>(d, t2 + k0, xs + k0 * kTStride, g, tg);
 #pragma unroll
                 for (int u2 = 0; u2 < 4; ++u2) d[u2] = -d[u2];
                 const int cc = c0 + 2 * tg;
