@@ -42,6 +42,11 @@ def _load():
         lib.oracle_delta_varlen.argtypes = [dp, dp, dp, ip, dp, dp, dp] + [i] * 6 + [ctypes.c_double]
         lib.oracle_layer_varlen.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [i] * 9
                                             + [ctypes.c_double, i])
+        lib.oracle_delta_varlen_capture.argtypes = ([dp, dp, dp, ip, dp, dp, dp, ip, ip, dp]
+                                                    + [i] * 6 + [ctypes.c_double, i])
+        lib.oracle_conv_capture.argtypes = [dp, ip, ip, dp] + [i] * 4
+        lib.oracle_layer_varlen_capture.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [ip, ip, dp, dp]
+                                                    + [i] * 9 + [ctypes.c_double, i, i])
         lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -162,6 +167,78 @@ def layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_i
         B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype])
     _check(rc, "layer_varlen")
     return out, conv_fin, state_fin
+
+
+def _active(active):
+    return None if active is None else _i32([int(active)])
+
+
+def delta_varlen_capture(y, qk, gb, offsets, state_init, H, HQ, K, V, counts, cap,
+                         active=None, scale=0.0):
+    """Recurrence with the compact capsule of the first captured tokens.
+
+    Returns (out, state_fin, capsule [B, cap*(H + HQ*K + H*V)]).  ``active``
+    None means no active flag; 0 disables the capture."""
+    y, qk, gb, state_init = map(_f64, (y, qk, gb, state_init))
+    offsets, counts, act = _i32(offsets), _i32(counts), _active(active)
+    N = y.shape[0]
+    B = offsets.size - 1
+    out = np.zeros((N, H, V))
+    fin = np.zeros((B, H, V, K))
+    capsule = np.zeros((B, cap * (H + HQ * K + H * V)))
+    rc = _load().oracle_delta_varlen_capture(
+        _p(y), _p(qk), _p(gb), _pi(offsets), _p(state_init), _p(out), _p(fin), _pi(counts),
+        _pi(act) if act is not None else None, _p(capsule), B, N, H, HQ, K, V, float(scale), cap)
+    _check(rc, "delta_varlen_capture")
+    return out, fin, capsule
+
+
+def conv_capture(x, offsets, counts, cap):
+    """Conv capture: updates [B, cap, C] of the first captured raw input rows."""
+    x = _f64(x)
+    offsets, counts = _i32(offsets), _i32(counts)
+    N, C = x.shape
+    B = offsets.size - 1
+    upd = np.zeros((B, cap, C))
+    rc = _load().oracle_conv_capture(_p(x), _pi(offsets), _pi(counts), _p(upd), B, N, C, cap)
+    _check(rc, "conv_capture")
+    return upd
+
+
+def layer_varlen_capture(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init,
+                         H, HQ, K, V, Kc, D, counts, cap, active=None, silu=True, scale=0.0,
+                         act_dtype="bf16"):
+    """The layer with capture.  Returns (out, conv_fin, state_fin, conv_updates, capsule)."""
+    qkv, w, a, b, A_log, dt_bias, conv_init, state_init = map(
+        _f64, (qkv, w, a, b, A_log, dt_bias, conv_init, state_init))
+    bias = _f64(bias)
+    offsets, counts, act = _i32(offsets), _i32(counts), _active(active)
+    N = qkv.shape[0]
+    B = offsets.size - 1
+    C = 2 * HQ * K + H * V
+    L = (Kc - 1) * D
+    out = np.zeros((N, H, V))
+    conv_fin = np.zeros((B, C, L))
+    state_fin = np.zeros((B, H, V, K))
+    upd = np.zeros((B, cap, C))
+    capsule = np.zeros((B, cap * (H + HQ * K + H * V)))
+    rc = _load().oracle_layer_varlen_capture(
+        _p(qkv), _p(w), _p(bias), _p(a), _p(b), _p(A_log), _p(dt_bias), _pi(offsets),
+        _p(conv_init), _p(conv_fin), _p(state_init), _p(out), _p(state_fin), _pi(counts),
+        _pi(act) if act is not None else None, _p(upd), _p(capsule),
+        B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype], cap)
+    _check(rc, "layer_varlen_capture")
+    return out, conv_fin, state_fin, upd, capsule
+
+
+def capsule_blocks(capsule, cap, H, HQ, K, V):
+    """Split a capsule [B, cap*(H+HQ*K+H*V)] into (g [B,cap,H], k [B,cap,HQ,K], delta [B,cap,H,V])."""
+    capsule = np.asarray(capsule)
+    B = capsule.shape[0]
+    g = capsule[:, :cap * H].reshape(B, cap, H)
+    k = capsule[:, cap * H:cap * (H + HQ * K)].reshape(B, cap, HQ, K)
+    d = capsule[:, cap * (H + HQ * K):].reshape(B, cap, H, V)
+    return g, k, d
 
 
 def delta_unrolled(q, k, v, g, beta, S0, scale):

@@ -22,6 +22,10 @@
  *       per (sequence, value head, state row): decay the state, retrieve
  *       with the decayed state, beta-scaled delta, rank-1 update, read out
  *       the updated state with q, multiply by scale; key head kh = h/(H/HQ).
+ *   [paged_ssm.rs, CONV_CAPTURE_* and DELTA_CAPTURE_* kernels]
+ *       capture of the first min(counts[b], capacity, len) tokens' updates:
+ *       raw conv input rows and the (g, normalised k, beta-scaled delta)
+ *       capsule from which S <- g S + delta k^T replays the prefix.
  *
  * Readings where the pages leave a step open are listed at each function.
  * Status codes: 0 ok, 2 bad shape, 4 malformed offsets.
@@ -188,21 +192,40 @@ int oracle_prepare(const double *y, const double *a, const double *bl,
  * That is S_t = g_t S_{t-1} + beta_t (v_t - g_t S_{t-1} k_t) k_t^T and
  * o_t = S_t (scale q_t), with value head h reading key head h / (H/HQ).
  */
-int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
-                        const int32_t *offsets, const double *init, double *out,
-                        double *fin, int B, int N, int H, int HQ, int K, int V,
-                        double scale) {
+/* Number of leading tokens of sequence b whose updates are captured:
+ * max(0, min(counts[b], cap, len)), or 0 when an active flag is given and is 0
+ * (paged_ssm.rs, DELTA_CAPTURE_INIT / CONV_CAPTURE_INIT). */
+static int captured_tokens(const int32_t *counts, const int32_t *active, int cap, int b,
+                           int len) {
+    if (active && active[0] == 0) return 0;
+    int n = counts[b];
+    if (n > cap) n = cap;
+    if (n > len) n = len;
+    return n > 0 ? n : 0;
+}
+
+/* The recurrence, optionally writing the compact capsule of the first
+ * captured tokens (capsule == NULL: no capture). */
+static int delta_recurrence(const double *y, const double *qk, const double *gb,
+                            const int32_t *offsets, const double *init, double *out,
+                            double *fin, int B, int N, int H, int HQ, int K, int V,
+                            double scale, const int32_t *counts, const int32_t *active,
+                            double *capsule, int cap) {
     if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ)
         return ORACLE_ERR_SHAPE;
     if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
     if (scale == 0.0) scale = 1.0 / sqrt((double)K);
     const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
     const int G = H / HQ;
+    const size_t width = (size_t)H + (size_t)HQ * K + (size_t)H * V;  /* per captured token */
+    if (capsule) memset(capsule, 0, sizeof(double) * (size_t)B * cap * width);
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < H; ++h) {
             const int kh = h / G;
             const int s = offsets[b], e = offsets[b + 1];
+            const int ncap = capsule ? captured_tokens(counts, active, cap, b, e - s) : 0;
+            double *cb = capsule ? capsule + (size_t)b * cap * width : NULL;
             double *S = (double *)malloc(sizeof(double) * (size_t)V * K);
             memcpy(S, init + ((size_t)b * H + h) * V * K, sizeof(double) * (size_t)V * K);
             for (int t = s; t < e; ++t) {
@@ -210,6 +233,13 @@ int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
                 const double *k = qk + (((size_t)N + t) * HQ + kh) * K;
                 const double g = gb[(size_t)t * H + h];
                 const double beta = gb[((size_t)N + t) * H + h];
+                const int slot = t - s;
+                if (slot < ncap) {  /* g of the head; k of the key head (its first value head) */
+                    cb[(size_t)slot * H + h] = g;
+                    if (h == kh * G)
+                        for (int i = 0; i < K; ++i)
+                            cb[(size_t)cap * H + ((size_t)slot * HQ + kh) * K + i] = k[i];
+                }
                 for (int vi = 0; vi < V; ++vi) {
                     double *row = S + (size_t)vi * K;
                     double retrieval = 0.0;
@@ -220,6 +250,8 @@ int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
                     double delta = y[(size_t)t * W + (size_t)2 * HQ * K + (size_t)h * V + vi];
                     delta -= retrieval;
                     delta *= beta;
+                    if (slot < ncap)  /* the beta-scaled delta of this state row */
+                        cb[(size_t)cap * (H + (size_t)HQ * K) + ((size_t)slot * H + h) * V + vi] = delta;
                     double readout = 0.0;
                     for (int i = 0; i < K; ++i) {
                         row[i] += k[i] * delta;
@@ -231,6 +263,57 @@ int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
             memcpy(fin + ((size_t)b * H + h) * V * K, S, sizeof(double) * (size_t)V * K);
             free(S);
         }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
+                        const int32_t *offsets, const double *init, double *out,
+                        double *fin, int B, int N, int H, int HQ, int K, int V,
+                        double scale) {
+    return delta_recurrence(y, qk, gb, offsets, init, out, fin, B, N, H, HQ, K, V, scale,
+                            NULL, NULL, NULL, 0);
+}
+
+/*
+ * [paged_ssm.rs, DELTA kernel with DELTA_CAPTURE_INIT / DELTA_CAPTURE_STEP;
+ *  GatedDeltaNet handler, state_update_capacity in [0, 8]]
+ * The recurrence of oracle_delta_varlen plus the compact transition capsule
+ *   capsule [B, cap * (H + HQ*K + H*V)], per sequence b and slot i < captured:
+ *     [i*H + h]                              g of token start+i, value head h
+ *     [cap*H + (i*HQ + kh)*K + ki]           normalised k of key head kh
+ *     [cap*(H + HQ*K) + (i*H + h)*V + vi]    beta-scaled delta of state row vi
+ *   and zero in every other slot; captured = max(0, min(counts[b], cap, len)),
+ *   or 0 for every sequence when active is given and active[0] == 0.
+ * Replaying S <- g S + delta k^T over the captured slots from the initial
+ * state gives the state after those tokens.
+ */
+int oracle_delta_varlen_capture(const double *y, const double *qk, const double *gb,
+                                const int32_t *offsets, const double *init, double *out,
+                                double *fin, const int32_t *counts, const int32_t *active,
+                                double *capsule, int B, int N, int H, int HQ, int K, int V,
+                                double scale, int cap) {
+    if (cap < 1 || cap > 8 || !counts || !capsule) return ORACLE_ERR_SHAPE;
+    return delta_recurrence(y, qk, gb, offsets, init, out, fin, B, N, H, HQ, K, V, scale,
+                            counts, active, capsule, cap);
+}
+
+/*
+ * [paged_ssm.rs, CONV_CAPTURE_INIT / CONV_CAPTURE_STEP]
+ *   updates [B, cap, C]: row i < captured of sequence b is the raw input
+ *   x[start_b + i, :]; every other row is zero.  captured = max(0,
+ *   min(counts[b], cap, len)); the conv operator has no active flag.
+ */
+int oracle_conv_capture(const double *x, const int32_t *offsets, const int32_t *counts,
+                        double *updates, int B, int N, int C, int cap) {
+    if (B < 1 || N < 0 || C < 1 || cap < 1 || cap > 8) return ORACLE_ERR_SHAPE;
+    if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
+    for (int b = 0; b < B; ++b) {
+        const int s = offsets[b];
+        const int n = captured_tokens(counts, NULL, cap, b, offsets[b + 1] - s);
+        for (int i = 0; i < cap; ++i)
+            for (int c = 0; c < C; ++c)
+                updates[((size_t)b * cap + i) * C + c] = i < n ? x[(size_t)(s + i) * C + c] : 0.0;
     }
     return ORACLE_OK;
 }
@@ -262,6 +345,38 @@ int oracle_layer_varlen(const double *qkv, const double *w, const double *bias,
     if (!rc) rc = oracle_prepare(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V);
     if (!rc) rc = oracle_delta_varlen(y, qk, gb, offsets, state_init, out, state_fin,
                                       B, N, H, HQ, K, V, scale);
+    free(y);
+    free(qk);
+    free(gb);
+    return rc;
+}
+
+/*
+ * The layer with capture: conv capture of the raw qkv rows and the delta
+ * capsule (both operators of paged_ssm.rs with state_update_capacity = cap),
+ * composed like oracle_layer_varlen.
+ */
+int oracle_layer_varlen_capture(const double *qkv, const double *w, const double *bias,
+                                const double *a, const double *bl, const double *A_log,
+                                const double *dt_bias, const int32_t *offsets,
+                                const double *conv_init, double *conv_fin,
+                                const double *state_init, double *out, double *state_fin,
+                                const int32_t *counts, const int32_t *active,
+                                double *conv_updates, double *capsule, int B, int N, int H,
+                                int HQ, int K, int V, int Kc, int D, int silu, double scale,
+                                int act_dtype, int cap) {
+    if (H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
+    const int C = 2 * HQ * K + H * V;
+    double *y = (double *)malloc(sizeof(double) * ((size_t)N * C + 1));
+    double *qk = (double *)malloc(sizeof(double) * ((size_t)2 * N * HQ * K + 1));
+    double *gb = (double *)malloc(sizeof(double) * ((size_t)2 * N * H + 1));
+    int rc = oracle_conv1d_varlen(qkv, w, bias, offsets, conv_init, y, conv_fin, B, N,
+                                  C, Kc, D, silu, act_dtype);
+    if (!rc) rc = oracle_conv_capture(qkv, offsets, counts, conv_updates, B, N, C, cap);
+    if (!rc) rc = oracle_prepare(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V);
+    if (!rc) rc = oracle_delta_varlen_capture(y, qk, gb, offsets, state_init, out, state_fin,
+                                              counts, active, capsule, B, N, H, HQ, K, V,
+                                              scale, cap);
     free(y);
     free(qk);
     free(gb);

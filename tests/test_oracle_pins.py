@@ -419,3 +419,102 @@ def test_layer_matches_unrolled_product_end_to_end():
                                              1.0 / math.sqrt(wl.K))
             np.testing.assert_allclose(out[s:e, h], o_u, rtol=1e-10, atol=1e-12)
             np.testing.assert_allclose(sfin[b, h], S_u, rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------------ state-update capture
+# paged_ssm.rs, CONV_CAPTURE_* and DELTA_CAPTURE_* (state_update_capacity): the
+# capsule holds per captured token the decay g, the normalised key and the
+# beta-scaled delta, so that a caller can replay S <- g S + delta k^T.
+
+def _capture_problem(seed, lens, H=4, HQ=2, K=8, V=6):
+    rng = _rng(seed)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N, B = int(offs[-1]), len(lens)
+    W = 2 * HQ * K + H * V
+    y = rng.standard_normal((N, W))
+    qk = rng.standard_normal((2, N, HQ, K))
+    qk /= np.linalg.norm(qk, axis=-1, keepdims=True)
+    gb = np.stack([rng.uniform(0.2, 1.0, (N, H)), rng.uniform(0.0, 1.0, (N, H))])
+    init = rng.standard_normal((B, H, V, K)) * 0.3
+    return offs, y, qk, gb, init
+
+
+def test_capsule_replays_the_state_of_the_captured_prefix():
+    lens, counts, cap = [5, 0, 12, 1, 3], [3, 4, 8, 2, -1], 4
+    H, HQ, K, V = 4, 2, 8, 6
+    offs, y, qk, gb, init = _capture_problem(11, lens, H, HQ, K, V)
+    _, _, capsule = oracle.delta_varlen_capture(y, qk, gb, offs, init, H, HQ, K, V, counts, cap)
+    g, k, d = oracle.capsule_blocks(capsule, cap, H, HQ, K, V)
+    for b, n in enumerate(lens):
+        m = max(0, min(counts[b], cap, n))
+        s = offs[b]
+        # the state after the first m tokens, from the recurrence on that prefix alone
+        _, fin_m = oracle.delta_varlen(y[s:s + m], qk[:, s:s + m], gb[:, s:s + m],
+                                       [0, m], init[b:b + 1], H, HQ, K, V)
+        for h in range(H):
+            S = init[b, h].copy()
+            for i in range(m):
+                S = g[b, i, h] * S + np.outer(d[b, i, h], k[b, i, h // (H // HQ)])
+            np.testing.assert_allclose(S, fin_m[0, h], rtol=1e-12, atol=1e-12)
+        # slots past the captured prefix stay zero
+        assert not g[b, m:].any() and not k[b, m:].any() and not d[b, m:].any()
+    # the captured g and k are the recurrence's inputs of those tokens
+    np.testing.assert_array_equal(g[2, :4], gb[0, offs[2]:offs[2] + 4])
+    np.testing.assert_array_equal(k[2, :4], qk[1, offs[2]:offs[2] + 4])
+
+
+def test_capsule_leaves_outputs_unchanged_and_active_flag_disables_it():
+    lens, cap = [4, 7], 8
+    H, HQ, K, V = 4, 2, 8, 6
+    offs, y, qk, gb, init = _capture_problem(12, lens, H, HQ, K, V)
+    out, fin = oracle.delta_varlen(y, qk, gb, offs, init, H, HQ, K, V)
+    o1, f1, c1 = oracle.delta_varlen_capture(y, qk, gb, offs, init, H, HQ, K, V, [9, 9], cap)
+    o2, f2, c2 = oracle.delta_varlen_capture(y, qk, gb, offs, init, H, HQ, K, V, [9, 9], cap,
+                                             active=1)
+    _, _, c0 = oracle.delta_varlen_capture(y, qk, gb, offs, init, H, HQ, K, V, [9, 9], cap,
+                                           active=0)
+    np.testing.assert_array_equal(o1, out)
+    np.testing.assert_array_equal(f1, fin)
+    np.testing.assert_array_equal(c1, c2)
+    assert not c0.any()
+    # counts above the length capture the whole sequence and nothing more
+    g, _, _ = oracle.capsule_blocks(c1, cap, H, HQ, K, V)
+    assert g[0, :4].all() and not g[0, 4:].any() and g[1, :7].all() and not g[1, 7:].any()
+
+
+def test_conv_capture_rows_end_in_the_final_conv_state():
+    # a sequence captured whole (len <= cap, len >= L): its last L captured
+    # rows are the final conv state the conv operator emits
+    rng = _rng(13)
+    lens, C, Kc, D, cap = [5, 2, 7], 6, 3, 1, 8
+    L = (Kc - 1) * D
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x = rng.standard_normal((offs[-1], C))
+    w = rng.standard_normal((C, Kc))
+    init = rng.standard_normal((len(lens), C, L))
+    _, fin = oracle.conv1d_varlen(x, w, None, offs, init, Kc, D, silu=False)
+    upd = oracle.conv_capture(x, offs, [8, 8, 3], cap)
+    for b, n in enumerate(lens):
+        m = min(8 if b < 2 else 3, n)
+        if m == n and n >= L:
+            np.testing.assert_array_equal(upd[b, n - L:n].T, fin[b])
+        assert not upd[b, m:].any()
+    np.testing.assert_array_equal(upd[2, :3], x[offs[2]:offs[2] + 3])
+
+
+def test_layer_capture_is_the_composition_of_the_operator_captures():
+    wl = workloads.scaled(workloads.WORKLOADS["tiny"], (3, 0, 9))
+    d = workloads.make_inputs(wl)
+    args = (d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+            d["offsets_list"], d["conv_init"], d["state_init"], wl.H, wl.HQ, wl.K, wl.V, wl.Kc,
+            wl.D)
+    out, cfin, sfin = oracle.layer_varlen(*args, act_dtype="f32")
+    o2, c2, s2, upd, capsule = oracle.layer_varlen_capture(*args, [2, 5, 6], 4, act_dtype="f32")
+    np.testing.assert_array_equal(o2, out)
+    np.testing.assert_array_equal(c2, cfin)
+    np.testing.assert_array_equal(s2, sfin)
+    np.testing.assert_array_equal(
+        upd, oracle.conv_capture(d["qkv"].double().numpy(), d["offsets_list"], [2, 5, 6], 4))
+    g, k, dl = oracle.capsule_blocks(capsule, 4, wl.H, wl.HQ, wl.K, wl.V)
+    assert g[0, :2].all() and not g[0, 2:].any() and not g[1].any() and g[2].all()
+    np.testing.assert_allclose(np.linalg.norm(k[2], axis=-1), 1.0, rtol=1e-9)
