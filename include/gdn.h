@@ -254,6 +254,64 @@ GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void 
                                      int V, int Kc, int D, int act, float scale, int dtype,
                                      void *stream);
 
+/*
+ * State-update capture (paged_ssm.rs, onnxruntime-ep-mlx 0.31.1: kernels
+ * CONV_CAPTURE_INIT/STEP and DELTA_CAPTURE_INIT/STEP; attribute
+ * state_update_capacity in [0, 8], inputs capture_count [B] int32 and the
+ * optional state_update_active [1] int32).  A capture call is the plain call
+ * plus these arguments:
+ *
+ *   cap      capacity, 1 .. GDN_CAPTURE_MAX tokens per sequence
+ *   counts   device int32 [B]: tokens wanted per sequence; sequence b
+ *            captures max(0, min(counts[b], cap, len_b)) tokens
+ *   active   device int32 [1] or NULL; active[0] == 0 captures nothing
+ *            (the capsule is all zero).  The conv capture has no such flag.
+ *   updates / conv_updates
+ *            device T [B, cap, C] (C = the conv's channel count, WIDTH for
+ *            the layer): row i < captured of sequence b is the RAW input row
+ *            x[start_b + i, :] (before the conv); other rows are zero.
+ *   capsule  device fp32 [B, cap * (H + HQ*K + H*V)], per sequence:
+ *              [i*H + h]                             g of token start_b + i, value head h
+ *              [cap*H + (i*HQ + kh)*K + ki]          its normalised key of key head kh
+ *              [cap*(H + HQ*K) + (i*H + h)*V + vi]   beta-scaled delta of state row vi
+ *            for slots i < captured, zero elsewhere.  From the initial state,
+ *            S <- g S + delta k^T over the captured slots gives the state
+ *            after those tokens (a caller verifying several draft tokens can
+ *            advance the state to any accepted prefix).
+ *
+ * Buffers are caller-owned and fully written (zeros included); outputs and
+ * final states are the same as the plain call's.  The capsule of a sequence
+ * taken by the chunked path is computed by a token-serial replay of its
+ * captured prefix in fp32.  Errors: GDN_ERR_SHAPE for cap outside [1, 8],
+ * GDN_ERR_NULL for a missing counts or capture buffer, GDN_ERR_OVERFLOW for
+ * buffers above int32 elements, then the plain call's errors.
+ */
+#define GDN_CAPTURE_MAX 8
+
+GDN_API int gdn_conv1d_varlen_capture(const void *x, const void *w, const void *bias,
+                                      const int32_t *offsets, const void *conv_init, void *y,
+                                      void *conv_fin, int cap, const int32_t *counts,
+                                      void *updates, int B, int N, int C, int Kc, int D, int act,
+                                      int dtype, void *stream);
+
+GDN_API int gdn_delta_varlen_capture(const void *y, const float *qk_norm, const float *g_beta,
+                                     const int32_t *offsets, const float *state_init, void *out,
+                                     float *state_fin, int cap, const int32_t *counts,
+                                     const int32_t *active, float *capsule, int B, int N, int H,
+                                     int HQ, int K, int V, float scale, int dtype, void *stream);
+
+/* conv_updates or capsule may be NULL (that capture is skipped), not both. */
+GDN_API int gdn_layer_varlen_capture(const void *qkv, const void *w, const void *bias,
+                                     const float *a, const float *b, const float *A_log,
+                                     const float *dt_bias, const int32_t *offsets,
+                                     const int32_t *offsets_host, const void *conv_init,
+                                     void *conv_fin, const float *state_init, void *out,
+                                     float *state_fin, int cap, const int32_t *counts,
+                                     const int32_t *active, void *conv_updates, float *capsule,
+                                     int B, int N, int H, int HQ, int K, int V, int Kc, int D,
+                                     int act, float scale, int dtype, void *workspace,
+                                     size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

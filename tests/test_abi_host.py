@@ -164,3 +164,39 @@ def test_kernel_events_hook_validates_id(lib):
     assert lib.gdn_set_kernel_events(3, None, None) == 2
     assert lib.gdn_set_kernel_events(-1, None, None) == 2
     assert lib.gdn_set_kernel_events(0, None, None) == 0
+
+
+def _layer_capture(lib, cap=4, counts=FAKE, active=None, conv_updates=FAKE, capsule=FAKE, **kw):
+    args = dict(qkv=FAKE, w=FAKE, bias=None, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE,
+                offsets=FAKE, offsets_host=None, conv_init=FAKE, conv_fin=FAKE,
+                state_init=FAKE, out=FAKE, state_fin=FAKE)
+    tail = dict(B=2, N=16, H=4, HQ=2, K=16, V=16, Kc=4, D=1, act=1, scale=0.0, dtype=0,
+                ws=FAKE, ws_bytes=1 << 30, stream=None)
+    for k, v in kw.items():
+        (args if k in args else tail)[k] = v
+    return lib.gdn_layer_varlen_capture(*args.values(), cap, counts, active, conv_updates,
+                                        capsule, *tail.values())
+
+
+def test_capture_calls_validate_capacity_counts_and_buffers(lib):
+    for cap in (0, -1, 9):
+        assert _layer_capture(lib, cap=cap) == 2
+        assert b"capacity" in lib.gdn_last_error()
+    assert _layer_capture(lib, counts=None) == 1
+    assert _layer_capture(lib, conv_updates=None, capsule=None) == 1
+    # then the plain call's own checks
+    assert _layer_capture(lib, K=257) == 2
+    assert _layer_capture(lib, ws=None) == 8
+    assert _layer_capture(lib, B=1 << 20, H=64, HQ=64, K=128, V=256) == 3
+    # the standalone operators
+    conv = lambda cap, counts, upd: lib.gdn_conv1d_varlen_capture(
+        FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, cap, counts, upd, 2, 16, 8, 4, 1, 1, 0, None)
+    assert conv(9, FAKE, FAKE) == 2
+    assert conv(2, None, FAKE) == 1
+    assert conv(2, FAKE, None) == 1
+    delta = lambda cap, counts, capsule: lib.gdn_delta_varlen_capture(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cap, counts, None, capsule, 2, 16, 4, 2, 16,
+        16, 0.0, 0, None)
+    assert delta(0, FAKE, FAKE) == 2
+    assert delta(2, None, FAKE) == 1
+    assert delta(2, FAKE, None) == 1

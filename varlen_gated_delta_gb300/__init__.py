@@ -26,11 +26,13 @@ __all__ = [
     "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_chunk_min_len",
     "gdn_launch_count", "gdn_set_kernel_events", "GDN_KERNEL_CONV", "GDN_KERNEL_CHUNKED",
     "GDN_KERNEL_SERIAL", "GDN_F32", "GDN_BF16", "GDN_ACT_NONE", "GDN_ACT_SILU",
-    "STATUS_NAMES",
+    "STATUS_NAMES", "GDN_CAPTURE_MAX", "gdn_conv1d_varlen_capture", "gdn_delta_varlen_capture",
+    "gdn_layer_varlen_capture",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 GDN_F32, GDN_BF16 = 0, 1
+GDN_CAPTURE_MAX = 8
 GDN_ACT_NONE, GDN_ACT_SILU = 0, 1
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_OVERFLOW",
                 4: "GDN_ERR_OFFSETS", 5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA",
@@ -74,10 +76,14 @@ def load_library():
     lib.gdn_set_chunk_min_len.argtypes = [i]
     lib.gdn_chunk_min_len.restype = i
     lib.gdn_launch_count.restype = ctypes.c_uint64
+    lib.gdn_conv1d_varlen_capture.argtypes = [vp] * 7 + [i, vp, vp] + [i] * 7 + [vp]
+    lib.gdn_delta_varlen_capture.argtypes = [vp] * 7 + [i, vp, vp, vp] + [i] * 6 + [f, i, vp]
+    lib.gdn_layer_varlen_capture.argtypes = [vp] * 14 + [i, vp, vp, vp, vp] + [i] * 9 + [f, i, vp, sz, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
-                 "gdn_workspace_status", "gdn_set_chunk_min_len"):
+                 "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_conv1d_varlen_capture",
+                 "gdn_delta_varlen_capture", "gdn_layer_varlen_capture"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -281,3 +287,112 @@ def gdn_layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, sta
     del keep
     _check(rc)
     return out, conv_fin, state_fin
+
+
+# ------------------------------------------------------------------ state-update capture
+
+def _capture_ptrs(counts, active, cap, B, dev):
+    if not 1 <= int(cap) <= GDN_CAPTURE_MAX:
+        raise GdnError(2, f"capture capacity {cap} outside [1, {GDN_CAPTURE_MAX}]")
+    return (_ptr(counts, "counts", torch.int32, (B,), dev),
+            _ptr(active, "active", torch.int32, (1,), dev))
+
+
+def gdn_conv1d_varlen_capture(x, w, bias, offsets, conv_init, counts, *, cap, Kc, D=1,
+                              act=GDN_ACT_SILU, y=None, conv_fin=None, updates=None):
+    """Conv with capture of the first raw input rows.  Returns (y, conv_fin, updates [B,cap,C])."""
+    lib = load_library()
+    N, C = x.shape
+    B = offsets.numel() - 1
+    L = (Kc - 1) * D
+    T = x.dtype
+    dev = x.device
+    y = torch.empty((N, C), dtype=T, device=dev) if y is None else y
+    conv_fin = torch.empty((B, C, L), dtype=T, device=dev) if conv_fin is None else conv_fin
+    updates = torch.empty((B, cap, C), dtype=T, device=dev) if updates is None else updates
+    cp, _ = _capture_ptrs(counts, None, cap, B, dev)
+    args = [_ptr(x, "x", T, (N, C), dev), _ptr(w, "w", T, (C, Kc), dev),
+            _ptr(bias, "bias", T, (C,), dev), _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
+            _ptr(conv_init, "conv_init", T, (B, C, L), dev), _ptr(y, "y", T, (N, C), dev),
+            _ptr(conv_fin, "conv_fin", T, (B, C, L), dev), int(cap), cp,
+            _ptr(updates, "updates", T, (B, cap, C), dev)]
+    _check(lib.gdn_conv1d_varlen_capture(*args, B, N, C, Kc, D, act, _dtype_code(x), _stream(dev)))
+    return y, conv_fin, updates
+
+
+def gdn_delta_varlen_capture(y, qk_norm, g_beta, offsets, state_init, counts, *, cap, H, HQ, K,
+                             V, active=None, scale=0.0, out=None, state_fin=None, capsule=None):
+    """Recurrence with the compact capsule.  Returns (out, state_fin, capsule [B, cap*(H+HQ*K+H*V)])."""
+    lib = load_library()
+    N = y.shape[0]
+    B = offsets.numel() - 1
+    dev = y.device
+    f32 = torch.float32
+    width = cap * (H + HQ * K + H * V)
+    out = torch.empty((N, H, V), dtype=y.dtype, device=dev) if out is None else out
+    state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev) if state_fin is None else state_fin
+    capsule = torch.empty((B, width), dtype=f32, device=dev) if capsule is None else capsule
+    cp, ap = _capture_ptrs(counts, active, cap, B, dev)
+    W = 2 * HQ * K + H * V
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
+            _ptr(g_beta, "g_beta", f32, (2, N, H), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", y.dtype, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev), int(cap), cp, ap,
+            _ptr(capsule, "capsule", f32, (B, width), dev)]
+    _check(lib.gdn_delta_varlen_capture(*args, B, N, H, HQ, K, V, float(scale), _dtype_code(y),
+                                        _stream(dev)))
+    return out, state_fin, capsule
+
+
+def gdn_layer_varlen_capture(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init,
+                             counts, *, cap, H, HQ, K, V, Kc=4, D=1, act=GDN_ACT_SILU, scale=0.0,
+                             active=None, offsets_host=None, out=None, conv_fin=None,
+                             state_fin=None, conv_updates=None, capsule=None, workspace=None,
+                             want_conv_updates=True, want_capsule=True):
+    """The layer with state-update capture.
+
+    Returns (out, conv_fin, state_fin, conv_updates [B,cap,WIDTH] T or None,
+    capsule [B, cap*(H+HQ*K+H*V)] f32 or None)."""
+    lib = load_library()
+    N, W = qkv.shape
+    B = offsets.numel() - 1
+    L = (Kc - 1) * D
+    T = qkv.dtype
+    dev = qkv.device
+    f32 = torch.float32
+    dcode = _dtype_code(qkv)
+    if W != 2 * HQ * K + H * V:
+        raise GdnError(2, f"qkv width {W} != 2*HQ*K + H*V = {2 * HQ * K + H * V}")
+    out = torch.empty((N, H, V), dtype=T, device=dev) if out is None else out
+    conv_fin = torch.empty((B, W, L), dtype=T, device=dev) if conv_fin is None else conv_fin
+    state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev) if state_fin is None else state_fin
+    width = cap * (H + HQ * K + H * V)
+    if conv_updates is None and want_conv_updates:
+        conv_updates = torch.empty((B, cap, W), dtype=T, device=dev)
+    if capsule is None and want_capsule:
+        capsule = torch.empty((B, width), dtype=f32, device=dev)
+    need = gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dcode)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    cp, ap = _capture_ptrs(counts, active, cap, B, dev)
+    hp, keep = _host_offsets(offsets_host)
+    args = [_ptr(qkv, "qkv", T, (N, W), dev), _ptr(w, "w", T, (W, Kc), dev),
+            _ptr(bias, "bias", T, (W,), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
+            _ptr(dt_bias, "dt_bias", f32, (H,), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev), hp,
+            _ptr(conv_init, "conv_init", T, (B, W, L), dev),
+            _ptr(conv_fin, "conv_fin", T, (B, W, L), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", T, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev), int(cap), cp, ap,
+            _ptr(conv_updates, "conv_updates", T, (B, cap, W), dev),
+            _ptr(capsule, "capsule", f32, (B, width), dev)]
+    rc = lib.gdn_layer_varlen_capture(*args, B, N, H, HQ, K, V, Kc, D, act, float(scale), dcode,
+                                      _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                      _stream(dev))
+    del keep
+    _check(rc)
+    return out, conv_fin, state_fin, conv_updates, capsule

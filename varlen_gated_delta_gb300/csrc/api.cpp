@@ -134,6 +134,22 @@ static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) 
 
 using namespace gdn;
 
+// Optional state-update capture of a call (nullptr: none).
+struct Capture {
+    int cap;
+    const int32_t *counts;
+    const int32_t *active;
+    void *conv_updates;
+    float *capsule;
+};
+
+static int check_capture(const Capture &c, const char *what) {
+    if (c.cap < 1 || c.cap > GDN_CAPTURE_MAX)
+        return fail(GDN_ERR_SHAPE, "%s: capture capacity %d outside [1, %d]", what, c.cap, GDN_CAPTURE_MAX);
+    if (!c.counts) return fail(GDN_ERR_NULL, "%s: capture counts is NULL", what);
+    return GDN_OK;
+}
+
 extern "C" {
 
 int gdn_version(void) { return GDN_ABI_VERSION; }
@@ -157,10 +173,9 @@ int gdn_set_kernel_events(int kernel, void *start, void *stop) {
     return GDN_OK;
 }
 
-int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int32_t *offsets,
-                      const void *conv_init, void *y, void *conv_fin, int B, int N, int C, int Kc,
-                      int D, int act, int dtype, void *stream) {
-    g_err[0] = 0;
+static int conv_impl(const void *x, const void *w, const void *bias, const int32_t *offsets,
+                     const void *conv_init, void *y, void *conv_fin, int B, int N, int C, int Kc,
+                     int D, int act, int dtype, void *stream, const Capture *cap) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
     if (B < 1 || N < 0 || C < 1 || Kc < 1 || D < 1)
@@ -179,9 +194,34 @@ int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int3
     p.prep = 0;
     cudaError_t e = launch_conv(p, dtype, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "conv kernel launch");
-    e = launch_conv_final(x, offsets, conv_init, conv_fin, B, N, C, (int)L, dtype, s);
+    e = launch_conv_final(x, offsets, conv_init, conv_fin, B, N, C, (int)L, dtype, s,
+                          cap ? cap->cap : 0, cap ? cap->counts : nullptr,
+                          cap ? cap->conv_updates : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "conv final-state kernel launch");
     return GDN_OK;
+}
+
+int gdn_conv1d_varlen(const void *x, const void *w, const void *bias, const int32_t *offsets,
+                      const void *conv_init, void *y, void *conv_fin, int B, int N, int C, int Kc,
+                      int D, int act, int dtype, void *stream) {
+    g_err[0] = 0;
+    return conv_impl(x, w, bias, offsets, conv_init, y, conv_fin, B, N, C, Kc, D, act, dtype,
+                     stream, nullptr);
+}
+
+int gdn_conv1d_varlen_capture(const void *x, const void *w, const void *bias,
+                              const int32_t *offsets, const void *conv_init, void *y,
+                              void *conv_fin, int cap, const int32_t *counts, void *updates,
+                              int B, int N, int C, int Kc, int D, int act, int dtype,
+                              void *stream) {
+    g_err[0] = 0;
+    const Capture c{cap, counts, nullptr, updates, nullptr};
+    int rc = check_capture(c, "conv1d capture");
+    if (rc) return rc;
+    if (!updates) return fail(GDN_ERR_NULL, "conv1d capture: updates is NULL");
+    if ((long)B * cap * C > INT_MAX) return fail(GDN_ERR_OVERFLOW, "conv capture B*cap*C exceeds int32");
+    return conv_impl(x, w, bias, offsets, conv_init, y, conv_fin, B, N, C, Kc, D, act, dtype,
+                     stream, &c);
 }
 
 int gdn_prepare(const void *y, const float *a, const float *b, const float *A_log,
@@ -204,11 +244,10 @@ int gdn_prepare(const void *y, const float *a, const float *b, const float *A_lo
     return GDN_OK;
 }
 
-int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
-                     const int32_t *offsets, const float *state_init, void *out, float *state_fin,
-                     int B, int N, int H, int HQ, int K, int V, float scale, int dtype,
-                     void *stream) {
-    g_err[0] = 0;
+static int delta_impl(const void *y, const float *qk_norm, const float *g_beta,
+                      const int32_t *offsets, const float *state_init, void *out,
+                      float *state_fin, int B, int N, int H, int HQ, int K, int V, float scale,
+                      int dtype, void *stream, const Capture *cap) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     long width;
     int rc = check_heads(H, HQ, K, V, &width);
@@ -225,9 +264,37 @@ int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
     p.serial_max_len = INT_MAX;
     p.max_len = INT_MAX;
     p.conv_fin = nullptr;
+    if (cap) {
+        p.cap = cap->cap; p.counts = cap->counts; p.active = cap->active; p.capsule = cap->capsule;
+    }
     cudaError_t e = launch_delta_serial(p, dtype, static_cast<cudaStream_t>(stream), false);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
     return GDN_OK;
+}
+
+int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
+                     const int32_t *offsets, const float *state_init, void *out, float *state_fin,
+                     int B, int N, int H, int HQ, int K, int V, float scale, int dtype,
+                     void *stream) {
+    g_err[0] = 0;
+    return delta_impl(y, qk_norm, g_beta, offsets, state_init, out, state_fin, B, N, H, HQ, K,
+                      V, scale, dtype, stream, nullptr);
+}
+
+int gdn_delta_varlen_capture(const void *y, const float *qk_norm, const float *g_beta,
+                             const int32_t *offsets, const float *state_init, void *out,
+                             float *state_fin, int cap, const int32_t *counts,
+                             const int32_t *active, float *capsule, int B, int N, int H, int HQ,
+                             int K, int V, float scale, int dtype, void *stream) {
+    g_err[0] = 0;
+    const Capture c{cap, counts, active, nullptr, capsule};
+    int rc = check_capture(c, "delta capture");
+    if (rc) return rc;
+    if (!capsule) return fail(GDN_ERR_NULL, "delta capture: capsule is NULL");
+    if ((long)B * cap * ((long)H + (long)HQ * K + (long)H * V) > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "delta capsule size exceeds int32");
+    return delta_impl(y, qk_norm, g_beta, offsets, state_init, out, state_fin, B, N, H, HQ, K,
+                      V, scale, dtype, stream, &c);
 }
 
 size_t gdn_workspace_bytes(int B, int N, int H, int HQ, int K, int V, int Kc, int D, int dtype) {
@@ -254,13 +321,13 @@ int gdn_workspace_status(const void *workspace, int *counts, void *stream) {
     return h.status;
 }
 
-int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const float *a,
-                     const float *b, const float *A_log, const float *dt_bias,
-                     const int32_t *offsets, const int32_t *offsets_host, const void *conv_init,
-                     void *conv_fin, const float *state_init, void *out, float *state_fin, int B,
-                     int N, int H, int HQ, int K, int V, int Kc, int D, int act, float scale,
-                     int dtype, void *workspace, size_t ws_bytes, void *stream) {
-    g_err[0] = 0;
+static int layer_impl(const void *qkv, const void *w, const void *bias, const float *a,
+                      const float *b, const float *A_log, const float *dt_bias,
+                      const int32_t *offsets, const int32_t *offsets_host, const void *conv_init,
+                      void *conv_fin, const float *state_init, void *out, float *state_fin,
+                      int B, int N, int H, int HQ, int K, int V, int Kc, int D, int act,
+                      float scale, int dtype, void *workspace, size_t ws_bytes, void *stream,
+                      const Capture *cap) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
     long width;
@@ -301,8 +368,9 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     }
     // tokens of token-serial sequences need the prepare step; with host
     // offsets a batch of chunked sequences only skips it
+    const bool capsule = cap && cap->capsule;
     bool need_prep = true;
-    if (offsets_host) {
+    if (offsets_host && !capsule) {
         need_prep = false;
         for (int i = 0; i < B && !need_prep; ++i) {
             const int len = offsets_host[i + 1] - offsets_host[i];
@@ -326,6 +394,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     cp.prep = need_prep ? 1 : 0; cp.qk = qk; cp.gb = gb; cp.a = a; cp.bl = b; cp.A_log = A_log; cp.dt_bias = dt_bias;
     cp.H = H; cp.HQ = HQ; cp.K = K; cp.V = V; cp.prep_max_len = serial_max;
     cp.header = hdr; cp.chunk_min_len = serial_max;
+    cp.prep_cap = capsule ? cap->cap : 0;  // the captured prefix of chunked sequences
     cp.seq_order = run_chunked ? order : nullptr; cp.VT = V / 128;
     bool fused = false;
     mark_before(GDN_KERNEL_CONV, s);
@@ -340,7 +409,7 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
     const float eff_scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
-    if (run_chunked) {
+    auto launch_chunked = [&]() -> int {
         ChunkLaunch cl{};
         cl.y = y; cl.a = a; cl.bl = b; cl.A_log = A_log; cl.dt_bias = dt_bias;
         cl.offsets = offsets; cl.seq_order = order; cl.header = hdr;
@@ -348,15 +417,16 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
         cl.scale = eff_scale; cl.max_units = max_units;
         mark_before(GDN_KERNEL_CHUNKED, s);
-        e = launch_delta_chunked(cl, s);
+        cudaError_t ce = launch_delta_chunked(cl, s);
         mark_after(GDN_KERNEL_CHUNKED, s);
-        if (e != cudaSuccess) return cuda_fail(e, "chunked kernel launch");
-    }
+        if (ce != cudaSuccess) return cuda_fail(ce, "chunked kernel launch");
+        return GDN_OK;
+    };
 
     DeltaParams dp{};
     dp.y = y; dp.qk = qk; dp.gb = gb; dp.offsets = offsets; dp.state_init = state_init;
     dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;
-    dp.scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
+    dp.scale = eff_scale;
     dp.serial_max_len = serial_max;
     dp.max_len = INT_MAX;  // unknown without host offsets
     if (offsets_host) {
@@ -372,11 +442,61 @@ int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const flo
     // programmatic dependent launch, its state loads with the conv kernel
     dp.conv_x = qkv; dp.conv_init = conv_init; dp.conv_fin = L > 0 ? conv_fin : nullptr;
     dp.conv_L = (int)L;
+    if (cap) {
+        dp.cap = cap->cap; dp.counts = cap->counts; dp.active = cap->active;
+        dp.conv_updates = cap->conv_updates; dp.capsule = cap->capsule;
+    }
+    // With a capsule the token-serial kernel also replays the captured prefix
+    // of chunked sequences from their initial state, so it runs before the
+    // chunked kernel (which may overwrite that state in place).
+    const bool serial_first = capsule && run_chunked;
+    if (run_chunked && !serial_first) {
+        rc = launch_chunked();
+        if (rc) return rc;
+    }
     mark_before(GDN_KERNEL_SERIAL, s);
     e = launch_delta_serial(dp, dtype, s, /*pdl=*/true);
     mark_after(GDN_KERNEL_SERIAL, s);
     if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
+    if (serial_first) {
+        rc = launch_chunked();
+        if (rc) return rc;
+    }
     return GDN_OK;
+}
+
+int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const float *a,
+                     const float *b, const float *A_log, const float *dt_bias,
+                     const int32_t *offsets, const int32_t *offsets_host, const void *conv_init,
+                     void *conv_fin, const float *state_init, void *out, float *state_fin, int B,
+                     int N, int H, int HQ, int K, int V, int Kc, int D, int act, float scale,
+                     int dtype, void *workspace, size_t ws_bytes, void *stream) {
+    g_err[0] = 0;
+    return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
+                      conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act, scale,
+                      dtype, workspace, ws_bytes, stream, nullptr);
+}
+
+int gdn_layer_varlen_capture(const void *qkv, const void *w, const void *bias, const float *a,
+                             const float *b, const float *A_log, const float *dt_bias,
+                             const int32_t *offsets, const int32_t *offsets_host,
+                             const void *conv_init, void *conv_fin, const float *state_init,
+                             void *out, float *state_fin, int cap, const int32_t *counts,
+                             const int32_t *active, void *conv_updates, float *capsule, int B,
+                             int N, int H, int HQ, int K, int V, int Kc, int D, int act,
+                             float scale, int dtype, void *workspace, size_t ws_bytes,
+                             void *stream) {
+    g_err[0] = 0;
+    const Capture c{cap, counts, active, conv_updates, capsule};
+    int rc = check_capture(c, "layer capture");
+    if (rc) return rc;
+    if (!conv_updates && !capsule) return fail(GDN_ERR_NULL, "layer capture: no capture buffer given");
+    if ((long)B * cap * (2L * HQ * K + (long)H * V) > INT_MAX ||
+        (long)B * cap * ((long)H + (long)HQ * K + (long)H * V) > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "layer capture buffers exceed int32 elements");
+    return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
+                      conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act, scale,
+                      dtype, workspace, ws_bytes, stream, &c);
 }
 
 }  // extern "C"

@@ -63,6 +63,18 @@ __device__ __forceinline__ bool seq_bounds(const int32_t *offsets, int B, int N,
            end <= N;
 }
 
+// Tokens of a sequence of `len` whose state updates are captured
+// (paged_ssm.rs, *_CAPTURE_INIT): max(0, min(counts[b], cap, len)), or 0 when
+// an active flag is given and is 0.
+__device__ __forceinline__ int captured_tokens(const int32_t *counts, const int32_t *active,
+                                               int cap, int b, int len) {
+    if (active != nullptr && __ldg(active) == 0) return 0;
+    int n = __ldg(counts + b);
+    n = n < cap ? n : cap;
+    n = n < len ? n : len;
+    return n > 0 ? n : 0;
+}
+
 // Index of the sequence holding token t (0 <= t < offsets[B]): the largest b
 // in [0, B) with offsets[b] <= t.  For nondecreasing offsets that sequence is
 // not empty and offsets[b] <= t < offsets[b+1].

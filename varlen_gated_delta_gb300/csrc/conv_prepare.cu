@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(kConvThreads)
                 for (int e = 0; e < VEC; ++e) ss = fmaf(yv[e], yv[e], ss);
                 for (int off = lanes_per_head >> 1; off > 0; off >>= 1)
                     ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                if (cvalid && c < qk_width && s_len[i] < p.prep_max_len) {
+                if (cvalid && c < qk_width &&
+                    (s_len[i] < p.prep_max_len || t - s_start[i] < p.prep_cap)) {
                     const float r = rsqrtf(ss + 1e-12f);
                     const int plane = c >= p.HQ * p.K;
                     const int cc = c - plane * p.HQ * p.K;
@@ -372,8 +373,9 @@ __global__ void __launch_bounds__(kConvThreads)
         if (tile_c == 0) {
             for (int i = threadIdx.x; i < TT * p.H; i += blockDim.x) {
                 const int ti = i / p.H, h = i % p.H;
-                if (s_seq[ti] < 0 || s_len[ti] >= p.prep_max_len) continue;
                 const int t = t0 + ti;
+                if (s_seq[ti] < 0 || (s_len[ti] >= p.prep_max_len && t - s_start[ti] >= p.prep_cap))
+                    continue;
                 float g, beta;
                 decay_rate(p, t, h, g, beta);
                 p.gb[(size_t)t * p.H + h] = g;
@@ -521,9 +523,9 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                     asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
                     Vec16<T> cur;
                     cur.u = *reinterpret_cast<const uint4 *>(ring + (r & (kRing - 1)) * CT);
-                    float(&xc)[VEC] = win[ph];
+                    float(&xc)[VEC] = win[ph];  // lanes past C read the ring's zero fill
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) xc[q] = cvalid ? to_f32(cur.v[q]) : 0.f;
+                    for (int q = 0; q < VEC; ++q) xc[q] = to_f32(cur.v[q]);
                     // the slot is free again: stream in row r + kRing
                     {
                         const int rn = r + kRing;
@@ -565,7 +567,9 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                     }
                     if (cvalid) *reinterpret_cast<uint4 *>(y + (size_t)t * C + c) = yo.u;
                     if constexpr (PREP) {
-                        if (c0 < qk_width && e - s < p.prep_max_len) {  // warp-uniform
+                        // tokens of token-serial sequences, and the captured prefix
+                        const bool prep_t = e - s < p.prep_max_len || t - s < p.prep_cap;
+                        if (c0 < qk_width && prep_t) {  // warp-uniform
                             float yv[VEC];
 #pragma unroll
                             for (int q = 0; q < VEC; ++q) yv[q] = to_f32(yo.v[q]);
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                                 for (int q = 0; q < VEC; ++q) dst[q] = yv[q] * rr;
                             }
                         }
-                        if (tile_c == 0 && e - s < p.prep_max_len) {
+                        if (tile_c == 0 && prep_t) {
                             for (int h = lane; h < p.H; h += 32) {
                                 float g, beta;
                                 decay_rate(p, t, h, g, beta);
@@ -632,7 +636,8 @@ cudaError_t launch_conv_stream(const ConvParams &p, cudaStream_t s) {
 template <typename T>
 __global__ void __launch_bounds__(256)
     conv_final_kernel(const T *__restrict__ x, const int32_t *__restrict__ offsets,
-                      const T *init, T *fin, int B, int N, int C, int L) {
+                      const T *init, T *fin, int B, int N, int C, int L, int cap,
+                      const int32_t *counts, T *updates) {
     pdl_wait_primary();  // the conv kernel reads init before fin may overwrite it
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)B * C) return;
@@ -646,6 +651,11 @@ __global__ void __launch_bounds__(256)
         const int local = len - L + j;
         const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
         frow[j] = v;
+    }
+    if (updates != nullptr) {  // CONV_CAPTURE: first raw input rows, zero beyond
+        const int n = captured_tokens(counts, nullptr, cap, b, len);
+        T *upd = updates + (size_t)b * cap * C + c;
+        for (int k = 0; k < cap; ++k) upd[(size_t)k * C] = k < n ? x[(size_t)(s + k) * C + c] : from_f32<T>(0.f);
     }
 }
 
@@ -804,8 +814,8 @@ cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t s, bool *fu
 
 cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void *init,
                               void *fin, int B, int N, int C, int L, int dtype,
-                              cudaStream_t s) {
-    if (L == 0) return cudaSuccess;
+                              cudaStream_t s, int cap, const int32_t *counts, void *updates) {
+    if (L == 0 && updates == nullptr) return cudaSuccess;
     const long total = (long)B * C;
     const long blocks = (total + 255) / 256;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
@@ -814,12 +824,12 @@ cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void 
         using T = __nv_bfloat16;
         e = launch_kernel(conv_final_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, s, true,
                           static_cast<const T *>(x), offsets, static_cast<const T *>(init),
-                          static_cast<T *>(fin), B, N, C, L);
+                          static_cast<T *>(fin), B, N, C, L, cap, counts, static_cast<T *>(updates));
     } else {
         e = launch_kernel(conv_final_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, true,
                           static_cast<const float *>(x), offsets,
                           static_cast<const float *>(init), static_cast<float *>(fin), B, N, C,
-                          L);
+                          L, cap, counts, static_cast<float *>(updates));
     }
     note_launch();
     return e;

@@ -26,7 +26,7 @@ namespace {
 constexpr int kSerialThreads = 128;
 
 // Final conv state of sequence b for the channel slice `slice` of `nslices`:
-// fin[b,c,j] = x~(len - L + j).  One thread per channel walks j upward and
+// fin[b,c,j] = x~(len - L + j), and the conv capture rows when asked for.  One thread per channel walks j upward and
 // reads index len + j >= j of its own row before writing index j, so the
 // final state may alias the initial one.
 template <typename T>
@@ -41,12 +41,20 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
     const T *init = static_cast<const T *>(p.conv_init);
     T *fin = static_cast<T *>(p.conv_fin);
     for (size_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
-        const T *irow = init + ((size_t)b * C + c) * L;
-        T *frow = fin + ((size_t)b * C + c) * L;
-        for (int j = 0; j < L; ++j) {
-            const int local = len - L + j;
-            const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
-            frow[j] = v;
+        if (fin != nullptr) {
+            const T *irow = init + ((size_t)b * C + c) * L;
+            T *frow = fin + ((size_t)b * C + c) * L;
+            for (int j = 0; j < L; ++j) {
+                const int local = len - L + j;
+                const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
+                frow[j] = v;
+            }
+        }
+        if (p.conv_updates != nullptr) {  // CONV_CAPTURE: first raw input rows, zero beyond
+            const int n = captured_tokens(p.counts, nullptr, p.cap, b, len);
+            T *upd = static_cast<T *>(p.conv_updates) + (size_t)b * p.cap * C + c;
+            for (int i = 0; i < p.cap; ++i)
+                upd[(size_t)i * C] = i < n ? x[(size_t)(s + i) * C + c] : from_f32<T>(0.f);
         }
     }
 }
@@ -54,7 +62,9 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
 // PF: prefetch the next token's operands while applying the current one
 // (sequences of several tokens); without it (one token per sequence, decode)
 // the kernel needs fewer registers and more CTAs keep state loads in flight.
-template <typename T, int KP, int RG, bool VEC4, bool PF>
+// CAPT: write the compact capsule of the first captured tokens (and run the
+// captured prefix of sequences owned by the chunked kernel, outputs untouched).
+template <typename T, int KP, int RG, bool VEC4, bool PF, bool CAPT>
 __global__ void __launch_bounds__(kSerialThreads)
     delta_serial_kernel(const DeltaParams p) {
     constexpr int EPL = 16;          // state values per lane per row
@@ -111,11 +121,14 @@ __global__ void __launch_bounds__(kSerialThreads)
         }
     };
 
+    // captured tokens (CAPT; counts and active are inputs of the call, not of
+    // the previous kernel, so they are read before the dependency wait)
+    const int ncap = CAPT ? captured_tokens(p.counts, p.active, p.cap, b, e - s) : 0;
     float S[RG][EPL];
     const size_t head_base = ((size_t)b * H + h) * V;
 #pragma unroll
     for (int r = 0; r < RG; ++r) {
-        if (own && vi[r] < V) {
+        if ((own || ncap > 0) && vi[r] < V) {
             const float *row = p.state_init + (head_base + vi[r]) * K;
 #pragma unroll
             for (int m = 0; m < 4; ++m) load4(row, kidx[m], &S[r][4 * m]);
@@ -128,8 +141,35 @@ __global__ void __launch_bounds__(kSerialThreads)
     // The state loads above are in flight; everything below reads what the
     // conv/prepare kernel wrote (when launched as its PDL dependent).
     pdl_wait_primary();
-    if (p.conv_fin != nullptr) conv_final_slice<T>(p, b, s, e, h * nrb + rb, H * nrb, W);
-    if (!own) return;
+    if (p.conv_fin != nullptr || p.conv_updates != nullptr)
+        conv_final_slice<T>(p, b, s, e, h * nrb + rb, H * nrb, W);
+
+    // capsule blocks of this sequence (CAPT): g [cap][H], k [cap][HQ][K], delta [cap][H][V]
+    float *cap_g = nullptr, *cap_k = nullptr, *cap_d = nullptr;
+    const bool key_owner = rb == 0 && warp == 0 && rlane == 0 && h == kh * (H / HQ);
+    if constexpr (CAPT) {
+        const int cap = p.cap;
+        float *base = p.capsule + (size_t)b * cap * ((size_t)H + (size_t)HQ * K + (size_t)H * V);
+        cap_g = base;
+        cap_k = base + (size_t)cap * H;
+        cap_d = base + (size_t)cap * (H + (size_t)HQ * K);
+        for (int i = ncap; i < cap; ++i) {  // slots past the captured prefix are zero
+            if (rb == 0 && warp == 0 && lane == 0) cap_g[(size_t)i * H + h] = 0.f;
+            if (key_owner)
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (kidx[m] + u < K) cap_k[((size_t)i * HQ + kh) * K + kidx[m] + u] = 0.f;
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+                if (sub == 0 && vi[r] < V) cap_d[((size_t)i * H + h) * V + vi[r]] = 0.f;
+        }
+    }
+    if (!own && ncap == 0) return;
+    // the chunked kernel owns the outputs and final state of long sequences:
+    // only their captured prefix runs here
+    const int t_end = own ? e : s + ncap;
 
     const T *y = static_cast<const T *>(p.y);
     T *out = static_cast<T *>(p.out);
@@ -150,12 +190,12 @@ __global__ void __launch_bounds__(kSerialThreads)
 #pragma unroll
         for (int r = 0; r < RG; ++r) v[r] = vi[r] < V ? to_f32(vrow[vi[r]]) : 0.f;
     };
-    if (s < e) fetch(s, qc, kc, vc, gc, bc);
+    if (s < t_end) fetch(s, qc, kc, vc, gc, bc);
 
-    for (int t = s; t < e; ++t) {
+    for (int t = s; t < t_end; ++t) {
         float qn[PF ? EPL : 1], kn[PF ? EPL : 1], vn[RG], gn = 1.f, bn = 0.f;
         if constexpr (PF) {
-            if (t + 1 < e) fetch(t + 1, qn, kn, vn, gn, bn);
+            if (t + 1 < t_end) fetch(t + 1, qn, kn, vn, gn, bn);
         }
 
         float kq = 0.f;
@@ -183,16 +223,33 @@ __global__ void __launch_bounds__(kSerialThreads)
                 sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], off);
             }
         }
+        const int slot = t - s;
+        if constexpr (CAPT) {
+            if (slot < ncap) {  // DELTA_CAPTURE_STEP: g and the normalised k of this token
+                if (rb == 0 && warp == 0 && lane == 0) cap_g[(size_t)slot * H + h] = gc;
+                if (key_owner)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (kidx[m] + u < K)
+                                cap_k[((size_t)slot * HQ + kh) * K + kidx[m] + u] = kc[4 * m + u];
+            }
+        }
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
             const float delta = bc * (vc[r] - gc * sk[r]);
             const float o = gc * sq[r] + delta * kq;
 #pragma unroll
             for (int u = 0; u < EPL; ++u) S[r][u] = fmaf(gc, S[r][u], delta * kc[u]);
-            if (sub == 0 && vi[r] < V)
-                out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
+            if (sub == 0 && vi[r] < V) {
+                if (own) out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
+                if constexpr (CAPT) {
+                    if (slot < ncap) cap_d[((size_t)slot * H + h) * V + vi[r]] = delta;
+                }
+            }
         }
-        if (t + 1 < e) {
+        if (t + 1 < t_end) {
             if constexpr (PF) {
 #pragma unroll
                 for (int u = 0; u < EPL; ++u) {
@@ -209,6 +266,7 @@ __global__ void __launch_bounds__(kSerialThreads)
         }
     }
 
+    if (!own) return;
 #pragma unroll
     for (int r = 0; r < RG; ++r) {
         if (vi[r] < V) {
@@ -229,15 +287,16 @@ cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s, bo
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     const bool pf = p.max_len > 1;
-    if (vec4 && pf)
-        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, true>, dim3((unsigned)blocks),
-                          dim3(kSerialThreads), 0, s, pdl, p);
+    const dim3 grid((unsigned)blocks), block(kSerialThreads);
+    if (p.capsule != nullptr)
+        e = vec4 ? launch_kernel(delta_serial_kernel<T, KP, RG, true, true, true>, grid, block, 0, s, pdl, p)
+                 : launch_kernel(delta_serial_kernel<T, KP, RG, false, true, true>, grid, block, 0, s, pdl, p);
+    else if (vec4 && pf)
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, true, false>, grid, block, 0, s, pdl, p);
     else if (vec4)
-        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, false>, dim3((unsigned)blocks),
-                          dim3(kSerialThreads), 0, s, pdl, p);
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, false, false>, grid, block, 0, s, pdl, p);
     else
-        e = launch_kernel(delta_serial_kernel<T, KP, RG, false, true>, dim3((unsigned)blocks),
-                          dim3(kSerialThreads), 0, s, pdl, p);
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, false, true, false>, grid, block, 0, s, pdl, p);
     note_launch();
     return e;
 }

@@ -33,6 +33,7 @@ struct ConvParams {
     float *qk, *gb;
     const float *a, *bl, *A_log, *dt_bias;
     int H, HQ, K, V, prep_max_len;
+    int prep_cap;  // also prepare the first prep_cap tokens of every sequence
     // block 0 validates offsets and writes counts when header != nullptr;
     // with seq_order != nullptr it also lists the sequences of at least
     // chunk_min_len tokens, longest first, and sets n_units = count * H * VT
@@ -66,6 +67,16 @@ struct DeltaParams {
     const void *conv_init;
     void *conv_fin;
     int conv_L;
+    // optional state-update capture (cap > 0): conv_updates [B, cap, W] T (raw
+    // input rows, written with the final conv state) and capsule
+    // [B, cap * (H + HQ*K + H*V)] fp32; captured tokens of sequence b:
+    // max(0, min(counts[b], cap, len)), none when active && active[0] == 0.
+    // Chunked sequences get their capsule from a capture-only pass here.
+    int cap;
+    const int32_t *counts;
+    const int32_t *active;
+    void *conv_updates;
+    float *capsule;
 };
 
 // Launch `kernel` on `s`; with pdl the launch may overlap the previous kernel
@@ -90,7 +101,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t s, bool *fused_prep);
 cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void *init,
                               void *fin, int B, int N, int C, int L, int dtype,
-                              cudaStream_t s);
+                              cudaStream_t s, int cap = 0, const int32_t *counts = nullptr,
+                              void *updates = nullptr);
 cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s, bool pdl);
 
