@@ -38,6 +38,9 @@ def _args():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "ragged", "long", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--capture", type=int, default=0,
+                    help="state-update capture capacity (1..8): time gdn_layer_varlen_capture "
+                         "with every sequence asking for that many tokens")
     ap.add_argument("--lens", default=None,
                     help="comma-separated sequence lengths replacing the workload's "
                          "(same head geometry and distributions; for small profiling cases)")
@@ -60,9 +63,20 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def algorithmic_bytes_delta(wl, N, B):
+def capture_bytes(wl, B, cap):
+    """Bytes a capture of capacity cap adds to the token-serial kernel: the
+    capsule and the conv capture rows written in full, the captured raw rows read."""
+    if cap <= 0:
+        return 0
+    esz = 2 if wl.dtype == "bf16" else 4
+    capsule = B * cap * (wl.H + wl.HQ * wl.K + wl.H * wl.V) * 4
+    rows = B * cap * wl.width * esz
+    return capsule + 2 * rows
+
+
+def algorithmic_bytes_delta(wl, N, B, cap=0):
     """Bytes the token-serial recurrence kernel must move per launch in the
-    layer call (it also writes the final conv state)."""
+    layer call (it also writes the final conv state and any capture)."""
     esz = 2 if wl.dtype == "bf16" else 4
     state = 2 * B * wl.H * wl.V * wl.K * 4            # read + write fp32 state
     qk = N * wl.HQ * 2 * wl.K * 4                     # normalised q and k (fp32)
@@ -70,7 +84,7 @@ def algorithmic_bytes_delta(wl, N, B):
     v = N * wl.H * wl.V * esz                         # v columns of the conv output
     out = N * wl.H * wl.V * esz
     conv_state = 2 * B * wl.width * wl.L * esz        # final conv state: read + write
-    return state + qk + gb + v + out + conv_state
+    return state + qk + gb + v + out + conv_state + capture_bytes(wl, B, cap)
 
 
 def algorithmic_bytes_layer(wl, N, B):
@@ -186,10 +200,19 @@ def run_reference(args, wl):
     ci, si = c(d["conv_init"]), c(d["state_init"])
     act = "bf16" if sample_wl.dtype == "bf16" else "f32"
 
+    cap = args.capture
+    counts = np.full(len(offs) - 1, cap, np.int32)
+
     def step():
-        oracle.layer_varlen(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ, sample_wl.K,
-                            sample_wl.V, sample_wl.Kc, sample_wl.D, silu=sample_wl.silu,
-                            scale=d["scale"], act_dtype=act)
+        if cap:
+            oracle.layer_varlen_capture(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ,
+                                        sample_wl.K, sample_wl.V, sample_wl.Kc, sample_wl.D,
+                                        counts, cap, silu=sample_wl.silu, scale=d["scale"],
+                                        act_dtype=act)
+        else:
+            oracle.layer_varlen(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ, sample_wl.K,
+                                sample_wl.V, sample_wl.Kc, sample_wl.D, silu=sample_wl.silu,
+                                scale=d["scale"], act_dtype=act)
 
     for _ in range(args.warmup):
         step()
@@ -204,7 +227,7 @@ def run_reference(args, wl):
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample": sample},
+        "config": {"workload": wl.name, "sample": sample, **({"capture": cap} if cap else {})},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -278,14 +301,28 @@ def run_ours(args, wl):
                      dtype=torch.uint8, device=dev)
     out = torch.empty((N, wl.H, wl.V), dtype=wl.torch_dtype, device=dev)
     conv_state, state = d["conv_init"], d["state_init"]
+    cap = args.capture
+    if cap:
+        counts = torch.full((B,), cap, dtype=torch.int32, device=dev)
+        conv_upd = torch.empty((B, cap, wl.width), dtype=wl.torch_dtype, device=dev)
+        capsule = torch.empty((B, cap * (wl.H + wl.HQ * wl.K + wl.H * wl.V)),
+                              dtype=torch.float32, device=dev)
+
+    def call(qkv, a, b, offsets):
+        # decode-style carry: the final states overwrite the initial ones in place
+        kw = dict(H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act,
+                  scale=d["scale"], offsets_host=offs, out=out, conv_fin=conv_state,
+                  state_fin=state, workspace=ws)
+        if cap:
+            gdn.gdn_layer_varlen_capture(qkv, d["w"], d["bias"], a, b, d["A_log"], d["dt_bias"],
+                                         offsets, conv_state, state, counts, cap=cap,
+                                         conv_updates=conv_upd, capsule=capsule, **kw)
+        else:
+            gdn.gdn_layer_varlen(qkv, d["w"], d["bias"], a, b, d["A_log"], d["dt_bias"],
+                                 offsets, conv_state, state, **kw)
 
     def step():
-        # decode-style carry: the final states overwrite the initial ones in place
-        gdn.gdn_layer_varlen(d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"],
-                             d["dt_bias"], d["offsets"], conv_state, state, H=wl.H, HQ=wl.HQ,
-                             K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act, scale=d["scale"],
-                             offsets_host=offs, out=out, conv_fin=conv_state, state_fin=state,
-                             workspace=ws)
+        call(d["qkv"], d["a"], d["b"], d["offsets"])
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
@@ -368,17 +405,18 @@ def run_ours(args, wl):
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_offs.numel() * 4
     d2h = out_host.numel() * out_host.element_size()
+    if cap:  # the caller also reads the capsule back
+        capsule_host = torch.empty(capsule.shape, dtype=capsule.dtype, pin_memory=True)
+        d2h += capsule_host.numel() * 4
 
     def e2e_step():
         for k in host:
             dev_in[k].copy_(host[k], non_blocking=True)
         dev_offs.copy_(host_offs, non_blocking=True)
-        gdn.gdn_layer_varlen(dev_in["qkv"], d["w"], d["bias"], dev_in["a"], dev_in["b"],
-                             d["A_log"], d["dt_bias"], dev_offs, conv_state, state, H=wl.H,
-                             HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act,
-                             scale=d["scale"], offsets_host=offs, out=out, conv_fin=conv_state,
-                             state_fin=state, workspace=ws)
+        call(dev_in["qkv"], dev_in["a"], dev_in["b"], dev_offs)
         out_host.copy_(out, non_blocking=True)
+        if cap:
+            capsule_host.copy_(capsule, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -400,11 +438,11 @@ def run_ours(args, wl):
         kavg = statistics.mean(kern_ms)
         value = world * N * args.steps / (ms * 1e-3)
         if dom == gdn.GDN_KERNEL_SERIAL:
-            kbytes = algorithmic_bytes_delta(wl, N, B)
+            kbytes = algorithmic_bytes_delta(wl, N, B, cap)
             achieved = kbytes / (kavg * 1e-3) / 1e9
             roof = {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": _profile_traffic("delta_serial", wl.name),
+                    "traffic": None if cap else _profile_traffic("delta_serial", wl.name),
                     "algorithmic_bytes": kbytes, "kernel_ms": kavg,
                     "peak_source": f"hbm_gbs of {peak_src}"}
         else:
@@ -423,13 +461,15 @@ def run_ours(args, wl):
             "config": {"workload": wl.name, "B": B, "N": N, "HQ": wl.HQ, "H": wl.H, "K": wl.K,
                        "V": wl.V, "Kc": wl.Kc, "D": wl.D, "state_carry": "in place",
                        "l2": "inputs larger than L2 (129 MB)",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       **({"capture": cap} if cap else {})},
             "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
             "roofline": roof,
             "e2e": {"value": world * N * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
-            "timing": "CUDA graph replay of one gdn_layer_varlen call per step",
+            "timing": "CUDA graph replay of one gdn_layer_varlen%s call per step"
+                      % ("_capture" if cap else ""),
             "ms_per_step_eager": eager_ms / args.steps,
             "clocks": clocks,
         }

@@ -164,3 +164,20 @@ def test_standalone_conv_and_delta_capture(dt):
                                             cpu64(d["state_init"]), wl.H, wl.HQ, wl.K, wl.V,
                                             counts, cap, scale=d["scale"])
     _check_capsule(W.scaled(wl, wl.lens, dtype="f32"), capsule, ref, cap)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_capture_one_token_batches(dt):
+    """Decode-shaped batches (one token or none per sequence) take the
+    one-token kernel variant with capture."""
+    lens = (1, 0, 1, 1, 0, 1, 1)
+    wl = W.scaled(W.WORKLOADS["decode"], lens, dtype=dt, H=8, HQ=4)
+    d = W.make_inputs(wl, DEV)
+    counts, cap = [8, 8, 0, 1, 3, -2, 2], 8
+    o0, c0, s0 = _plain(wl, d, offsets_host=d["offsets_list"])
+    o1, c1, s1, upd, capsule = _capture(wl, d, counts, cap, offsets_host=d["offsets_list"])
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(c0, c1) and torch.equal(s0, s1)
+    ref = _oracle(wl, d, counts, cap)
+    np.testing.assert_array_equal(cpu64(upd), ref[3])
+    _check_capsule(wl, capsule, ref[4], cap)

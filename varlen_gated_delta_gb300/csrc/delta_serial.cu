@@ -153,17 +153,18 @@ __global__ void __launch_bounds__(kSerialThreads)
         cap_g = base;
         cap_k = base + (size_t)cap * H;
         cap_d = base + (size_t)cap * (H + (size_t)HQ * K);
-        for (int i = ncap; i < cap; ++i) {  // slots past the captured prefix are zero
-            if (rb == 0 && warp == 0 && lane == 0) cap_g[(size_t)i * H + h] = 0.f;
-            if (key_owner)
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (kidx[m] + u < K) cap_k[((size_t)i * HQ + kh) * K + kidx[m] + u] = 0.f;
-#pragma unroll
-            for (int r = 0; r < RG; ++r)
-                if (sub == 0 && vi[r] < V) cap_d[((size_t)i * H + h) * V + vi[r]] = 0.f;
+        // slots past the captured prefix are zero (the whole block writes them,
+        // consecutive threads on consecutive floats)
+        const int nz = cap - ncap, tid = threadIdx.x, nt = blockDim.x;
+        for (int q = tid; q < nz * rows_cta; q += nt) {
+            const int i = ncap + q / rows_cta, row = rb * rows_cta + q % rows_cta;
+            if (row < V) cap_d[((size_t)i * H + h) * V + row] = 0.f;
+        }
+        if (rb == 0) {
+            for (int q = tid; q < nz; q += nt) cap_g[(size_t)(ncap + q) * H + h] = 0.f;
+            if (h == kh * (H / HQ))
+                for (int q = tid; q < nz * K; q += nt)
+                    cap_k[((size_t)(ncap + q / K) * HQ + kh) * K + q % K] = 0.f;
         }
     }
     if (!own && ncap == 0) return;
@@ -288,7 +289,9 @@ cudaError_t launch_serial_kp(const DeltaParams &p, bool vec4, cudaStream_t s, bo
     cudaError_t e;
     const bool pf = p.max_len > 1;
     const dim3 grid((unsigned)blocks), block(kSerialThreads);
-    if (p.capsule != nullptr)
+    if (p.capsule != nullptr && vec4 && !pf)
+        e = launch_kernel(delta_serial_kernel<T, KP, RG, true, false, true>, grid, block, 0, s, pdl, p);
+    else if (p.capsule != nullptr)
         e = vec4 ? launch_kernel(delta_serial_kernel<T, KP, RG, true, true, true>, grid, block, 0, s, pdl, p)
                  : launch_kernel(delta_serial_kernel<T, KP, RG, false, true, true>, grid, block, 0, s, pdl, p);
     else if (vec4 && pf)
