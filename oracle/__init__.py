@@ -47,6 +47,11 @@ def _load():
         lib.oracle_conv_capture.argtypes = [dp, ip, ip, dp] + [i] * 4
         lib.oracle_layer_varlen_capture.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [ip, ip, dp, dp]
                                                     + [i] * 9 + [ctypes.c_double, i, i])
+        lib.oracle_prepare_ex.argtypes = [dp] * 7 + [i] * 6
+        lib.oracle_delta_varlen_ex.argtypes = ([dp, dp, dp, ip, dp, dp, dp] + [i] * 6
+                                               + [ctypes.c_double, i])
+        lib.oracle_layer_varlen_ex.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [i] * 9
+                                               + [ctypes.c_double, i, i])
         lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -166,6 +171,65 @@ def layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_i
         _p(conv_init), _p(conv_fin), _p(state_init), _p(out), _p(state_fin),
         B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype])
     _check(rc, "layer_varlen")
+    return out, conv_fin, state_fin
+
+
+# rule / activation options (paged_ssm.rs GatedDeltaNet attributes); 0 = the
+# default gated delta rule with softplus gate, sigmoid rate and L2-normalised q, k
+OPT_NO_DECAY = 1      # update_rule linear / delta, or no decay input: g = 1
+OPT_NO_RETRIEVE = 2   # update_rule linear / gated: delta = beta v
+OPT_GATE_EXP = 4      # gate_activation none: g = exp(a)
+OPT_NO_BETA = 8       # no beta input: beta = 1
+OPT_BETA_RAW = 16     # beta_activation none: beta = b
+OPT_NO_QK_NORM = 32   # qk_l2_norm 0
+
+
+def prepare_ex(y, a, b, A_log, dt_bias, H, HQ, K, V, opts):
+    """Prepare with options; a / b / A_log / dt_bias may be None where unused."""
+    y = _f64(y)
+    N = y.shape[0]
+    a, b, A_log, dt_bias = (_f64(x) for x in (a, b, A_log, dt_bias))
+    qk = np.zeros((2, N, HQ, K))
+    gb = np.zeros((2, N, H))
+    rc = _load().oracle_prepare_ex(_p(y), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(qk), _p(gb),
+                                   N, H, HQ, K, V, int(opts))
+    _check(rc, "prepare_ex")
+    return qk, gb
+
+
+def delta_varlen_ex(y, qk, gb, offsets, state_init, H, HQ, K, V, opts, scale=0.0):
+    """Recurrence with options (OPT_NO_RETRIEVE acts here)."""
+    y, qk, gb, state_init = map(_f64, (y, qk, gb, state_init))
+    offsets = _i32(offsets)
+    N = y.shape[0]
+    B = offsets.size - 1
+    out = np.zeros((N, H, V))
+    fin = np.zeros((B, H, V, K))
+    rc = _load().oracle_delta_varlen_ex(_p(y), _p(qk), _p(gb), _pi(offsets), _p(state_init),
+                                        _p(out), _p(fin), B, N, H, HQ, K, V, float(scale),
+                                        int(opts))
+    _check(rc, "delta_varlen_ex")
+    return out, fin
+
+
+def layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init,
+                    H, HQ, K, V, Kc, D, opts, silu=True, scale=0.0, act_dtype="bf16"):
+    """The layer with rule / activation options.  Returns (out, conv_fin, state_fin)."""
+    qkv, w, conv_init, state_init = map(_f64, (qkv, w, conv_init, state_init))
+    a, b, A_log, dt_bias, bias = (_f64(x) for x in (a, b, A_log, dt_bias, bias))
+    offsets = _i32(offsets)
+    N = qkv.shape[0]
+    B = offsets.size - 1
+    C = 2 * HQ * K + H * V
+    L = (Kc - 1) * D
+    out = np.zeros((N, H, V))
+    conv_fin = np.zeros((B, C, L))
+    state_fin = np.zeros((B, H, V, K))
+    rc = _load().oracle_layer_varlen_ex(
+        _p(qkv), _p(w), _p(bias), _p(a), _p(b), _p(A_log), _p(dt_bias), _pi(offsets),
+        _p(conv_init), _p(conv_fin), _p(state_init), _p(out), _p(state_fin),
+        B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype], int(opts))
+    _check(rc, "layer_varlen_ex")
     return out, conv_fin, state_fin
 
 

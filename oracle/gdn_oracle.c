@@ -22,6 +22,9 @@
  *       per (sequence, value head, state row): decay the state, retrieve
  *       with the decayed state, beta-scaled delta, rank-1 update, read out
  *       the updated state with q, multiply by scale; key head kh = h/(H/HQ).
+ *   [paged_ssm.rs, GatedDeltaNet attributes update_rule, gate_activation,
+ *    beta_activation, qk_l2_norm; flags DECAY, RETRIEVE, SOFTPLUS, BETA,
+ *    SIGMOID, NORM]  the rule and activation variants (oracle_*_ex).
  *   [paged_ssm.rs, CONV_CAPTURE_* and DELTA_CAPTURE_* kernels]
  *       capture of the first min(counts[b], capacity, len) tokens' updates:
  *       raw conv input rows and the (g, normalised k, beta-scaled delta)
@@ -140,11 +143,32 @@ int oracle_conv1d_varlen(const double *x, const double *w, const double *bias,
  * root; softplus(x) = max(x,0) + log(1 + exp(-|x|)) (= logaddexp(x, 0));
  * A_log is rounded to float32 before exp (the rate-activation graph casts it).
  */
-int oracle_prepare(const double *y, const double *a, const double *bl,
-                   const double *A_log, const double *dt_bias, double *qk,
-                   double *gb, int N, int H, int HQ, int K, int V) {
+/* Rule and activation options (paged_ssm.rs, GatedDeltaNet attributes
+ * update_rule, gate_activation, beta_activation, qk_l2_norm and the optional
+ * decay / beta inputs); 0 is the default method (gated_delta, softplus gate,
+ * sigmoid rate, L2-normalised q and k). */
+#define OPT_NO_DECAY 1     /* update_rule linear or delta, or no decay input: g = 1 */
+#define OPT_NO_RETRIEVE 2  /* update_rule linear or gated: delta = beta v */
+#define OPT_GATE_EXP 4     /* gate_activation none: g = exp(a) */
+#define OPT_NO_BETA 8      /* no beta input: beta = 1 */
+#define OPT_BETA_RAW 16    /* beta_activation none: beta = b */
+#define OPT_NO_QK_NORM 32  /* qk_l2_norm 0: q and k used as they are */
+
+/*
+ * [paged_ssm.rs, DELTA_PREPARE with flags NORM, DECAY, SOFTPLUS, BETA, SIGMOID]
+ *   q, k scaled by rsqrt(sum^2 + 1e-12) when NORM (else by 1);
+ *   g = exp(x) with x = -exp(A_log) softplus(a + dt_bias) under SOFTPLUS, x = a
+ *   otherwise, and g = 1 without DECAY; rate = sigmoid(b) under SIGMOID, b
+ *   otherwise, and 1 without BETA.
+ */
+int oracle_prepare_ex(const double *y, const double *a, const double *bl,
+                      const double *A_log, const double *dt_bias, double *qk,
+                      double *gb, int N, int H, int HQ, int K, int V, int opts) {
     if (N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
     const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
+    const int norm = !(opts & OPT_NO_QK_NORM), decay = !(opts & OPT_NO_DECAY);
+    const int softplus_gate = !(opts & OPT_GATE_EXP), has_beta = !(opts & OPT_NO_BETA);
+    const int sigmoid = !(opts & OPT_BETA_RAW);
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < N; ++t) {
         for (int kh = 0; kh < HQ; ++kh) {
@@ -155,24 +179,38 @@ int oracle_prepare(const double *y, const double *a, const double *bl,
                 nq += q[i] * q[i];
                 nk += k[i] * k[i];
             }
-            double rq = 1.0 / sqrt(nq + 1e-12);
-            double rk = 1.0 / sqrt(nk + 1e-12);
+            double rq = norm ? 1.0 / sqrt(nq + 1e-12) : 1.0;
+            double rk = norm ? 1.0 / sqrt(nk + 1e-12) : 1.0;
             for (int i = 0; i < K; ++i) {
                 qk[((size_t)t * HQ + kh) * K + i] = q[i] * rq;
                 qk[(((size_t)N + t) * HQ + kh) * K + i] = k[i] * rk;
             }
         }
         for (int h = 0; h < H; ++h) {
-            double x = a[(size_t)t * H + h] + dt_bias[h];
-            double softplus = fmax(x, 0.0) + log1p(exp(-fabs(x)));
-            double alog = round_f32(A_log[h]);
-            double g = exp(-exp(alog) * softplus);
-            double beta = 1.0 / (1.0 + exp(-bl[(size_t)t * H + h]));
+            double g = 1.0;
+            if (decay) {
+                double x = a[(size_t)t * H + h];
+                if (softplus_gate) {
+                    x += dt_bias[h];
+                    double softplus = fmax(x, 0.0) + log1p(exp(-fabs(x)));
+                    double alog = round_f32(A_log[h]);
+                    x = -exp(alog) * softplus;
+                }
+                g = exp(x);
+            }
+            double beta = has_beta ? bl[(size_t)t * H + h] : 1.0;
+            if (has_beta && sigmoid) beta = 1.0 / (1.0 + exp(-beta));
             gb[(size_t)t * H + h] = g;
             gb[((size_t)N + t) * H + h] = beta;
         }
     }
     return ORACLE_OK;
+}
+
+int oracle_prepare(const double *y, const double *a, const double *bl,
+                   const double *A_log, const double *dt_bias, double *qk,
+                   double *gb, int N, int H, int HQ, int K, int V) {
+    return oracle_prepare_ex(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V, 0);
 }
 
 /*
@@ -210,7 +248,8 @@ static int delta_recurrence(const double *y, const double *qk, const double *gb,
                             const int32_t *offsets, const double *init, double *out,
                             double *fin, int B, int N, int H, int HQ, int K, int V,
                             double scale, const int32_t *counts, const int32_t *active,
-                            double *capsule, int cap) {
+                            double *capsule, int cap, int opts) {
+    const int retrieve = !(opts & OPT_NO_RETRIEVE);
     if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ)
         return ORACLE_ERR_SHAPE;
     if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
@@ -248,7 +287,7 @@ static int delta_recurrence(const double *y, const double *qk, const double *gb,
                         retrieval += k[i] * row[i];
                     }
                     double delta = y[(size_t)t * W + (size_t)2 * HQ * K + (size_t)h * V + vi];
-                    delta -= retrieval;
+                    if (retrieve) delta -= retrieval;  /* RETRIEVE: delta rules only */
                     delta *= beta;
                     if (slot < ncap)  /* the beta-scaled delta of this state row */
                         cb[(size_t)cap * (H + (size_t)HQ * K) + ((size_t)slot * H + h) * V + vi] = delta;
@@ -272,7 +311,17 @@ int oracle_delta_varlen(const double *y, const double *qk, const double *gb,
                         double *fin, int B, int N, int H, int HQ, int K, int V,
                         double scale) {
     return delta_recurrence(y, qk, gb, offsets, init, out, fin, B, N, H, HQ, K, V, scale,
-                            NULL, NULL, NULL, 0);
+                            NULL, NULL, NULL, 0, 0);
+}
+
+/* The recurrence with rule options (only OPT_NO_RETRIEVE acts here; the
+ * decay and rate options act in oracle_prepare_ex). */
+int oracle_delta_varlen_ex(const double *y, const double *qk, const double *gb,
+                           const int32_t *offsets, const double *init, double *out,
+                           double *fin, int B, int N, int H, int HQ, int K, int V,
+                           double scale, int opts) {
+    return delta_recurrence(y, qk, gb, offsets, init, out, fin, B, N, H, HQ, K, V, scale,
+                            NULL, NULL, NULL, 0, opts);
 }
 
 /*
@@ -295,7 +344,7 @@ int oracle_delta_varlen_capture(const double *y, const double *qk, const double 
                                 double scale, int cap) {
     if (cap < 1 || cap > 8 || !counts || !capsule) return ORACLE_ERR_SHAPE;
     return delta_recurrence(y, qk, gb, offsets, init, out, fin, B, N, H, HQ, K, V, scale,
-                            counts, active, capsule, cap);
+                            counts, active, capsule, cap, 0);
 }
 
 /*
@@ -377,6 +426,30 @@ int oracle_layer_varlen_capture(const double *qkv, const double *w, const double
     if (!rc) rc = oracle_delta_varlen_capture(y, qk, gb, offsets, state_init, out, state_fin,
                                               counts, active, capsule, B, N, H, HQ, K, V,
                                               scale, cap);
+    free(y);
+    free(qk);
+    free(gb);
+    return rc;
+}
+
+/* The layer with rule / activation options (see OPT_*). */
+int oracle_layer_varlen_ex(const double *qkv, const double *w, const double *bias,
+                           const double *a, const double *bl, const double *A_log,
+                           const double *dt_bias, const int32_t *offsets,
+                           const double *conv_init, double *conv_fin,
+                           const double *state_init, double *out, double *state_fin,
+                           int B, int N, int H, int HQ, int K, int V, int Kc, int D,
+                           int silu, double scale, int act_dtype, int opts) {
+    if (H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
+    const int C = 2 * HQ * K + H * V;
+    double *y = (double *)malloc(sizeof(double) * ((size_t)N * C + 1));
+    double *qk = (double *)malloc(sizeof(double) * ((size_t)2 * N * HQ * K + 1));
+    double *gb = (double *)malloc(sizeof(double) * ((size_t)2 * N * H + 1));
+    int rc = oracle_conv1d_varlen(qkv, w, bias, offsets, conv_init, y, conv_fin, B, N,
+                                  C, Kc, D, silu, act_dtype);
+    if (!rc) rc = oracle_prepare_ex(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V, opts);
+    if (!rc) rc = oracle_delta_varlen_ex(y, qk, gb, offsets, state_init, out, state_fin,
+                                         B, N, H, HQ, K, V, scale, opts);
     free(y);
     free(qk);
     free(gb);

@@ -518,3 +518,92 @@ def test_layer_capture_is_the_composition_of_the_operator_captures():
     g, k, dl = oracle.capsule_blocks(capsule, 4, wl.H, wl.HQ, wl.K, wl.V)
     assert g[0, :2].all() and not g[0, 2:].any() and not g[1].any() and g[2].all()
     np.testing.assert_allclose(np.linalg.norm(k[2], axis=-1), 1.0, rtol=1e-9)
+
+
+# ------------------------------------------------------------------ rule / activation variants
+# paged_ssm.rs GatedDeltaNet: update_rule linear | gated | delta | gated_delta (decay <=> gated*,
+# retrieval <=> *delta), gate_activation none (g = exp(a)) | softplus, beta_activation none |
+# sigmoid, optional beta input, qk_l2_norm 0 | 1.
+
+def _variant_problem(seed, T=9, H=2, HQ=1, K=5, V=4):
+    rng = _rng(seed)
+    W = 2 * HQ * K + H * V
+    y = rng.standard_normal((T, W))
+    a = rng.standard_normal((T, H)) - 0.5
+    b = rng.standard_normal((T, H))
+    A_log = rng.uniform(0, math.log(16), H)
+    dt_bias = rng.standard_normal(H)
+    S0 = rng.standard_normal((1, H, V, K)) * 0.3
+    return y, a, b, A_log, dt_bias, S0, (H, HQ, K, V)
+
+
+def test_linear_rule_is_the_plain_sum_of_outer_products():
+    y, a, b, A_log, dt, S0, (H, HQ, K, V) = _variant_problem(21)
+    opts = oracle.OPT_NO_DECAY | oracle.OPT_NO_RETRIEVE | oracle.OPT_NO_BETA | oracle.OPT_NO_QK_NORM
+    qk, gb = oracle.prepare_ex(y, None, None, None, None, H, HQ, K, V, opts)
+    assert (gb == 1.0).all()
+    out, fin = oracle.delta_varlen_ex(y, qk, gb, [0, len(y)], S0, H, HQ, K, V, opts, scale=0.5)
+    q, k, v = y[:, :K], y[:, K:2 * K], y[:, 2 * K:].reshape(len(y), H, V)
+    for h in range(H):
+        S = S0[0, h].copy()
+        for t in range(len(y)):
+            S = S + np.outer(v[t, h], k[t])
+            np.testing.assert_allclose(out[t, h], 0.5 * S @ q[t], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(fin[0, h], S0[0, h] + v[:, h].T @ k, rtol=1e-12, atol=1e-12)
+
+
+def test_gated_rule_is_the_decayed_sum():
+    # S_T = gamma_T S_0 + sum_t (gamma_T / gamma_t) beta_t v_t k_t^T
+    y, a, b, A_log, dt, S0, (H, HQ, K, V) = _variant_problem(22)
+    opts = oracle.OPT_NO_RETRIEVE
+    qk, gb = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, opts)
+    _, fin = oracle.delta_varlen_ex(y, qk, gb, [0, len(y)], S0, H, HQ, K, V, opts)
+    k, v = qk[1, :, 0], y[:, 2 * K:].reshape(len(y), H, V)
+    for h in range(H):
+        lg = np.log(gb[0, :, h])
+        tail = np.exp(np.cumsum(lg[::-1])[::-1] - lg)   # prod_{s > t} g_s
+        gT = np.exp(lg.sum())
+        S = gT * S0[0, h] + sum(tail[t] * gb[1, t, h] * np.outer(v[t, h], k[t])
+                                for t in range(len(y)))
+        np.testing.assert_allclose(fin[0, h], S, rtol=1e-10, atol=1e-12)
+
+
+def test_delta_rule_is_the_unrolled_product_without_decay():
+    y, a, b, A_log, dt, S0, (H, HQ, K, V) = _variant_problem(23)
+    opts = oracle.OPT_NO_DECAY
+    qk, gb = oracle.prepare_ex(y, None, b, None, None, H, HQ, K, V, opts)
+    out, fin = oracle.delta_varlen_ex(y, qk, gb, [0, len(y)], S0, H, HQ, K, V, opts, scale=1.0)
+    for h in range(H):
+        o_ref, S_ref = oracle.delta_unrolled(qk[0, :, 0], qk[1, :, 0],
+                                             y[:, 2 * K + h * V:2 * K + (h + 1) * V],
+                                             np.ones(len(y)), gb[1, :, h], S0[0, h], 1.0)
+        np.testing.assert_allclose(fin[0, h], S_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(out[:, h], o_ref, rtol=1e-10, atol=1e-12)
+
+
+def test_gate_and_rate_activations():
+    y, a, b, A_log, dt, S0, (H, HQ, K, V) = _variant_problem(24)
+    _, gb = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V,
+                              oracle.OPT_GATE_EXP | oracle.OPT_BETA_RAW)
+    np.testing.assert_allclose(gb[0], np.exp(a), rtol=1e-15)        # g = exp(a)
+    np.testing.assert_array_equal(gb[1], b)                          # beta = b
+    _, gb0 = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, 0)
+    _, gb1 = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, oracle.OPT_NO_BETA)
+    np.testing.assert_array_equal(gb1[0], gb0[0])
+    assert (gb1[1] == 1.0).all()
+    # qk_l2_norm 0 passes q and k through
+    qk, _ = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, oracle.OPT_NO_QK_NORM)
+    np.testing.assert_array_equal(qk[0, :, 0], y[:, :K])
+    np.testing.assert_array_equal(qk[1, :, 0], y[:, K:2 * K])
+
+
+def test_layer_options_zero_is_the_default_layer():
+    wl = workloads.scaled(workloads.WORKLOADS["tiny"], (4, 6))
+    d = workloads.make_inputs(wl)
+    args = (d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+            d["offsets_list"], d["conv_init"], d["state_init"], wl.H, wl.HQ, wl.K, wl.V, wl.Kc,
+            wl.D)
+    ref = oracle.layer_varlen(*args, act_dtype="f32")
+    got = oracle.layer_varlen_ex(*args, 0, act_dtype="f32")
+    for x, r in zip(got, ref):
+        np.testing.assert_array_equal(x, r)
