@@ -255,6 +255,52 @@ GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void 
                                      void *stream);
 
 /*
+ * Rule and activation options (paged_ssm.rs, GatedDeltaNet attributes
+ * update_rule, gate_activation, beta_activation, qk_l2_norm and its optional
+ * decay / beta inputs; kernel flags DECAY, RETRIEVE, SOFTPLUS, BETA, SIGMOID,
+ * NORM).  A bitmask; 0 is the default method of the plain calls: the
+ * gated_delta rule, softplus gate g = exp(-exp(A_log) softplus(a + dt_bias)),
+ * sigmoid rate and L2-normalised q and k.
+ *   update_rule gated_delta: 0;   delta: GDN_OPT_NO_DECAY;
+ *   gated: GDN_OPT_NO_RETRIEVE;   linear: GDN_OPT_NO_DECAY | GDN_OPT_NO_RETRIEVE.
+ */
+#define GDN_OPT_NO_DECAY 1     /* g = 1 (no decay input; a may be NULL) */
+#define GDN_OPT_NO_RETRIEVE 2  /* delta = beta v: no retrieval S k */
+#define GDN_OPT_GATE_EXP 4     /* gate_activation none: g = exp(a) (A_log, dt_bias unused) */
+#define GDN_OPT_NO_BETA 8      /* no beta input: beta = 1 (b may be NULL) */
+#define GDN_OPT_BETA_RAW 16    /* beta_activation none: beta = b */
+#define GDN_OPT_NO_QK_NORM 32  /* qk_l2_norm 0: q and k are used as they are */
+#define GDN_OPT_ALL 63
+
+/*
+ * The calls with rule / activation options (GDN_OPT_*, above); opts = 0 is
+ * the plain call.  gdn_layer_varlen_ex also takes the capture arguments
+ * documented below (cap = 0: no capture, the capture pointers are ignored).
+ * Pointers an option makes unused may be NULL (a with GDN_OPT_NO_DECAY,
+ * A_log and dt_bias without the softplus gate, b with GDN_OPT_NO_BETA).
+ * Errors: GDN_ERR_UNSUPPORTED for unknown option bits, GDN_ERR_NULL for a
+ * pointer the options need, then the plain call's errors.
+ */
+GDN_API int gdn_prepare_ex(const void *y, const float *a, const float *b, const float *A_log,
+                           const float *dt_bias, float *qk_norm, float *g_beta, int N, int H,
+                           int HQ, int K, int V, int opts, int dtype, void *stream);
+
+GDN_API int gdn_delta_varlen_ex(const void *y, const float *qk_norm, const float *g_beta,
+                                const int32_t *offsets, const float *state_init, void *out,
+                                float *state_fin, int B, int N, int H, int HQ, int K, int V,
+                                float scale, int opts, int dtype, void *stream);
+
+GDN_API int gdn_layer_varlen_ex(const void *qkv, const void *w, const void *bias, const float *a,
+                                const float *b, const float *A_log, const float *dt_bias,
+                                const int32_t *offsets, const int32_t *offsets_host,
+                                const void *conv_init, void *conv_fin, const float *state_init,
+                                void *out, float *state_fin, int opts, int cap,
+                                const int32_t *counts, const int32_t *active, void *conv_updates,
+                                float *capsule, int B, int N, int H, int HQ, int K, int V, int Kc,
+                                int D, int act, float scale, int dtype, void *workspace,
+                                size_t ws_bytes, void *stream);
+
+/*
  * State-update capture (paged_ssm.rs, onnxruntime-ep-mlx 0.31.1: kernels
  * CONV_CAPTURE_INIT/STEP and DELTA_CAPTURE_INIT/STEP; attribute
  * state_update_capacity in [0, 8], inputs capture_count [B] int32 and the

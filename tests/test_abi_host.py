@@ -200,3 +200,23 @@ def test_capture_calls_validate_capacity_counts_and_buffers(lib):
     assert delta(0, FAKE, FAKE) == 2
     assert delta(2, None, FAKE) == 1
     assert delta(2, FAKE, None) == 1
+
+
+def test_option_calls_validate_option_bits_and_needed_inputs(lib):
+    def layer_ex(opts, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE):
+        return lib.gdn_layer_varlen_ex(FAKE, FAKE, None, a, b, A_log, dt_bias, FAKE, None, FAKE,
+                                       FAKE, FAKE, FAKE, FAKE, opts, 0, None, None, None, None,
+                                       2, 16, 4, 2, 16, 16, 4, 1, 1, 0.0, 0, FAKE, 1 << 30, None)
+    assert layer_ex(64) == 5 and b"option" in lib.gdn_last_error()
+    assert layer_ex(0, a=None) == 1
+    assert layer_ex(0, b=None) == 1
+    assert layer_ex(0, A_log=None) == 1
+    assert layer_ex(gdn.GDN_OPT_GATE_EXP, b=None) == 1          # the exp gate still needs a and b
+    assert layer_ex(gdn.GDN_OPT_NO_DECAY, b=None) == 1
+    assert layer_ex(gdn.GDN_OPT_NO_BETA, a=None) == 1
+    assert lib.gdn_prepare_ex(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 2, 16, 16, 0, 0,
+                              None) == 1
+    assert lib.gdn_prepare_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 2, 16, 16, 128, 0,
+                              None) == 5
+    assert lib.gdn_delta_varlen_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 16, 4, 2, 16, 16,
+                                   0.0, 99, 0, None) == 5

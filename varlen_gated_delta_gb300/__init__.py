@@ -27,12 +27,20 @@ __all__ = [
     "gdn_launch_count", "gdn_set_kernel_events", "GDN_KERNEL_CONV", "GDN_KERNEL_CHUNKED",
     "GDN_KERNEL_SERIAL", "GDN_F32", "GDN_BF16", "GDN_ACT_NONE", "GDN_ACT_SILU",
     "STATUS_NAMES", "GDN_CAPTURE_MAX", "gdn_conv1d_varlen_capture", "gdn_delta_varlen_capture",
-    "gdn_layer_varlen_capture",
+    "gdn_layer_varlen_capture", "gdn_prepare_ex", "gdn_delta_varlen_ex", "gdn_layer_varlen_ex",
+    "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
+    "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 GDN_F32, GDN_BF16 = 0, 1
 GDN_CAPTURE_MAX = 8
+# rule / activation options (gdn.h GDN_OPT_*); 0 = gated delta, softplus gate,
+# sigmoid rate, L2-normalised q and k
+GDN_OPT_NO_DECAY, GDN_OPT_NO_RETRIEVE, GDN_OPT_GATE_EXP = 1, 2, 4
+GDN_OPT_NO_BETA, GDN_OPT_BETA_RAW, GDN_OPT_NO_QK_NORM = 8, 16, 32
+RULE_OPTS = {"gated_delta": 0, "delta": GDN_OPT_NO_DECAY, "gated": GDN_OPT_NO_RETRIEVE,
+             "linear": GDN_OPT_NO_DECAY | GDN_OPT_NO_RETRIEVE}
 GDN_ACT_NONE, GDN_ACT_SILU = 0, 1
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_OVERFLOW",
                 4: "GDN_ERR_OFFSETS", 5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA",
@@ -79,11 +87,15 @@ def load_library():
     lib.gdn_conv1d_varlen_capture.argtypes = [vp] * 7 + [i, vp, vp] + [i] * 7 + [vp]
     lib.gdn_delta_varlen_capture.argtypes = [vp] * 7 + [i, vp, vp, vp] + [i] * 6 + [f, i, vp]
     lib.gdn_layer_varlen_capture.argtypes = [vp] * 14 + [i, vp, vp, vp, vp] + [i] * 9 + [f, i, vp, sz, vp]
+    lib.gdn_prepare_ex.argtypes = [vp] * 7 + [i] * 7 + [vp]
+    lib.gdn_delta_varlen_ex.argtypes = [vp] * 7 + [i] * 6 + [f, i, i, vp]
+    lib.gdn_layer_varlen_ex.argtypes = [vp] * 14 + [i, i, vp, vp, vp, vp] + [i] * 9 + [f, i, vp, sz, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
                  "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_conv1d_varlen_capture",
-                 "gdn_delta_varlen_capture", "gdn_layer_varlen_capture"):
+                 "gdn_delta_varlen_capture", "gdn_layer_varlen_capture", "gdn_prepare_ex",
+                 "gdn_delta_varlen_ex", "gdn_layer_varlen_ex"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -396,3 +408,99 @@ def gdn_layer_varlen_capture(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_i
     del keep
     _check(rc)
     return out, conv_fin, state_fin, conv_updates, capsule
+
+
+# ------------------------------------------------------------------ rule / activation options
+
+def gdn_prepare_ex(y, a, b, A_log, dt_bias, *, H, HQ, K, V, opts, qk_norm=None, g_beta=None):
+    """gdn_prepare with GDN_OPT_* options (unused inputs may be None)."""
+    lib = load_library()
+    N = y.shape[0]
+    dev = y.device
+    f32 = torch.float32
+    qk_norm = torch.empty((2, N, HQ, K), dtype=f32, device=dev) if qk_norm is None else qk_norm
+    g_beta = torch.empty((2, N, H), dtype=f32, device=dev) if g_beta is None else g_beta
+    W = 2 * HQ * K + H * V
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
+            _ptr(dt_bias, "dt_bias", f32, (H,), dev),
+            _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
+            _ptr(g_beta, "g_beta", f32, (2, N, H), dev)]
+    _check(lib.gdn_prepare_ex(*args, N, H, HQ, K, V, int(opts), _dtype_code(y), _stream(dev)))
+    return qk_norm, g_beta
+
+
+def gdn_delta_varlen_ex(y, qk_norm, g_beta, offsets, state_init, *, H, HQ, K, V, opts, scale=0.0,
+                        out=None, state_fin=None):
+    """gdn_delta_varlen with GDN_OPT_* options (GDN_OPT_NO_RETRIEVE acts here)."""
+    lib = load_library()
+    N = y.shape[0]
+    B = offsets.numel() - 1
+    dev = y.device
+    f32 = torch.float32
+    out = torch.empty((N, H, V), dtype=y.dtype, device=dev) if out is None else out
+    state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev) if state_fin is None else state_fin
+    W = 2 * HQ * K + H * V
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
+            _ptr(g_beta, "g_beta", f32, (2, N, H), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", y.dtype, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev)]
+    _check(lib.gdn_delta_varlen_ex(*args, B, N, H, HQ, K, V, float(scale), int(opts),
+                                   _dtype_code(y), _stream(dev)))
+    return out, state_fin
+
+
+def gdn_layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, state_init, *,
+                        H, HQ, K, V, opts, Kc=4, D=1, act=GDN_ACT_SILU, scale=0.0,
+                        offsets_host=None, out=None, conv_fin=None, state_fin=None,
+                        workspace=None, cap=0, counts=None, active=None, conv_updates=None,
+                        capsule=None):
+    """The layer with GDN_OPT_* options and, with cap > 0, state-update capture.
+
+    Returns (out, conv_fin, state_fin) or, with capture, also (conv_updates, capsule)."""
+    lib = load_library()
+    N, W = qkv.shape
+    B = offsets.numel() - 1
+    L = (Kc - 1) * D
+    T = qkv.dtype
+    dev = qkv.device
+    f32 = torch.float32
+    dcode = _dtype_code(qkv)
+    if W != 2 * HQ * K + H * V:
+        raise GdnError(2, f"qkv width {W} != 2*HQ*K + H*V = {2 * HQ * K + H * V}")
+    out = torch.empty((N, H, V), dtype=T, device=dev) if out is None else out
+    conv_fin = torch.empty((B, W, L), dtype=T, device=dev) if conv_fin is None else conv_fin
+    state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev) if state_fin is None else state_fin
+    width = cap * (H + HQ * K + H * V)
+    cp = ap = None
+    if cap:
+        cp, ap = _capture_ptrs(counts, active, cap, B, dev)
+        conv_updates = (torch.empty((B, cap, W), dtype=T, device=dev) if conv_updates is None
+                        else conv_updates)
+        capsule = torch.empty((B, width), dtype=f32, device=dev) if capsule is None else capsule
+    need = gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dcode)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    hp, keep = _host_offsets(offsets_host)
+    args = [_ptr(qkv, "qkv", T, (N, W), dev), _ptr(w, "w", T, (W, Kc), dev),
+            _ptr(bias, "bias", T, (W,), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
+            _ptr(dt_bias, "dt_bias", f32, (H,), dev),
+            _ptr(offsets, "offsets", torch.int32, (B + 1,), dev), hp,
+            _ptr(conv_init, "conv_init", T, (B, W, L), dev),
+            _ptr(conv_fin, "conv_fin", T, (B, W, L), dev),
+            _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
+            _ptr(out, "out", T, (N, H, V), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, V, K), dev), int(opts), int(cap), cp, ap,
+            _ptr(conv_updates, "conv_updates", T, (B, cap, W), dev) if cap else None,
+            _ptr(capsule, "capsule", f32, (B, width), dev) if cap else None]
+    rc = lib.gdn_layer_varlen_ex(*args, B, N, H, HQ, K, V, Kc, D, act, float(scale), dcode,
+                                 _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                 _stream(dev))
+    del keep
+    _check(rc)
+    if cap:
+        return out, conv_fin, state_fin, conv_updates, capsule
+    return out, conv_fin, state_fin

@@ -143,6 +143,20 @@ struct Capture {
     float *capsule;
 };
 
+// Pointers the rule options need: the decay logits a unless GDN_OPT_NO_DECAY,
+// A_log and dt_bias for the softplus gate, the rate logits b unless
+// GDN_OPT_NO_BETA.
+static int check_opts(int opts, int N, const float *a, const float *b, const float *A_log,
+                      const float *dt_bias, const char *what) {
+    if (opts & ~GDN_OPT_ALL) return fail(GDN_ERR_UNSUPPORTED, "%s: unknown option bits 0x%x", what, opts);
+    const bool decay = !(opts & GDN_OPT_NO_DECAY);
+    if (decay && !(opts & GDN_OPT_GATE_EXP) && (!A_log || !dt_bias))
+        return fail(GDN_ERR_NULL, "%s: A_log / dt_bias is NULL (softplus gate)", what);
+    if (N > 0 && decay && !a) return fail(GDN_ERR_NULL, "%s: decay logits a is NULL", what);
+    if (N > 0 && !(opts & GDN_OPT_NO_BETA) && !b) return fail(GDN_ERR_NULL, "%s: rate logits b is NULL", what);
+    return GDN_OK;
+}
+
 static int check_capture(const Capture &c, const char *what) {
     if (c.cap < 1 || c.cap > GDN_CAPTURE_MAX)
         return fail(GDN_ERR_SHAPE, "%s: capture capacity %d outside [1, %d]", what, c.cap, GDN_CAPTURE_MAX);
@@ -224,30 +238,46 @@ int gdn_conv1d_varlen_capture(const void *x, const void *w, const void *bias,
                      stream, &c);
 }
 
-int gdn_prepare(const void *y, const float *a, const float *b, const float *A_log,
-                const float *dt_bias, float *qk_norm, float *g_beta, int N, int H, int HQ, int K,
-                int V, int dtype, void *stream) {
-    g_err[0] = 0;
+static int prepare_impl(const void *y, const float *a, const float *b, const float *A_log,
+                        const float *dt_bias, float *qk_norm, float *g_beta, int N, int H,
+                        int HQ, int K, int V, int opts, int dtype, void *stream) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     long width;
     int rc = check_heads(H, HQ, K, V, &width);
     if (rc) return rc;
     if (N < 0) return fail(GDN_ERR_SHAPE, "N=%d < 0", N);
-    if (N > 0 && (!y || !a || !b || !qk_norm || !g_beta)) return fail(GDN_ERR_NULL, "prepare: a required pointer is NULL");
-    if (!A_log || !dt_bias) return fail(GDN_ERR_NULL, "prepare: A_log / dt_bias is NULL");
+    if (N > 0 && (!y || !qk_norm || !g_beta)) return fail(GDN_ERR_NULL, "prepare: a required pointer is NULL");
+    rc = check_opts(opts, N, a, b, A_log, dt_bias, "prepare");
+    if (rc) return rc;
     if ((long)N * H > INT_MAX / 2 || (long)N * HQ * 32 > INT_MAX) return fail(GDN_ERR_OVERFLOW, "prepare dispatch exceeds int32");
     PrepParams p{};
     p.y = y; p.a = a; p.bl = b; p.A_log = A_log; p.dt_bias = dt_bias; p.qk = qk_norm; p.gb = g_beta;
-    p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
+    p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V; p.opts = opts;
     cudaError_t e = launch_prepare(p, dtype, static_cast<cudaStream_t>(stream), false);
     if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     return GDN_OK;
 }
 
+int gdn_prepare(const void *y, const float *a, const float *b, const float *A_log,
+                const float *dt_bias, float *qk_norm, float *g_beta, int N, int H, int HQ, int K,
+                int V, int dtype, void *stream) {
+    g_err[0] = 0;
+    return prepare_impl(y, a, b, A_log, dt_bias, qk_norm, g_beta, N, H, HQ, K, V, 0, dtype, stream);
+}
+
+int gdn_prepare_ex(const void *y, const float *a, const float *b, const float *A_log,
+                   const float *dt_bias, float *qk_norm, float *g_beta, int N, int H, int HQ,
+                   int K, int V, int opts, int dtype, void *stream) {
+    g_err[0] = 0;
+    return prepare_impl(y, a, b, A_log, dt_bias, qk_norm, g_beta, N, H, HQ, K, V, opts, dtype,
+                        stream);
+}
+
 static int delta_impl(const void *y, const float *qk_norm, const float *g_beta,
                       const int32_t *offsets, const float *state_init, void *out,
                       float *state_fin, int B, int N, int H, int HQ, int K, int V, float scale,
-                      int dtype, void *stream, const Capture *cap) {
+                      int dtype, void *stream, const Capture *cap, int opts = 0) {
+    if (opts & ~GDN_OPT_ALL) return fail(GDN_ERR_UNSUPPORTED, "delta: unknown option bits 0x%x", opts);
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     long width;
     int rc = check_heads(H, HQ, K, V, &width);
@@ -264,6 +294,7 @@ static int delta_impl(const void *y, const float *qk_norm, const float *g_beta,
     p.serial_max_len = INT_MAX;
     p.max_len = INT_MAX;
     p.conv_fin = nullptr;
+    p.opts = opts;
     if (cap) {
         p.cap = cap->cap; p.counts = cap->counts; p.active = cap->active; p.capsule = cap->capsule;
     }
@@ -279,6 +310,15 @@ int gdn_delta_varlen(const void *y, const float *qk_norm, const float *g_beta,
     g_err[0] = 0;
     return delta_impl(y, qk_norm, g_beta, offsets, state_init, out, state_fin, B, N, H, HQ, K,
                       V, scale, dtype, stream, nullptr);
+}
+
+int gdn_delta_varlen_ex(const void *y, const float *qk_norm, const float *g_beta,
+                        const int32_t *offsets, const float *state_init, void *out,
+                        float *state_fin, int B, int N, int H, int HQ, int K, int V,
+                        float scale, int opts, int dtype, void *stream) {
+    g_err[0] = 0;
+    return delta_impl(y, qk_norm, g_beta, offsets, state_init, out, state_fin, B, N, H, HQ, K,
+                      V, scale, dtype, stream, nullptr, opts);
 }
 
 int gdn_delta_varlen_capture(const void *y, const float *qk_norm, const float *g_beta,
@@ -327,7 +367,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
                       void *conv_fin, const float *state_init, void *out, float *state_fin,
                       int B, int N, int H, int HQ, int K, int V, int Kc, int D, int act,
                       float scale, int dtype, void *workspace, size_t ws_bytes, void *stream,
-                      const Capture *cap) {
+                      const Capture *cap, int opts = 0) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
     long width;
@@ -339,9 +379,11 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     if (L >= INT_MAX) return fail(GDN_ERR_OVERFLOW, "receptive field (Kc-1)*D exceeds int32");
     if (L > 4096) return fail(GDN_ERR_UNSUPPORTED, "receptive field L=%ld above 4096", L);
     if (Kc > 64) return fail(GDN_ERR_UNSUPPORTED, "conv width Kc=%d above 64", Kc);
-    if (!w || !A_log || !dt_bias || !offsets || !state_init || !state_fin ||
-        (N > 0 && (!qkv || !a || !b || !out)) || (L > 0 && (!conv_init || !conv_fin)))
+    if (!w || !offsets || !state_init || !state_fin || (N > 0 && (!qkv || !out)) ||
+        (L > 0 && (!conv_init || !conv_fin)))
         return fail(GDN_ERR_NULL, "layer: a required pointer is NULL");
+    rc = check_opts(opts, N, a, b, A_log, dt_bias, "layer");
+    if (rc) return rc;
     if ((long)B * H * V * 32 > INT_MAX || (long)B * width > INT_MAX)
         return fail(GDN_ERR_OVERFLOW, "layer dispatch size exceeds int32");
     if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
@@ -395,6 +437,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     cp.H = H; cp.HQ = HQ; cp.K = K; cp.V = V; cp.prep_max_len = serial_max;
     cp.header = hdr; cp.chunk_min_len = serial_max;
     cp.prep_cap = capsule ? cap->cap : 0;  // the captured prefix of chunked sequences
+    cp.opts = opts;
     cp.seq_order = run_chunked ? order : nullptr; cp.VT = V / 128;
     bool fused = false;
     mark_before(GDN_KERNEL_CONV, s);
@@ -404,7 +447,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     if (need_prep && !fused && N > 0) {
         PrepParams pp{};
         pp.y = y; pp.a = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias; pp.qk = qk; pp.gb = gb;
-        pp.N = N; pp.H = H; pp.HQ = HQ; pp.K = K; pp.V = V;
+        pp.N = N; pp.H = H; pp.HQ = HQ; pp.K = K; pp.V = V; pp.opts = opts;
         e = launch_prepare(pp, dtype, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
@@ -415,7 +458,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         cl.offsets = offsets; cl.seq_order = order; cl.header = hdr;
         cl.state_init = state_init; cl.state_fin = state_fin; cl.out = out;
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
-        cl.scale = eff_scale; cl.max_units = max_units;
+        cl.scale = eff_scale; cl.max_units = max_units; cl.opts = opts;
         mark_before(GDN_KERNEL_CHUNKED, s);
         cudaError_t ce = launch_delta_chunked(cl, s);
         mark_after(GDN_KERNEL_CHUNKED, s);
@@ -442,6 +485,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     // programmatic dependent launch, its state loads with the conv kernel
     dp.conv_x = qkv; dp.conv_init = conv_init; dp.conv_fin = L > 0 ? conv_fin : nullptr;
     dp.conv_L = (int)L;
+    dp.opts = opts;
     if (cap) {
         dp.cap = cap->cap; dp.counts = cap->counts; dp.active = cap->active;
         dp.conv_updates = cap->conv_updates; dp.capsule = cap->capsule;
@@ -497,6 +541,31 @@ int gdn_layer_varlen_capture(const void *qkv, const void *w, const void *bias, c
     return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
                       conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act, scale,
                       dtype, workspace, ws_bytes, stream, &c);
+}
+
+int gdn_layer_varlen_ex(const void *qkv, const void *w, const void *bias, const float *a,
+                        const float *b, const float *A_log, const float *dt_bias,
+                        const int32_t *offsets, const int32_t *offsets_host,
+                        const void *conv_init, void *conv_fin, const float *state_init,
+                        void *out, float *state_fin, int opts, int cap, const int32_t *counts,
+                        const int32_t *active, void *conv_updates, float *capsule, int B, int N,
+                        int H, int HQ, int K, int V, int Kc, int D, int act, float scale,
+                        int dtype, void *workspace, size_t ws_bytes, void *stream) {
+    g_err[0] = 0;
+    if (cap == 0)
+        return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
+                          conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act,
+                          scale, dtype, workspace, ws_bytes, stream, nullptr, opts);
+    const Capture c{cap, counts, active, conv_updates, capsule};
+    int rc = check_capture(c, "layer capture");
+    if (rc) return rc;
+    if (!conv_updates && !capsule) return fail(GDN_ERR_NULL, "layer capture: no capture buffer given");
+    if ((long)B * cap * (2L * HQ * K + (long)H * V) > INT_MAX ||
+        (long)B * cap * ((long)H + (long)HQ * K + (long)H * V) > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "layer capture buffers exceed int32 elements");
+    return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
+                      conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act, scale,
+                      dtype, workspace, ws_bytes, stream, &c, opts);
 }
 
 }  // extern "C"

@@ -101,6 +101,33 @@ __device__ __forceinline__ void decay_and_rate(float a, float dt_bias, float A_l
     beta = 1.f / (1.f + expf(-b));
 }
 
+// g and beta of token-head element i (head h) under the rule options
+// (GDN_OPT_*): g = 1 without decay, exp(a) for the exp gate, else the softplus
+// gate above; beta = 1 without a rate input, b raw, or sigmoid(b).
+__device__ __forceinline__ void gates_opt(const float *a, const float *b, size_t i,
+                                          const float *A_log, const float *dt_bias, int h,
+                                          int opts, float &g, float &beta) {
+    if (opts == 0) {
+        decay_and_rate(__ldg(a + i), __ldg(dt_bias + h), __ldg(A_log + h), __ldg(b + i), g, beta);
+        return;
+    }
+    g = 1.f;
+    if (!(opts & GDN_OPT_NO_DECAY)) {
+        float x = __ldg(a + i);
+        if (!(opts & GDN_OPT_GATE_EXP)) {
+            x += __ldg(dt_bias + h);
+            const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+            x = -expf(__ldg(A_log + h)) * softplus;
+        }
+        g = expf(x);
+    }
+    beta = 1.f;
+    if (!(opts & GDN_OPT_NO_BETA)) {
+        beta = __ldg(b + i);
+        if (!(opts & GDN_OPT_BETA_RAW)) beta = 1.f / (1.f + expf(-beta));
+    }
+}
+
 // log(g) for the same (token, value head), kept in the log domain.
 __device__ __forceinline__ float log_decay(float a, float dt_bias, float A_log) {
     const float x = a + dt_bias;

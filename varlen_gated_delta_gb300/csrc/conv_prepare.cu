@@ -103,8 +103,7 @@ __device__ __forceinline__ void store_pair(Vec16<T> &v, int q, float a, float b)
 
 __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, float &g,
                                            float &beta) {
-    decay_and_rate(__ldg(p.a + (size_t)t * p.H + h), __ldg(p.dt_bias + h), __ldg(p.A_log + h),
-                   __ldg(p.bl + (size_t)t * p.H + h), g, beta);
+    gates_opt(p.a, p.bl, (size_t)t * p.H + h, p.A_log, p.dt_bias, h, p.opts, g, beta);
 }
 
 // Block 0 of the conv launch checks the whole offsets array, records the
@@ -358,7 +357,7 @@ __global__ void __launch_bounds__(kConvThreads)
                     ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 if (cvalid && c < qk_width &&
                     (s_len[i] < p.prep_max_len || t - s_start[i] < p.prep_cap)) {
-                    const float r = rsqrtf(ss + 1e-12f);
+                    const float r = (p.opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(ss + 1e-12f);
                     const int plane = c >= p.HQ * p.K;
                     const int cc = c - plane * p.HQ * p.K;
                     float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
@@ -579,7 +578,7 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                             for (int o = lanes_per_head >> 1; o > 0; o >>= 1)
                                 ss += __shfl_xor_sync(0xffffffffu, ss, o);
                             if (cvalid && c < qk_width) {
-                                const float rr = rsqrtf(ss + 1e-12f);
+                                const float rr = (p.opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(ss + 1e-12f);
                                 const int plane = c >= p.HQ * p.K;
                                 const int cc = c - plane * p.HQ * p.K;
                                 float *dst = p.qk + (((size_t)plane * N + t) * p.HQ + cc / p.K) * p.K + cc % p.K;
@@ -699,7 +698,8 @@ __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const 
                 nk += __shfl_xor_sync(0xffffffffu, nk, off);
             }
             if (act) {
-                const float rq = rsqrtf(nq + 1e-12f), rk = rsqrtf(nk + 1e-12f);
+                const bool nn = p.opts & GDN_OPT_NO_QK_NORM;
+                const float rq = nn ? 1.f : rsqrtf(nq + 1e-12f), rk = nn ? 1.f : rsqrtf(nk + 1e-12f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
                     qdst[lane * VEC + e] = q[e] * rq;
@@ -718,7 +718,8 @@ __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const 
             }
             nq = group_sum<32>(nq);
             nk = group_sum<32>(nk);
-            const float rq = rsqrtf(nq + 1e-12f), rk = rsqrtf(nk + 1e-12f);
+            const bool nn = p.opts & GDN_OPT_NO_QK_NORM;
+                const float rq = nn ? 1.f : rsqrtf(nq + 1e-12f), rk = nn ? 1.f : rsqrtf(nk + 1e-12f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = lane + 32 * j;
@@ -733,8 +734,7 @@ __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const 
         if (i >= (long)p.N * p.H) return;
         const int h = (int)(i % p.H);
         float g, beta;
-        decay_and_rate(__ldg(p.a + i), __ldg(p.dt_bias + h), __ldg(p.A_log + h), __ldg(p.bl + i),
-                       g, beta);
+        gates_opt(p.a, p.bl, (size_t)i, p.A_log, p.dt_bias, h, p.opts, g, beta);
         p.gb[i] = g;
         p.gb[(size_t)p.N * p.H + i] = beta;
     }

@@ -91,6 +91,7 @@ struct ChunkParams {
     int B, N, H, HQ, V, VT;
     float scale;
     int tma_store;  // full output tiles leave through omap
+    int opts;       // GDN_OPT_* rule / activation options
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -150,13 +151,25 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // log2 g = -exp(A_log) softplus(a + dt_bias) log2(e), beta = sigmoid(b), with
 // the special-function-unit exponential and logarithm (this path computes in
 // bf16 operands; their few-ulp error is far below that rounding).
-// neg_ea_log2e = -exp(A_log) log2(e) of the head.
+// neg_ea_log2e = -exp(A_log) log2(e) of the head.  The rule options
+// (GDN_OPT_*) give log2 g = 0 without decay, a log2(e) for the exp gate,
+// beta = 1 without a rate input and beta = b for the raw rate.
 __device__ __forceinline__ void chunk_gates(float a, float b, bool valid, float dt_bias,
-                                            float neg_ea_log2e, float *lg, float *beta) {
-    const float x = a + dt_bias;
-    const float softplus = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
-    *lg = valid ? neg_ea_log2e * softplus : 0.f;
-    *beta = valid ? __fdividef(1.f, 1.f + __expf(-b)) : 0.f;
+                                            float neg_ea_log2e, int opts, float *lg,
+                                            float *beta) {
+    float l = 0.f, r = 1.f;
+    if (!(opts & GDN_OPT_NO_DECAY)) {
+        if (opts & GDN_OPT_GATE_EXP) {
+            l = a * 1.4426950408889634f;
+        } else {
+            const float x = a + dt_bias;
+            const float softplus = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+            l = neg_ea_log2e * softplus;
+        }
+    }
+    if (!(opts & GDN_OPT_NO_BETA)) r = (opts & GDN_OPT_BETA_RAW) ? b : __fdividef(1.f, 1.f + __expf(-b));
+    *lg = valid ? l : 0.f;
+    *beta = valid ? r : 0.f;
 }
 
 // f[lane] for a register array (a tree of selects on the lane bits, so the
@@ -307,8 +320,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int kh = h / G;
         const int qcol = kh * 128, kcol = HQ * 128 + kh * 128;
         const int vcol = 2 * HQ * 128 + h * V + vt * 128;
-        const float dtb = __ldg(p.dt_bias + h);
-        const float neg_ea = -expf(__ldg(p.A_log + h)) * 1.4426950408889634f;
+        const int opts = p.opts;
+        const bool need_a = !(opts & GDN_OPT_NO_DECAY), need_b = !(opts & GDN_OPT_NO_BETA);
+        const bool softplus_gate = need_a && !(opts & GDN_OPT_GATE_EXP);
+        const float dtb = softplus_gate ? __ldg(p.dt_bias + h) : 0.f;
+        const float neg_ea = softplus_gate ? -expf(__ldg(p.A_log + h)) * 1.4426950408889634f : 0.f;
         const size_t state_row = ((size_t)seq * H + h) * V + vt * 128 + row;
 
         // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
@@ -347,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         float ga = 0.f, gbl = 0.f;
         if (tid < 64) {
             if (tid < e - s) {
-                ga = ld_nc_f32(p.a + (size_t)(s + tid) * H + h);
-                gbl = ld_nc_f32(p.bl + (size_t)(s + tid) * H + h);
+                if (need_a) ga = ld_nc_f32(p.a + (size_t)(s + tid) * H + h);
+                if (need_b) gbl = ld_nc_f32(p.bl + (size_t)(s + tid) * H + h);
             }
-            chunk_gates(ga, gbl, tid < e - s, dtb, neg_ea, v_lg + tid, v_beta + tid);
+            chunk_gates(ga, gbl, tid < e - s, dtb, neg_ea, opts, v_lg + tid, v_beta + tid);
         }
 
 #pragma unroll 1
@@ -366,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (*s_abort) break;
             // the next chunk's gate logits -> shared memory, consumed by chunk_gates below
             if (tid < 64 && t0 + kC + tid < e) {
-                cp_async_4(v_na + tid, p.a + (size_t)(t0 + kC + tid) * H + h);
-                cp_async_4(v_nb + tid, p.bl + (size_t)(t0 + kC + tid) * H + h);
+                if (need_a) cp_async_4(v_na + tid, p.a + (size_t)(t0 + kC + tid) * H + h);
+                if (need_b) cp_async_4(v_nb + tid, p.bl + (size_t)(t0 + kC + tid) * H + h);
                 cp_async_commit();
             }
 
@@ -391,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (diag_warp && !krow) {
                 float dq[32];
                 ld32f(kColD1 + 64 + hc * 32, dq);
-                rq = rsqrtf(lane_pick(dq, lane) + 1e-12f);
+                rq = (opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(lane_pick(dq, lane) + 1e-12f);
             }
             float d1[32];  // columns [32 hc, 32 hc + 32) of K K^T (k rows) or Q K^T (q rows)
             if (!upper_warp) ld32f(kColD1 + hc * 32, d1);
@@ -401,13 +417,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const float lbC = __shfl_sync(0xffffffffu, hi, 31);
                 const float lb = hc == 0 ? lo : hi;  // t_row = 32 hc + lane
                 if (krow) {
-                    const float rk = rsqrtf(lane_pick(d1, lane) + 1e-12f);
+                    const float rk = (opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(lane_pick(d1, lane) + 1e-12f);
                     const float ck = lg2f(rk) - lb;
                     const float be = v_beta[t_row];
+                    // without retrieval A = 0 (T = I) and W = 0: Delta = diag(beta) V
+                    const float fr = (opts & GDN_OPT_NO_RETRIEVE) ? 0.f : 1.f;
                     v_lb[t_row] = lb;
                     v_ck[t_row] = ck;
-                    v_fa[t_row] = be * rk;
-                    v_ws[t_row] = be * rk * ex2f(lb);
+                    v_fa[t_row] = fr * be * rk;
+                    v_ws[t_row] = fr * be * rk * ex2f(lb);
                     v_c[t_row] = ex2f(lbC + ck);
                 } else {
                     v_fp[t_row] = p.scale * rq;
@@ -653,8 +671,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (tid < 64 && n + 1 < nchunks) {
                 const bool valid = t0 + kC + tid < e;
                 cp_async_wait_all();
-                chunk_gates(valid ? v_na[tid] : 0.f, valid ? v_nb[tid] : 0.f, valid, dtb, neg_ea,
-                            v_lg + tid, v_beta + tid);
+                chunk_gates(valid && need_a ? v_na[tid] : 0.f, valid && need_b ? v_nb[tid] : 0.f,
+                            valid, dtb, neg_ea, opts, v_lg + tid, v_beta + tid);
             }
             wait_mma();
 
@@ -834,6 +852,7 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     p.B = c.B; p.N = c.N; p.H = c.H; p.HQ = c.HQ; p.V = c.V; p.VT = c.V / 128;
     p.scale = c.scale;
     p.tma_store = tma_store;
+    p.opts = c.opts;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(chunked_delta_kernel,

@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kSerialThreads)
     const T *y = static_cast<const T *>(p.y);
     T *out = static_cast<T *>(p.out);
     const float scale = p.scale;
+    const bool retrieve = !(p.opts & GDN_OPT_NO_RETRIEVE);
 
     float qc[EPL], kc[EPL], vc[RG], gc = 1.f, bc = 0.f;
     auto fetch = [&](int t, float *q, float *k, float *v, float &g, float &beta) {
@@ -239,7 +240,8 @@ __global__ void __launch_bounds__(kSerialThreads)
         }
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
-            const float delta = bc * (vc[r] - gc * sk[r]);
+            // RETRIEVE (delta rules): subtract the decayed state's retrieval S k
+            const float delta = bc * (retrieve ? vc[r] - gc * sk[r] : vc[r]);
             const float o = gc * sq[r] + delta * kq;
 #pragma unroll
             for (int u = 0; u < EPL; ++u) S[r][u] = fmaf(gc, S[r][u], delta * kc[u]);

@@ -8,6 +8,8 @@
 
 #include <utility>
 
+#include "gdn.h"  // GDN_OPT_* rule / activation options
+
 namespace gdn {
 
 // Workspace header written by the device (first 256 bytes of a workspace).
@@ -34,6 +36,7 @@ struct ConvParams {
     const float *a, *bl, *A_log, *dt_bias;
     int H, HQ, K, V, prep_max_len;
     int prep_cap;  // also prepare the first prep_cap tokens of every sequence
+    int opts;      // GDN_OPT_* rule / activation options
     // block 0 validates offsets and writes counts when header != nullptr;
     // with seq_order != nullptr it also lists the sequences of at least
     // chunk_min_len tokens, longest first, and sets n_units = count * H * VT
@@ -48,6 +51,7 @@ struct PrepParams {
     const float *a, *bl, *A_log, *dt_bias;
     float *qk, *gb;
     int N, H, HQ, K, V;
+    int opts;  // GDN_OPT_*
 };
 
 struct DeltaParams {
@@ -77,6 +81,7 @@ struct DeltaParams {
     const int32_t *active;
     void *conv_updates;
     float *capsule;
+    int opts;  // GDN_OPT_* (GDN_OPT_NO_RETRIEVE acts here)
 };
 
 // Launch `kernel` on `s`; with pdl the launch may overlap the previous kernel
@@ -118,6 +123,7 @@ struct ChunkLaunch {
     int B, N, H, HQ, V, W;
     float scale;
     long max_units;  // upper bound on work units (grid sizing)
+    int opts;        // GDN_OPT_*
 };
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
