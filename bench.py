@@ -38,6 +38,9 @@ def _args():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "ragged", "long", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rule", default="gated_delta",
+                    choices=["gated_delta", "delta", "gated", "linear"],
+                    help="update rule (delta: no decay; gated: no retrieval; linear: neither)")
     ap.add_argument("--capture", type=int, default=0,
                     help="state-update capture capacity (1..8): time gdn_layer_varlen_capture "
                          "with every sequence asking for that many tokens")
@@ -202,9 +205,14 @@ def run_reference(args, wl):
 
     cap = args.capture
     counts = np.full(len(offs) - 1, cap, np.int32)
+    opts = {"gated_delta": 0, "delta": 1, "gated": 2, "linear": 3}[args.rule]
 
     def step():
-        if cap:
+        if opts:
+            oracle.layer_varlen_ex(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ, sample_wl.K,
+                                   sample_wl.V, sample_wl.Kc, sample_wl.D, opts,
+                                   silu=sample_wl.silu, scale=d["scale"], act_dtype=act)
+        elif cap:
             oracle.layer_varlen_capture(*inputs, offs, ci, si, sample_wl.H, sample_wl.HQ,
                                         sample_wl.K, sample_wl.V, sample_wl.Kc, sample_wl.D,
                                         counts, cap, silu=sample_wl.silu, scale=d["scale"],
@@ -227,7 +235,8 @@ def run_reference(args, wl):
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample": sample, **({"capture": cap} if cap else {})},
+        "config": {"workload": wl.name, "sample": sample, **({"capture": cap} if cap else {}),
+                   **({"rule": args.rule} if opts else {})},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -308,12 +317,20 @@ def run_ours(args, wl):
         capsule = torch.empty((B, cap * (wl.H + wl.HQ * wl.K + wl.H * wl.V)),
                               dtype=torch.float32, device=dev)
 
+    opts = gdn.RULE_OPTS[args.rule]
+
     def call(qkv, a, b, offsets):
         # decode-style carry: the final states overwrite the initial ones in place
         kw = dict(H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act,
                   scale=d["scale"], offsets_host=offs, out=out, conv_fin=conv_state,
                   state_fin=state, workspace=ws)
-        if cap:
+        if opts:
+            gdn.gdn_layer_varlen_ex(qkv, d["w"], d["bias"], a, b, d["A_log"], d["dt_bias"],
+                                    offsets, conv_state, state, opts=opts, cap=cap,
+                                    counts=counts if cap else None,
+                                    conv_updates=conv_upd if cap else None,
+                                    capsule=capsule if cap else None, **kw)
+        elif cap:
             gdn.gdn_layer_varlen_capture(qkv, d["w"], d["bias"], a, b, d["A_log"], d["dt_bias"],
                                          offsets, conv_state, state, counts, cap=cap,
                                          conv_updates=conv_upd, capsule=capsule, **kw)
@@ -462,14 +479,15 @@ def run_ours(args, wl):
                        "V": wl.V, "Kc": wl.Kc, "D": wl.D, "state_carry": "in place",
                        "l2": "inputs larger than L2 (129 MB)",
                        "parallelism": f"replicas x{world}",
-                       **({"capture": cap} if cap else {})},
+                       **({"capture": cap} if cap else {}),
+                       **({"rule": args.rule} if opts else {})},
             "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
             "roofline": roof,
             "e2e": {"value": world * N * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "timing": "CUDA graph replay of one gdn_layer_varlen%s call per step"
-                      % ("_capture" if cap else ""),
+                      % ("_ex" if opts else "_capture" if cap else ""),
             "ms_per_step_eager": eager_ms / args.steps,
             "clocks": clocks,
         }
