@@ -52,6 +52,7 @@ def _load():
                                                + [ctypes.c_double, i])
         lib.oracle_layer_varlen_ex.argtypes = ([dp] * 7 + [ip] + [dp] * 5 + [i] * 9
                                                + [ctypes.c_double, i, i])
+        lib.oracle_dense_delta.argtypes = [dp] * 8 + [i] * 5 + [ctypes.c_double]
         lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -231,6 +232,20 @@ def layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, stat
         B, N, H, HQ, K, V, Kc, D, int(bool(silu)), float(scale), _ROUND[act_dtype], int(opts))
     _check(rc, "layer_varlen_ex")
     return out, conv_fin, state_fin
+
+
+def dense_delta(q, k, v, g, beta, state_init, per_channel=False, scale=0.0, want_state=True):
+    """Dense-layout recurrence: q, k, v [B,S,H,n], g [B,S,H] or [B,S,H,n], beta [B,S,H],
+    state_init [B,H,n,n] or None (zero).  Returns (out, state_fin or None)."""
+    q, k, v, g, beta, state_init = map(_f64, (q, k, v, g, beta, state_init))
+    B, S, H, n = q.shape
+    out = np.zeros((B, S, H, n))
+    fin = np.zeros((B, H, n, n)) if want_state else None
+    rc = _load().oracle_dense_delta(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_init),
+                                    _p(out), _p(fin), B, S, H, n, int(bool(per_channel)),
+                                    float(scale))
+    _check(rc, "dense_delta")
+    return out, fin
 
 
 def _active(active):

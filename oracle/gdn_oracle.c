@@ -25,6 +25,8 @@
  *   [paged_ssm.rs, GatedDeltaNet attributes update_rule, gate_activation,
  *    beta_activation, qk_l2_norm; flags DECAY, RETRIEVE, SOFTPLUS, BETA,
  *    SIGMOID, NORM]  the rule and activation variants (oracle_*_ex).
+ *   [rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet]  the dense-layout call,
+ *       optional per-key-channel gate (oracle_dense_delta).
  *   [paged_ssm.rs, CONV_CAPTURE_* and DELTA_CAPTURE_* kernels]
  *       capture of the first min(counts[b], capacity, len) tokens' updates:
  *       raw conv input rows and the (g, normalised k, beta-scaled delta)
@@ -454,6 +456,56 @@ int oracle_layer_varlen_ex(const double *qkv, const double *w, const double *bia
     free(qk);
     free(gb);
     return rc;
+}
+
+/*
+ * [rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet (dense layout, gate_per_channel,
+ *  carry_state), with the recurrence of the DELTA kernel of paged_ssm.rs]
+ *   q, k, v, out [B, S, H, n]; g [B, S, H] or, per channel, [B, S, H, n];
+ *   beta [B, S, H]; state [B, H, n, n] (row vi, column key ki).
+ * Per (b, h, vi) and token in order: S[vi, :] *= g (per column when per
+ * channel); r = S[vi, :] . k; delta = beta (v[vi] - r); S[vi, :] += delta k;
+ * out[vi] = scale (S[vi, :] . q).  q, k, g, beta are used as given.  A NULL
+ * state_init starts from zero; a NULL state_fin is not written.  The thunk
+ * names its math without stating it; this is the DELTA kernel's order.
+ */
+int oracle_dense_delta(const double *q, const double *k, const double *v, const double *g,
+                       const double *beta, const double *state_init, double *out,
+                       double *state_fin, int B, int S, int H, int n, int per_channel,
+                       double scale) {
+    if (B < 1 || S < 0 || H < 1 || n < 1) return ORACLE_ERR_SHAPE;
+    if (scale == 0.0) scale = 1.0 / sqrt((double)n);
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double *St = (double *)malloc(sizeof(double) * (size_t)n * n);
+            const size_t head = ((size_t)b * H + h) * n * n;
+            for (size_t i = 0; i < (size_t)n * n; ++i) St[i] = state_init ? state_init[head + i] : 0.0;
+            for (int t = 0; t < S; ++t) {
+                const size_t row = ((size_t)b * S + t) * H + h;
+                const double *qt = q + row * n, *kt = k + row * n, *vt = v + row * n;
+                for (int vi = 0; vi < n; ++vi) {
+                    double *sr = St + (size_t)vi * n;
+                    double retrieval = 0.0;
+                    for (int i = 0; i < n; ++i) {
+                        sr[i] *= per_channel ? g[row * n + i] : g[row];
+                        retrieval += kt[i] * sr[i];
+                    }
+                    const double delta = beta[row] * (vt[vi] - retrieval);
+                    double readout = 0.0;
+                    for (int i = 0; i < n; ++i) {
+                        sr[i] += kt[i] * delta;
+                        readout += qt[i] * sr[i];
+                    }
+                    out[row * n + vi] = readout * scale;
+                }
+            }
+            if (state_fin)
+                for (size_t i = 0; i < (size_t)n * n; ++i) state_fin[head + i] = St[i];
+            free(St);
+        }
+    }
+    return ORACLE_OK;
 }
 
 /* Number of OpenMP threads the oracle's parallel loops use (1 without OpenMP). */

@@ -607,3 +607,56 @@ def test_layer_options_zero_is_the_default_layer():
     got = oracle.layer_varlen_ex(*args, 0, act_dtype="f32")
     for x, r in zip(got, ref):
         np.testing.assert_array_equal(x, r)
+
+
+# ------------------------------------------------------------------ dense layout (f4) and
+# per-key-channel gate (f3): rlx-cpu thunk/types.rs Thunk::GatedDeltaNet
+
+def _dense_problem(seed, B=2, S=6, H=2, n=5):
+    rng = _rng(seed)
+    q = rng.standard_normal((B, S, H, n))
+    k = rng.standard_normal((B, S, H, n))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, S, H, n))
+    g = rng.uniform(0.3, 1.0, (B, S, H))
+    gc = rng.uniform(0.3, 1.0, (B, S, H, n))
+    beta = rng.uniform(0.0, 1.0, (B, S, H))
+    S0 = rng.standard_normal((B, H, n, n)) * 0.3
+    return q, k, v, g, gc, beta, S0
+
+
+def test_dense_scalar_gate_equals_the_varlen_recurrence():
+    q, k, v, g, _, beta, S0 = _dense_problem(31)
+    B, S, H, n = q.shape
+    out, fin = oracle.dense_delta(q, k, v, g, beta, S0, scale=0.7)
+    # the same problem in the packed layout (HQ = H, prepared q and k as given)
+    N = B * S
+    y = np.concatenate([q.reshape(N, H * n), k.reshape(N, H * n), v.reshape(N, H * n)], axis=1)
+    qk = np.stack([q.reshape(N, H, n), k.reshape(N, H, n)])
+    gb = np.stack([g.reshape(N, H), beta.reshape(N, H)])
+    o2, f2 = oracle.delta_varlen(y, qk, gb, [b * S for b in range(B + 1)], S0, H, H, n, n,
+                                 scale=0.7)
+    np.testing.assert_allclose(out.reshape(N, H, n), o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(fin, f2, rtol=1e-12, atol=1e-12)
+
+
+def test_dense_per_channel_gate_reduces_and_decays_columns():
+    q, k, v, g, gc, beta, S0 = _dense_problem(32)
+    # a per-channel gate equal in every channel is the scalar gate
+    o1, f1 = oracle.dense_delta(q, k, v, g, beta, S0)
+    o2, f2 = oracle.dense_delta(q, k, v, np.repeat(g[..., None], q.shape[-1], -1), beta, S0,
+                                per_channel=True)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(f2, f1, rtol=1e-13, atol=1e-13)
+    # with beta = 0 nothing is written: each key column decays by its own product
+    o3, f3 = oracle.dense_delta(q, k, v, gc, np.zeros_like(beta), S0, per_channel=True)
+    decay = np.prod(gc, axis=1)                                 # [B, H, n]
+    np.testing.assert_allclose(f3, S0 * decay[:, :, None, :], rtol=1e-12, atol=1e-14)
+    # and the read-out is the decayed state applied to q, scaled
+    cum = np.cumprod(gc, axis=1)                                # [B, S, H, n]
+    ref = np.einsum("bhij,bshj,bshj->bshi", S0, cum, q) / np.sqrt(q.shape[-1])
+    np.testing.assert_allclose(o3, ref, rtol=1e-12, atol=1e-13)
+    # no initial state means a zero one
+    o4, _ = oracle.dense_delta(q, k, v, g, beta, None)
+    o5, _ = oracle.dense_delta(q, k, v, g, beta, np.zeros_like(S0))
+    np.testing.assert_array_equal(o4, o5)
