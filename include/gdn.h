@@ -358,6 +358,34 @@ GDN_API int gdn_layer_varlen_capture(const void *qkv, const void *w, const void 
                                      int act, float scale, int dtype, void *workspace,
                                      size_t ws_bytes, void *stream);
 
+/*
+ * gdn_gated_delta_dense - the recurrence on the dense layout of the
+ * GatedDeltaNet CPU thunk (rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet:
+ * q, k, v [b, s, h, n]; g, beta [b, s, h]; gate_per_channel makes g
+ * [b, s, h, n]; state [b, h, n, n] resumed from and written back in place
+ * with carry_state).  The thunk defers its math to an operator not on the
+ * page; this call applies the DELTA kernel of paged_ssm.rs to the values as
+ * given, per (sequence, head, state row vi) and token in order:
+ *   S <- S diag(g) (scalar g: S <- g S);  r = S k;  delta = beta (v[vi] - r);
+ *   S <- S + delta k^T;  out[vi] = scale (S q)[vi]
+ * with no convolution and no normalisation (q, k, g, beta as passed).
+ *
+ *   q, k, v, out  device T [B, S, H, n]   (n <= 256; v uses n value channels)
+ *   g             device fp32 [B, S, H], or [B, S, H, n] when gate_per_channel
+ *   beta          device fp32 [B, S, H]
+ *   state_init    device fp32 [B, H, n, n] (row vi, column key ki) or NULL for
+ *                 a zero initial state (carry_state false)
+ *   state_fin     device fp32 [B, H, n, n] or NULL (not written); may alias
+ *                 state_init (in-place carry)
+ *   scale         0 means 1/sqrt(n)
+ * Errors: GDN_ERR_SHAPE, GDN_ERR_OVERFLOW, GDN_ERR_NULL, GDN_ERR_UNSUPPORTED
+ * (dtype), GDN_ERR_CUDA.  Sequences run on the token-serial kernel.
+ */
+GDN_API int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const float *g,
+                                  const float *beta, const float *state_init, void *out,
+                                  float *state_fin, int B, int S, int H, int n,
+                                  int gate_per_channel, float scale, int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -220,3 +220,14 @@ def test_option_calls_validate_option_bits_and_needed_inputs(lib):
                               None) == 5
     assert lib.gdn_delta_varlen_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 16, 4, 2, 16, 16,
                                    0.0, 99, 0, None) == 5
+
+
+def test_dense_call_validation(lib):
+    dense = lambda B=2, S=4, H=2, n=16, perch=0, q=FAKE: lib.gdn_gated_delta_dense(
+        q, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, B, S, H, n, perch, 0.0, 0, None)
+    assert dense(n=257) == 2
+    assert dense(n=0) == 2
+    assert dense(B=0) == 2
+    assert dense(perch=2) == 2
+    assert dense(q=None) == 1
+    assert dense(B=1 << 16, S=1 << 10, H=64, n=128) == 3

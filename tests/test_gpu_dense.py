@@ -1,0 +1,84 @@
+"""GPU parity of the dense-layout call (rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet:
+q, k, v [b, s, h, n], g [b, s, h] or per key channel [b, s, h, n], beta [b, s, h],
+state [b, h, n, n] carried in place) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_gated_delta_gb300 as gdn
+from gdn_testlib import cpu64, max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from varlen_gated_delta_gb300 import build
+    build.build()
+    gdn.load_library()
+    yield
+
+
+def _inputs(B, S, H, n, dt, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    r = lambda *s: torch.randn(*s, generator=g, device=DEV)
+    q = r(B, S, H, n).to(dt)
+    k = torch.nn.functional.normalize(r(B, S, H, n), dim=-1).to(dt)
+    v = r(B, S, H, n).to(dt)
+    gate = torch.sigmoid(r(B, S, H) + 2.0)
+    gate_c = torch.sigmoid(r(B, S, H, n) + 2.0)
+    beta = torch.sigmoid(r(B, S, H))
+    state = r(B, H, n, n) * 0.1
+    return q, k, v, gate, gate_c, beta, state
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n", [16, 100, 128])
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_dense_matches_oracle(dt, n, per_channel):
+    B, S, H = 3, 9, 4
+    q, k, v, gate, gate_c, beta, state = _inputs(B, S, H, n, dt, 101 + n)
+    gg = gate_c if per_channel else gate
+    keep = state.clone()
+    out, fin = gdn.gdn_gated_delta_dense(q, k, v, gg, beta, state, gate_per_channel=per_channel,
+                                         scale=0.5)
+    o_ref, s_ref = oracle.dense_delta(cpu64(q), cpu64(k), cpu64(v), cpu64(gg), cpu64(beta),
+                                      cpu64(keep), per_channel=per_channel, scale=0.5)
+    torch.cuda.synchronize()
+    assert fin.data_ptr() == state.data_ptr()           # carried in place
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(fin), s_ref)
+    tol = TOL[dt]
+    assert eo <= tol and es <= tol, f"out {eo:.3e} (max-abs {max_abs(cpu64(out), o_ref):.3e}), state {es:.3e}"
+
+
+def test_dense_without_carried_state_starts_from_zero():
+    B, S, H, n = 2, 5, 2, 128
+    q, k, v, gate, _, beta, _ = _inputs(B, S, H, n, torch.float32, 7)
+    out, fin = gdn.gdn_gated_delta_dense(q, k, v, gate, beta)
+    o_ref, _ = oracle.dense_delta(cpu64(q), cpu64(k), cpu64(v), cpu64(gate), cpu64(beta), None,
+                                  want_state=False)
+    torch.cuda.synchronize()
+    assert fin is None
+    assert rel_l2(cpu64(out), o_ref) <= 1e-4
+
+
+def test_dense_split_sequence_resume_equals_one_call():
+    B, S, H, n = 2, 12, 2, 64
+    q, k, v, gate, gate_c, beta, state = _inputs(B, S, H, n, torch.float32, 9)
+    one = state.clone()
+    o_all, _ = gdn.gdn_gated_delta_dense(q, k, v, gate_c, beta, one, gate_per_channel=True)
+    st = state.clone()
+    parts = []
+    for a, b in ((0, 5), (5, 12)):
+        sl = lambda x: x[:, a:b].contiguous()
+        o, _ = gdn.gdn_gated_delta_dense(sl(q), sl(k), sl(v), sl(gate_c), sl(beta), st,
+                                         gate_per_channel=True)
+        parts.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(parts, 1), o_all)
+    assert torch.equal(st, one)

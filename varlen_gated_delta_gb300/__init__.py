@@ -29,7 +29,7 @@ __all__ = [
     "STATUS_NAMES", "GDN_CAPTURE_MAX", "gdn_conv1d_varlen_capture", "gdn_delta_varlen_capture",
     "gdn_layer_varlen_capture", "gdn_prepare_ex", "gdn_delta_varlen_ex", "gdn_layer_varlen_ex",
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
-    "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS",
+    "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,12 +90,13 @@ def load_library():
     lib.gdn_prepare_ex.argtypes = [vp] * 7 + [i] * 7 + [vp]
     lib.gdn_delta_varlen_ex.argtypes = [vp] * 7 + [i] * 6 + [f, i, i, vp]
     lib.gdn_layer_varlen_ex.argtypes = [vp] * 14 + [i, i, vp, vp, vp, vp] + [i] * 9 + [f, i, vp, sz, vp]
+    lib.gdn_gated_delta_dense.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
                  "gdn_workspace_status", "gdn_set_chunk_min_len", "gdn_conv1d_varlen_capture",
                  "gdn_delta_varlen_capture", "gdn_layer_varlen_capture", "gdn_prepare_ex",
-                 "gdn_delta_varlen_ex", "gdn_layer_varlen_ex"):
+                 "gdn_delta_varlen_ex", "gdn_layer_varlen_ex", "gdn_gated_delta_dense"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -504,3 +505,35 @@ def gdn_layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, 
     if cap:
         return out, conv_fin, state_fin, conv_updates, capsule
     return out, conv_fin, state_fin
+
+
+# ------------------------------------------------------------------ dense layout
+
+def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=False, scale=0.0,
+                          out=None, state_fin=None, carry_state=None):
+    """Recurrence on dense q, k, v [B, S, H, n] (g [B,S,H] or [B,S,H,n], beta [B,S,H]).
+
+    ``state`` [B, H, n, n] f32 is the initial state (None: zero).  With
+    ``carry_state`` (default: a state was given) the final state is written
+    back into ``state`` in place.  Returns (out [B,S,H,n], final state or None)."""
+    lib = load_library()
+    B, S, H, n = q.shape
+    T = q.dtype
+    dev = q.device
+    f32 = torch.float32
+    carry = (state is not None) if carry_state is None else bool(carry_state)
+    if carry and state is None:
+        raise GdnError(1, "carry_state needs a state tensor")
+    out = torch.empty((B, S, H, n), dtype=T, device=dev) if out is None else out
+    if state_fin is None and carry:
+        state_fin = state
+    gshape = (B, S, H, n) if gate_per_channel else (B, S, H)
+    args = [_ptr(q, "q", T, (B, S, H, n), dev), _ptr(k, "k", T, (B, S, H, n), dev),
+            _ptr(v, "v", T, (B, S, H, n), dev), _ptr(g, "g", f32, gshape, dev),
+            _ptr(beta, "beta", f32, (B, S, H), dev),
+            _ptr(state, "state", f32, (B, H, n, n), dev),
+            _ptr(out, "out", T, (B, S, H, n), dev),
+            _ptr(state_fin, "state_fin", f32, (B, H, n, n), dev)]
+    _check(lib.gdn_gated_delta_dense(*args, B, S, H, n, int(bool(gate_per_channel)), float(scale),
+                                     _dtype_code(q), _stream(dev)))
+    return out, state_fin

@@ -543,6 +543,31 @@ int gdn_layer_varlen_capture(const void *qkv, const void *w, const void *bias, c
                       dtype, workspace, ws_bytes, stream, &c);
 }
 
+int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *state_init, void *out,
+                          float *state_fin, int B, int S, int H, int n, int gate_per_channel,
+                          float scale, int dtype, void *stream) {
+    g_err[0] = 0;
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+    if (B < 1 || S < 0 || H < 1 || n < 1)
+        return fail(GDN_ERR_SHAPE, "dense: need B>=1, S>=0, H>=1, n>=1 (B=%d S=%d H=%d n=%d)", B, S, H, n);
+    if (n > 256) return fail(GDN_ERR_SHAPE, "dense: head size n=%d above 256", n);
+    if (gate_per_channel != 0 && gate_per_channel != 1)
+        return fail(GDN_ERR_SHAPE, "dense: gate_per_channel must be 0 or 1");
+    if ((long)B * S * H * n > INT_MAX || (long)B * H * n * 32 > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "dense: tensor or dispatch size exceeds int32");
+    if (S > 0 && (!q || !k || !v || !g || !beta || !out))
+        return fail(GDN_ERR_NULL, "dense: a required pointer is NULL");
+    if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
+    DenseParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_init = state_init; p.out = out;
+    p.state_fin = state_fin; p.B = B; p.S = S; p.H = H; p.n = n; p.per_channel = gate_per_channel;
+    p.scale = scale == 0.f ? 1.f / std::sqrt((float)n) : scale;
+    cudaError_t e = launch_delta_dense(p, dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dense kernel launch");
+    return GDN_OK;
+}
+
 int gdn_layer_varlen_ex(const void *qkv, const void *w, const void *bias, const float *a,
                         const float *b, const float *A_log, const float *dt_bias,
                         const int32_t *offsets, const int32_t *offsets_host,

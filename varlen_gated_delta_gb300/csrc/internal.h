@@ -125,6 +125,20 @@ struct ChunkLaunch {
     long max_units;  // upper bound on work units (grid sizing)
     int opts;        // GDN_OPT_*
 };
+// Dense-layout recurrence (q, k, v, out [B, S, H, n] T; g [B, S, H] or, with
+// per_channel, [B, S, H, n] f32; beta [B, S, H] f32; state [B, H, n, n] f32,
+// state_init NULL = zero, state_fin NULL = not written).
+struct DenseParams {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const float *state_init;
+    void *out;
+    float *state_fin;
+    int B, S, H, n, per_channel;
+    float scale;
+};
+cudaError_t launch_delta_dense(const DenseParams &p, int dtype, cudaStream_t s);
+
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
 
