@@ -41,6 +41,9 @@ def _args():
     ap.add_argument("--rule", default="gated_delta",
                     choices=["gated_delta", "delta", "gated", "linear"],
                     help="update rule (delta: no decay; gated: no retrieval; linear: neither)")
+    ap.add_argument("--dense", default=None, choices=["scalar", "per_channel"],
+                    help="time the dense-layout call (q, k, v [B, S, H, n]) on the workload's "
+                         "batch and head geometry (equal lengths), scalar or per-channel gate")
     ap.add_argument("--capture", type=int, default=0,
                     help="state-update capture capacity (1..8): time gdn_layer_varlen_capture "
                          "with every sequence asking for that many tokens")
@@ -498,6 +501,80 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_dense(args, wl):
+    """The dense-layout call (rlx-cpu GatedDeltaNet thunk layout) on the
+    workload's batch, length and head geometry (n = K = V, H heads for q/k/v)."""
+    import torch
+
+    import varlen_gated_delta_gb300 as gdn
+    from varlen_gated_delta_gb300 import build as gdn_build
+
+    lens = wl.lengths()
+    if len(set(lens)) != 1 or wl.K != wl.V:
+        raise SystemExit("--dense needs equal sequence lengths and K == V")
+    B, S, H, n = len(lens), lens[0], wl.H, wl.K
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gdn_build.build()
+    gdn.load_library()
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 77)
+    r = lambda *sh: torch.randn(*sh, generator=g, device=dev)
+    T = wl.torch_dtype
+    q, v = r(B, S, H, n).to(T), r(B, S, H, n).to(T)
+    k = torch.nn.functional.normalize(r(B, S, H, n), dim=-1).to(T)
+    perch = args.dense == "per_channel"
+    gate = torch.sigmoid(r(B, S, H, n) + 2.0) if perch else torch.sigmoid(r(B, S, H) + 2.0)
+    beta = torch.sigmoid(r(B, S, H))
+    state = r(B, H, n, n) * 0.05
+    out = torch.empty((B, S, H, n), dtype=T, device=dev)
+
+    def step():
+        gdn.gdn_gated_delta_dense(q, k, v, gate, beta, state, gate_per_channel=perch, out=out)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    esz = 2 if T == torch.bfloat16 else 4
+    N = B * S
+    kbytes = (2 * B * H * n * n * 4 + 4 * N * H * n * esz + N * H * 4
+              + (N * H * n * 4 if perch else N * H * 4))
+    hbm, _, _, peak_src = _peaks()
+    achieved = kbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "gated-delta dense tokens/s", "value": N / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name}-dense", "B": B, "S": S, "H": H, "n": n,
+                   "gate": args.dense, "state_carry": "in place"},
+        "roofline": {"kernel": "delta_dense_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "algorithmic_bytes": kbytes, "kernel_ms": ms,
+                     "peak_source": f"hbm_gbs of {peak_src}"},
+        "timing": "CUDA graph replay of one gdn_gated_delta_dense call per step",
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = _args()
     from varlen_gated_delta_gb300 import workloads as W
@@ -507,6 +584,8 @@ def main():
                       name=f"{wl.name}-{args.lens.replace(',', 'x')}")
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.dense:
+        run_dense(args, wl)
     else:
         run_ours(args, wl)
 

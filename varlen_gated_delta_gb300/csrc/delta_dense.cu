@@ -21,7 +21,8 @@ namespace {
 
 constexpr int kDenseThreads = 128;
 
-template <typename T, int KP, int RG, bool PERCH>
+// VEC4: n % 4 == 0 and 16-byte aligned states (state rows move as float4).
+template <typename T, int KP, int RG, bool PERCH, bool VEC4>
 __global__ void __launch_bounds__(kDenseThreads) delta_dense_kernel(const DenseParams p) {
     constexpr int EPL = 16;           // state values per lane per row
     constexpr int LPR = KP / EPL;     // lanes per row
@@ -50,14 +51,21 @@ __global__ void __launch_bounds__(kDenseThreads) delta_dense_kernel(const DenseP
 #pragma unroll
     for (int r = 0; r < RG; ++r)
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 4; ++m) {
+            const bool in = p.state_init != nullptr && vi[r] < n;
+            if constexpr (VEC4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (in && kidx[m] < n)
+                    x = *reinterpret_cast<const float4 *>(p.state_init + (head + vi[r]) * n + kidx[m]);
+                st[r][4 * m] = x.x; st[r][4 * m + 1] = x.y; st[r][4 * m + 2] = x.z; st[r][4 * m + 3] = x.w;
+            } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int kk = kidx[m] + u;
-                st[r][4 * m + u] = (p.state_init != nullptr && vi[r] < n && kk < n)
-                                       ? p.state_init[(head + vi[r]) * n + kk]
-                                       : 0.f;
+                for (int u = 0; u < 4; ++u) {
+                    const int kk = kidx[m] + u;
+                    st[r][4 * m + u] = (in && kk < n) ? p.state_init[(head + vi[r]) * n + kk] : 0.f;
+                }
             }
+        }
 
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
@@ -119,10 +127,18 @@ __global__ void __launch_bounds__(kDenseThreads) delta_dense_kernel(const DenseP
     for (int r = 0; r < RG; ++r)
         if (vi[r] < n)
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < 4; ++m) {
+                float *dst = p.state_fin + (head + vi[r]) * n + kidx[m];
+                if constexpr (VEC4) {
+                    if (kidx[m] < n)  // streaming store: not read again by this call
+                        __stcs(reinterpret_cast<float4 *>(dst),
+                               make_float4(st[r][4 * m], st[r][4 * m + 1], st[r][4 * m + 2], st[r][4 * m + 3]));
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (kidx[m] + u < n) p.state_fin[(head + vi[r]) * n + kidx[m] + u] = st[r][4 * m + u];
+                    for (int u = 0; u < 4; ++u)
+                        if (kidx[m] + u < n) dst[u] = st[r][4 * m + u];
+                }
+            }
 }
 
 template <typename T, int KP, int RG>
@@ -134,9 +150,15 @@ cudaError_t launch_dense_kp(const DenseParams &p, cudaStream_t s) {
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks), block(kDenseThreads);
-    cudaError_t e = p.per_channel
-                        ? launch_kernel(delta_dense_kernel<T, KP, RG, true>, grid, block, 0, s, false, p)
-                        : launch_kernel(delta_dense_kernel<T, KP, RG, false>, grid, block, 0, s, false, p);
+    const bool vec4 = p.n % 4 == 0 && ((uintptr_t)p.state_init % 16 == 0) &&
+                      ((uintptr_t)p.state_fin % 16 == 0);
+    cudaError_t e;
+    if (vec4)
+        e = p.per_channel ? launch_kernel(delta_dense_kernel<T, KP, RG, true, true>, grid, block, 0, s, false, p)
+                          : launch_kernel(delta_dense_kernel<T, KP, RG, false, true>, grid, block, 0, s, false, p);
+    else
+        e = p.per_channel ? launch_kernel(delta_dense_kernel<T, KP, RG, true, false>, grid, block, 0, s, false, p)
+                          : launch_kernel(delta_dense_kernel<T, KP, RG, false, false>, grid, block, 0, s, false, p);
     note_launch();
     return e;
 }
