@@ -110,11 +110,10 @@ __device__ __forceinline__ void st_sw128_8(unsigned char *tile, int row, int c8,
     *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = q;
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// TF32 operand of mma.sync: the fp32 bits as they are (the tensor core reads
+// the top 19 bits, i.e. rounds toward zero; the explicit round-to-nearest
+// conversion cost a dependent instruction per operand on the merge chain).
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x); }
 
 // 2^x and log2(x) on the special-function unit.
 __device__ __forceinline__ float ex2f(float x) {
