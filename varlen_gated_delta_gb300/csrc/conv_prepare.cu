@@ -101,6 +101,21 @@ __device__ __forceinline__ void store_pair(Vec16<T> &v, int q, float a, float b)
     }
 }
 
+// SiLU z sigmoid(z) = z (1 + tanh(z/2)) / 2 of a conv output stored in T: for
+// bf16 with the special-function unit's tanh (relative error about 2^-11,
+// below the output's rounding step), for fp32 with the fast exponential and
+// division (a few fp32 ulp).
+template <typename T>
+__device__ __forceinline__ float silu_for(float z) {
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+        float h;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(h) : "f"(0.5f * z));
+        return 0.5f * z * (1.f + h);
+    } else {
+        return __fdividef(z, 1.f + __expf(-z));
+    }
+}
+
 __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, float &g,
                                            float &beta) {
     gates_opt(p.a, p.bl, (size_t)t * p.H + h, p.A_log, p.dt_bias, h, p.opts, g, beta);
@@ -341,9 +356,7 @@ __global__ void __launch_bounds__(kConvThreads)
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
             float z = acc[e];
-            // SiLU with the fast exponential and division: their error
-            // (a few fp32 ulp) is far below the rounding of the output to T
-            if (p.silu) z = __fdividef(z, 1.f + __expf(-z));
+            if (p.silu) z = silu_for<T>(z);
             yv[e] = round_through<T>(z);  // the conv output is stored in T
         }
         if (cvalid) store_f<T, VEC>(y + (size_t)t * C + c, yv);
@@ -510,6 +523,10 @@ __global__ void __launch_bounds__(kConvThreads, 2)
     const int qk_width = PREP ? 2 * p.HQ * p.K : 0;
     const int lanes_per_head = PREP ? p.K / VEC : 1;
 
+    const size_t xstep = (size_t)D * C;
+    const T *xfirst = x + (size_t)tb * C + (cvalid ? c : 0);
+    const T *xnext = xfirst + kRing * xstep;
+    T *yfirst = y + (size_t)tb * C + (cvalid ? c : 0);
     for (int r0 = 0; r0 < n; r0 += KC) {
         [&]<int... PH>(std::integer_sequence<int, PH...>) {
             (
@@ -528,9 +545,9 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                     // the slot is free again: stream in row r + kRing
                     {
                         const int rn = r + kRing;
-                        cp_async16(ring + (r & (kRing - 1)) * CT,
-                                   x + (size_t)(rn < n ? tb + D * rn : tb) * C + (cvalid ? c : 0),
+                        cp_async16(ring + (r & (kRing - 1)) * CT, rn < n ? xnext : xfirst,
                                    rn < n && cvalid);
+                        xnext += xstep;
                         cp_async_commit();
                     }
                     if (r == 0 || t >= e) {  // run start or next sequence (warp-uniform)
@@ -542,6 +559,7 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                         }
                         if (seq_ok) fill_window(t, std::integral_constant<int, ph>{});
                     }
+                    T *yrow = yfirst + (size_t)r * xstep;
                     if (!seq_ok) return;
                     float acc[VEC];
 #pragma unroll
@@ -556,15 +574,13 @@ __global__ void __launch_bounds__(kConvThreads, 2)
 #pragma unroll
                     for (int q = 0; q < VEC; q += 2) {
                         float z0 = acc[q], z1 = acc[q + 1];
-                        // SiLU with the fast exponential and division: their error
-                        // (a few fp32 ulp) is far below the rounding of the output to T
                         if (p.silu) {
-                            z0 = __fdividef(z0, 1.f + __expf(-z0));
-                            z1 = __fdividef(z1, 1.f + __expf(-z1));
+                            z0 = silu_for<T>(z0);
+                            z1 = silu_for<T>(z1);
                         }
                         store_pair<T>(yo, q, z0, z1);  // the conv output is stored in T
                     }
-                    if (cvalid) *reinterpret_cast<uint4 *>(y + (size_t)t * C + c) = yo.u;
+                    if (cvalid) *reinterpret_cast<uint4 *>(yrow) = yo.u;
                     if constexpr (PREP) {
                         // tokens of token-serial sequences, and the captured prefix
                         const bool prep_t = e - s < p.prep_max_len || t - s < p.prep_cap;
