@@ -196,6 +196,20 @@ GDN_API int gdn_chunk_min_len(void);
 /* Number of kernels this library has launched in this process. */
 GDN_API uint64_t gdn_launch_count(void);
 
+/*
+ * Segment-parallel chunked path: when a layer call (with offsets_host) has a
+ * single chunked sequence of at least gdn_segment_min_len() tokens and too
+ * few (head, V tile) units to fill the GPU, the sequence is cut into up to 8
+ * segments run in parallel: each segment's transition S_end = S_start M + L
+ * is computed from a zero start, the start states are chained, and every
+ * segment is rerun from its start state.  gdn_set_segment_min_len(n): n > 0
+ * sets the length (default 16384), 0 restores the default.  Process-wide.
+ * The workspace holds the segment buffers when N >= 2 * that length
+ * (gdn_workspace_bytes follows the setting).
+ */
+GDN_API int gdn_set_segment_min_len(int n);
+GDN_API int gdn_segment_min_len(void);
+
 /* Kernels that gdn_set_kernel_events can bracket. */
 typedef enum gdn_kernel_id {
     GDN_KERNEL_CONV = 0,    /* conv (+ fused prepare) pass */

@@ -129,3 +129,52 @@ def test_chunked_resume_across_calls():
     assert torch.equal(c2, cfin)
     assert rel_l2(cpu64(torch.cat([o1, o2])), cpu64(out)) <= 5e-3
     assert rel_l2(cpu64(s2), cpu64(sfin)) <= 5e-3
+
+
+# ------------------------------------------------------------------ segment-parallel path
+
+import contextlib
+
+
+@contextlib.contextmanager
+def segment_threshold(n):
+    gdn.gdn_set_segment_min_len(n)
+    try:
+        yield
+    finally:
+        gdn.gdn_set_segment_min_len(0)
+
+
+@pytest.mark.parametrize("lens,over", [
+    ((1000,), {"H": 8, "HQ": 4}),                                 # 8 segments of 128 tokens
+    ((5, 1500, 40, 1), {"H": 8, "HQ": 4}),                        # one chunked sequence among serial ones
+    ((1100,), {"H": 4, "HQ": 2, "V": 256, "D": 2, "a_mean": -1.0, "b_std": 2.0}),  # long geometry
+])
+def test_segment_parallel_matches_oracle_and_the_unsegmented_path(lens, over):
+    wl, d = _case(lens, **over)
+    with segment_threshold(1 << 30):
+        n0 = gdn.gdn_launch_count()
+        plain = run_layer(wl, d, offsets_host=d["offsets_list"])
+        n_plain = gdn.gdn_launch_count() - n0
+    with segment_threshold(256):
+        n0 = gdn.gdn_launch_count()
+        out, cfin, sfin = run_layer(wl, d, offsets_host=d["offsets_list"])
+        n_seg = gdn.gdn_launch_count() - n0
+    assert n_seg == n_plain + 2   # two chunked launches and the combine step instead of one
+    _check(wl, d, out, cfin, sfin)
+    torch.cuda.synchronize()
+    assert rel_l2(cpu64(out), cpu64(plain[0])) <= TOL
+    assert rel_l2(cpu64(sfin), cpu64(plain[2])) <= TOL
+    assert torch.equal(cfin, plain[1])
+
+
+def test_segment_parallel_in_place_carry():
+    wl, d = _case((900,), H=8, HQ=4)
+    ref = oracle_layer(wl, d)
+    st, cs = d["state_init"].clone(), d["conv_init"].clone()
+    with segment_threshold(256):
+        out, cfin, sfin = run_layer(wl, dict(d, state_init=st, conv_init=cs),
+                                    offsets_host=d["offsets_list"], state_fin=st, conv_fin=cs)
+    torch.cuda.synchronize()
+    assert sfin.data_ptr() == st.data_ptr()
+    assert rel_l2(cpu64(out), ref[0]) <= TOL and rel_l2(cpu64(sfin), ref[2]) <= TOL

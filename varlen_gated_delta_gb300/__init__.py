@@ -30,6 +30,7 @@ __all__ = [
     "gdn_layer_varlen_capture", "gdn_prepare_ex", "gdn_delta_varlen_ex", "gdn_layer_varlen_ex",
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
     "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
+    "gdn_set_segment_min_len", "gdn_segment_min_len",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,6 +91,9 @@ def load_library():
     lib.gdn_prepare_ex.argtypes = [vp] * 7 + [i] * 7 + [vp]
     lib.gdn_delta_varlen_ex.argtypes = [vp] * 7 + [i] * 6 + [f, i, i, vp]
     lib.gdn_layer_varlen_ex.argtypes = [vp] * 14 + [i, i, vp, vp, vp, vp] + [i] * 9 + [f, i, vp, sz, vp]
+    lib.gdn_set_segment_min_len.argtypes = [i]
+    lib.gdn_set_segment_min_len.restype = i
+    lib.gdn_segment_min_len.restype = i
     lib.gdn_gated_delta_dense.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
@@ -537,3 +541,12 @@ def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=Fals
     _check(lib.gdn_gated_delta_dense(*args, B, S, H, n, int(bool(gate_per_channel)), float(scale),
                                      _dtype_code(q), _stream(dev)))
     return out, state_fin
+
+
+def gdn_set_segment_min_len(n: int) -> None:
+    """Length from which a lone chunked sequence runs segment-parallel (0: default)."""
+    _check(load_library().gdn_set_segment_min_len(int(n)))
+
+
+def gdn_segment_min_len() -> int:
+    return int(load_library().gdn_segment_min_len())

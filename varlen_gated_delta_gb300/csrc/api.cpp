@@ -82,6 +82,25 @@ static int chunk_min_len() {
     return v > 0 ? v : default_chunk_min_len();
 }
 
+// Length from which a lone chunked sequence may be cut into segments that run
+// in parallel (segment-parallel chunked path); 0 = default.
+static std::atomic<int> g_segment_min_len{0};
+static int segment_min_len() {
+    int v = g_segment_min_len.load(std::memory_order_relaxed);
+    return v > 0 ? v : 16384;
+}
+
+static int sm_count_host() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n = v > 0 ? v : 1;
+    }
+    return n;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static bool dtype_ok(int dtype) { return dtype == GDN_F32 || dtype == GDN_BF16; }
@@ -109,7 +128,7 @@ static int check_offsets_host(const int32_t *offsets_host, int B, int N) {
 }
 
 struct WsLayout {
-    size_t header, order, y, qk, gb, total;
+    size_t header, order, y, qk, gb, seg, total;  // seg: 0 when no segment buffers fit
 };
 
 static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) {
@@ -126,6 +145,12 @@ static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) 
     off += align256((size_t)2 * N * HQ * K * 4);
     l.gb = off;
     off += align256((size_t)2 * N * H * 4);
+    // segment buffers when a sequence can be long enough to be segmented
+    l.seg = 0;
+    if (N >= 2 * segment_min_len() && K == 128 && V % 128 == 0) {
+        l.seg = off;
+        off += align256(segment_floats(H, V) * 4);
+    }
     l.total = off;
     return l;
 }
@@ -179,6 +204,14 @@ int gdn_set_chunk_min_len(int n) {
 }
 
 int gdn_chunk_min_len(void) { return chunk_min_len(); }
+
+int gdn_set_segment_min_len(int n) {
+    if (n < 0) return fail(GDN_ERR_SHAPE, "segment length %d < 0", n);
+    g_segment_min_len.store(n, std::memory_order_relaxed);
+    return GDN_OK;
+}
+
+int gdn_segment_min_len(void) { return segment_min_len(); }
 
 int gdn_set_kernel_events(int kernel, void *start, void *stop) {
     if (kernel < 0 || kernel > 2) return fail(GDN_ERR_SHAPE, "unknown kernel id %d", kernel);
@@ -408,6 +441,28 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         run_chunked = n > 0;
         max_units = n * H * (V / 128);
     }
+    // One lone chunked sequence that leaves most of the GPU idle is cut into
+    // segments run in parallel (two chunked launches and a combine step).
+    int nseg = 1, seg_len = 0;
+    if (run_chunked && offsets_host && lay.seg != 0) {
+        int n_long = 0, len = 0;
+        for (int i = 0; i < B; ++i) {
+            const int l = offsets_host[i + 1] - offsets_host[i];
+            if (l >= thr) { ++n_long; len = l; }
+        }
+        // the most segments for which both chunked launches fit in one wave
+        // of CTA slots: P (head, V tile) units in the rerun, (P - 1) (head,
+        // V tile + transition tile) units in the first pass
+        const long VT = V / 128, slots = 2L * sm_count_host();
+        long want = 0;
+        for (long P = 2; P <= kMaxSegments; ++P)
+            if (P * H * VT <= slots && (P - 1) * H * (VT + 1) <= slots) want = P;
+        if (n_long == 1 && len >= segment_min_len() && want >= 2) {
+            seg_len = (int)((((len + want - 1) / want) + 63) / 64 * 64);
+            nseg = (len + seg_len - 1) / seg_len;
+            if (nseg < 2) nseg = 1;
+        }
+    }
     // tokens of token-serial sequences need the prepare step; with host
     // offsets a batch of chunked sequences only skips it
     const bool capsule = cap && cap->capsule;
@@ -459,8 +514,15 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         cl.state_init = state_init; cl.state_fin = state_fin; cl.out = out;
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
         cl.scale = eff_scale; cl.max_units = max_units; cl.opts = opts;
+        if (nseg > 1) {
+            float *segb = reinterpret_cast<float *>(ws + lay.seg);
+            cl.nseg = nseg; cl.seg_len = seg_len;
+            cl.seg_M = segb;
+            cl.seg_L = cl.seg_M + (size_t)(kMaxSegments - 1) * H * 128 * 128;
+            cl.seg_S = cl.seg_L + (size_t)(kMaxSegments - 1) * H * V * 128;
+        }
         mark_before(GDN_KERNEL_CHUNKED, s);
-        cudaError_t ce = launch_delta_chunked(cl, s);
+        cudaError_t ce = nseg > 1 ? launch_delta_chunked_segmented(cl, s) : launch_delta_chunked(cl, s);
         mark_after(GDN_KERNEL_CHUNKED, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "chunked kernel launch");
         return GDN_OK;

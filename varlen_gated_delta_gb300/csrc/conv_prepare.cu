@@ -188,6 +188,8 @@ __device__ void schedule_block(const ConvParams &p) {
         p.header->n_chunked = ok ? s_chunked : 0;
         p.header->n_units = (ok && p.seq_order != nullptr) ? s_chunked * p.H * p.VT : 0;
         p.header->next_unit = 0;
+        p.header->seg_next[0] = 0;
+        p.header->seg_next[1] = 0;
     }
 }
 

@@ -92,6 +92,18 @@ struct ChunkParams {
     float scale;
     int tma_store;  // full output tiles leave through omap
     int opts;       // GDN_OPT_* rule / activation options
+    // Segment-parallel mode for one long sequence (seq_order[0]) cut into nseg
+    // segments of seg_len tokens.  seg_mode 1: segments 0..nseg-2 from a zero
+    // state, plus a 128-row tile starting from the identity with v = 0 whose
+    // final state is the segment's transition M (S_end = S_start M + L);
+    // writes M and the local final state L, no outputs.  seg_mode 2: every
+    // segment from its true start state (seg_S), writing
+    // outputs; the last segment writes state_fin.  seg_S[0] is a copy of the
+    // initial state, so state_fin may alias state_init.
+    int seg_mode, nseg, seg_len, seg_units;
+    unsigned int *counter;   // work counter of this launch
+    float *seg_M, *seg_L;    // [nseg-1][H][128][128], [nseg-1][H][V][128]
+    const float *seg_S;      // [nseg][H][V][128]: start states of the segments
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     const int H = p.H, HQ = p.HQ, V = p.V;
     const int G = H / HQ;
-    const int n_units = p.header->n_units;
+    const int n_units = p.seg_mode ? p.seg_units : p.header->n_units;
     uint32_t gchunk = 0;      // chunks loaded by this CTA (parity of the stage barrier)
     uint32_t mma_phase = 0;   // completed MMA commits
 
@@ -307,14 +319,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
 
     while (true) {
-        if (tid == 0) *s_unit = (int)atomicAdd(&p.header->next_unit, 1u);
+        if (tid == 0) *s_unit = (int)atomicAdd(p.counter, 1u);
         __syncthreads();
         const int u = *s_unit;
         if (u >= n_units || *s_abort) break;
-        const int seq = p.seq_order[u / (H * p.VT)];
-        const int h = (u / p.VT) % H;
-        const int vt = u % p.VT;
-        const int s = p.offsets[seq], e = p.offsets[seq + 1];
+        int seq, h, vt, seg = 0;
+        bool mtile = false;  // the transition tile of a segment (seg_mode 1)
+        if (p.seg_mode == 0) {
+            seq = p.seq_order[u / (H * p.VT)];
+            h = (u / p.VT) % H;
+            vt = u % p.VT;
+        } else {
+            const int tiles = p.VT + (p.seg_mode == 1);
+            seq = p.seq_order[0];
+            seg = u / (H * tiles);
+            h = (u / tiles) % H;
+            const int tile = u % tiles;
+            mtile = tile == p.VT;
+            vt = mtile ? 0 : tile;
+        }
+        int s = p.offsets[seq], e = p.offsets[seq + 1];
+        if (p.seg_mode) {  // this segment's tokens
+            s += seg * p.seg_len;
+            e = min(e, s + p.seg_len);
+        }
+        const bool write_out = p.seg_mode != 1;
         const int nchunks = (e - s + kC - 1) / kC;
         const int kh = h / G;
         const int qcol = kh * 128, kcol = HQ * 128 + kh * 128;
@@ -329,16 +358,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
         {
             const float *src = p.state_init + state_row * 128 + hc * 64;
+            if (p.seg_mode == 2)
+                src = p.seg_S + ((((size_t)seg * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
+                if (p.seg_mode == 1) {  // zero, or the identity for the transition tile
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(src + c0 + j);
-                    r[j] = __float_as_uint(f.x);
-                    r[j + 1] = __float_as_uint(f.y);
-                    r[j + 2] = __float_as_uint(f.z);
-                    r[j + 3] = __float_as_uint(f.w);
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(mtile && row == hc * 64 + c0 + j ? 1.f : 0.f);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(src + c0 + j);
+                        r[j] = __float_as_uint(f.x);
+                        r[j + 1] = __float_as_uint(f.y);
+                        r[j + 2] = __float_as_uint(f.z);
+                        r[j + 3] = __float_as_uint(f.w);
+                    }
                 }
                 tmem_st32(lane_base + kColS + hc * 64 + c0, r);
             }
@@ -612,10 +649,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColD2, sdesc_sw128(kq + ks * 2048, 16384, 1024),
                              sdesc_sw128(tw + ks * 32, 16, 1024), id, ks > 0);
+                if (!mtile)  // the transition tile has v = 0: Delta = -W S0^T only
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColD3, sdesc_sw128(vb + ks * 2048, 8192, 1024),
-                             sdesc_sw128(tb + ks * 32, 16, 1024), id, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem + kColD3, sdesc_sw128(vb + ks * 2048, 8192, 1024),
+                                 sdesc_sw128(tb + ks * 32, 16, 1024), id, ks > 0);
                 mma_commit(bar_mma);
             }
             wait_mma();
@@ -656,14 +694,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
                     mma_bf16(tmem + kColD3, sdesc_sw128(s0 + aoff, 16, 1024),
-                             sdesc_sw128(wt + ks * 2048, 8192, 1024), idn, 1);
+                             sdesc_sw128(wt + ks * 2048, 8192, 1024), idn, !(mtile && ks == 0));
                 }
+                if (write_out)
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tmem + kColD4, sdesc_sw128(s0 + aoff, 16, 1024),
-                             sdesc_sw128(kq + 8192 + aoff, 16, 1024), idq, ks > 0);
-                }
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tmem + kColD4, sdesc_sw128(s0 + aoff, 16, 1024),
+                                 sdesc_sw128(kq + 8192 + aoff, 16, 1024), idq, ks > 0);
+                    }
                 mma_commit(bar_mma);
             }
             // gates of the next chunk while the MMAs run (this chunk is done with them)
@@ -697,10 +736,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint32_t pp = smem_u32(sm + kOffP);
                 const uint32_t id5 = idesc_bf16(128, 64, false, false);
                 const uint32_t id6 = idesc_bf16(128, 128, false, true);
+                if (write_out)
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + kColD5, sdesc_sw128(dt + ks * 32, 16, 1024),
-                             sdesc_sw128(pp + ks * 32, 16, 1024), id5, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem + kColD5, sdesc_sw128(dt + ks * 32, 16, 1024),
+                                 sdesc_sw128(pp + ks * 32, 16, 1024), id5, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tmem + kColS, sdesc_sw128(dt2 + ks * 32, 16, 1024),
@@ -714,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // ---- E4: o[vi, t] = s_t (S0 Q^T)[vi, t] + (Delta^T P^T)[vi, t], staged as a
             // [64 t][128 vi] bf16 tile in the (now free) Delta buffers, then written
             // as 16-byte rows
+            if (write_out)
             {
                 __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffOut);
 #pragma unroll
@@ -756,8 +797,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (*s_abort) break;
 
         // final state row `row`, columns [64 hc, 64 hc + 64) -> global
-        {
+        if (p.seg_mode != 2 || seg == p.nseg - 1) {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
+            if (p.seg_mode == 1)
+                dst = mtile ? p.seg_M + ((((size_t)seg * H + h) * 128 + row) * 128 + hc * 64)
+                            : p.seg_L + ((((size_t)seg * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -819,10 +863,12 @@ bool chunked_supported(int dtype, int K, int V, int W) {
     return dtype == 1 && K == 128 && V % 128 == 0 && W % 8 == 0;
 }
 
-cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
+namespace {
+
+// Tensor maps and kernel parameters of a chunked launch.
+cudaError_t chunk_setup(const ChunkLaunch &c, CUtensorMap &map, CUtensorMap &omap, ChunkParams &p) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)c.W, (cuuint64_t)(c.N > 0 ? c.N : 1)};
     const cuuint64_t strides[1] = {(cuuint64_t)c.W * 2};
     const cuuint32_t box[2] = {64, 64};
@@ -832,7 +878,6 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     // output tiles [64 t][128 vi] of out viewed as [N, H V] (no swizzle)
-    CUtensorMap omap;
     int tma_store = 0;
     if ((reinterpret_cast<uintptr_t>(c.out) & 15) == 0 && c.N > 0) {
         const cuuint64_t odims[2] = {(cuuint64_t)c.H * c.V, (cuuint64_t)c.N};
@@ -843,7 +888,7 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     if (!tma_store) omap = map;  // unused
-    ChunkParams p{};
+    p = ChunkParams{};
     p.a = c.a; p.bl = c.bl; p.A_log = c.A_log; p.dt_bias = c.dt_bias;
     p.offsets = c.offsets; p.seq_order = c.seq_order; p.header = c.header;
     p.state_init = c.state_init; p.state_fin = c.state_fin;
@@ -852,6 +897,7 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     p.scale = c.scale;
     p.tma_store = tma_store;
     p.opts = c.opts;
+    p.counter = &c.header->next_unit;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(chunked_delta_kernel,
@@ -859,14 +905,99 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const long max_units = c.max_units;
+    return cudaSuccess;
+}
+
+cudaError_t chunk_launch(const CUtensorMap &map, const CUtensorMap &omap, const ChunkParams &p,
+                         long units, cudaStream_t s) {
     const long slots = (long)sm_count() * kCtasPerSm;
-    const int grid = (int)(max_units < slots ? max_units : slots);
+    const int grid = (int)(units < slots ? units : slots);
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = launch_kernel(chunked_delta_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s,
                                   true, map, omap, p);
     note_launch();
     return e;
+}
+
+// Start states of the segments of the long sequence seq_order[0]:
+// S_0 = state_init, S_{q+1} = S_q M_q + L_q (rows of S independent), written
+// to seg_S [nseg][H][V][128].  One block per (value head, 32 state rows), one
+// thread per state column.
+__global__ void __launch_bounds__(128) segment_combine_kernel(const ChunkParams p) {
+    pdl_wait_primary();  // M and L come from the previous (phase 1) launch
+    __shared__ float srow[32][128];
+    const int V = p.V, H = p.H, nrb = V / 32;
+    const int h = blockIdx.x / nrb, r0 = (blockIdx.x % nrb) * 32, j = threadIdx.x;
+    const int seq = p.seq_order[0];
+    float *S = const_cast<float *>(p.seg_S);
+    for (int r = 0; r < 32; ++r) {
+        const float x = p.state_init[(((size_t)seq * H + h) * V + r0 + r) * 128 + j];
+        srow[r][j] = x;
+        S[(((size_t)h) * V + r0 + r) * 128 + j] = x;
+    }
+    __syncthreads();
+    for (int q = 0; q + 1 < p.nseg; ++q) {
+        float acc[32];
+        const float *L = p.seg_L + (((size_t)q * H + h) * V + r0) * 128 + j;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) acc[r] = L[(size_t)r * 128];
+        const float *M = p.seg_M + ((size_t)q * H + h) * 128 * 128 + j;
+#pragma unroll 4
+        for (int k = 0; k < 128; ++k) {
+            const float m = M[(size_t)k * 128];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) acc[r] = fmaf(srow[r][k], m, acc[r]);
+        }
+        __syncthreads();
+        float *dst = S + (((size_t)(q + 1) * H + h) * V + r0) * 128 + j;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            srow[r][j] = acc[r];
+            dst[(size_t)r * 128] = acc[r];
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
+    CUtensorMap map, omap;
+    ChunkParams p;
+    cudaError_t e = chunk_setup(c, map, omap, p);
+    if (e != cudaSuccess) return e;
+    return chunk_launch(map, omap, p, c.max_units, s);
+}
+
+// One long chunked sequence (seq_order[0]) in c.nseg segments of c.seg_len
+// tokens: phase 1 computes each segment's transition M and local final state
+// L from a zero start (segments 0..nseg-2, in parallel), the combine kernel
+// chains the start states S_{q+1} = S_q M_q + L_q, and phase 2 reruns every
+// segment from its start state (in parallel), writing the outputs.
+cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s) {
+    CUtensorMap map, omap;
+    ChunkParams p;
+    cudaError_t e = chunk_setup(c, map, omap, p);
+    if (e != cudaSuccess) return e;
+    const int VT = c.V / 128;
+    p.nseg = c.nseg;
+    p.seg_len = c.seg_len;
+    p.seg_M = c.seg_M;
+    p.seg_L = c.seg_L;
+    p.seg_S = c.seg_S;
+    p.seg_mode = 1;
+    p.seg_units = (c.nseg - 1) * c.H * (VT + 1);
+    p.counter = &c.header->seg_next[0];
+    e = chunk_launch(map, omap, p, p.seg_units, s);
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(segment_combine_kernel, dim3((unsigned)(c.H * (c.V / 32))), dim3(128), 0, s,
+                      true, p);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    p.seg_mode = 2;
+    p.seg_units = c.nseg * c.H * VT;
+    p.counter = &c.header->seg_next[1];
+    return chunk_launch(map, omap, p, p.seg_units, s);
 }
 
 }  // namespace gdn

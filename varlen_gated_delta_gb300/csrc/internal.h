@@ -19,7 +19,8 @@ struct WsHeader {
     int n_chunked;       // sequences run by the chunked kernel
     int n_units;         // chunked work units
     unsigned int next_unit;  // work counter of the persistent chunked kernel
-    int pad[59];
+    unsigned int seg_next[2];  // work counters of the two segmented chunked launches
+    int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -124,7 +125,18 @@ struct ChunkLaunch {
     float scale;
     long max_units;  // upper bound on work units (grid sizing)
     int opts;        // GDN_OPT_*
+    // segment-parallel mode for one long chunked sequence (nseg > 1): see
+    // launch_delta_chunked_segmented; seg_M [nseg-1][H][128][128],
+    // seg_L [nseg-1][H][V][128], seg_S [nseg][H][V][128]
+    int nseg, seg_len;
+    float *seg_M, *seg_L, *seg_S;
 };
+// Workspace floats of the segment buffers for up to kMaxSegments segments.
+constexpr int kMaxSegments = 8;
+inline size_t segment_floats(int H, int V) {  // M, L of nseg-1 segments; start states of nseg
+    return (size_t)(kMaxSegments - 1) * H * ((size_t)128 * 128 + (size_t)V * 128) +
+           (size_t)kMaxSegments * H * V * 128;
+}
 // Dense-layout recurrence (q, k, v, out [B, S, H, n] T; g [B, S, H] or, with
 // per_channel, [B, S, H, n] f32; beta [B, S, H] f32; state [B, H, n, n] f32,
 // state_init NULL = zero, state_fin NULL = not written).
@@ -141,6 +153,7 @@ cudaError_t launch_delta_dense(const DenseParams &p, int dtype, cudaStream_t s);
 
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
+cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s);
 
 // Whether launch_conv can fuse the prepare step for this geometry.
 bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int nptrs);
