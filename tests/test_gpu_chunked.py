@@ -145,12 +145,16 @@ def segment_threshold(n):
         gdn.gdn_set_segment_min_len(0)
 
 
-@pytest.mark.parametrize("lens,over", [
-    ((1000,), {"H": 8, "HQ": 4}),                                 # 8 segments of 128 tokens
-    ((5, 1500, 40, 1), {"H": 8, "HQ": 4}),                        # one chunked sequence among serial ones
-    ((1100,), {"H": 4, "HQ": 2, "V": 256, "D": 2, "a_mean": -1.0, "b_std": 2.0}),  # long geometry
+@pytest.mark.parametrize("lens,over,segmented", [
+    ((1000,), {"H": 8, "HQ": 4}, True),                           # 8 segments of 128 tokens
+    ((5, 1500, 40, 1), {"H": 8, "HQ": 4}, True),                  # one chunked sequence among serial ones
+    ((1100,), {"H": 4, "HQ": 2, "V": 256, "D": 2, "a_mean": -1.0, "b_std": 2.0}, True),  # long geometry
+    ((900, 1300), {"H": 8, "HQ": 4}, True),                       # two long sequences
+    ((700, 5, 1200, 300, 1), {"H": 8, "HQ": 4}, True),            # three, one with fewer segments
+    ((1500, 100), {"H": 8, "HQ": 4}, False),                      # a short chunked sequence beside
+    ((300, 400, 500, 600, 700), {"H": 4, "HQ": 2}, False),        # more than the buffers hold
 ])
-def test_segment_parallel_matches_oracle_and_the_unsegmented_path(lens, over):
+def test_segment_parallel_matches_oracle_and_the_unsegmented_path(lens, over, segmented):
     wl, d = _case(lens, **over)
     with segment_threshold(1 << 30):
         n0 = gdn.gdn_launch_count()
@@ -160,7 +164,8 @@ def test_segment_parallel_matches_oracle_and_the_unsegmented_path(lens, over):
         n0 = gdn.gdn_launch_count()
         out, cfin, sfin = run_layer(wl, d, offsets_host=d["offsets_list"])
         n_seg = gdn.gdn_launch_count() - n0
-    assert n_seg == n_plain + 2   # two chunked launches and the combine step instead of one
+    # segmented: two chunked launches and the combine step instead of one
+    assert n_seg == n_plain + (2 if segmented else 0)
     _check(wl, d, out, cfin, sfin)
     torch.cuda.synchronize()
     assert rel_l2(cpu64(out), cpu64(plain[0])) <= TOL
@@ -168,8 +173,9 @@ def test_segment_parallel_matches_oracle_and_the_unsegmented_path(lens, over):
     assert torch.equal(cfin, plain[1])
 
 
-def test_segment_parallel_in_place_carry():
-    wl, d = _case((900,), H=8, HQ=4)
+@pytest.mark.parametrize("lens", [(900,), (600, 1000)])
+def test_segment_parallel_in_place_carry(lens):
+    wl, d = _case(lens, H=8, HQ=4)
     ref = oracle_layer(wl, d)
     st, cs = d["state_init"].clone(), d["conv_init"].clone()
     with segment_threshold(256):

@@ -82,7 +82,7 @@ static int chunk_min_len() {
     return v > 0 ? v : default_chunk_min_len();
 }
 
-// Length from which a lone chunked sequence may be cut into segments that run
+// Length from which long chunked sequences may be cut into segments that run
 // in parallel (segment-parallel chunked path); 0 = default.
 static std::atomic<int> g_segment_min_len{0};
 static int segment_min_len() {
@@ -129,6 +129,7 @@ static int check_offsets_host(const int32_t *offsets_host, int B, int N) {
 
 struct WsLayout {
     size_t header, order, y, qk, gb, seg, total;  // seg: 0 when no segment buffers fit
+    int seg_seqs;                                 // sequences the segment buffers hold
 };
 
 static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) {
@@ -145,11 +146,15 @@ static WsLayout ws_layout(int B, int N, int H, int HQ, int K, int V, int dtype) 
     off += align256((size_t)2 * N * HQ * K * 4);
     l.gb = off;
     off += align256((size_t)2 * N * H * 4);
-    // segment buffers when a sequence can be long enough to be segmented
+    // segment buffers when a sequence can be long enough to be segmented, for
+    // as many such sequences as N tokens can hold (at most kMaxSegSeqs)
     l.seg = 0;
-    if (N >= 2 * segment_min_len() && K == 128 && V % 128 == 0) {
+    l.seg_seqs = 0;
+    if (N >= segment_min_len() && K == 128 && V % 128 == 0) {
+        const long n = N / segment_min_len();
+        l.seg_seqs = (int)(n < kMaxSegSeqs ? n : kMaxSegSeqs);
         l.seg = off;
-        off += align256(segment_floats(H, V) * 4);
+        off += align256(segment_floats(H, V, l.seg_seqs) * 4);
     }
     l.total = off;
     return l;
@@ -441,26 +446,30 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         run_chunked = n > 0;
         max_units = n * H * (V / 128);
     }
-    // One lone chunked sequence that leaves most of the GPU idle is cut into
-    // segments run in parallel (two chunked launches and a combine step).
-    int nseg = 1, seg_len = 0;
+    // Long chunked sequences that leave most of the GPU idle are cut into
+    // segments run in parallel (two chunked launches and a combine step):
+    // when every chunked sequence has at least gdn_segment_min_len() tokens
+    // and there are at most the segment buffers' count of them.
+    int nseg = 1, nseq_seg = 0;
     if (run_chunked && offsets_host && lay.seg != 0) {
-        int n_long = 0, len = 0;
+        int n_long = 0, n_chunked = 0;
         for (int i = 0; i < B; ++i) {
             const int l = offsets_host[i + 1] - offsets_host[i];
-            if (l >= thr) { ++n_long; len = l; }
+            if (l >= thr) {
+                ++n_chunked;
+                n_long += l >= segment_min_len();
+            }
         }
         // the most segments for which both chunked launches fit in one wave
-        // of CTA slots: P (head, V tile) units in the rerun, (P - 1) (head,
-        // V tile + transition tile) units in the first pass
+        // of CTA slots: P (head, V tile) units per sequence in the rerun,
+        // (P - 1) (head, V tile + transition tile) units in the first pass
         const long VT = V / 128, slots = 2L * sm_count_host();
         long want = 0;
         for (long P = 2; P <= kMaxSegments; ++P)
-            if (P * H * VT <= slots && (P - 1) * H * (VT + 1) <= slots) want = P;
-        if (n_long == 1 && len >= segment_min_len() && want >= 2) {
-            seg_len = (int)((((len + want - 1) / want) + 63) / 64 * 64);
-            nseg = (len + seg_len - 1) / seg_len;
-            if (nseg < 2) nseg = 1;
+            if (n_long * P * H * VT <= slots && n_long * (P - 1) * H * (VT + 1) <= slots) want = P;
+        if (n_long >= 1 && n_long == n_chunked && n_long <= lay.seg_seqs && want >= 2) {
+            nseg = (int)want;
+            nseq_seg = n_long;
         }
     }
     // tokens of token-serial sequences need the prepare step; with host
@@ -516,10 +525,10 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         cl.scale = eff_scale; cl.max_units = max_units; cl.opts = opts;
         if (nseg > 1) {
             float *segb = reinterpret_cast<float *>(ws + lay.seg);
-            cl.nseg = nseg; cl.seg_len = seg_len;
+            cl.nseg = nseg; cl.nseq_seg = nseq_seg;
             cl.seg_M = segb;
-            cl.seg_L = cl.seg_M + (size_t)(kMaxSegments - 1) * H * 128 * 128;
-            cl.seg_S = cl.seg_L + (size_t)(kMaxSegments - 1) * H * V * 128;
+            cl.seg_L = cl.seg_M + (size_t)lay.seg_seqs * segment_m_floats(H);
+            cl.seg_S = cl.seg_L + (size_t)lay.seg_seqs * segment_l_floats(H, V);
         }
         mark_before(GDN_KERNEL_CHUNKED, s);
         cudaError_t ce = nseg > 1 ? launch_delta_chunked_segmented(cl, s) : launch_delta_chunked(cl, s);

@@ -92,19 +92,27 @@ struct ChunkParams {
     float scale;
     int tma_store;  // full output tiles leave through omap
     int opts;       // GDN_OPT_* rule / activation options
-    // Segment-parallel mode for one long sequence (seq_order[0]) cut into nseg
-    // segments of seg_len tokens.  seg_mode 1: segments 0..nseg-2 from a zero
+    // Segment-parallel mode for nseq_seg long sequences (seq_order[0..]) cut
+    // into up to nseg segments each (segments_of).  seg_mode 1: segments 0..nseg-2 from a zero
     // state, plus a 128-row tile starting from the identity with v = 0 whose
     // final state is the segment's transition M (S_end = S_start M + L);
     // writes M and the local final state L, no outputs.  seg_mode 2: every
     // segment from its true start state (seg_S), writing
     // outputs; the last segment writes state_fin.  seg_S[0] is a copy of the
     // initial state, so state_fin may alias state_init.
-    int seg_mode, nseg, seg_len, seg_units;
+    int seg_mode, nseg, nseq_seg, seg_units;
     unsigned int *counter;   // work counter of this launch
-    float *seg_M, *seg_L;    // [nseg-1][H][128][128], [nseg-1][H][V][128]
-    const float *seg_S;      // [nseg][H][V][128]: start states of the segments
+    // per segmented sequence i (seq_order[i], i < nseq_seg):
+    float *seg_M, *seg_L;    // [i][nseg-1][H][128][128], [i][nseg-1][H][V][128]
+    const float *seg_S;      // [i][nseg][H][V][128]: start states of the segments
 };
+
+// Segment length of a sequence of len tokens cut into at most nseg segments
+// (a multiple of the chunk) and the number of non-empty segments.
+__device__ __forceinline__ void segments_of(int len, int nseg, int &seg_len, int &count) {
+    seg_len = ((len + nseg - 1) / nseg + kC - 1) / kC * kC;
+    count = seg_len > 0 ? (len + seg_len - 1) / seg_len : 0;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncthreads();
         const int u = *s_unit;
         if (u >= n_units || *s_abort) break;
-        int seq, h, vt, seg = 0;
+        int seq, h, vt, seg = 0, sidx = 0, nseg_here = 1;
         bool mtile = false;  // the transition tile of a segment (seg_mode 1)
         if (p.seg_mode == 0) {
             seq = p.seq_order[u / (H * p.VT)];
@@ -331,17 +339,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             vt = u % p.VT;
         } else {
             const int tiles = p.VT + (p.seg_mode == 1);
-            seq = p.seq_order[0];
-            seg = u / (H * tiles);
-            h = (u / tiles) % H;
-            const int tile = u % tiles;
+            const int per_seq = (p.seg_mode == 1 ? p.nseg - 1 : p.nseg) * H * tiles;
+            sidx = u / per_seq;
+            const int r = u % per_seq;
+            seq = p.seq_order[sidx];
+            seg = r / (H * tiles);
+            h = (r / tiles) % H;
+            const int tile = r % tiles;
             mtile = tile == p.VT;
             vt = mtile ? 0 : tile;
         }
         int s = p.offsets[seq], e = p.offsets[seq + 1];
-        if (p.seg_mode) {  // this segment's tokens
-            s += seg * p.seg_len;
-            e = min(e, s + p.seg_len);
+        if (p.seg_mode) {  // this segment's tokens (units past the sequence's last segment are empty)
+            int seg_len;
+            segments_of(e - s, p.nseg, seg_len, nseg_here);
+            if (seg >= (p.seg_mode == 1 ? nseg_here - 1 : nseg_here)) {
+                __syncthreads();  // every thread has read s_unit before thread 0 rewrites it
+                continue;
+            }
+            s += seg * seg_len;
+            e = min(e, s + seg_len);
         }
         const bool write_out = p.seg_mode != 1;
         const int nchunks = (e - s + kC - 1) / kC;
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         {
             const float *src = p.state_init + state_row * 128 + hc * 64;
             if (p.seg_mode == 2)
-                src = p.seg_S + ((((size_t)seg * H + h) * V + vt * 128 + row) * 128 + hc * 64);
+                src = p.seg_S + (((((size_t)sidx * p.nseg + seg) * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -797,11 +814,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (*s_abort) break;
 
         // final state row `row`, columns [64 hc, 64 hc + 64) -> global
-        if (p.seg_mode != 2 || seg == p.nseg - 1) {
+        if (p.seg_mode != 2 || seg == nseg_here - 1) {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
+            const size_t sq = (size_t)sidx * (p.nseg - 1) + seg;  // (sequence, segment) of phase 1
             if (p.seg_mode == 1)
-                dst = mtile ? p.seg_M + ((((size_t)seg * H + h) * 128 + row) * 128 + hc * 64)
-                            : p.seg_L + ((((size_t)seg * H + h) * V + vt * 128 + row) * 128 + hc * 64);
+                dst = mtile ? p.seg_M + (((sq * H + h) * 128 + row) * 128 + hc * 64)
+                            : p.seg_L + (((sq * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -919,29 +937,33 @@ cudaError_t chunk_launch(const CUtensorMap &map, const CUtensorMap &omap, const 
     return e;
 }
 
-// Start states of the segments of the long sequence seq_order[0]:
+// Start states of the segments of each segmented sequence i (seq_order[i]):
 // S_0 = state_init, S_{q+1} = S_q M_q + L_q (rows of S independent), written
-// to seg_S [nseg][H][V][128].  One block per (value head, 32 state rows), one
-// thread per state column.
+// to seg_S.  One block per (sequence, value head, 32 state rows), one thread
+// per state column.
 __global__ void __launch_bounds__(128) segment_combine_kernel(const ChunkParams p) {
     pdl_wait_primary();  // M and L come from the previous (phase 1) launch
     __shared__ float srow[32][128];
     const int V = p.V, H = p.H, nrb = V / 32;
-    const int h = blockIdx.x / nrb, r0 = (blockIdx.x % nrb) * 32, j = threadIdx.x;
-    const int seq = p.seq_order[0];
-    float *S = const_cast<float *>(p.seg_S);
+    const int sidx = blockIdx.x / (H * nrb);
+    const int h = (blockIdx.x / nrb) % H, r0 = (blockIdx.x % nrb) * 32, j = threadIdx.x;
+    const int seq = p.seq_order[sidx];
+    int seg_len, count;
+    segments_of(p.offsets[seq + 1] - p.offsets[seq], p.nseg, seg_len, count);
+    float *S = const_cast<float *>(p.seg_S) + (size_t)sidx * p.nseg * H * V * 128;
     for (int r = 0; r < 32; ++r) {
         const float x = p.state_init[(((size_t)seq * H + h) * V + r0 + r) * 128 + j];
         srow[r][j] = x;
         S[(((size_t)h) * V + r0 + r) * 128 + j] = x;
     }
     __syncthreads();
-    for (int q = 0; q + 1 < p.nseg; ++q) {
+    for (int q = 0; q + 1 < count; ++q) {
+        const size_t sq = (size_t)sidx * (p.nseg - 1) + q;
         float acc[32];
-        const float *L = p.seg_L + (((size_t)q * H + h) * V + r0) * 128 + j;
+        const float *L = p.seg_L + ((sq * H + h) * V + r0) * 128 + j;
 #pragma unroll
         for (int r = 0; r < 32; ++r) acc[r] = L[(size_t)r * 128];
-        const float *M = p.seg_M + ((size_t)q * H + h) * 128 * 128 + j;
+        const float *M = p.seg_M + (sq * H + h) * 128 * 128 + j;
 #pragma unroll 4
         for (int k = 0; k < 128; ++k) {
             const float m = M[(size_t)k * 128];
@@ -969,11 +991,12 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     return chunk_launch(map, omap, p, c.max_units, s);
 }
 
-// One long chunked sequence (seq_order[0]) in c.nseg segments of c.seg_len
-// tokens: phase 1 computes each segment's transition M and local final state
-// L from a zero start (segments 0..nseg-2, in parallel), the combine kernel
-// chains the start states S_{q+1} = S_q M_q + L_q, and phase 2 reruns every
-// segment from its start state (in parallel), writing the outputs.
+// c.nseq_seg long chunked sequences (seq_order[0..]), each cut into up to
+// c.nseg segments: phase 1 computes each segment's transition M and local
+// final state L from a zero start (all but the last segment of every
+// sequence, in parallel), the combine kernel chains the start states
+// S_{q+1} = S_q M_q + L_q, and phase 2 reruns every segment from its start
+// state (in parallel), writing the outputs.
 cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s) {
     CUtensorMap map, omap;
     ChunkParams p;
@@ -981,21 +1004,21 @@ cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s)
     if (e != cudaSuccess) return e;
     const int VT = c.V / 128;
     p.nseg = c.nseg;
-    p.seg_len = c.seg_len;
+    p.nseq_seg = c.nseq_seg;
     p.seg_M = c.seg_M;
     p.seg_L = c.seg_L;
     p.seg_S = c.seg_S;
     p.seg_mode = 1;
-    p.seg_units = (c.nseg - 1) * c.H * (VT + 1);
+    p.seg_units = c.nseq_seg * (c.nseg - 1) * c.H * (VT + 1);
     p.counter = &c.header->seg_next[0];
     e = chunk_launch(map, omap, p, p.seg_units, s);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(segment_combine_kernel, dim3((unsigned)(c.H * (c.V / 32))), dim3(128), 0, s,
-                      true, p);
+    e = launch_kernel(segment_combine_kernel, dim3((unsigned)(c.nseq_seg * c.H * (c.V / 32))),
+                      dim3(128), 0, s, true, p);
     note_launch();
     if (e != cudaSuccess) return e;
     p.seg_mode = 2;
-    p.seg_units = c.nseg * c.H * VT;
+    p.seg_units = c.nseq_seg * c.nseg * c.H * VT;
     p.counter = &c.header->seg_next[1];
     return chunk_launch(map, omap, p, p.seg_units, s);
 }

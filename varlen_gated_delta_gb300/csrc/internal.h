@@ -125,17 +125,20 @@ struct ChunkLaunch {
     float scale;
     long max_units;  // upper bound on work units (grid sizing)
     int opts;        // GDN_OPT_*
-    // segment-parallel mode for one long chunked sequence (nseg > 1): see
-    // launch_delta_chunked_segmented; seg_M [nseg-1][H][128][128],
+    // segment-parallel mode for nseq_seg long chunked sequences (nseg > 1): see
+    // launch_delta_chunked_segmented; per sequence seg_M [nseg-1][H][128][128],
     // seg_L [nseg-1][H][V][128], seg_S [nseg][H][V][128]
-    int nseg, seg_len;
+    int nseg, nseq_seg;
     float *seg_M, *seg_L, *seg_S;
 };
-// Workspace floats of the segment buffers for up to kMaxSegments segments.
+// Segment buffers: up to kMaxSegments segments of up to kMaxSegSeqs sequences.
 constexpr int kMaxSegments = 8;
-inline size_t segment_floats(int H, int V) {  // M, L of nseg-1 segments; start states of nseg
-    return (size_t)(kMaxSegments - 1) * H * ((size_t)128 * 128 + (size_t)V * 128) +
-           (size_t)kMaxSegments * H * V * 128;
+constexpr int kMaxSegSeqs = 4;
+inline size_t segment_m_floats(int H) { return (size_t)(kMaxSegments - 1) * H * 128 * 128; }
+inline size_t segment_l_floats(int H, int V) { return (size_t)(kMaxSegments - 1) * H * V * 128; }
+inline size_t segment_floats(int H, int V, int nseq) {  // M, L of nseg-1 segments; starts of nseg
+    return (size_t)nseq * (segment_m_floats(H) + segment_l_floats(H, V) +
+                           (size_t)kMaxSegments * H * V * 128);
 }
 // Dense-layout recurrence (q, k, v, out [B, S, H, n] T; g [B, S, H] or, with
 // per_channel, [B, S, H, n] f32; beta [B, S, H] f32; state [B, H, n, n] f32,
