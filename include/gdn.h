@@ -197,18 +197,34 @@ GDN_API int gdn_chunk_min_len(void);
 GDN_API uint64_t gdn_launch_count(void);
 
 /*
- * Segment-parallel chunked path: when a layer call (with offsets_host) has a
- * single chunked sequence of at least gdn_segment_min_len() tokens and too
- * few (head, V tile) units to fill the GPU, the sequence is cut into up to 8
- * segments run in parallel: each segment's transition S_end = S_start M + L
- * is computed from a zero start, the start states are chained, and every
- * segment is rerun from its start state.  gdn_set_segment_min_len(n): n > 0
- * sets the length (default 16384), 0 restores the default.  Process-wide.
- * The workspace holds the segment buffers when N >= 2 * that length
- * (gdn_workspace_bytes follows the setting).
+ * Segment-parallel chunked path (the chunk map is linear in the start state:
+ * S_end = S_start M + L).  When a layer call has offsets_host, every chunked
+ * sequence has at least gdn_segment_min_len() tokens and there are at most 4
+ * of them (and as many as N / gdn_segment_min_len()), sequence i may be cut
+ * into P_i <= 8 segments run in parallel: each segment's M and L are computed
+ * from a zero start, the start states are chained, and every segment is rerun
+ * from its start state.  The counts come from gdn_segment_plan.
+ * gdn_set_segment_min_len(n): n > 0 sets the length (default 16384), 0
+ * restores the default.  Process-wide.  The workspace holds the segment
+ * buffers when N >= that length (gdn_workspace_bytes follows the setting).
  */
 GDN_API int gdn_set_segment_min_len(int n);
 GDN_API int gdn_segment_min_len(void);
+
+/*
+ * The segment counts a layer call with these host offsets would use on a GPU
+ * with sm_count SMs (two chunked CTAs per SM), for H value heads of V
+ * channels (V a multiple of 128).  Host-only, no GPU needed.
+ *   offsets_host  int32 [B+1] host, valid packing (0 = offsets[0] <= ... = N)
+ *   counts        int32 [B] host, written: P_i for each segmented sequence,
+ *                 1 for every other sequence
+ * Returns the number of segmented sequences (0: the call runs unsegmented),
+ * or a negative GDN_ERR_* code for NULL pointers or invalid sizes.
+ * Capacity: the buffers of one workspace hold min(4, N / gdn_segment_min_len())
+ * segmented sequences.
+ */
+GDN_API int gdn_segment_plan(const int32_t *offsets_host, int B, int H, int V, int sm_count,
+                             int32_t *counts);
 
 /* Kernels that gdn_set_kernel_events can bracket. */
 typedef enum gdn_kernel_id {

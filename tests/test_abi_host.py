@@ -231,3 +231,61 @@ def test_dense_call_validation(lib):
     assert dense(perch=2) == 2
     assert dense(q=None) == 1
     assert dense(B=1 << 16, S=1 << 10, H=64, n=128) == 3
+
+
+def _offs(lens):
+    out = [0]
+    for n in lens:
+        out.append(out[-1] + n)
+    return out
+
+
+def test_segment_plan_follows_the_slot_budget():
+    """Host-side segment planner on a 152-SM GPU (304 chunked CTA slots).
+
+    Hand-derived: with 32 value heads of 256 channels a segment costs 64 rerun
+    units and 96 first-pass units, so sum P <= 4 and sum (P - 1) <= 3."""
+    plan = gdn.gdn_segment_plan
+    assert gdn.gdn_segment_min_len() == 16384
+    assert plan(_offs([131072]), 32, 256, 152) == [4]
+    assert plan(_offs([65536, 65536]), 32, 256, 152) == [2, 2]
+    # unequal lengths: the longer sequence takes the extra segments
+    # (100000 in 3 segments of 33344 tokens, beside 30000 unsegmented)
+    assert plan(_offs([100000, 30000]), 32, 256, 152) == [3, 1]
+    # four sequences fill the rerun already: nothing to gain
+    assert plan(_offs([32768] * 4), 32, 256, 152) == [1] * 4
+    # a short chunked sequence beside a long one, and serial sequences
+    assert plan(_offs([131072, 5000]), 32, 256, 152) == [1, 1]
+    assert plan(_offs([40, 131072, 1]), 32, 256, 152) == [1, 4, 1]
+    assert plan([0], 32, 256, 152) == []
+    with pytest.raises(gdn.GdnError):
+        plan(_offs([100]), 32, 100, 152)
+    with pytest.raises(gdn.GdnError):
+        plan([0, 10, 5], 32, 256, 152)
+
+
+def test_segment_plan_with_a_low_threshold():
+    plan = gdn.gdn_segment_plan
+    gdn.gdn_set_segment_min_len(256)
+    try:
+        # 8 heads of 128 channels: 8 rerun and 16 first-pass units a segment;
+        # the length caps a sequence at 8 segments of 128 tokens
+        assert plan(_offs([1000]), 8, 128, 152) == [8]
+        # more than four long sequences exceed the segment buffers
+        assert plan(_offs([300, 400, 500, 600, 700]), 4, 128, 152) == [1] * 5
+        # a chunked sequence under the threshold keeps everything unsegmented
+        assert plan(_offs([1500, 100]), 8, 128, 152) == [1, 1]
+        lens = [700, 5, 1200, 300, 1]
+        P = plan(_offs(lens), 8, 128, 152)
+        assert P[1] == 1 and P[4] == 1 and all(2 <= p <= 8 for p in (P[0], P[2]))
+        assert sum(P[i] for i in (0, 2, 3)) * 8 <= 304
+        assert sum(P[i] - 1 for i in (0, 2, 3)) * 16 <= 304
+        # every segment is a whole number of 64-token chunks and none is empty
+        for n, p in zip(lens, P):
+            if p > 1:
+                seg = -(-(-(-n // p)) // 64) * 64
+                assert (p - 1) * seg < n <= p * seg
+        # too few SMs for even one extra segment
+        assert plan(_offs([1000]), 8, 128, 4) == [1]
+    finally:
+        gdn.gdn_set_segment_min_len(0)

@@ -181,3 +181,22 @@ def test_capture_one_token_batches(dt):
     ref = _oracle(wl, d, counts, cap)
     np.testing.assert_array_equal(cpu64(upd), ref[3])
     _check_capsule(wl, capsule, ref[4], cap)
+
+
+def test_capture_with_segment_parallel_sequences():
+    """Long sequences cut into segments: the capsule still comes from the
+    token-serial replay of the captured prefix, and capture changes no output
+    bit of the segmented call."""
+    from test_gpu_chunked import segment_threshold
+    lens = (600, 3, 900)
+    wl = W.scaled(W.WORKLOADS["decode"], lens, H=8, HQ=4)
+    d = W.make_inputs(wl, DEV)
+    counts, cap = [8, 2, 5], 8
+    with segment_threshold(256):
+        o0, c0, s0 = _plain(wl, d, offsets_host=d["offsets_list"])
+        o1, c1, s1, upd, capsule = _capture(wl, d, counts, cap, offsets_host=d["offsets_list"])
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(c0, c1) and torch.equal(s0, s1)
+    ref = _oracle(wl, d, counts, cap)
+    np.testing.assert_array_equal(cpu64(upd), ref[3])
+    _check_capsule(wl, capsule, ref[4], cap)

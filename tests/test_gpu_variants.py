@@ -128,3 +128,22 @@ def test_variant_standalone_prepare_and_delta(case):
     torch.cuda.synchronize()
     assert rel_l2(c(qk), qk_ref) <= 1e-6 and rel_l2(c(gbeta), gb_ref) <= 1e-6
     assert rel_l2(c(out), o_ref) <= 1e-5 and rel_l2(c(sfin), s_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_variant_segment_parallel_bf16(case):
+    """Every rule through the segment-parallel chunked path: the transition of
+    a segment is the rule's own chunk map, so each variant must chain right."""
+    from test_gpu_chunked import segment_threshold
+    opts = CASES[case]
+    wl = W.scaled(W.WORKLOADS["decode"], (700, 5, 900), H=8, HQ=4)
+    d, a, b, A_log, dt = _inputs(wl, opts)
+    n0 = gdn.gdn_launch_count()
+    with segment_threshold(1 << 30):
+        _run(wl, d, a, b, A_log, dt, opts)
+    n_plain = gdn.gdn_launch_count() - n0
+    n0 = gdn.gdn_launch_count()
+    with segment_threshold(256):
+        got = _run(wl, d, a, b, A_log, dt, opts)
+    assert gdn.gdn_launch_count() - n0 == n_plain + 2
+    _check(wl, got, _oracle(wl, d, a, b, A_log, dt, opts))

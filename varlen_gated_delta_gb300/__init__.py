@@ -30,7 +30,7 @@ __all__ = [
     "gdn_layer_varlen_capture", "gdn_prepare_ex", "gdn_delta_varlen_ex", "gdn_layer_varlen_ex",
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
     "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
-    "gdn_set_segment_min_len", "gdn_segment_min_len",
+    "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -94,6 +94,8 @@ def load_library():
     lib.gdn_set_segment_min_len.argtypes = [i]
     lib.gdn_set_segment_min_len.restype = i
     lib.gdn_segment_min_len.restype = i
+    lib.gdn_segment_plan.argtypes = [vp, i, i, i, i, vp]
+    lib.gdn_segment_plan.restype = i
     lib.gdn_gated_delta_dense.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
@@ -544,9 +546,21 @@ def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=Fals
 
 
 def gdn_set_segment_min_len(n: int) -> None:
-    """Length from which a lone chunked sequence runs segment-parallel (0: default)."""
+    """Length from which chunked sequences may run segment-parallel (0: default)."""
     _check(load_library().gdn_set_segment_min_len(int(n)))
 
 
 def gdn_segment_min_len() -> int:
     return int(load_library().gdn_segment_min_len())
+
+
+def gdn_segment_plan(offsets, H: int, V: int, sm_count: int) -> list:
+    """Segment count per sequence that a layer call with these host offsets
+    would use on a GPU of sm_count SMs (1 for sequences run unsegmented)."""
+    offs = (ctypes.c_int32 * len(offsets))(*[int(x) for x in offsets])
+    B = len(offsets) - 1
+    counts = (ctypes.c_int32 * max(B, 1))()
+    rc = load_library().gdn_segment_plan(offs, B, int(H), int(V), int(sm_count), counts)
+    if rc < 0:
+        _check(-rc)
+    return [int(counts[i]) for i in range(B)]

@@ -127,6 +127,87 @@ static int check_offsets_host(const int32_t *offsets_host, int B, int N) {
     return GDN_OK;
 }
 
+// Segment plan of a call: which chunked sequences are cut into how many
+// segments.  n = 0: no segmentation.
+struct SegmentPlan {
+    int n = 0;
+    int seq[kMaxSegSeqs] = {};
+    int m0[kMaxSegSeqs + 1] = {};  // prefix sums of P_i - 1
+    int s0[kMaxSegSeqs + 1] = {};  // prefix sums of P_i
+};
+
+// Length of the segments of len tokens cut into P (a multiple of the chunk).
+static long segment_len(long len, long P) { return ((len + P - 1) / P + 63) / 64 * 64; }
+
+// Segmentation applies when every chunked sequence (>= thr tokens) has at
+// least gdn_segment_min_len() tokens and there are at most max_seqs of them.
+// Counts P_i are raised one at a time on the sequence whose segments are
+// longest while both chunked launches still fit in one wave of CTA slots:
+// sum P_i (head, V tile) units in the rerun, sum (P_i - 1) (head, V tile +
+// transition tile) units in the first pass.  The two passes take about the
+// longest phase-1 segment plus the longest segment; the plan with the least
+// of that is kept when it is no longer than the longest sequence (what the
+// unsegmented chunked launch takes).
+static SegmentPlan plan_segments(const int32_t *offsets_host, int B, int H, int V, int thr,
+                                 int max_seqs, int sm_count) {
+    SegmentPlan best;
+    int seq[kMaxSegSeqs];
+    long len[kMaxSegSeqs], P[kMaxSegSeqs];
+    int n = 0;
+    for (int i = 0; i < B; ++i) {
+        const long l = offsets_host[i + 1] - offsets_host[i];
+        if (l < thr) continue;
+        if (l < segment_min_len() || n == max_seqs || n == kMaxSegSeqs) return best;
+        seq[n] = i;
+        len[n] = l;
+        P[n] = 1;
+        ++n;
+    }
+    if (n == 0) return best;
+    const long VT = V / 128, slots = 2L * sm_count;
+    long plain = 0;
+    for (int i = 0; i < n; ++i) plain = len[i] > plain ? len[i] : plain;
+    if ((long)n * H * VT > slots) return best;  // the rerun alone would not fit one wave
+    long best_cost = plain + 1;
+    while (true) {
+        int arg = 0;
+        for (int i = 1; i < n; ++i)
+            if (segment_len(len[i], P[i]) > segment_len(len[arg], P[arg])) arg = i;
+        if (P[arg] == kMaxSegments) break;
+        long sumP = 0, sumP1 = 0;
+        for (int i = 0; i < n; ++i) {
+            sumP += P[i] + (i == arg);
+            sumP1 += P[i] + (i == arg) - 1;
+        }
+        if (sumP * H * VT > slots || sumP1 * H * (VT + 1) > slots) break;
+        ++P[arg];
+        long cost1 = 0, cost2 = 0;
+        for (int i = 0; i < n; ++i) {
+            const long sl = segment_len(len[i], P[i]);
+            if (P[i] > 1 && sl > cost1) cost1 = sl;
+            if (sl > cost2) cost2 = sl;
+        }
+        if (cost1 + cost2 < best_cost) {
+            best_cost = cost1 + cost2;
+            best.n = n;
+            best.m0[0] = best.s0[0] = 0;
+            for (int i = 0; i < n; ++i) {
+                // the segments segments_of makes: never more than P_i
+                const long sl = segment_len(len[i], P[i]);
+                const long cnt = (len[i] + sl - 1) / sl;
+                best.seq[i] = seq[i];
+                best.s0[i + 1] = best.s0[i] + (int)cnt;
+                best.m0[i + 1] = best.m0[i] + (int)cnt - 1;
+            }
+        }
+    }
+    for (int i = best.n; i < kMaxSegSeqs; ++i) {  // unused entries repeat the totals
+        best.s0[i + 1] = best.s0[i];
+        best.m0[i + 1] = best.m0[i];
+    }
+    return best;
+}
+
 struct WsLayout {
     size_t header, order, y, qk, gb, seg, total;  // seg: 0 when no segment buffers fit
     int seg_seqs;                                 // sequences the segment buffers hold
@@ -217,6 +298,24 @@ int gdn_set_segment_min_len(int n) {
 }
 
 int gdn_segment_min_len(void) { return segment_min_len(); }
+
+int gdn_segment_plan(const int32_t *offsets_host, int B, int H, int V, int sm_count,
+                     int32_t *counts) {
+    // errors are returned negated: a non-negative result is a count
+    if (!offsets_host || !counts) return -set_error(GDN_ERR_NULL, "offsets_host and counts are required");
+    if (B < 0 || H <= 0 || V <= 0 || V % 128 != 0 || sm_count <= 0)
+        return -set_error(GDN_ERR_SHAPE, "B >= 0, H > 0, V a positive multiple of 128, sm_count > 0");
+    const int N = B > 0 ? offsets_host[B] : 0;
+    const int rc = check_offsets_host(offsets_host, B, N);
+    if (rc) return -rc;
+    for (int i = 0; i < B; ++i) counts[i] = 1;
+    if (N < segment_min_len()) return 0;
+    const long cap = N / segment_min_len();
+    const SegmentPlan p = plan_segments(offsets_host, B, H, V, chunk_min_len(),
+                                        (int)(cap < kMaxSegSeqs ? cap : kMaxSegSeqs), sm_count);
+    for (int i = 0; i < p.n; ++i) counts[p.seq[i]] = p.s0[i + 1] - p.s0[i];
+    return p.n;
+}
 
 int gdn_set_kernel_events(int kernel, void *start, void *stop) {
     if (kernel < 0 || kernel > 2) return fail(GDN_ERR_SHAPE, "unknown kernel id %d", kernel);
@@ -447,31 +546,11 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         max_units = n * H * (V / 128);
     }
     // Long chunked sequences that leave most of the GPU idle are cut into
-    // segments run in parallel (two chunked launches and a combine step):
-    // when every chunked sequence has at least gdn_segment_min_len() tokens
-    // and there are at most the segment buffers' count of them.
-    int nseg = 1, nseq_seg = 0;
-    if (run_chunked && offsets_host && lay.seg != 0) {
-        int n_long = 0, n_chunked = 0;
-        for (int i = 0; i < B; ++i) {
-            const int l = offsets_host[i + 1] - offsets_host[i];
-            if (l >= thr) {
-                ++n_chunked;
-                n_long += l >= segment_min_len();
-            }
-        }
-        // the most segments for which both chunked launches fit in one wave
-        // of CTA slots: P (head, V tile) units per sequence in the rerun,
-        // (P - 1) (head, V tile + transition tile) units in the first pass
-        const long VT = V / 128, slots = 2L * sm_count_host();
-        long want = 0;
-        for (long P = 2; P <= kMaxSegments; ++P)
-            if (n_long * P * H * VT <= slots && n_long * (P - 1) * H * (VT + 1) <= slots) want = P;
-        if (n_long >= 1 && n_long == n_chunked && n_long <= lay.seg_seqs && want >= 2) {
-            nseg = (int)want;
-            nseq_seg = n_long;
-        }
-    }
+    // segments run in parallel (two chunked launches and a combine step).
+    const SegmentPlan seg = run_chunked && offsets_host && lay.seg != 0
+                                ? plan_segments(offsets_host, B, H, V, thr, lay.seg_seqs,
+                                                sm_count_host())
+                                : SegmentPlan{};
     // tokens of token-serial sequences need the prepare step; with host
     // offsets a batch of chunked sequences only skips it
     const bool capsule = cap && cap->capsule;
@@ -523,15 +602,20 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         cl.state_init = state_init; cl.state_fin = state_fin; cl.out = out;
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
         cl.scale = eff_scale; cl.max_units = max_units; cl.opts = opts;
-        if (nseg > 1) {
+        if (seg.n > 0) {
             float *segb = reinterpret_cast<float *>(ws + lay.seg);
-            cl.nseg = nseg; cl.nseq_seg = nseq_seg;
+            cl.nseq_seg = seg.n;
+            for (int i = 0; i < kMaxSegSeqs; ++i) cl.seg_seq[i] = seg.seq[i];
+            for (int i = 0; i <= kMaxSegSeqs; ++i) {
+                cl.seg_m0[i] = seg.m0[i];
+                cl.seg_s0[i] = seg.s0[i];
+            }
             cl.seg_M = segb;
             cl.seg_L = cl.seg_M + (size_t)lay.seg_seqs * segment_m_floats(H);
             cl.seg_S = cl.seg_L + (size_t)lay.seg_seqs * segment_l_floats(H, V);
         }
         mark_before(GDN_KERNEL_CHUNKED, s);
-        cudaError_t ce = nseg > 1 ? launch_delta_chunked_segmented(cl, s) : launch_delta_chunked(cl, s);
+        cudaError_t ce = seg.n > 0 ? launch_delta_chunked_segmented(cl, s) : launch_delta_chunked(cl, s);
         mark_after(GDN_KERNEL_CHUNKED, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "chunked kernel launch");
         return GDN_OK;

@@ -92,19 +92,22 @@ struct ChunkParams {
     float scale;
     int tma_store;  // full output tiles leave through omap
     int opts;       // GDN_OPT_* rule / activation options
-    // Segment-parallel mode for nseq_seg long sequences (seq_order[0..]) cut
-    // into up to nseg segments each (segments_of).  seg_mode 1: segments 0..nseg-2 from a zero
+    // Segment-parallel mode for nseq_seg long sequences seg_seq[i], sequence i
+    // cut into up to P_i = seg_s0[i+1] - seg_s0[i] segments (segments_of).
+    // seg_mode 1: every segment but the last of each sequence from a zero
     // state, plus a 128-row tile starting from the identity with v = 0 whose
     // final state is the segment's transition M (S_end = S_start M + L);
     // writes M and the local final state L, no outputs.  seg_mode 2: every
-    // segment from its true start state (seg_S), writing
-    // outputs; the last segment writes state_fin.  seg_S[0] is a copy of the
-    // initial state, so state_fin may alias state_init.
-    int seg_mode, nseg, nseq_seg, seg_units;
-    unsigned int *counter;   // work counter of this launch
-    // per segmented sequence i (seq_order[i], i < nseq_seg):
-    float *seg_M, *seg_L;    // [i][nseg-1][H][128][128], [i][nseg-1][H][V][128]
-    const float *seg_S;      // [i][nseg][H][V][128]: start states of the segments
+    // segment from its true start state (seg_S), writing outputs; the last
+    // segment writes state_fin.  A sequence's first start state is a copy of
+    // its initial state, so state_fin may alias state_init.
+    int seg_mode, nseq_seg, seg_units;
+    int seg_seq[kMaxSegSeqs];
+    int seg_m0[kMaxSegSeqs + 1];  // first phase-1 segment of each sequence (P_i - 1 each)
+    int seg_s0[kMaxSegSeqs + 1];  // first segment of each sequence (P_i each)
+    unsigned int *counter;        // work counter of this launch
+    float *seg_M, *seg_L;  // [phase-1 segment][H][128][128], [phase-1 segment][H][V][128]
+    const float *seg_S;    // [segment][H][V][128]: start states of the segments
 };
 
 // Segment length of a sequence of len tokens cut into at most nseg segments
@@ -331,28 +334,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncthreads();
         const int u = *s_unit;
         if (u >= n_units || *s_abort) break;
-        int seq, h, vt, seg = 0, sidx = 0, nseg_here = 1;
+        int seq, h, vt, q = 0, seg = 0, nseg_here = 1;
         bool mtile = false;  // the transition tile of a segment (seg_mode 1)
         if (p.seg_mode == 0) {
             seq = p.seq_order[u / (H * p.VT)];
             h = (u / p.VT) % H;
             vt = u % p.VT;
         } else {
+            // q: the segment's index among this launch's segments, numbering
+            // the M / L (seg_mode 1) or start-state (seg_mode 2) buffers.
+            // Constant indices only: a dynamic index into the parameter
+            // arrays would copy them to local memory.
             const int tiles = p.VT + (p.seg_mode == 1);
-            const int per_seq = (p.seg_mode == 1 ? p.nseg - 1 : p.nseg) * H * tiles;
-            sidx = u / per_seq;
-            const int r = u % per_seq;
-            seq = p.seq_order[sidx];
-            seg = r / (H * tiles);
-            h = (r / tiles) % H;
-            const int tile = r % tiles;
+            q = u / (H * tiles);
+            h = (u / tiles) % H;
+            const int tile = u % tiles;
             mtile = tile == p.VT;
             vt = mtile ? 0 : tile;
+            seq = p.seg_seq[0];
+            seg = q;
+            nseg_here = p.seg_s0[1];
+#pragma unroll
+            for (int i = 1; i < kMaxSegSeqs; ++i) {
+                const int f = p.seg_mode == 1 ? p.seg_m0[i] : p.seg_s0[i];
+                if (i < p.nseq_seg && q >= f) {
+                    seq = p.seg_seq[i];
+                    seg = q - f;
+                    nseg_here = p.seg_s0[i + 1] - p.seg_s0[i];
+                }
+            }
         }
         int s = p.offsets[seq], e = p.offsets[seq + 1];
         if (p.seg_mode) {  // this segment's tokens (units past the sequence's last segment are empty)
             int seg_len;
-            segments_of(e - s, p.nseg, seg_len, nseg_here);
+            segments_of(e - s, nseg_here, seg_len, nseg_here);
             if (seg >= (p.seg_mode == 1 ? nseg_here - 1 : nseg_here)) {
                 __syncthreads();  // every thread has read s_unit before thread 0 rewrites it
                 continue;
@@ -365,18 +380,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int kh = h / G;
         const int qcol = kh * 128, kcol = HQ * 128 + kh * 128;
         const int vcol = 2 * HQ * 128 + h * V + vt * 128;
+        const size_t state_row = ((size_t)seq * H + h) * V + vt * 128 + row;
         const int opts = p.opts;
         const bool need_a = !(opts & GDN_OPT_NO_DECAY), need_b = !(opts & GDN_OPT_NO_BETA);
         const bool softplus_gate = need_a && !(opts & GDN_OPT_GATE_EXP);
         const float dtb = softplus_gate ? __ldg(p.dt_bias + h) : 0.f;
         const float neg_ea = softplus_gate ? -expf(__ldg(p.A_log + h)) * 1.4426950408889634f : 0.f;
-        const size_t state_row = ((size_t)seq * H + h) * V + vt * 128 + row;
 
         // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
         {
             const float *src = p.state_init + state_row * 128 + hc * 64;
             if (p.seg_mode == 2)
-                src = p.seg_S + (((((size_t)sidx * p.nseg + seg) * H + h) * V + vt * 128 + row) * 128 + hc * 64);
+                src = p.seg_S + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -816,10 +831,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // final state row `row`, columns [64 hc, 64 hc + 64) -> global
         if (p.seg_mode != 2 || seg == nseg_here - 1) {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
-            const size_t sq = (size_t)sidx * (p.nseg - 1) + seg;  // (sequence, segment) of phase 1
             if (p.seg_mode == 1)
-                dst = mtile ? p.seg_M + (((sq * H + h) * 128 + row) * 128 + hc * 64)
-                            : p.seg_L + (((sq * H + h) * V + vt * 128 + row) * 128 + hc * 64);
+                dst = mtile ? p.seg_M + ((((size_t)q * H + h) * 128 + row) * 128 + hc * 64)
+                            : p.seg_L + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -937,8 +951,8 @@ cudaError_t chunk_launch(const CUtensorMap &map, const CUtensorMap &omap, const 
     return e;
 }
 
-// Start states of the segments of each segmented sequence i (seq_order[i]):
-// S_0 = state_init, S_{q+1} = S_q M_q + L_q (rows of S independent), written
+// Start states of the segments of each segmented sequence i (seg_seq[i]):
+// S_0 = state_init, S_{j+1} = S_j M_j + L_j (rows of S independent), written
 // to seg_S.  One block per (sequence, value head, 32 state rows), one thread
 // per state column.
 __global__ void __launch_bounds__(128) segment_combine_kernel(const ChunkParams p) {
@@ -947,10 +961,11 @@ __global__ void __launch_bounds__(128) segment_combine_kernel(const ChunkParams 
     const int V = p.V, H = p.H, nrb = V / 32;
     const int sidx = blockIdx.x / (H * nrb);
     const int h = (blockIdx.x / nrb) % H, r0 = (blockIdx.x % nrb) * 32, j = threadIdx.x;
-    const int seq = p.seq_order[sidx];
+    const int seq = p.seg_seq[sidx];
     int seg_len, count;
-    segments_of(p.offsets[seq + 1] - p.offsets[seq], p.nseg, seg_len, count);
-    float *S = const_cast<float *>(p.seg_S) + (size_t)sidx * p.nseg * H * V * 128;
+    segments_of(p.offsets[seq + 1] - p.offsets[seq], p.seg_s0[sidx + 1] - p.seg_s0[sidx], seg_len,
+                count);
+    float *S = const_cast<float *>(p.seg_S) + (size_t)p.seg_s0[sidx] * H * V * 128;
     for (int r = 0; r < 32; ++r) {
         const float x = p.state_init[(((size_t)seq * H + h) * V + r0 + r) * 128 + j];
         srow[r][j] = x;
@@ -958,7 +973,7 @@ __global__ void __launch_bounds__(128) segment_combine_kernel(const ChunkParams 
     }
     __syncthreads();
     for (int q = 0; q + 1 < count; ++q) {
-        const size_t sq = (size_t)sidx * (p.nseg - 1) + q;
+        const size_t sq = (size_t)p.seg_m0[sidx] + q;
         float acc[32];
         const float *L = p.seg_L + ((sq * H + h) * V + r0) * 128 + j;
 #pragma unroll
@@ -991,25 +1006,30 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     return chunk_launch(map, omap, p, c.max_units, s);
 }
 
-// c.nseq_seg long chunked sequences (seq_order[0..]), each cut into up to
-// c.nseg segments: phase 1 computes each segment's transition M and local
-// final state L from a zero start (all but the last segment of every
-// sequence, in parallel), the combine kernel chains the start states
-// S_{q+1} = S_q M_q + L_q, and phase 2 reruns every segment from its start
-// state (in parallel), writing the outputs.
+// c.nseq_seg long chunked sequences (c.seg_seq), sequence i cut into up to
+// c.seg_s0[i+1] - c.seg_s0[i] segments: phase 1 computes each segment's
+// transition M and local final state L from a zero start (all but the last
+// segment of every sequence, in parallel), the combine kernel chains the start
+// states S_{j+1} = S_j M_j + L_j, and phase 2 reruns every segment from its
+// start state (in parallel), writing the outputs.
 cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s) {
     CUtensorMap map, omap;
     ChunkParams p;
     cudaError_t e = chunk_setup(c, map, omap, p);
     if (e != cudaSuccess) return e;
+    if (c.nseq_seg < 1 || c.nseq_seg > kMaxSegSeqs) return cudaErrorInvalidValue;
     const int VT = c.V / 128;
-    p.nseg = c.nseg;
     p.nseq_seg = c.nseq_seg;
+    for (int i = 0; i < kMaxSegSeqs; ++i) p.seg_seq[i] = c.seg_seq[i];
+    for (int i = 0; i <= kMaxSegSeqs; ++i) {
+        p.seg_m0[i] = c.seg_m0[i];
+        p.seg_s0[i] = c.seg_s0[i];
+    }
     p.seg_M = c.seg_M;
     p.seg_L = c.seg_L;
     p.seg_S = c.seg_S;
     p.seg_mode = 1;
-    p.seg_units = c.nseq_seg * (c.nseg - 1) * c.H * (VT + 1);
+    p.seg_units = c.seg_m0[c.nseq_seg] * c.H * (VT + 1);
     p.counter = &c.header->seg_next[0];
     e = chunk_launch(map, omap, p, p.seg_units, s);
     if (e != cudaSuccess) return e;
@@ -1018,7 +1038,7 @@ cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s)
     note_launch();
     if (e != cudaSuccess) return e;
     p.seg_mode = 2;
-    p.seg_units = c.nseq_seg * c.nseg * c.H * VT;
+    p.seg_units = c.seg_s0[c.nseq_seg] * c.H * VT;
     p.counter = &c.header->seg_next[1];
     return chunk_launch(map, omap, p, p.seg_units, s);
 }

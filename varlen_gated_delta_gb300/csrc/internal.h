@@ -112,6 +112,11 @@ cudaError_t launch_conv_final(const void *x, const int32_t *offsets, const void 
 cudaError_t launch_prepare(const PrepParams &p, int dtype, cudaStream_t s, bool pdl);
 cudaError_t launch_delta_serial(const DeltaParams &p, int dtype, cudaStream_t s, bool pdl);
 
+// Segment-parallel chunked path: at most kMaxSegments segments per sequence,
+// at most kMaxSegSeqs segmented sequences per call.
+constexpr int kMaxSegments = 8;
+constexpr int kMaxSegSeqs = 4;
+
 // Chunked (tensor-core) recurrence for sequences listed in seq_order.
 struct ChunkLaunch {
     const void *y;  // conv output [N, W] bf16
@@ -125,18 +130,19 @@ struct ChunkLaunch {
     float scale;
     long max_units;  // upper bound on work units (grid sizing)
     int opts;        // GDN_OPT_*
-    // segment-parallel mode for nseq_seg long chunked sequences (nseg > 1): see
-    // launch_delta_chunked_segmented; per sequence seg_M [nseg-1][H][128][128],
-    // seg_L [nseg-1][H][V][128], seg_S [nseg][H][V][128]
-    int nseg, nseq_seg;
+    // segment-parallel mode (nseq_seg > 0): sequences seg_seq[i], i < nseq_seg,
+    // sequence i in P_i = seg_s0[i+1] - seg_s0[i] segments, seg_m0[i] =
+    // sum over j < i of (P_j - 1); see launch_delta_chunked_segmented.
+    // seg_M [seg_m0[n]][H][128][128], seg_L [seg_m0[n]][H][V][128],
+    // seg_S [seg_s0[n]][H][V][128]
+    int nseq_seg;
+    int seg_seq[kMaxSegSeqs], seg_m0[kMaxSegSeqs + 1], seg_s0[kMaxSegSeqs + 1];
     float *seg_M, *seg_L, *seg_S;
 };
 // Segment buffers: up to kMaxSegments segments of up to kMaxSegSeqs sequences.
-constexpr int kMaxSegments = 8;
-constexpr int kMaxSegSeqs = 4;
 inline size_t segment_m_floats(int H) { return (size_t)(kMaxSegments - 1) * H * 128 * 128; }
 inline size_t segment_l_floats(int H, int V) { return (size_t)(kMaxSegments - 1) * H * V * 128; }
-inline size_t segment_floats(int H, int V, int nseq) {  // M, L of nseg-1 segments; starts of nseg
+inline size_t segment_floats(int H, int V, int nseq) {  // M, L of P-1 segments; starts of P
     return (size_t)nseq * (segment_m_floats(H) + segment_l_floats(H, V) +
                            (size_t)kMaxSegments * H * V * 128);
 }
