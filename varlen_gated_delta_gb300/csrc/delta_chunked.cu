@@ -547,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int g = lane >> 2, tg = lane & 3;
             if (warp < 2) {
                 const int blk = warp * 2 + (lane >> 4), c = lane & 15, base = blk * 16;
-                // column i of the block (A[base + r][base + i], r > i) is row i of A^T;
-                // each column is loaded one step ahead of its use
+                // column i of the block (A[base + r][base + i], r > i) is row i of A^T
+                // (loaded right before its use: prefetching one step ahead costs
+                // registers that the rest of the loop spills for)
                 auto load_col = [&](int i, float (&av)[16]) {
                     const float *acol = sAt + (base + i) * kAtStride + base;
 #pragma unroll
@@ -562,18 +563,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         }
                     }
                 };
-                float pr[16], tc[16], av0[16], av1[16];
+                float pr[16], tc[16], av0[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) pr[r] = 0.f;
-                load_col(0, av0);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float (&cur)[16] = (i & 1) ? av1 : av0;
-                    float (&nxt)[16] = (i & 1) ? av0 : av1;
-                    if (i + 1 < 15) load_col(i + 1, nxt);
+                    if (i < 15) load_col(i, av0);
                     tc[i] = (i == c) ? 1.f : (i > c ? -pr[i] : 0.f);
 #pragma unroll
-                    for (int r = i + 1; r < 16; ++r) pr[r] = fmaf(cur[r], tc[i], pr[r]);
+                    for (int r = i + 1; r < 16; ++r) pr[r] = fmaf(av0[r], tc[i], pr[r]);
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) sT[(base + r) * kTStride + base + c] = tc[r];
@@ -698,7 +696,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int c8 = 0; c8 < 4; ++c8) st_sw128_8(sm + kOffWt, row, hc * 4 + c8, f + c8 * 8);
                 const float gC = ex2f(v_lb[63]);
                 unsigned char *s0 = sm + kOffS0 + hc * 16384;  // this half is one K-block
-#pragma unroll
+                // (rolled loops here and in E4 keep the kernel under 128 registers
+                // with fewer spills)
+#pragma unroll 1
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(lane_base + kColS + hc * 64 + c0, r);
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (write_out)
             {
                 __nv_bfloat16 *otile = reinterpret_cast<__nv_bfloat16 *>(sm + kOffOut);
-#pragma unroll
+#pragma unroll 1
                 for (int c16 = 0; c16 < 2; ++c16) {
                     uint32_t r4[16], r5[16];
                     tmem_ld16(lane_base + kColD4 + hc * 32 + c16 * 16, r4);
