@@ -60,6 +60,27 @@ def _dist():
     return world, rank, local
 
 
+def _replica_seed(wl, rank):
+    """Each rank's replica draws its own batch (weak scaling, no shared work)."""
+    return wl.seed + 1000 * rank
+
+
+def _max_over_ranks(values, device):
+    """Per-rank timings -> their maximum over the ranks of the process group
+    (unchanged without one); the job is as slow as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def _job_tokens_per_s(world, tokens_per_rank, steps, ms):
+    """Whole-job throughput: the tokens of all ranks over the max-over-ranks time."""
+    return world * tokens_per_rank * steps / (ms * 1e-3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -304,7 +325,7 @@ def run_ours(args, wl):
         dist.barrier()
     gdn.load_library()
 
-    d = W.make_inputs(wl, dev, seed=wl.seed + 1000 * rank)
+    d = W.make_inputs(wl, dev, seed=_replica_seed(wl, rank))
     offs = d["offsets_list"]
     N, B = offs[-1], len(offs) - 1
     act = gdn.GDN_ACT_SILU if wl.silu else gdn.GDN_ACT_NONE
@@ -509,14 +530,11 @@ def run_ours(args, wl):
     # the last step's output and capsule, read back on the host, are this step's results
     torch.testing.assert_close(out_host[last].to(dev), outs[last], rtol=0, atol=0)
 
-    t = torch.tensor([ms, e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = t.tolist()
+    ms, e2e_ms = _max_over_ranks([ms, e2e_ms], dev)
     if rank == 0:
         hbm, tf, tf_s, peak_src = _peaks()
         kavg = statistics.mean(kern_ms)
-        value = world * N * args.steps / (ms * 1e-3)
+        value = _job_tokens_per_s(world, N, args.steps, ms)
         if dom == gdn.GDN_KERNEL_SERIAL:
             kbytes = algorithmic_bytes_delta(wl, N, B, cap)
             achieved = kbytes / (kavg * 1e-3) / 1e9
@@ -546,7 +564,7 @@ def run_ours(args, wl):
                        **({"rule": args.rule} if opts else {})},
             "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
             "roofline": roof,
-            "e2e": {"value": world * N * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": _job_tokens_per_s(world, N, args.steps, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipeline": ("one serial step (copies, call, read-back) replayed as a "
                                  "CUDA graph") if small else
@@ -567,8 +585,12 @@ def run_ours(args, wl):
 
 def run_dense(args, wl):
     """The dense-layout call (rlx-cpu GatedDeltaNet thunk layout) on the
-    workload's batch, length and head geometry (n = K = V, H heads for q/k/v)."""
+    workload's batch, length and head geometry (n = K = V, H heads for q/k/v).
+    A one-GPU measurement: under torchrun only rank 0 runs it."""
     import torch
+
+    if _dist()[1] != 0:
+        return
 
     import varlen_gated_delta_gb300 as gdn
     from varlen_gated_delta_gb300 import build as gdn_build
