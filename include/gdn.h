@@ -244,6 +244,21 @@ typedef enum gdn_kernel_id {
  */
 GDN_API int gdn_set_kernel_events(int kernel, void *start, void *stop);
 
+/*
+ * Self-test of the failure path: launches one warp on `stream` that waits, with
+ * the same bounded wait as every mbarrier wait of the chunked kernel, for a
+ * barrier phase that never completes.  After about limit_us microseconds of
+ * GPU global time the wait gives up and the kernel writes GDN_ERR_TIMEOUT to
+ * *status (device int32; GDN_OK would mean the wait completed, which cannot
+ * happen) and returns; the context stays usable.  Asynchronous: read *status
+ * after synchronising the stream.
+ *   status    int32 device pointer (written)
+ *   limit_us  1 .. 1000000
+ * Returns GDN_ERR_NULL / GDN_ERR_SHAPE for bad arguments, GDN_ERR_CUDA if the
+ * launch fails, else GDN_OK.
+ */
+GDN_API int gdn_selftest_wait_timeout(int32_t *status, int limit_us, void *stream);
+
 /* Size of the static device scratch used by gdn_layer_varlen_noalloc. */
 #define GDN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

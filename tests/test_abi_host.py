@@ -289,3 +289,10 @@ def test_segment_plan_with_a_low_threshold():
         assert plan(_offs([1000]), 8, 128, 4) == [1]
     finally:
         gdn.gdn_set_segment_min_len(0)
+
+
+def test_selftest_wait_timeout_validates_before_launch(lib):
+    assert lib.gdn_selftest_wait_timeout(None, 1000, None) == 1          # GDN_ERR_NULL
+    bogus = ctypes.c_void_p(256)  # never dereferenced: the limit is checked first
+    assert lib.gdn_selftest_wait_timeout(bogus, 0, None) == 2            # GDN_ERR_SHAPE
+    assert lib.gdn_selftest_wait_timeout(bogus, 1000001, None) == 2

@@ -31,6 +31,7 @@ __all__ = [
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
     "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
     "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
+    "gdn_selftest_wait_timeout",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -96,6 +97,8 @@ def load_library():
     lib.gdn_segment_min_len.restype = i
     lib.gdn_segment_plan.argtypes = [vp, i, i, i, i, vp]
     lib.gdn_segment_plan.restype = i
+    lib.gdn_selftest_wait_timeout.argtypes = [vp, i, vp]
+    lib.gdn_selftest_wait_timeout.restype = i
     lib.gdn_gated_delta_dense.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp]
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
@@ -552,6 +555,16 @@ def gdn_set_segment_min_len(n: int) -> None:
 
 def gdn_segment_min_len() -> int:
     return int(load_library().gdn_segment_min_len())
+
+
+def gdn_selftest_wait_timeout(limit_us: int, device=None) -> int:
+    """Run the bounded-wait self-test on the current stream and return the
+    status the kernel wrote (GDN_ERR_TIMEOUT = 7 when the wait gave up)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    _check(load_library().gdn_selftest_wait_timeout(ctypes.c_void_p(status.data_ptr()),
+                                                    int(limit_us), _stream(dev)))
+    return int(status.item())
 
 
 def gdn_segment_plan(offsets, H: int, V: int, sm_count: int) -> list:
