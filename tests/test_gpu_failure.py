@@ -5,6 +5,8 @@ the chunked kernel uses, on a barrier phase nothing completes.  The wait must
 give up after its limit, the kernel must report GDN_ERR_TIMEOUT and return,
 and the context must stay usable for the next layer call.
 """
+import ctypes
+
 import pytest
 import torch
 
@@ -27,12 +29,20 @@ def _lib():
 @pytest.mark.parametrize("limit_us", [2000, 50000])
 def test_bounded_wait_gives_up_after_its_limit(limit_us):
     torch.cuda.set_device(0)
+    # a first launch loads the library's kernels; time a later one
+    assert gdn.gdn_selftest_wait_timeout(100) == GDN_ERR_TIMEOUT
+    lib = gdn.load_library()
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    status = gdn.gdn_selftest_wait_timeout(limit_us)
-    e1.record()
     torch.cuda.synchronize()
-    assert status == GDN_ERR_TIMEOUT
+    e0.record(stream)
+    rc = lib.gdn_selftest_wait_timeout(ctypes.c_void_p(status.data_ptr()), limit_us,
+                                       ctypes.c_void_p(stream.cuda_stream))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(status.item()) == GDN_ERR_TIMEOUT
     ms = e0.elapsed_time(e1)
     assert limit_us * 1e-3 * 0.9 <= ms <= limit_us * 1e-3 + 50.0, ms
 
