@@ -151,6 +151,7 @@ def segment_threshold(n):
     ((1100,), {"H": 4, "HQ": 2, "V": 256, "D": 2, "a_mean": -1.0, "b_std": 2.0}, True),  # long geometry
     ((900, 1300), {"H": 8, "HQ": 4}, True),                       # two long sequences
     ((700, 5, 1200, 300, 1), {"H": 8, "HQ": 4}, True),            # three, one with fewer segments
+    ((300, 900, 500, 700), {"H": 4, "HQ": 2}, True),              # four: as many as the buffers hold
     ((1500, 100), {"H": 8, "HQ": 4}, False),                      # a short chunked sequence beside
     ((300, 400, 500, 600, 700), {"H": 4, "HQ": 2}, False),        # more than the buffers hold
 ])
