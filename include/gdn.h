@@ -216,10 +216,12 @@ GDN_API int gdn_segment_min_len(void);
  * with sm_count SMs (two chunked CTAs per SM), for H value heads of V
  * channels (V a multiple of 128).  Host-only, no GPU needed.
  *   offsets_host  int32 [B+1] host, valid packing (0 = offsets[0] <= ... = N)
- *   counts        int32 [B] host, written: P_i for each segmented sequence,
- *                 1 for every other sequence
- * Returns the number of segmented sequences (0: the call runs unsegmented),
- * or a negative GDN_ERR_* code for NULL pointers or invalid sizes.
+ *   counts        int32 [B] host, written: P_i for each chunked sequence of a
+ *                 segmented call (1 for one that keeps a single segment), 1 for
+ *                 every other sequence
+ * Returns the number of chunked sequences the segment-parallel launches run
+ * (some may keep P_i = 1; 0: the call runs unsegmented), or a negative
+ * GDN_ERR_* code (negated) for NULL pointers, invalid sizes or bad offsets.
  * Capacity: the buffers of one workspace hold min(4, N / gdn_segment_min_len())
  * segmented sequences.
  */
