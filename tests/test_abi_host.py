@@ -296,3 +296,41 @@ def test_selftest_wait_timeout_validates_before_launch(lib):
     bogus = ctypes.c_void_p(256)  # never dereferenced: the limit is checked first
     assert lib.gdn_selftest_wait_timeout(bogus, 0, None) == 2            # GDN_ERR_SHAPE
     assert lib.gdn_selftest_wait_timeout(bogus, 1000001, None) == 2
+
+
+def test_segment_plan_invariants_on_random_batches():
+    """Random batches: every plan fits one wave of CTA slots in both passes,
+    gives no sequence more than 8 segments, cuts every segmented sequence into
+    exactly its count of non-empty whole-chunk segments, and only segments
+    when every chunked sequence is long and there are at most four."""
+    import random
+    rng = random.Random(20261203)
+    plan = gdn.gdn_segment_plan
+    chunk_min = gdn.gdn_chunk_min_len()
+    for trial in range(300):
+        min_len = rng.choice([64, 256, 1000, 4096])
+        gdn.gdn_set_segment_min_len(min_len)
+        try:
+            B = rng.randint(1, 7)
+            lens = [rng.choice([0, rng.randint(1, 63), rng.randint(64, 3 * min_len),
+                                rng.randint(min_len, 12 * min_len)]) for _ in range(B)]
+            H, V, sms = rng.randint(1, 40), rng.choice([128, 256]), rng.randint(1, 160)
+            P = plan(_offs(lens), H, V, sms)
+        finally:
+            gdn.gdn_set_segment_min_len(0)
+        assert len(P) == B and all(1 <= p <= 8 for p in P)
+        chunked = [i for i, n in enumerate(lens) if n >= chunk_min]
+        if any(p > 1 for p in P):
+            N = sum(lens)
+            assert all(lens[i] >= min_len for i in chunked), (lens, P)
+            assert len(chunked) <= min(4, N // min_len)
+            VT = V // 128
+            assert sum(P[i] for i in chunked) * H * VT <= 2 * sms
+            assert sum(P[i] - 1 for i in chunked) * H * (VT + 1) <= 2 * sms
+            for i in chunked:
+                n, p = lens[i], P[i]
+                seg = -(-(-(-n // p)) // 64) * 64          # segment length, whole chunks
+                assert (p - 1) * seg < n <= p * seg, (n, p, seg)
+        for i, n in enumerate(lens):
+            if n < chunk_min:
+                assert P[i] == 1
