@@ -1,0 +1,134 @@
+"""The chunked (WY/UT) form of the recurrence, written out in fp64 on the CPU
+the way the tensor-core kernel factorises it, against the token-serial oracle.
+
+The pages give only the token recurrence (paged_ssm.rs, DELTA kernel): per
+token S_t = g_t S_{t-1} + beta_t (v_t - g_t S_{t-1} k_t) k_t^T, o_t = S_t (scale q_t)
+with q, k L2-normalised.  The chunked form is derived from it: over a chunk of
+C tokens with gamma_t = prod_{s<=t} g_s and Gamma[t, i] = gamma_t / gamma_i,
+  (I + A) Delta = diag(beta) V - diag(beta gamma) K S_0^T,  A[t, i] = beta_t Gamma[t, i] k_t.k_i (i < t),
+  o_t = scale gamma_t (Q S_0^T)[t] + sum_{i<=t} scale Gamma[t, i] (q_t.k_i) Delta[i],
+  S_C = gamma_C S_0 + Delta^T diag(Gamma[C, .]) K,
+so the chunk maps the state linearly from the right, S_C = S_0 M + L.  The
+kernel keeps the decays in log2 (lb_t = sum log2 g, ck_i = log2 r_k(i) - lb_i,
+2^(lb_t + ck_i) = r_k(i) Gamma[t, i]) and applies the norms r = rsqrt(|x|^2 + 1e-12)
+as row factors of the raw q and k.  These tests pin that algebra, the ragged
+last chunk (beta = 0, log g = 0 padding) and the segment composition used for
+long sequences, with no GPU involved.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+C = 64
+
+
+def _norm_factor(x):
+    return 1.0 / np.sqrt((x * x).sum(-1) + 1e-12)
+
+
+def chunk_forward(S0, q, k, v, g, beta, scale, mistake=None):
+    """Chunk by chunk, as the kernel does: raw q, k [T, K], v [T, V], g, beta [T],
+    S0 [R, K] (R state rows; v may be None for the transition map).  Returns
+    (out [T, R], S [R, K]).  `mistake` plants one plausible slip (tests only)."""
+    T, K = k.shape
+    R = S0.shape[0]
+    S = S0.copy()
+    out = np.zeros((T, R))
+    for t0 in range(0, T, C):
+        n = min(C, T - t0)
+        qc, kc = np.zeros((C, K)), np.zeros((C, K))
+        vc = np.zeros((C, R))
+        lg, bc = np.zeros(C), np.zeros(C)         # padding: log g = 0, beta = 0
+        qc[:n], kc[:n] = q[t0:t0 + n], k[t0:t0 + n]
+        if v is not None:
+            vc[:n] = v[t0:t0 + n]
+        lg[:n], bc[:n] = np.log2(g[t0:t0 + n]), beta[t0:t0 + n]
+        rq, rk = _norm_factor(qc), _norm_factor(kc)
+        lb = np.cumsum(lg)                          # log2 gamma_t
+        if mistake == "exclusive_decay":
+            lb = lb - lg
+        ck = np.log2(rk) - lb                       # log2 r_k(i) - lb_i
+        E = 2.0 ** (lb[:, None] + ck[None, :])      # r_k(i) Gamma[t, i]
+        KK, QK = kc @ kc.T, qc @ kc.T
+        A = np.tril((bc * rk)[:, None] * E * KK, -1)
+        P = np.tril((scale * rq)[:, None] * E * QK, -1 if mistake == "strict_P" else 0)
+        Tm = np.linalg.inv(np.eye(C) + A)
+        gam = 2.0 ** lb
+        Wm = (Tm * (bc * rk * gam)[None, :]) @ kc   # T diag(beta r_k gamma) K
+        Delta = (Tm * bc[None, :]) @ vc - Wm @ S.T  # [C, R]
+        o = (scale * rq * gam)[:, None] * (qc @ S.T) + P @ Delta
+        out[t0:t0 + n] = o[:n]
+        c = 2.0 ** (lb[-1] + ck)                    # r_k(t) Gamma[C, t]
+        if mistake == "no_carry_decay":
+            c = rk
+        S = 2.0 ** lb[-1] * S + (Delta * c[:, None]).T @ kc
+    return out, S
+
+
+def _case(T, K, V, seed, strong=False):
+    rng = np.random.default_rng(seed)
+    q, k = rng.normal(size=(T, K)), rng.normal(size=(T, K))
+    v = rng.normal(size=(T, V))
+    g = rng.uniform(0.05, 0.6, T) if strong else rng.uniform(0.7, 1.0, T)
+    beta = rng.uniform(0.0, 1.0, T)
+    S0 = rng.normal(scale=0.3, size=(V, K))
+    return q, k, v, g, beta, S0
+
+
+def _oracle(q, k, v, g, beta, S0, scale):
+    """The token-serial oracle on one sequence, one head (H = HQ = 1)."""
+    T, K = k.shape
+    V = v.shape[1]
+    y = np.concatenate([np.zeros((T, 2 * K)), v], axis=1)      # only v is read from y
+    qk = np.stack([q * _norm_factor(q)[:, None], k * _norm_factor(k)[:, None]])[:, :, None, :]
+    gb = np.stack([g, beta])[:, :, None]
+    out, fin = oracle.delta_varlen(y, qk, gb, [0, T], S0[None, None], 1, 1, K, V, scale=scale)
+    return out[:, 0], fin[0, 0]
+
+
+@pytest.mark.parametrize("T,K,V,strong", [(150, 16, 16, False), (64, 8, 12, False),
+                                           (200, 16, 8, True), (1, 4, 4, False)])
+def test_chunked_form_equals_the_token_recurrence(T, K, V, strong):
+    q, k, v, g, beta, S0 = _case(T, K, V, seed=T + K, strong=strong)
+    scale = 1.0 / np.sqrt(K)
+    out, S = chunk_forward(S0, q, k, v, g, beta, scale)
+    o_ref, s_ref = _oracle(q, k, v, g, beta, S0, scale)
+    np.testing.assert_allclose(out, o_ref, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, s_ref, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("mistake", ["exclusive_decay", "strict_P", "no_carry_decay"])
+def test_planted_mistakes_break_the_match(mistake):
+    """Non-vacuity: an off-by-one in the cumulative decay, a read-out that
+    misses the token's own update, or a state update without the decay to the
+    chunk end each fail the comparison."""
+    q, k, v, g, beta, S0 = _case(130, 8, 8, seed=3)
+    scale = 0.5
+    o_ref, s_ref = _oracle(q, k, v, g, beta, S0, scale)
+    out, S = chunk_forward(S0, q, k, v, g, beta, scale, mistake=mistake)
+    assert max(np.abs(out - o_ref).max(), np.abs(S - s_ref).max()) > 1e-3
+
+
+@pytest.mark.parametrize("cuts", [(64,), (128, 192), (64, 128, 192, 256)])
+def test_segments_compose_through_the_linear_chunk_map(cuts):
+    """Segment-parallel path: each segment's transition M (identity start,
+    v = 0) and local final state L (zero start) chain to the true start states,
+    S_{j+1} = S_j M_j + L_j; rerunning each segment from its start state gives
+    the outputs and the final state of one pass."""
+    T, K, V = 300, 12, 10
+    q, k, v, g, beta, S0 = _case(T, K, V, seed=11)
+    scale = 0.3
+    o_ref, s_ref = _oracle(q, k, v, g, beta, S0, scale)
+    bounds = [0, *cuts, T]
+    S = S0
+    outs = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        sl = slice(a, b)
+        o, _ = chunk_forward(S, q[sl], k[sl], v[sl], g[sl], beta[sl], scale)   # rerun
+        outs.append(o)
+        _, M = chunk_forward(np.eye(K), q[sl], k[sl], None, g[sl], beta[sl], scale)
+        _, L = chunk_forward(np.zeros((V, K)), q[sl], k[sl], v[sl], g[sl], beta[sl], scale)
+        S = S @ M + L
+    np.testing.assert_allclose(np.concatenate(outs), o_ref, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, s_ref, rtol=1e-9, atol=1e-11)
