@@ -426,12 +426,35 @@ GDN_API int gdn_layer_varlen_capture(const void *qkv, const void *w, const void 
  *                 state_init (in-place carry)
  *   scale         0 means 1/sqrt(n)
  * Errors: GDN_ERR_SHAPE, GDN_ERR_OVERFLOW, GDN_ERR_NULL, GDN_ERR_UNSUPPORTED
- * (dtype), GDN_ERR_CUDA.  Sequences run on the token-serial kernel.
+ * (dtype), GDN_ERR_CUDA.  Sequences run on the token-serial kernel (see
+ * gdn_gated_delta_dense_ws for the chunked route).
  */
 GDN_API int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const float *g,
                                   const float *beta, const float *state_init, void *out,
                                   float *state_fin, int B, int S, int H, int n,
                                   int gate_per_channel, float scale, int dtype, void *stream);
+
+/*
+ * gdn_gated_delta_dense_ws - gdn_gated_delta_dense with a caller workspace, so
+ * that long sequences can take the chunked tensor-core kernel: for bf16, n =
+ * 128, a scalar gate, S >= gdn_chunk_min_len() and 16-byte aligned q, k, v and
+ * out, a packing kernel writes the rows [q | k | v] of every token and ln g
+ * into the workspace and the chunked kernel runs them with the values as
+ * given (exp gate of ln g, raw beta, no q/k normalisation).  Gates below
+ * 1e-30 are taken as 1e-30 on that route (the chunk keeps decays in the log
+ * domain).  Other calls run exactly as gdn_gated_delta_dense and need no
+ * workspace.
+ *   workspace  device, 256-byte aligned, gdn_dense_workspace_bytes() bytes
+ *              (0 from that query: no chunked route for this geometry)
+ * Errors: as gdn_gated_delta_dense, plus GDN_ERR_WORKSPACE when the chunked
+ * route applies and the workspace is missing, misaligned or too small.
+ */
+GDN_API size_t gdn_dense_workspace_bytes(int B, int S, int H, int n, int dtype);
+GDN_API int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const float *state_init, void *out,
+                                     float *state_fin, int B, int S, int H, int n,
+                                     int gate_per_channel, float scale, int dtype,
+                                     void *workspace, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -334,3 +334,11 @@ def test_segment_plan_invariants_on_random_batches():
         for i, n in enumerate(lens):
             if n < chunk_min:
                 assert P[i] == 1
+
+
+def test_dense_workspace_query(lib):
+    assert lib.gdn_dense_workspace_bytes(2, 300, 4, 128, 1) > 0
+    assert lib.gdn_dense_workspace_bytes(2, 300, 4, 64, 1) == 0      # no chunked route for n != 128
+    assert lib.gdn_dense_workspace_bytes(2, 300, 4, 128, 0) == 0     # nor for fp32
+    big = lib.gdn_dense_workspace_bytes(8, 4096, 32, 128, 1)
+    assert big >= 8 * 4096 * 3 * 32 * 128 * 2                       # the packed rows at least

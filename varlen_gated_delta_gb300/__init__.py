@@ -31,7 +31,7 @@ __all__ = [
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
     "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
     "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
-    "gdn_selftest_wait_timeout",
+    "gdn_selftest_wait_timeout", "gdn_dense_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -100,6 +100,10 @@ def load_library():
     lib.gdn_selftest_wait_timeout.argtypes = [vp, i, vp]
     lib.gdn_selftest_wait_timeout.restype = i
     lib.gdn_gated_delta_dense.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp]
+    lib.gdn_gated_delta_dense_ws.argtypes = [vp] * 8 + [i] * 5 + [f, i, vp, ctypes.c_size_t, vp]
+    lib.gdn_gated_delta_dense_ws.restype = i
+    lib.gdn_dense_workspace_bytes.argtypes = [i] * 5
+    lib.gdn_dense_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
@@ -518,13 +522,21 @@ def gdn_layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, 
 
 # ------------------------------------------------------------------ dense layout
 
+def gdn_dense_workspace_bytes(B: int, S: int, H: int, n: int, dtype: int = GDN_BF16) -> int:
+    """Workspace of the dense call's chunked route (0: no chunked route)."""
+    return int(load_library().gdn_dense_workspace_bytes(B, S, H, n, dtype))
+
+
 def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=False, scale=0.0,
-                          out=None, state_fin=None, carry_state=None):
+                          out=None, state_fin=None, carry_state=None, workspace=None):
     """Recurrence on dense q, k, v [B, S, H, n] (g [B,S,H] or [B,S,H,n], beta [B,S,H]).
 
     ``state`` [B, H, n, n] f32 is the initial state (None: zero).  With
     ``carry_state`` (default: a state was given) the final state is written
-    back into ``state`` in place.  Returns (out [B,S,H,n], final state or None)."""
+    back into ``state`` in place.  With ``workspace`` (uint8 device tensor of
+    gdn_dense_workspace_bytes, or True to allocate one) long bf16 sequences
+    take the chunked tensor-core kernel.  Returns (out [B,S,H,n], final state
+    or None)."""
     lib = load_library()
     B, S, H, n = q.shape
     T = q.dtype
@@ -543,8 +555,19 @@ def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=Fals
             _ptr(state, "state", f32, (B, H, n, n), dev),
             _ptr(out, "out", T, (B, S, H, n), dev),
             _ptr(state_fin, "state_fin", f32, (B, H, n, n), dev)]
-    _check(lib.gdn_gated_delta_dense(*args, B, S, H, n, int(bool(gate_per_channel)), float(scale),
-                                     _dtype_code(q), _stream(dev)))
+    if workspace is None:
+        _check(lib.gdn_gated_delta_dense(*args, B, S, H, n, int(bool(gate_per_channel)),
+                                         float(scale), _dtype_code(q), _stream(dev)))
+        return out, state_fin
+    if workspace is True:
+        nb = gdn_dense_workspace_bytes(B, S, H, n, _dtype_code(q))
+        workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise GdnError(2, "workspace must be a contiguous uint8 tensor on the inputs' device")
+    _check(lib.gdn_gated_delta_dense_ws(*args, B, S, H, n, int(bool(gate_per_channel)),
+                                        float(scale), _dtype_code(q),
+                                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                        _stream(dev)))
     return out, state_fin
 
 

@@ -698,11 +698,9 @@ int gdn_layer_varlen_capture(const void *qkv, const void *w, const void *bias, c
                       dtype, workspace, ws_bytes, stream, &c);
 }
 
-int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const float *g,
-                          const float *beta, const float *state_init, void *out,
-                          float *state_fin, int B, int S, int H, int n, int gate_per_channel,
-                          float scale, int dtype, void *stream) {
-    g_err[0] = 0;
+static int dense_check(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, void *out, int B, int S, int H, int n,
+                       int gate_per_channel, float scale, int dtype) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     if (B < 1 || S < 0 || H < 1 || n < 1)
         return fail(GDN_ERR_SHAPE, "dense: need B>=1, S>=0, H>=1, n>=1 (B=%d S=%d H=%d n=%d)", B, S, H, n);
@@ -714,12 +712,111 @@ int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const flo
     if (S > 0 && (!q || !k || !v || !g || !beta || !out))
         return fail(GDN_ERR_NULL, "dense: a required pointer is NULL");
     if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
+    return GDN_OK;
+}
+
+static int dense_serial(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *state_init, void *out, float *state_fin,
+                        int B, int S, int H, int n, int gate_per_channel, float scale, int dtype,
+                        void *stream) {
     DenseParams p{};
     p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_init = state_init; p.out = out;
     p.state_fin = state_fin; p.B = B; p.S = S; p.H = H; p.n = n; p.per_channel = gate_per_channel;
     p.scale = scale == 0.f ? 1.f / std::sqrt((float)n) : scale;
     cudaError_t e = launch_delta_dense(p, dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dense kernel launch");
+    return GDN_OK;
+}
+
+int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *state_init, void *out,
+                          float *state_fin, int B, int S, int H, int n, int gate_per_channel,
+                          float scale, int dtype, void *stream) {
+    g_err[0] = 0;
+    int rc = dense_check(q, k, v, g, beta, out, B, S, H, n, gate_per_channel, scale, dtype);
+    if (rc) return rc;
+    return dense_serial(q, k, v, g, beta, state_init, out, state_fin, B, S, H, n,
+                        gate_per_channel, scale, dtype, stream);
+}
+
+// Workspace of the dense call's chunked route: header, order, offsets, packed
+// rows y [B S, 3 H n] bf16, log gates [B S, H], a zero initial state and a
+// final-state scratch [B, H, n, n] (for NULL state_init / state_fin).
+struct DenseWs {
+    size_t header, order, offsets, y, a, zero, fin, total;
+};
+static DenseWs dense_ws_layout(int B, int S, int H, int n) {
+    DenseWs l;
+    const size_t N = (size_t)B * S, st = (size_t)B * H * n * n * 4;
+    size_t off = 0;
+    l.header = off; off += align256(sizeof(WsHeader));
+    l.order = off; off += align256((size_t)B * 4);
+    l.offsets = off; off += align256((size_t)(B + 1) * 4);
+    l.y = off; off += align256(N * 3 * H * n * 2);
+    l.a = off; off += align256(N * H * 4);
+    l.zero = off; off += align256(st);
+    l.fin = off; off += align256(st);
+    l.total = off;
+    return l;
+}
+
+size_t gdn_dense_workspace_bytes(int B, int S, int H, int n, int dtype) {
+    if (dtype != GDN_BF16 || n != 128 || B < 1 || S < 1 || H < 1) return 0;
+    if ((long)B * S * H * n * 3 > INT_MAX) return 0;
+    return dense_ws_layout(B, S, H, n).total;
+}
+
+int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *state_init, void *out,
+                             float *state_fin, int B, int S, int H, int n, int gate_per_channel,
+                             float scale, int dtype, void *workspace, size_t ws_bytes,
+                             void *stream) {
+    g_err[0] = 0;
+    int rc = dense_check(q, k, v, g, beta, out, B, S, H, n, gate_per_channel, scale, dtype);
+    if (rc) return rc;
+    const bool aligned = ((uintptr_t)q & 15) == 0 && ((uintptr_t)k & 15) == 0 &&
+                         ((uintptr_t)v & 15) == 0 && ((uintptr_t)out & 15) == 0;
+    const size_t need = gdn_dense_workspace_bytes(B, S, H, n, dtype);
+    const bool chunked = need > 0 && !gate_per_channel && S >= chunk_min_len() && aligned &&
+                         chunked_supported(dtype, n, n, 3 * H * n);
+    if (!chunked)
+        return dense_serial(q, k, v, g, beta, state_init, out, state_fin, B, S, H, n,
+                            gate_per_channel, scale, dtype, stream);
+    if (!workspace || ((uintptr_t)workspace & 255) != 0)
+        return fail(GDN_ERR_WORKSPACE, "dense: workspace must be a non-NULL 256-byte aligned device pointer");
+    if (ws_bytes < need) return fail(GDN_ERR_WORKSPACE, "dense: workspace has %zu bytes, needs %zu", ws_bytes, need);
+    const DenseWs lay = dense_ws_layout(B, S, H, n);
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const float *s0 = state_init;
+    if (!s0) {
+        cudaError_t e = cudaMemsetAsync(ws + lay.zero, 0, (size_t)B * H * n * n * 4, st);
+        if (e != cudaSuccess) return cuda_fail(e, "dense: zero initial state");
+        s0 = reinterpret_cast<const float *>(ws + lay.zero);
+    }
+    float *sf = state_fin ? state_fin : reinterpret_cast<float *>(ws + lay.fin);
+    DensePack pk{};
+    pk.q = q; pk.k = k; pk.v = v; pk.g = g;
+    pk.y = ws + lay.y; pk.a = reinterpret_cast<float *>(ws + lay.a);
+    pk.offsets = reinterpret_cast<int32_t *>(ws + lay.offsets);
+    pk.order = reinterpret_cast<int32_t *>(ws + lay.order);
+    pk.header = reinterpret_cast<WsHeader *>(ws + lay.header);
+    pk.B = B; pk.S = S; pk.H = H; pk.n = n;
+    cudaError_t e = launch_dense_pack(pk, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dense pack kernel launch");
+    ChunkLaunch cl{};
+    cl.y = pk.y; cl.a = pk.a; cl.bl = beta; cl.A_log = nullptr; cl.dt_bias = nullptr;
+    cl.offsets = pk.offsets; cl.seq_order = pk.order; cl.header = pk.header;
+    cl.state_init = s0; cl.state_fin = sf; cl.out = out;
+    cl.B = B; cl.N = B * S; cl.H = H; cl.HQ = H; cl.V = n; cl.W = 3 * H * n;
+    cl.scale = scale == 0.f ? 1.f / std::sqrt((float)n) : scale;
+    cl.max_units = (long)B * H * (n / 128);
+    // the dense call's values as given: exp gate of ln g, raw rate, no q/k norm
+    cl.opts = GDN_OPT_GATE_EXP | GDN_OPT_BETA_RAW | GDN_OPT_NO_QK_NORM;
+    mark_before(GDN_KERNEL_CHUNKED, st);
+    e = launch_delta_chunked(cl, st);
+    mark_after(GDN_KERNEL_CHUNKED, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dense: chunked kernel launch");
     return GDN_OK;
 }
 

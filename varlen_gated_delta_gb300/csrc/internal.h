@@ -160,6 +160,21 @@ struct DenseParams {
 };
 cudaError_t launch_delta_dense(const DenseParams &p, int dtype, cudaStream_t s);
 
+// Dense layout -> the chunked kernel's packed inputs (bf16, scalar gate): the
+// rows [q | k | v] of every token into y [B S, 3 H n], a = ln(max(g, 1e-30))
+// [B S, H] (the kernel's exp gate), offsets i S, the sequence order and the
+// workspace header for B H (n / 128) units.
+struct DensePack {
+    const void *q, *k, *v;
+    const float *g;
+    void *y;
+    float *a;
+    int32_t *offsets, *order;
+    WsHeader *header;
+    int B, S, H, n;
+};
+cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
+
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
 cudaError_t launch_delta_chunked_segmented(const ChunkLaunch &c, cudaStream_t s);
