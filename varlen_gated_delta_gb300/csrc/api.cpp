@@ -90,15 +90,13 @@ static int segment_min_len() {
     return v > 0 ? v : 16384;
 }
 
+// SM count of the current device (asked per call: a process may drive
+// several devices).
 static int sm_count_host() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n = v > 0 ? v : 1;
-    }
-    return n;
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v > 0 ? v : 1;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

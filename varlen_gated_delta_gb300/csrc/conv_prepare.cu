@@ -634,14 +634,13 @@ cudaError_t launch_conv_stream(const ConvParams &p, cudaStream_t s) {
     const long blocks = ttiles * n_ctiles;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     const size_t smem = kRingBytes + (p.B + 1 <= kOffsetsCache ? sizeof(int) * (p.B + 1) : 0);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(conv_stream_kernel<T, VEC, PREP, KC, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(kRingBytes + sizeof(int) * kOffsetsCache));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(conv_stream_kernel<T, VEC, PREP, KC, D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(kRingBytes + sizeof(int) * kOffsetsCache));
+    });
+    if (e != cudaSuccess) return e;
     conv_stream_kernel<T, VEC, PREP, KC, D><<<(unsigned)blocks, kConvThreads, smem, s>>>(p, (int)R, n_ctiles);
     note_launch();
     return cudaGetLastError();

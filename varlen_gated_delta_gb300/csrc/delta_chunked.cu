@@ -930,14 +930,11 @@ cudaError_t chunk_setup(const ChunkLaunch &c, CUtensorMap &map, CUtensorMap &oma
     p.tma_store = tma_store;
     p.opts = c.opts;
     p.counter = &c.header->next_unit;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunked_delta_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    return cudaSuccess;
+    static std::atomic<uint64_t> attr_set{0};
+    return once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(chunked_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    });
 }
 
 cudaError_t chunk_launch(const CUtensorMap &map, const CUtensorMap &omap, const ChunkParams &p,

@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "gdn.h"  // GDN_OPT_* rule / activation options
@@ -23,6 +24,21 @@ struct WsHeader {
     int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+// Runs set() once per device (ids below 64; others every time) and records
+// success in `done`: for per-device function attributes such as a kernel's
+// dynamic shared memory limit.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<uint64_t> &done, F set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 struct ConvParams {
     const void *x, *w, *bias;
