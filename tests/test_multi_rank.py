@@ -88,3 +88,12 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the JSON line carries every key of the benchmark contract
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["metric"] == "gated-delta layer tokens/s" and line["unit"] == "tokens/s"
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["config"]["workload"] == "tiny" and line["steps"] == 2
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["cores"] >= 1
