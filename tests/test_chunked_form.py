@@ -132,3 +132,45 @@ def test_segments_compose_through_the_linear_chunk_map(cuts):
         S = S @ M + L
     np.testing.assert_allclose(np.concatenate(outs), o_ref, rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(S, s_ref, rtol=1e-9, atol=1e-11)
+
+
+# ------------------------------------------------------------------ per-key-channel decay
+
+def chunk_forward_diag(S0, q, k, v, g, beta, scale, C=16):
+    """The chunked form with a per-key-channel gate g [T, K] (the dense call's
+    gate_per_channel), values as given (no normalisation): with Gam_t = prod_{s<=t} g_s
+    per channel inside a chunk, kt_t = k_t * Gam_t, kh_i = k_i / Gam_i, qt_t = q_t * Gam_t,
+      (I + A) Delta = diag(beta) V - diag(beta) Kt S_0^T,  A[t, i] = beta_t kt_t.kh_i (i < t),
+      o = scale (Qt S_0^T + tril(Qt Kh^T) Delta),
+      S_C = S_0 diag(Gam_C) + Delta^T (Kh * Gam_C).
+    kh grows like 1 / Gam, so the chunk is short (the form a per-channel kernel
+    would take, with this sub-chunk inside its 64-token chunk)."""
+    T, K = k.shape
+    S = S0.copy()
+    out = np.zeros((T, S0.shape[0]))
+    for t0 in range(0, T, C):
+        sl = slice(t0, min(T, t0 + C))
+        qc, kc, vc, gc, bc = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        Gam = np.cumprod(gc, axis=0)
+        kt, kh, qt = kc * Gam, kc / Gam, qc * Gam
+        n = kc.shape[0]
+        A = np.tril(bc[:, None] * (kt @ kh.T), -1)
+        Delta = np.linalg.solve(np.eye(n) + A, bc[:, None] * vc - bc[:, None] * (kt @ S.T))
+        out[sl] = scale * (qt @ S.T + np.tril(qt @ kh.T) @ Delta)
+        S = S * Gam[-1][None, :] + Delta.T @ (kh * Gam[-1][None, :])
+    return out, S
+
+
+@pytest.mark.parametrize("T,n", [(50, 8), (33, 16)])
+def test_per_channel_chunked_form_equals_the_dense_recurrence(T, n):
+    rng = np.random.default_rng(T * n)
+    q, k, v = rng.normal(size=(T, n)), rng.normal(size=(T, n)) / np.sqrt(n), rng.normal(size=(T, n))
+    g = rng.uniform(0.6, 1.0, size=(T, n))
+    beta = rng.uniform(0.0, 1.0, T)
+    S0 = rng.normal(scale=0.2, size=(n, n))
+    out, S = chunk_forward_diag(S0, q, k, v, g, beta, 0.7)
+    o_ref, s_ref = oracle.dense_delta(q[None, :, None], k[None, :, None], v[None, :, None],
+                                      g[None, :, None], beta[None, :, None], S0[None, None],
+                                      per_channel=True, scale=0.7)
+    np.testing.assert_allclose(out, o_ref[0, :, 0], rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, s_ref[0, 0], rtol=1e-9, atol=1e-11)
