@@ -16,6 +16,7 @@ from varlen_gated_delta_gb300 import build as gdn_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
+HEADER_DIR = os.path.dirname(HEADER)
 
 
 @pytest.fixture(scope="module")
@@ -342,3 +343,38 @@ def test_dense_workspace_query(lib):
     assert lib.gdn_dense_workspace_bytes(2, 300, 4, 128, 0) == 0     # nor for fp32
     big = lib.gdn_dense_workspace_bytes(8, 4096, 32, 128, 1)
     assert big >= 8 * 4096 * 3 * 32 * 128 * 2                       # the packed rows at least
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path, lib):
+    """A C11 program includes gdn.h, links libgdn.so and calls the host-only
+    entry points (no GPU needed): the boundary is usable without C++ or torch."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "probe.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "gdn.h"
+int main(void) {
+    int32_t offs[3] = {0, 100000, 130000};
+    int32_t counts[2] = {0, 0};
+    size_t ws = gdn_workspace_bytes(2, 130000, 32, 16, 128, 256, 4, 2, GDN_BF16);
+    int n = gdn_segment_plan(offs, 2, 32, 256, 152, counts);
+    int bad = gdn_set_chunk_min_len(-1);
+    printf("%d %zu %d %d %d %d\n", gdn_version() > 0, ws, n, counts[0], counts[1], bad);
+    return 0;
+}
+""")
+    exe = tmp_path / "probe"
+    libdir = os.path.dirname(gdn.library_path())
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-I", HEADER_DIR, str(src), "-o", str(exe),
+                        "-L", libdir, "-lgdn", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    ok, ws, n, c0, c1, bad = r.stdout.split()
+    assert ok == "1" and int(ws) > 0 and int(bad) != 0
+    # 100000 and 30000 tokens (both long): the longer one gets the extra segments
+    assert int(n) == 2 and (int(c0), int(c1)) == (3, 1)
