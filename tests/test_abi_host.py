@@ -378,3 +378,23 @@ int main(void) {
     assert ok == "1" and int(ws) > 0 and int(bad) != 0
     # 100000 and 30000 tokens (both long): the longer one gets the extra segments
     assert int(n) == 2 and (int(c0), int(c1)) == (3, 1)
+
+
+def test_workspace_includes_segment_buffers_from_the_segment_length():
+    """The layer workspace holds segment buffers (transitions, local states and
+    start states for min(4, N / min_len) sequences) once N reaches
+    gdn_segment_min_len(); below it, none."""
+    H, V = 8, 128
+    per_seq = (7 * H * 128 * 128 + 7 * H * V * 128 + 8 * H * V * 128) * 4
+    gdn.gdn_set_segment_min_len(1000)
+    try:
+        below = gdn.gdn_workspace_bytes(1, 999, H, 4, 128, V, 4, 1, gdn.GDN_BF16)
+        one = gdn.gdn_workspace_bytes(1, 1000, H, 4, 128, V, 4, 1, gdn.GDN_BF16)
+        four = gdn.gdn_workspace_bytes(1, 9000, H, 4, 128, V, 4, 1, gdn.GDN_BF16)
+        plain9000 = None
+        gdn.gdn_set_segment_min_len(1 << 30)
+        plain9000 = gdn.gdn_workspace_bytes(1, 9000, H, 4, 128, V, 4, 1, gdn.GDN_BF16)
+    finally:
+        gdn.gdn_set_segment_min_len(0)
+    assert 0 <= one - below - per_seq < 16384                # one sequence's buffers (+ one token's rows)
+    assert four - plain9000 == pytest.approx(4 * per_seq, abs=512)   # capped at four sequences
