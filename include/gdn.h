@@ -68,7 +68,7 @@ typedef enum gdn_status {
     GDN_ERR_SHAPE = 2,       /* inconsistent or out-of-range geometry */
     GDN_ERR_OVERFLOW = 3,    /* a size or launch grid exceeds its integer range */
     GDN_ERR_OFFSETS = 4,     /* offsets[0] != 0, offsets[B] != N or decreasing */
-    GDN_ERR_UNSUPPORTED = 5, /* valid request this build does not implement */
+    GDN_ERR_UNSUPPORTED = 5, /* valid request the library does not implement */
     GDN_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has detail) */
     GDN_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
     GDN_ERR_WORKSPACE = 8    /* workspace missing, misaligned or too small */
