@@ -3,7 +3,11 @@
 One step = one gdn_layer_varlen call (conv -> prepare -> recurrence) over one
 batch of the workload, inputs resident in HBM.  Default workload: the decode
 step (64 sequences x 1 token, HQ=16, H=32, K=V=128, bf16, fp32 state
-[64,32,128,128] carried in place).  Prints ONE JSON line (rank 0).
+[64,32,128,128] carried in place).  Prints ONE JSON line (rank 0).  With the
+default workload the line also carries, under "workloads", the same
+measurement of the prefill (8 x 4096), ragged (32 x U[1, 8192]) and long
+(1 x 131072, V=256, D=2) workloads, whose dominant kernel is the chunked
+tensor-core kernel (roofline against the bf16 tensor peak).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the fp64 CPU oracle, timed on host cores)
@@ -38,6 +42,9 @@ def _args():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "ragged", "long", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="the default (decode) line without the prefill, ragged and long "
+                         "records")
     ap.add_argument("--rule", default="gated_delta",
                     choices=["gated_delta", "delta", "gated", "linear"],
                     help="update rule (delta: no decay; gated: no retrieval; linear: neither)")
@@ -282,6 +289,8 @@ def _oracle_sample(wl):
 
 
 def cpu_baseline(wl, budget_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload
+    (``_oracle_sample``), repeated for about ``budget_s`` seconds."""
     import numpy as np
 
     import oracle
@@ -306,24 +315,19 @@ def cpu_baseline(wl, budget_s=12.0):
             "kind": "oracle", "sample": f"{sample}; {reps} repetitions in {dt:.1f} s"}
 
 
-def run_ours(args, wl):
+def _measure(args, wl, dev, world, rank, local, gdn, W):
+    """One workload through gdn_layer_varlen: device-resident steps (CUDA graph
+    replays), the dominant kernel alone (library events inside the same
+    replays) and the end-to-end run with host buffers.  Returns the record of
+    rank 0 (None elsewhere).
+
+    The layer carries its states in place, as a decode loop does.  Two
+    independent state sets alternate from step to step, so the state a step
+    reads was last touched two steps earlier, with at least one full state
+    (268 MB on the decode batch, more than the 129 MB L2) streamed in between:
+    no step finds the state it reads still in L2."""
     import torch
     import torch.distributed as dist
-
-    import varlen_gated_delta_gb300 as gdn
-    from varlen_gated_delta_gb300 import build as gdn_build
-    from varlen_gated_delta_gb300 import workloads as W
-
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    if rank == 0:
-        gdn_build.build()
-    if world > 1:
-        dist.barrier()
-    gdn.load_library()
 
     d = W.make_inputs(wl, dev, seed=_replica_seed(wl, rank))
     offs = d["offsets_list"]
@@ -333,7 +337,8 @@ def run_ours(args, wl):
                                              gdn.GDN_BF16 if wl.dtype == "bf16" else gdn.GDN_F32),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((N, wl.H, wl.V), dtype=wl.torch_dtype, device=dev)
-    conv_state, state = d["conv_init"], d["state_init"]
+    conv_states = [d["conv_init"], d["conv_init"].clone()]
+    states = [d["state_init"], d["state_init"].clone()]
     cap = args.capture
     if cap:
         counts = torch.full((B,), cap, dtype=torch.int32, device=dev)
@@ -343,9 +348,10 @@ def run_ours(args, wl):
 
     opts = gdn.RULE_OPTS[args.rule]
 
-    def call(qkv, a, b, offsets, out_t=None, capsule_t=None):
+    def call(qkv, a, b, offsets, sset, out_t=None, capsule_t=None):
         # decode-style carry: the final states overwrite the initial ones in place
         out_t = out if out_t is None else out_t
+        conv_state, state = conv_states[sset], states[sset]
         kw = dict(H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, act=act,
                   scale=d["scale"], offsets_host=offs, out=out_t, conv_fin=conv_state,
                   state_fin=state, workspace=ws)
@@ -365,38 +371,43 @@ def run_ours(args, wl):
             gdn.gdn_layer_varlen(qkv, d["w"], d["bias"], a, b, d["A_log"], d["dt_bias"],
                                  offsets, conv_state, state, **kw)
 
-    def step():
-        call(d["qkv"], d["a"], d["b"], d["offsets"])
+    def step(sset):
+        call(d["qkv"], d["a"], d["b"], d["offsets"], sset)
 
     stream = torch.cuda.current_stream(dev)
-    for _ in range(max(3, args.warmup)):
-        step()
+    warm = max(3, args.warmup)
+    for i in range(warm):
+        step(i & 1)
     torch.cuda.synchronize()
     gdn.gdn_workspace_status(ws)
 
     # eager steps (one library call per step from Python)
     eager0, eager1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     eager0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i & 1)
     eager1.record(stream)
     torch.cuda.synchronize()
     eager_ms = eager0.elapsed_time(eager1)
 
-    # the same step captured once in a CUDA graph (launch-bound decode), replayed
+    # each state set's step captured once in a CUDA graph (launch-bound
+    # decode), replayed alternately
     launches_per_step0 = gdn.gdn_launch_count()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        step()
+        step(0)
     stream.wait_stream(side)
     torch.cuda.synchronize()
     launches_per_step = gdn.gdn_launch_count() - launches_per_step0
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
+    graphs = []
+    for sset in (0, 1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(sset)
+        graphs.append(g)
+    for i in range(warm):
+        graphs[i & 1].replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -407,8 +418,8 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
+    for i in range(args.steps):
+        graphs[i & 1].replay()
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -417,7 +428,8 @@ def run_ours(args, wl):
     ms = e0.elapsed_time(e1)
 
     # dominant kernel, timed inside the same layer calls with CUDA events the
-    # library records on its stream right around that kernel's launch
+    # library records on its stream right around that kernel's launch; the
+    # other state set's step runs between two timed steps, as in the timed run
     dom = (gdn.GDN_KERNEL_SERIAL if max(wl.lengths()) < gdn.gdn_chunk_min_len()
            else gdn.GDN_KERNEL_CHUNKED)
     k_start = torch.cuda.Event(enable_timing=True)
@@ -431,12 +443,13 @@ def run_ours(args, wl):
         # captured in a graph like the timed steps, so no CPU gap sits inside
         kgraph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(kgraph):
-            step()
+            step(0)
     finally:
         gdn.gdn_set_kernel_events(dom, None, None)
-    for i in range(max(3, args.warmup) + args.steps):
+    for i in range(warm + args.steps):
+        graphs[1].replay()
         kgraph.replay()
-        if i >= max(3, args.warmup):
+        if i >= warm:
             torch.cuda.synchronize()
             kern_ms.append(k_start.elapsed_time(k_stop))
     clocks = sampler.stop()
@@ -475,7 +488,7 @@ def run_ours(args, wl):
         comp.wait_event(in_ready[j])
         if i >= 2:  # step i - 2's output has left
             comp.wait_event(out_free[j])
-        call(dev_in[j]["qkv"], dev_in[j]["a"], dev_in[j]["b"], dev_offs[j], out_t=outs[j],
+        call(dev_in[j]["qkv"], dev_in[j]["a"], dev_in[j]["b"], dev_offs[j], j, out_t=outs[j],
              capsule_t=caps[j] if cap else None)
         in_free[j].record(comp)
         out_ready[j].record(comp)
@@ -522,52 +535,102 @@ def run_ours(args, wl):
     torch.testing.assert_close(out_host[last].to(dev), outs[last], rtol=0, atol=0)
 
     ms, e2e_ms = _max_over_ranks([ms, e2e_ms], dev)
+    if rank != 0:
+        return None
+    hbm, tf, tf_s, peak_src = _peaks()
+    kavg = statistics.mean(kern_ms)
+    value = _job_tokens_per_s(world, N, args.steps, ms)
+    if dom == gdn.GDN_KERNEL_SERIAL:
+        kbytes = algorithmic_bytes_delta(wl, N, B, cap)
+        achieved = kbytes / (kavg * 1e-3) / 1e9
+        roof = {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None if cap else _profile_traffic("delta_serial", wl.name),
+                "algorithmic_bytes": kbytes, "kernel_ms": kavg,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    else:
+        kflops = chunked_flops(wl, N)
+        achieved = kflops / (kavg * 1e-3) / 1e12
+        roof = {"kernel": "chunked_delta_kernel", "bound": "tensor", "achieved": achieved,
+                "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf,
+                "traffic": _profile_traffic("chunked_delta", wl.name),
+                "algorithmic_flops": kflops, "kernel_ms": kavg,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+    rec = {
+        "metric": "gated-delta layer tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": warm,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "B": B, "N": N, "HQ": wl.HQ, "H": wl.H, "K": wl.K,
+                   "V": wl.V, "Kc": wl.Kc, "D": wl.D,
+                   "state_carry": "in place, two state sets alternating",
+                   "l2": "inputs larger than L2 (129 MB); the state a step reads was last "
+                         "touched two steps before",
+                   "parallelism": f"replicas x{world}",
+                   **({"capture": cap} if cap else {}),
+                   **({"rule": args.rule} if opts else {})},
+        "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
+        "roofline": roof,
+        "e2e": {"value": _job_tokens_per_s(world, N, args.steps, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipeline": "copies on two streams, double-buffered, overlapping the "
+                            "neighbouring steps' compute" +
+                            (" (the whole run replayed as one CUDA graph)" if small else "")},
+        "gpu_launches": launches,
+        "timing": "CUDA graph replay of one gdn_layer_varlen%s call per step"
+                  % ("_ex" if opts else "_capture" if cap else ""),
+        "ms_per_step_eager": eager_ms / args.steps,
+        "clocks": clocks,
+    }
+    return rec
+
+
+# Workloads measured beside the default (decode) one in the same JSON line,
+# so that one run reports both halves of the metric: decode (HBM-bound) and
+# prefill (tensor-core bound).
+EXTRA_WORKLOADS = ("prefill", "ragged", "long")
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import varlen_gated_delta_gb300 as gdn
+    from varlen_gated_delta_gb300 import build as gdn_build
+    from varlen_gated_delta_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
     if rank == 0:
-        hbm, tf, tf_s, peak_src = _peaks()
-        kavg = statistics.mean(kern_ms)
-        value = _job_tokens_per_s(world, N, args.steps, ms)
-        if dom == gdn.GDN_KERNEL_SERIAL:
-            kbytes = algorithmic_bytes_delta(wl, N, B, cap)
-            achieved = kbytes / (kavg * 1e-3) / 1e9
-            roof = {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
-                    "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": None if cap else _profile_traffic("delta_serial", wl.name),
-                    "algorithmic_bytes": kbytes, "kernel_ms": kavg,
-                    "peak_source": f"hbm_gbs of {peak_src}"}
-        else:
-            kflops = chunked_flops(wl, N)
-            achieved = kflops / (kavg * 1e-3) / 1e12
-            roof = {"kernel": "chunked_delta_kernel", "bound": "tensor", "achieved": achieved,
-                    "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf,
-                    "traffic": _profile_traffic("chunked_delta", wl.name),
-                    "algorithmic_flops": kflops, "kernel_ms": kavg,
-                    "peak_source": f"bf16_tflops (burst) of {peak_src}"}
-        line = {
-            "metric": "gated-delta layer tokens/s", "value": value, "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
-            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "B": B, "N": N, "HQ": wl.HQ, "H": wl.H, "K": wl.K,
-                       "V": wl.V, "Kc": wl.Kc, "D": wl.D, "state_carry": "in place",
-                       "l2": "inputs larger than L2 (129 MB)",
-                       "parallelism": f"replicas x{world}",
-                       **({"capture": cap} if cap else {}),
-                       **({"rule": args.rule} if opts else {})},
-            "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
-            "roofline": roof,
-            "e2e": {"value": _job_tokens_per_s(world, N, args.steps, e2e_ms), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "pipeline": "copies on two streams, double-buffered, overlapping the "
-                                "neighbouring steps' compute" +
-                                (" (the whole run replayed as one CUDA graph)" if small else "")},
-            "gpu_launches": launches,
-            "timing": "CUDA graph replay of one gdn_layer_varlen%s call per step"
-                      % ("_ex" if opts else "_capture" if cap else ""),
-            "ms_per_step_eager": eager_ms / args.steps,
-            "clocks": clocks,
-        }
+        gdn_build.build()
+    if world > 1:
+        dist.barrier()
+    gdn.load_library()
+
+    line = _measure(args, wl, dev, world, rank, local, gdn, W)
+    extras = {}
+    plain = not (args.lens or args.capture or args.rule != "gated_delta")
+    if plain and wl.name == "decode" and not args.no_extra:
+        for name in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            rec = _measure(args, W.WORKLOADS[name], dev, world, rank, local, gdn, W)
+            if rank == 0:
+                if not args.no_cpu_baseline:
+                    rec["cpu_baseline"] = cpu_baseline(W.WORKLOADS[name], budget_s=8.0)
+                for k in ("n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                          "vs_baseline", "data", "metric", "unit"):
+                    rec.pop(k, None)
+                extras[name] = rec
+    if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
+        if extras:
+            line["workloads"] = extras
+            line["gpu_launches_all_workloads"] = line["gpu_launches"] + sum(
+                r["gpu_launches"] for r in extras.values())
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -288,9 +288,15 @@ GDN_API int gdn_selftest_wait_timeout(int32_t *status, int limit_us, void *strea
  *   part that must start cleared is cleared on `stream` before use.  Calls
  *   that overlap on the GPU (for example on two streams) race on the array:
  *   serialise them.
- * - gdn_workspace_status() can read the status of the last call only through
- *   the regular entry point's workspace; here errors in host-provided
- *   offsets are reported synchronously when offsets_host is given.
+ * - Errors in the offsets are reported only when offsets_host is given
+ *   (synchronously, before any launch).  Without it the device-side check
+ *   still skips malformed sequences, but its status word sits in the static
+ *   array, which gdn_workspace_status() cannot read: pass offsets_host when
+ *   the offsets may be malformed.
+ * - The device address is cached per device ordinal for the life of the
+ *   process.  After cudaDeviceReset() on a device (or with a context other
+ *   than the device's primary context current) that cached address is no
+ *   longer valid: do not call this entry point on that device afterwards.
  */
 GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void *bias,
                                      const float *a, const float *b, const float *A_log,

@@ -1,12 +1,10 @@
-"""Shared helpers for the GPU parity tests: error metrics and the reduction of a
-layer problem to one (sequence, value head, state row).
+"""Shared helpers for the parity tests: error metrics, the full oracle layer,
+and a full-size comparison that solves the oracle in time slices.
 
-State rows of the recurrence are independent given the key/query of their
-key head, and the conv is depthwise, so the outputs o[t, h, vi] of sequence b
-and the final state row S[b, h, vi, :] only depend on the columns
-(q head kh, k head kh, v channel (h, vi)) of that sequence.  ``reduced_row``
-extracts exactly those inputs as a 1-key-head / 1-value-head / V=1 problem
-that the oracle solves in seconds even for a 131072-token sequence.
+A sequence can be cut anywhere and resumed from the fp64 delta state and the
+conv state (its last L raw inputs) that the oracle returns, with the same fp64
+operations as one call, so ``full_layer_parity`` keeps only one slice of fp64
+inputs and outputs on the host however long the sequences are.
 """
 from __future__ import annotations
 
@@ -46,29 +44,59 @@ def oracle_layer(wl, d, act_dtype=None):
                                act_dtype=act)
 
 
-def reduced_row(wl, d, b, h, vi):
-    """Oracle outputs o[s:e, h, vi] and S_fin[b, h, vi, :] from the reduced problem."""
+class _ErrAcc:
+    """Running relative-L2 and max-abs error over pieces of one tensor."""
+
+    def __init__(self):
+        self.num = 0.0
+        self.den = 0.0
+        self.max = 0.0
+        self.n = 0
+
+    def add(self, x, ref):
+        x = np.asarray(x, dtype=np.float64).ravel()
+        ref = np.asarray(ref, dtype=np.float64).ravel()
+        self.num += float(np.dot(x - ref, x - ref))
+        self.den += float(np.dot(ref, ref))
+        if x.size:
+            self.max = max(self.max, float(np.max(np.abs(x - ref))))
+        self.n += x.size
+
+    @property
+    def rel(self) -> float:
+        return float(np.sqrt(self.num / self.den)) if self.den > 0 else float(np.sqrt(self.num))
+
+
+def full_layer_parity(wl, d, out, cfin, sfin, slice_tokens=4096):
+    """Every element of a layer call's outputs against the oracle.
+
+    The oracle solves the batch one sequence at a time, and each sequence in
+    time slices of ``slice_tokens`` tokens: a slice starts from the fp64 delta
+    state and the conv state (raw inputs) the previous slice returned, which is
+    the single-call recurrence exactly (the state is carried unrounded), so the
+    host holds one slice of fp64 inputs and outputs at a time.  Returns the
+    error accumulators of ``out`` and ``state_fin`` and the number of conv
+    final-state elements that differ (must be 0: the final conv state is a
+    bit copy of raw inputs)."""
     offs = d["offsets_list"]
-    s, e = offs[b], offs[b + 1]
-    G = wl.H // wl.HQ
-    kh = h // G
-    K, V, HQ = wl.K, wl.V, wl.HQ
-    cols = (list(range(kh * K, (kh + 1) * K))
-            + list(range(HQ * K + kh * K, HQ * K + (kh + 1) * K))
-            + [2 * HQ * K + h * V + vi])
-    idx = torch.tensor(cols, device=d["qkv"].device)
-    qkv = cpu64(d["qkv"][s:e].index_select(1, idx))
-    w = cpu64(d["w"].index_select(0, idx))
-    bias = None if d["bias"] is None else cpu64(d["bias"].index_select(0, idx))
-    conv_init = cpu64(d["conv_init"][b:b + 1].index_select(1, idx))
-    a = cpu64(d["a"][s:e, h:h + 1])
-    bl = cpu64(d["b"][s:e, h:h + 1])
-    A_log = cpu64(d["A_log"][h:h + 1])
-    dt = cpu64(d["dt_bias"][h:h + 1])
-    S0 = cpu64(d["state_init"][b:b + 1, h:h + 1, vi:vi + 1, :])
     act = "bf16" if wl.dtype == "bf16" else "f32"
-    out, _, fin = oracle.layer_varlen(qkv, w, bias, a, bl, A_log, dt,
-                                      np.array([0, e - s], np.int32), conv_init, S0,
-                                      1, 1, K, 1, wl.Kc, wl.D, silu=wl.silu, scale=d["scale"],
-                                      act_dtype=act)
-    return out[:, 0, 0], fin[0, 0, 0]
+    w = cpu64(d["w"])
+    bias = None if d["bias"] is None else cpu64(d["bias"])
+    A_log, dt_bias = cpu64(d["A_log"]), cpu64(d["dt_bias"])
+    eo, es = _ErrAcc(), _ErrAcc()
+    conv_mismatch = 0
+    for b in range(len(offs) - 1):
+        s, e = offs[b], offs[b + 1]
+        conv_state = cpu64(d["conv_init"][b:b + 1])
+        S = cpu64(d["state_init"][b:b + 1])
+        for t0 in range(s, e, slice_tokens):
+            t1 = min(e, t0 + slice_tokens)
+            o_ref, conv_state, S = oracle.layer_varlen(
+                cpu64(d["qkv"][t0:t1]), w, bias, cpu64(d["a"][t0:t1]), cpu64(d["b"][t0:t1]),
+                A_log, dt_bias, np.array([0, t1 - t0], np.int32), conv_state, S,
+                wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D, silu=wl.silu, scale=d["scale"],
+                act_dtype=act)
+            eo.add(cpu64(out[t0:t1]), o_ref)
+        es.add(cpu64(sfin[b:b + 1]), S)
+        conv_mismatch += int(np.count_nonzero(cpu64(cfin[b:b + 1]) != conv_state))
+    return eo, es, conv_mismatch

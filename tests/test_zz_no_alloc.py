@@ -5,9 +5,10 @@ runtime without a device allocator, a plugin whose host framework owns all
 device memory, a latency-critical loop that cannot take cudaMalloc's implicit
 synchronisation).  It uses a fixed 16 MiB device array inside the library
 instead of a caller workspace.  These tests call it through the C ABI
-directly and compare it with gdn_layer_varlen (which takes a workspace) on
-the decode workload, twice in a row, since every call shares the static
-array and must not depend on what the previous call left there.
+directly and compare it bit for bit with gdn_layer_varlen (which takes a
+workspace) on the decode workload and on a batch with a chunked sequence,
+twice in a row each, since every call shares the static array and must not
+depend on what the previous call left there.
 
 This file is named to be collected last.
 """
@@ -50,9 +51,10 @@ def _noalloc(lib, wl, d, out, conv_fin, state_fin, N=None):
         ctypes.c_float(d["scale"]), gdn.GDN_BF16, ctypes.c_void_p(stream))
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
-    wl = W.WORKLOADS["decode"]
-    d = W.make_inputs(wl, DEV)
+def _compare_two_calls(lib, wl, d):
+    """Two noalloc calls in a row, each bit-identical to gdn_layer_varlen: both
+    run the same kernels on the same inputs, so any difference would be left
+    over in the shared static array by the previous call."""
     ref_out, ref_conv, ref_state = gdn.gdn_layer_varlen(
         d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["offsets"],
         d["conv_init"], d["state_init"], H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D,
@@ -65,8 +67,24 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
         assert rc == 0, lib.gdn_last_error()
         torch.cuda.synchronize()
         assert torch.equal(conv_fin, ref_conv)
-        assert _rel_l2(out, ref_out) <= 2e-2
-        assert _rel_l2(state_fin, ref_state) <= 2e-2
+        assert torch.equal(out, ref_out), _rel_l2(out, ref_out)
+        assert torch.equal(state_fin, ref_state), _rel_l2(state_fin, ref_state)
+
+
+def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
+    wl = W.WORKLOADS["decode"]
+    _compare_two_calls(lib, wl, W.make_inputs(wl, DEV))
+
+
+def test_noalloc_chunked_batch_after_decode(lib):
+    """A batch with a 300-token sequence (the chunked tensor-core kernel, its
+    work counters and schedule live in the static array) and a 40-token one
+    (token-serial), after the decode calls above: under the 16 MiB limit at
+    the decode head geometry."""
+    wl = W.scaled(W.WORKLOADS["decode"], (40, 300), name="noalloc-chunked")
+    need = gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D)
+    assert need <= 16 * 1024 * 1024
+    _compare_two_calls(lib, wl, W.make_inputs(wl, DEV))
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):

@@ -364,7 +364,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
             }
         }
-        int s = p.offsets[seq], e = p.offsets[seq + 1];
+        int s, e;
+        if (!seq_bounds(p.offsets, p.B, p.N, seq, s, e)) {
+            // malformed offsets (the schedule lists no unit then; this guard
+            // keeps every load and store inside [0, N) regardless)
+            __syncthreads();  // every thread has read s_unit before thread 0 rewrites it
+            continue;
+        }
         if (p.seg_mode) {  // this segment's tokens (units past the sequence's last segment are empty)
             int seg_len;
             segments_of(e - s, nseg_here, seg_len, nseg_here);
