@@ -183,15 +183,20 @@ OPT_GATE_EXP = 4      # gate_activation none: g = exp(a)
 OPT_NO_BETA = 8       # no beta input: beta = 1
 OPT_BETA_RAW = 16     # beta_activation none: beta = b
 OPT_NO_QK_NORM = 32   # qk_l2_norm 0
+OPT_GATE_PER_CHANNEL = 64  # gate_per_channel: a [N, H, K]; gates g [N, H, K] then beta [N, H]
 
 
 def prepare_ex(y, a, b, A_log, dt_bias, H, HQ, K, V, opts):
-    """Prepare with options; a / b / A_log / dt_bias may be None where unused."""
+    """Prepare with options; a / b / A_log / dt_bias may be None where unused.
+
+    The gates come back as [2, N, H] (g, beta), or with OPT_GATE_PER_CHANNEL
+    as one flat array: g [N, H, K] followed by beta [N, H]."""
     y = _f64(y)
     N = y.shape[0]
     a, b, A_log, dt_bias = (_f64(x) for x in (a, b, A_log, dt_bias))
     qk = np.zeros((2, N, HQ, K))
-    gb = np.zeros((2, N, H))
+    gb = (np.zeros(N * H * K + N * H) if opts & OPT_GATE_PER_CHANNEL
+          else np.zeros((2, N, H)))
     rc = _load().oracle_prepare_ex(_p(y), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(qk), _p(gb),
                                    N, H, HQ, K, V, int(opts))
     _check(rc, "prepare_ex")
@@ -199,7 +204,8 @@ def prepare_ex(y, a, b, A_log, dt_bias, H, HQ, K, V, opts):
 
 
 def delta_varlen_ex(y, qk, gb, offsets, state_init, H, HQ, K, V, opts, scale=0.0):
-    """Recurrence with options (OPT_NO_RETRIEVE acts here)."""
+    """Recurrence with options (OPT_NO_RETRIEVE and OPT_GATE_PER_CHANNEL act
+    here; with the latter gb is g [N, H, K] followed by beta [N, H])."""
     y, qk, gb, state_init = map(_f64, (y, qk, gb, state_init))
     offsets = _i32(offsets)
     N = y.shape[0]

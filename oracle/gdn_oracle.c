@@ -155,6 +155,13 @@ int oracle_conv1d_varlen(const double *x, const double *w, const double *bias,
 #define OPT_NO_BETA 8      /* no beta input: beta = 1 */
 #define OPT_BETA_RAW 16    /* beta_activation none: beta = b */
 #define OPT_NO_QK_NORM 32  /* qk_l2_norm 0: q and k used as they are */
+/* Per-key-channel gate [rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet,
+ * gate_per_channel], on the packed layout: one decay logit per key channel,
+ * a [N, H, K], and g [N, H, K].  The gate activation is the scalar one applied
+ * to each channel's logit (A_log and dt_bias stay per head).  Storage of the
+ * prepared gates: gb = g [N, H, K] followed by beta [N, H].  In the
+ * recurrence, column i of every state row of head h decays by g[t, h, i]. */
+#define OPT_GATE_PER_CHANNEL 64
 
 /*
  * [paged_ssm.rs, DELTA_PREPARE with flags NORM, DECAY, SOFTPLUS, BETA, SIGMOID]
@@ -171,6 +178,7 @@ int oracle_prepare_ex(const double *y, const double *a, const double *bl,
     const int norm = !(opts & OPT_NO_QK_NORM), decay = !(opts & OPT_NO_DECAY);
     const int softplus_gate = !(opts & OPT_GATE_EXP), has_beta = !(opts & OPT_NO_BETA);
     const int sigmoid = !(opts & OPT_BETA_RAW);
+    const int per_channel = (opts & OPT_GATE_PER_CHANNEL) != 0;
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < N; ++t) {
         for (int kh = 0; kh < HQ; ++kh) {
@@ -189,21 +197,24 @@ int oracle_prepare_ex(const double *y, const double *a, const double *bl,
             }
         }
         for (int h = 0; h < H; ++h) {
-            double g = 1.0;
-            if (decay) {
-                double x = a[(size_t)t * H + h];
-                if (softplus_gate) {
-                    x += dt_bias[h];
-                    double softplus = fmax(x, 0.0) + log1p(exp(-fabs(x)));
-                    double alog = round_f32(A_log[h]);
-                    x = -exp(alog) * softplus;
+            const int nch = per_channel ? K : 1;  /* gates of this (token, head) */
+            for (int i = 0; i < nch; ++i) {
+                double g = 1.0;
+                if (decay) {
+                    double x = a[((size_t)t * H + h) * nch + i];
+                    if (softplus_gate) {
+                        x += dt_bias[h];
+                        double softplus = fmax(x, 0.0) + log1p(exp(-fabs(x)));
+                        double alog = round_f32(A_log[h]);
+                        x = -exp(alog) * softplus;
+                    }
+                    g = exp(x);
                 }
-                g = exp(x);
+                gb[((size_t)t * H + h) * nch + i] = g;
             }
             double beta = has_beta ? bl[(size_t)t * H + h] : 1.0;
             if (has_beta && sigmoid) beta = 1.0 / (1.0 + exp(-beta));
-            gb[(size_t)t * H + h] = g;
-            gb[((size_t)N + t) * H + h] = beta;
+            gb[(size_t)N * H * nch + (size_t)t * H + h] = beta;
         }
     }
     return ORACLE_OK;
@@ -252,8 +263,11 @@ static int delta_recurrence(const double *y, const double *qk, const double *gb,
                             double scale, const int32_t *counts, const int32_t *active,
                             double *capsule, int cap, int opts) {
     const int retrieve = !(opts & OPT_NO_RETRIEVE);
+    const int per_channel = (opts & OPT_GATE_PER_CHANNEL) != 0;
     if (B < 1 || N < 0 || H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ)
         return ORACLE_ERR_SHAPE;
+    if (per_channel && capsule) return ORACLE_ERR_SHAPE;  /* the capsule holds one g per head */
+    const size_t nch = per_channel ? (size_t)K : 1;
     if (check_offsets(offsets, B, N)) return ORACLE_ERR_OFFSETS;
     if (scale == 0.0) scale = 1.0 / sqrt((double)K);
     const size_t W = (size_t)2 * HQ * K + (size_t)H * V;
@@ -272,8 +286,9 @@ static int delta_recurrence(const double *y, const double *qk, const double *gb,
             for (int t = s; t < e; ++t) {
                 const double *q = qk + ((size_t)t * HQ + kh) * K;
                 const double *k = qk + (((size_t)N + t) * HQ + kh) * K;
-                const double g = gb[(size_t)t * H + h];
-                const double beta = gb[((size_t)N + t) * H + h];
+                const double *gt = gb + ((size_t)t * H + h) * nch;  /* g, or g per key channel */
+                const double g = gt[0];
+                const double beta = gb[(size_t)N * H * nch + (size_t)t * H + h];
                 const int slot = t - s;
                 if (slot < ncap) {  /* g of the head; k of the key head (its first value head) */
                     cb[(size_t)slot * H + h] = g;
@@ -285,7 +300,7 @@ static int delta_recurrence(const double *y, const double *qk, const double *gb,
                     double *row = S + (size_t)vi * K;
                     double retrieval = 0.0;
                     for (int i = 0; i < K; ++i) {
-                        row[i] *= g;
+                        row[i] *= per_channel ? gt[i] : g;
                         retrieval += k[i] * row[i];
                     }
                     double delta = y[(size_t)t * W + (size_t)2 * HQ * K + (size_t)h * V + vi];
@@ -444,9 +459,10 @@ int oracle_layer_varlen_ex(const double *qkv, const double *w, const double *bia
                            int silu, double scale, int act_dtype, int opts) {
     if (H < 1 || HQ < 1 || K < 1 || V < 1 || H % HQ) return ORACLE_ERR_SHAPE;
     const int C = 2 * HQ * K + H * V;
+    const size_t ngate = (opts & OPT_GATE_PER_CHANNEL) ? (size_t)K : 1;
     double *y = (double *)malloc(sizeof(double) * ((size_t)N * C + 1));
     double *qk = (double *)malloc(sizeof(double) * ((size_t)2 * N * HQ * K + 1));
-    double *gb = (double *)malloc(sizeof(double) * ((size_t)2 * N * H + 1));
+    double *gb = (double *)malloc(sizeof(double) * ((size_t)N * H * (ngate + 1) + 1));
     int rc = oracle_conv1d_varlen(qkv, w, bias, offsets, conv_init, y, conv_fin, B, N,
                                   C, Kc, D, silu, act_dtype);
     if (!rc) rc = oracle_prepare_ex(y, a, bl, A_log, dt_bias, qk, gb, N, H, HQ, K, V, opts);

@@ -660,3 +660,120 @@ def test_dense_per_channel_gate_reduces_and_decays_columns():
     o4, _ = oracle.dense_delta(q, k, v, g, beta, None)
     o5, _ = oracle.dense_delta(q, k, v, g, beta, np.zeros_like(S0))
     np.testing.assert_array_equal(o4, o5)
+
+
+# ------------------------------------------------------------------ per-key-channel gate on the
+# packed layout (f3): rlx-cpu thunk/types.rs Thunk::GatedDeltaNet gate_per_channel, with the
+# scalar gate activation applied to one decay logit per key channel, a [N, H, K]
+
+def _pc_problem(seed, lens=(5, 0, 7), H=4, HQ=2, K=6, V=3):
+    rng = _rng(seed)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(offs[-1])
+    W = 2 * HQ * K + H * V
+    y = rng.standard_normal((N, W))
+    a = rng.standard_normal((N, H, K)) - 0.5
+    b = rng.standard_normal((N, H))
+    A_log = rng.uniform(0, math.log(16), H)
+    dt_bias = rng.standard_normal(H)
+    S0 = rng.standard_normal((len(lens), H, V, K)) * 0.3
+    return offs, y, a, b, A_log, dt_bias, S0, (H, HQ, K, V)
+
+
+def test_per_channel_prepare_applies_the_gate_to_each_channel():
+    offs, y, a, b, A_log, dt, S0, (H, HQ, K, V) = _pc_problem(41)
+    N = y.shape[0]
+    qk, gb = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, oracle.OPT_GATE_PER_CHANNEL)
+    g, beta = gb[:N * H * K].reshape(N, H, K), gb[N * H * K:].reshape(N, H)
+    a32 = torch.tensor(A_log, dtype=torch.float32).double()
+    ref = torch.exp(-torch.exp(a32)[None, :, None]
+                    * F.softplus(torch.from_numpy(a) + torch.from_numpy(dt)[None, :, None]))
+    np.testing.assert_allclose(g, ref.numpy(), rtol=1e-14)
+    np.testing.assert_allclose(beta, torch.sigmoid(torch.from_numpy(b)).numpy(), rtol=1e-15)
+    qk0, _ = oracle.prepare_ex(y, a[..., 0], b, A_log, dt, H, HQ, K, V, 0)
+    np.testing.assert_array_equal(qk, qk0)
+
+
+def test_per_channel_uniform_logits_equal_the_scalar_gate_layer():
+    offs, y, a, b, A_log, dt, S0, (H, HQ, K, V) = _pc_problem(42)
+    a_uni = np.repeat(a[..., :1], K, axis=-1)
+    qk1, gb1 = oracle.prepare_ex(y, a_uni, b, A_log, dt, H, HQ, K, V, oracle.OPT_GATE_PER_CHANNEL)
+    o1, f1 = oracle.delta_varlen_ex(y, qk1, gb1, offs, S0, H, HQ, K, V,
+                                    oracle.OPT_GATE_PER_CHANNEL)
+    qk0, gb0 = oracle.prepare_ex(y, a[..., 0], b, A_log, dt, H, HQ, K, V, 0)
+    o0, f0 = oracle.delta_varlen_ex(y, qk0, gb0, offs, S0, H, HQ, K, V, 0)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(f1, f0)
+
+
+def test_per_channel_recurrence_matches_the_dense_oracle_and_the_unrolled_product():
+    offs, y, a, b, A_log, dt, S0, (H, HQ, K, V) = _pc_problem(43, lens=(6, 6), H=2, HQ=2, K=5,
+                                                            V=5)
+    N, G = y.shape[0], H // HQ
+    qk, gb = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V, oracle.OPT_GATE_PER_CHANNEL)
+    out, fin = oracle.delta_varlen_ex(y, qk, gb, offs, S0, H, HQ, K, V,
+                                      oracle.OPT_GATE_PER_CHANNEL, scale=0.6)
+    g, beta = gb[:N * H * K].reshape(N, H, K), gb[N * H * K:].reshape(N, H)
+    v = y[:, 2 * HQ * K:].reshape(N, H, V)
+    # (i) the dense-layout oracle (its own pins above) on the same two equal-length sequences
+    B, S = 2, 6
+    q4 = qk[0][:, np.arange(H) // G].reshape(B, S, H, K)
+    k4 = qk[1][:, np.arange(H) // G].reshape(B, S, H, K)
+    od, fd = oracle.dense_delta(q4, k4, v.reshape(B, S, H, V), g.reshape(B, S, H, K),
+                                beta.reshape(B, S, H), S0, per_channel=True, scale=0.6)
+    np.testing.assert_allclose(out, od.reshape(N, H, V), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(fin, fd, rtol=1e-12, atol=1e-13)
+    # (ii) the explicit product form with diagonal decays, A_t = diag(g_t) (I - beta_t k_t k_t^T):
+    #      S_t = S_0 A_1 .. A_t + sum_i beta_i v_i k_i^T A_{i+1} .. A_t, rebuilt from scratch
+    for bb in range(B):
+        s, e = offs[bb], offs[bb + 1]
+        for h in range(H):
+            kh = h // G
+            A = [np.diag(g[t, h]) @ (np.eye(K) - beta[t, h] * np.outer(qk[1, t, kh], qk[1, t, kh]))
+                 for t in range(s, e)]
+            for tt in range(1, e - s + 1):
+                St = S0[bb, h].copy()
+                for m in A[:tt]:
+                    St = St @ m
+                for i in range(tt):
+                    term = beta[s + i, h] * np.outer(v[s + i, h], qk[1, s + i, kh])
+                    for m in A[i + 1:tt]:
+                        term = term @ m
+                    St = St + term
+                np.testing.assert_allclose(out[s + tt - 1, h], 0.6 * St @ qk[0, s + tt - 1, kh],
+                                           rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(fin[bb, h], St, rtol=1e-10, atol=1e-12)
+
+
+def test_per_channel_beta0_decays_each_key_column_by_its_own_product():
+    offs, y, a, b, A_log, dt, S0, (H, HQ, K, V) = _pc_problem(44, lens=(4, 3))
+    N = y.shape[0]
+    qk, gb = oracle.prepare_ex(y, a, b, A_log, dt, H, HQ, K, V,
+                               oracle.OPT_GATE_PER_CHANNEL | oracle.OPT_BETA_RAW)
+    gb[N * H * K:] = 0.0                                   # beta = 0: nothing is written
+    _, fin = oracle.delta_varlen_ex(y, qk, gb, offs, S0, H, HQ, K, V, oracle.OPT_GATE_PER_CHANNEL)
+    g = gb[:N * H * K].reshape(N, H, K)
+    for bb in range(2):
+        decay = np.prod(g[offs[bb]:offs[bb + 1]], axis=0)      # [H, K]
+        np.testing.assert_allclose(fin[bb], S0[bb] * decay[:, None, :], rtol=1e-13, atol=1e-15)
+
+
+def test_per_channel_layer_is_the_composition():
+    wl = workloads.scaled(workloads.WORKLOADS["tiny"], (4, 0, 6))
+    d = workloads.make_inputs(wl)
+    rng = _rng(45)
+    a = rng.standard_normal((wl.N, wl.H, wl.K))
+    opts = oracle.OPT_GATE_PER_CHANNEL
+    out, cfin, sfin = oracle.layer_varlen_ex(d["qkv"], d["w"], d["bias"], a, d["b"], d["A_log"],
+                                             d["dt_bias"], d["offsets_list"], d["conv_init"],
+                                             d["state_init"], wl.H, wl.HQ, wl.K, wl.V, wl.Kc,
+                                             wl.D, opts, act_dtype="f32")
+    y, c2 = oracle.conv1d_varlen(d["qkv"], d["w"], d["bias"], d["offsets_list"], d["conv_init"],
+                                 wl.Kc, wl.D, silu=True, round_to="f32")
+    qk, gb = oracle.prepare_ex(y, a, d["b"], d["A_log"], d["dt_bias"], wl.H, wl.HQ, wl.K, wl.V,
+                               opts)
+    o2, s2 = oracle.delta_varlen_ex(y, qk, gb, d["offsets_list"], d["state_init"], wl.H, wl.HQ,
+                                    wl.K, wl.V, opts, scale=d["scale"])
+    np.testing.assert_array_equal(cfin, c2)
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(sfin, s2)
