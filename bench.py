@@ -48,6 +48,9 @@ def _args():
     ap.add_argument("--rule", default="gated_delta",
                     choices=["gated_delta", "delta", "gated", "linear"],
                     help="update rule (delta: no decay; gated: no retrieval; linear: neither)")
+    ap.add_argument("--gate", default="scalar", choices=["scalar", "per_channel"],
+                    help="per_channel: the layer with one decay logit per key channel, "
+                         "a [N, H, K] (GDN_OPT_GATE_PER_CHANNEL; token-serial kernel)")
     ap.add_argument("--dense", default=None, choices=["scalar", "per_channel"],
                     help="time the dense-layout call (q, k, v [B, S, H, n]) on the workload's "
                          "batch and head geometry (equal lengths), scalar or per-channel gate")
@@ -108,9 +111,10 @@ def capture_bytes(wl, B, cap):
     return capsule + 2 * rows
 
 
-def algorithmic_bytes_delta(wl, N, B, cap=0):
+def algorithmic_bytes_delta(wl, N, B, cap=0, per_channel=False):
     """Bytes the token-serial recurrence kernel must move per launch in the
-    layer call (it also writes the final conv state and any capture)."""
+    layer call (it also writes the final conv state and any capture; with the
+    per-channel gate it reads the decay logits a [N, H, K])."""
     esz = 2 if wl.dtype == "bf16" else 4
     state = 2 * B * wl.H * wl.V * wl.K * 4            # read + write fp32 state
     qk = N * wl.HQ * 2 * wl.K * 4                     # normalised q and k (fp32)
@@ -118,7 +122,8 @@ def algorithmic_bytes_delta(wl, N, B, cap=0):
     v = N * wl.H * wl.V * esz                         # v columns of the conv output
     out = N * wl.H * wl.V * esz
     conv_state = 2 * B * wl.width * wl.L * esz        # final conv state: read + write
-    return state + qk + gb + v + out + conv_state + capture_bytes(wl, B, cap)
+    pc = N * wl.H * wl.K * 4 if per_channel else 0
+    return state + qk + gb + v + out + conv_state + pc + capture_bytes(wl, B, cap)
 
 
 def algorithmic_bytes_layer(wl, N, B):
@@ -347,6 +352,10 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
                               dtype=torch.float32, device=dev)
 
     opts = gdn.RULE_OPTS[args.rule]
+    if args.gate == "per_channel":  # one decay logit per key channel
+        opts |= gdn.GDN_OPT_GATE_PER_CHANNEL
+        gpc = torch.Generator(device=dev).manual_seed(wl.seed + 500)
+        d["a"] = torch.randn((N, wl.H, wl.K), generator=gpc, device=dev) * wl.a_std + wl.a_mean
 
     def call(qkv, a, b, offsets, sset, out_t=None, capsule_t=None):
         # decode-style carry: the final states overwrite the initial ones in place
@@ -541,7 +550,7 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
     kavg = statistics.mean(kern_ms)
     value = _job_tokens_per_s(world, N, args.steps, ms)
     if dom == gdn.GDN_KERNEL_SERIAL:
-        kbytes = algorithmic_bytes_delta(wl, N, B, cap)
+        kbytes = algorithmic_bytes_delta(wl, N, B, cap, per_channel=args.gate == "per_channel")
         achieved = kbytes / (kavg * 1e-3) / 1e9
         roof = {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -568,7 +577,8 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
                          "touched two steps before",
                    "parallelism": f"replicas x{world}",
                    **({"capture": cap} if cap else {}),
-                   **({"rule": args.rule} if opts else {})},
+                   **({"rule": args.rule} if args.rule != "gated_delta" else {}),
+                   **({"gate": "per_channel"} if args.gate == "per_channel" else {})},
         "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
         "roofline": roof,
         "e2e": {"value": _job_tokens_per_s(world, N, args.steps, e2e_ms), "unit": "tokens/s",
@@ -612,7 +622,8 @@ def run_ours(args, wl):
 
     line = _measure(args, wl, dev, world, rank, local, gdn, W)
     extras = {}
-    plain = not (args.lens or args.capture or args.rule != "gated_delta")
+    plain = not (args.lens or args.capture or args.rule != "gated_delta"
+                 or args.gate != "scalar")
     if plain and wl.name == "decode" and not args.no_extra:
         for name in EXTRA_WORKLOADS:
             torch.cuda.empty_cache()

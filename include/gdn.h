@@ -323,7 +323,23 @@ GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void 
 #define GDN_OPT_NO_BETA 8      /* no beta input: beta = 1 (b may be NULL) */
 #define GDN_OPT_BETA_RAW 16    /* beta_activation none: beta = b */
 #define GDN_OPT_NO_QK_NORM 32  /* qk_l2_norm 0: q and k are used as they are */
-#define GDN_OPT_ALL 63
+/*
+ * Per-key-channel gate (rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet,
+ * gate_per_channel) on the packed layout: every key channel of a (token, value
+ * head) has its own decay.  With this bit:
+ *   gdn_layer_varlen_ex, gdn_prepare_ex: a is [N, H, K] fp32, one decay logit
+ *     per key channel; the gate activation is the scalar one applied to each
+ *     logit (softplus gate with the head's A_log and dt_bias, or exp with
+ *     GDN_OPT_GATE_EXP).
+ *   gdn_prepare_ex writes g_beta as g [N, H, K] followed by beta [N, H]
+ *     (N*H*(K+1) floats); gdn_delta_varlen_ex reads that layout.
+ *   The recurrence decays column i of every state row of head h by g[t, h, i]:
+ *     S_t = S_{t-1} diag(g_t) + beta_t (v_t - S_{t-1} diag(g_t) k_t) k_t^T.
+ *   Every sequence runs on the token-serial kernel (no chunked form).  Not
+ *   combinable with state-update capture (GDN_ERR_UNSUPPORTED).
+ */
+#define GDN_OPT_GATE_PER_CHANNEL 64
+#define GDN_OPT_ALL 127
 
 /*
  * The calls with rule / activation options (GDN_OPT_*, above); opts = 0 is

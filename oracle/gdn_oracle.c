@@ -26,7 +26,8 @@
  *    beta_activation, qk_l2_norm; flags DECAY, RETRIEVE, SOFTPLUS, BETA,
  *    SIGMOID, NORM]  the rule and activation variants (oracle_*_ex).
  *   [rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet]  the dense-layout call,
- *       optional per-key-channel gate (oracle_dense_delta).
+ *       optional per-key-channel gate (oracle_dense_delta), and the same
+ *       per-channel gate on the packed layout (OPT_GATE_PER_CHANNEL).
  *   [paged_ssm.rs, CONV_CAPTURE_* and DELTA_CAPTURE_* kernels]
  *       capture of the first min(counts[b], capacity, len) tokens' updates:
  *       raw conv input rows and the (g, normalised k, beta-scaled delta)

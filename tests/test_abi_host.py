@@ -208,7 +208,8 @@ def test_option_calls_validate_option_bits_and_needed_inputs(lib):
         return lib.gdn_layer_varlen_ex(FAKE, FAKE, None, a, b, A_log, dt_bias, FAKE, None, FAKE,
                                        FAKE, FAKE, FAKE, FAKE, opts, 0, None, None, None, None,
                                        2, 16, 4, 2, 16, 16, 4, 1, 1, 0.0, 0, FAKE, 1 << 30, None)
-    assert layer_ex(64) == 5 and b"option" in lib.gdn_last_error()
+    assert layer_ex(128) == 5 and b"option" in lib.gdn_last_error()
+    assert layer_ex(gdn.GDN_OPT_GATE_PER_CHANNEL, a=None) == 1   # per-channel logits needed
     assert layer_ex(0, a=None) == 1
     assert layer_ex(0, b=None) == 1
     assert layer_ex(0, A_log=None) == 1
@@ -219,8 +220,14 @@ def test_option_calls_validate_option_bits_and_needed_inputs(lib):
                               None) == 1
     assert lib.gdn_prepare_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 2, 16, 16, 128, 0,
                               None) == 5
+    # the per-channel gate cannot be captured (the capsule holds one g per head)
+    counts = FAKE
+    assert lib.gdn_layer_varlen_ex(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                   FAKE, FAKE, FAKE, FAKE, gdn.GDN_OPT_GATE_PER_CHANNEL, 2, counts,
+                                   None, FAKE, FAKE, 2, 16, 4, 2, 16, 16, 4, 1, 1, 0.0, 0, FAKE,
+                                   1 << 30, None) == 5
     assert lib.gdn_delta_varlen_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 16, 4, 2, 16, 16,
-                                   0.0, 99, 0, None) == 5
+                                   0.0, 131, 0, None) == 5
 
 
 def test_dense_call_validation(lib):

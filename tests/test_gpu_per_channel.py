@@ -1,0 +1,134 @@
+"""GPU parity of the per-key-channel gate on the packed layout
+(GDN_OPT_GATE_PER_CHANNEL; rlx-cpu thunk/types.rs, Thunk::GatedDeltaNet,
+gate_per_channel): decay logits a [N, H, K], one gate per key channel, state
+columns decayed separately.  Checked against the fp64 oracle (its pins are in
+test_oracle_pins.py) through the layer, the standalone prepare and the
+standalone recurrence; every sequence runs on the token-serial kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_gated_delta_gb300 as gdn
+from varlen_gated_delta_gb300 import workloads as W
+from gdn_testlib import cpu64, max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+PC = gdn.GDN_OPT_GATE_PER_CHANNEL
+
+
+def _case(base, lens, seed_shift=0, **over):
+    wl = W.scaled(W.WORKLOADS[base], lens, name="per-channel", **over)
+    d = W.make_inputs(wl, DEV)
+    g = torch.Generator(device=DEV).manual_seed(wl.seed + 500 + seed_shift)
+    # per-channel decay logits with the workload's mean and spread
+    d["a"] = torch.randn((wl.N, wl.H, wl.K), generator=g, device=DEV) * wl.a_std + wl.a_mean
+    return wl, d
+
+
+def _layer(wl, d, opts=PC, **kw):
+    return gdn.gdn_layer_varlen_ex(d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"],
+                                   d["dt_bias"], d["offsets"], d["conv_init"], d["state_init"],
+                                   H=wl.H, HQ=wl.HQ, K=wl.K, V=wl.V, Kc=wl.Kc, D=wl.D, opts=opts,
+                                   scale=d["scale"], **kw)
+
+
+def _oracle_layer(wl, d, opts=PC):
+    return oracle.layer_varlen_ex(cpu64(d["qkv"]), cpu64(d["w"]),
+                                  None if d["bias"] is None else cpu64(d["bias"]),
+                                  cpu64(d["a"]), cpu64(d["b"]), cpu64(d["A_log"]),
+                                  cpu64(d["dt_bias"]), d["offsets_list"], cpu64(d["conv_init"]),
+                                  cpu64(d["state_init"]), wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D,
+                                  opts, silu=wl.silu, scale=d["scale"],
+                                  act_dtype="bf16" if wl.dtype == "bf16" else "f32")
+
+
+GEOMS = [
+    ("tiny-f32", "tiny", (5, 0, 11, 1), {}),
+    ("decode-bf16", "decode", (1,) * 16, dict(H=8, HQ=4)),
+    ("mixed-bf16", "decode", (3, 70, 0, 9, 130), dict(H=4, HQ=2)),
+    ("long-geometry-bf16", "long", (40, 7), dict(H=2, HQ=1)),
+    ("f32-k64-v48", "tiny", (6, 17), dict(K=64, V=48, H=2, HQ=1)),
+]
+
+
+@pytest.mark.parametrize("host_offsets", [True, False])
+@pytest.mark.parametrize("geom", GEOMS, ids=[g[0] for g in GEOMS])
+def test_per_channel_layer_matches_oracle(geom, host_offsets):
+    _, base, lens, over = geom
+    wl, d = _case(base, lens, **over)
+    out, cfin, sfin = _layer(wl, d, offsets_host=d["offsets_list"] if host_offsets else None)
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cpu64(cfin), c_ref)
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL[wl.dtype] and es <= TOL[wl.dtype], (
+        f"out {eo:.3e} (max-abs {max_abs(cpu64(out), o_ref):.3e}) state {es:.3e}")
+
+
+@pytest.mark.parametrize("extra", [0, gdn.GDN_OPT_GATE_EXP, gdn.RULE_OPTS["gated"],
+                                   gdn.GDN_OPT_BETA_RAW | gdn.GDN_OPT_NO_BETA])
+def test_per_channel_with_rule_options(extra):
+    wl, d = _case("tiny", (7, 12), seed_shift=1)
+    if extra & gdn.GDN_OPT_GATE_EXP:
+        d["a"] = -torch.nn.functional.softplus(d["a"]) * 0.5
+    opts = PC | extra
+    out, cfin, sfin = _layer(wl, d, opts=opts, offsets_host=d["offsets_list"])
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d, opts=opts)
+    torch.cuda.synchronize()
+    assert rel_l2(cpu64(out), o_ref) <= TOL["f32"] and rel_l2(cpu64(sfin), s_ref) <= TOL["f32"]
+
+
+def test_per_channel_standalone_prepare_and_delta():
+    wl, d = _case("decode", (4, 0, 9), seed_shift=2, H=4, HQ=2, K=128, V=64)
+    y = d["qkv"]   # stands in for a conv output
+    qk, gb = gdn.gdn_prepare_ex(y, d["a"], d["b"], d["A_log"], d["dt_bias"], H=wl.H, HQ=wl.HQ,
+                                K=wl.K, V=wl.V, opts=PC)
+    qk_ref, gb_ref = oracle.prepare_ex(cpu64(y), cpu64(d["a"]), cpu64(d["b"]), cpu64(d["A_log"]),
+                                       cpu64(d["dt_bias"]), wl.H, wl.HQ, wl.K, wl.V, PC)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(cpu64(qk), qk_ref, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(cpu64(gb), gb_ref, rtol=2e-5, atol=1e-30)
+    # the recurrence on the oracle's own prepared values (fp32 copies)
+    qk32 = torch.tensor(qk_ref, dtype=torch.float32, device=DEV)
+    gb32 = torch.tensor(gb_ref, dtype=torch.float32, device=DEV)
+    out, sfin = gdn.gdn_delta_varlen_ex(y, qk32, gb32, d["offsets"], d["state_init"], H=wl.H,
+                                        HQ=wl.HQ, K=wl.K, V=wl.V, opts=PC, scale=0.0)
+    o_ref, s_ref = oracle.delta_varlen_ex(cpu64(y), cpu64(qk32), cpu64(gb32), d["offsets_list"],
+                                          cpu64(d["state_init"]), wl.H, wl.HQ, wl.K, wl.V, PC)
+    torch.cuda.synchronize()
+    assert rel_l2(cpu64(out), o_ref) <= TOL["bf16"] and rel_l2(cpu64(sfin), s_ref) <= 1e-5
+
+
+def test_per_channel_layer_equals_composed_calls_bitwise():
+    wl, d = _case("decode", (3, 17, 0, 1, 90), seed_shift=3, H=4, HQ=2)
+    out, cfin, sfin = _layer(wl, d)
+    y, c2 = gdn.gdn_conv1d_varlen(d["qkv"], d["w"], d["bias"], d["offsets"], d["conv_init"],
+                                  Kc=wl.Kc, D=wl.D)
+    qk, gb = gdn.gdn_prepare_ex(y, d["a"], d["b"], d["A_log"], d["dt_bias"], H=wl.H, HQ=wl.HQ,
+                                K=wl.K, V=wl.V, opts=PC)
+    o2, s2 = gdn.gdn_delta_varlen_ex(y, qk, gb, d["offsets"], d["state_init"], H=wl.H, HQ=wl.HQ,
+                                     K=wl.K, V=wl.V, opts=PC, scale=d["scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(cfin, c2) and torch.equal(out, o2) and torch.equal(sfin, s2)
+
+
+def test_uniform_per_channel_logits_match_the_scalar_gate():
+    wl, d = _case("tiny", (9, 4), seed_shift=4)
+    scalar = dict(d, a=d["a"][:, :, 0].contiguous())
+    uniform = dict(d, a=d["a"][:, :, :1].expand(-1, -1, wl.K).contiguous())
+    o1, _, s1 = _layer(wl, uniform)
+    o0, _, s0 = _layer(wl, scalar, opts=0)
+    torch.cuda.synchronize()
+    assert rel_l2(cpu64(o1), cpu64(o0)) <= 1e-5 and rel_l2(cpu64(s1), cpu64(s0)) <= 1e-5
+
+
+def test_per_channel_with_capture_is_rejected():
+    wl, d = _case("tiny", (3, 4), seed_shift=5)
+    counts = torch.full((wl.B,), 2, dtype=torch.int32, device=DEV)
+    with pytest.raises(gdn.GdnError) as ei:
+        _layer(wl, d, cap=2, counts=counts)
+    assert ei.value.status == 5

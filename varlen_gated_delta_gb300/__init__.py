@@ -29,7 +29,8 @@ __all__ = [
     "STATUS_NAMES", "GDN_CAPTURE_MAX", "gdn_conv1d_varlen_capture", "gdn_delta_varlen_capture",
     "gdn_layer_varlen_capture", "gdn_prepare_ex", "gdn_delta_varlen_ex", "gdn_layer_varlen_ex",
     "GDN_OPT_NO_DECAY", "GDN_OPT_NO_RETRIEVE", "GDN_OPT_GATE_EXP", "GDN_OPT_NO_BETA",
-    "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "RULE_OPTS", "gdn_gated_delta_dense",
+    "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "GDN_OPT_GATE_PER_CHANNEL", "RULE_OPTS",
+    "gdn_gated_delta_dense",
     "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
     "gdn_selftest_wait_timeout", "gdn_dense_workspace_bytes",
 ]
@@ -41,6 +42,7 @@ GDN_CAPTURE_MAX = 8
 # sigmoid rate, L2-normalised q and k
 GDN_OPT_NO_DECAY, GDN_OPT_NO_RETRIEVE, GDN_OPT_GATE_EXP = 1, 2, 4
 GDN_OPT_NO_BETA, GDN_OPT_BETA_RAW, GDN_OPT_NO_QK_NORM = 8, 16, 32
+GDN_OPT_GATE_PER_CHANNEL = 64  # a [N, H, K]: one decay per key channel
 RULE_OPTS = {"gated_delta": 0, "delta": GDN_OPT_NO_DECAY, "gated": GDN_OPT_NO_RETRIEVE,
              "linear": GDN_OPT_NO_DECAY | GDN_OPT_NO_RETRIEVE}
 GDN_ACT_NONE, GDN_ACT_SILU = 0, 1
@@ -427,26 +429,32 @@ def gdn_layer_varlen_capture(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_i
 # ------------------------------------------------------------------ rule / activation options
 
 def gdn_prepare_ex(y, a, b, A_log, dt_bias, *, H, HQ, K, V, opts, qk_norm=None, g_beta=None):
-    """gdn_prepare with GDN_OPT_* options (unused inputs may be None)."""
+    """gdn_prepare with GDN_OPT_* options (unused inputs may be None).  With
+    GDN_OPT_GATE_PER_CHANNEL, a is [N, H, K] and g_beta is g [N, H, K] followed
+    by beta [N, H], flat."""
     lib = load_library()
     N = y.shape[0]
     dev = y.device
     f32 = torch.float32
+    pc = bool(int(opts) & GDN_OPT_GATE_PER_CHANNEL)
+    gshape = (N * H * (K + 1),) if pc else (2, N, H)   # per channel: g [N,H,K] then beta [N,H]
     qk_norm = torch.empty((2, N, HQ, K), dtype=f32, device=dev) if qk_norm is None else qk_norm
-    g_beta = torch.empty((2, N, H), dtype=f32, device=dev) if g_beta is None else g_beta
+    g_beta = torch.empty(gshape, dtype=f32, device=dev) if g_beta is None else g_beta
     W = 2 * HQ * K + H * V
-    args = [_ptr(y, "y", None, (N, W), dev), _ptr(a, "a", f32, (N, H), dev),
+    args = [_ptr(y, "y", None, (N, W), dev), _ptr(a, "a", f32, (N, H, K) if pc else (N, H), dev),
             _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
             _ptr(dt_bias, "dt_bias", f32, (H,), dev),
             _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
-            _ptr(g_beta, "g_beta", f32, (2, N, H), dev)]
+            _ptr(g_beta, "g_beta", f32, gshape, dev)]
     _check(lib.gdn_prepare_ex(*args, N, H, HQ, K, V, int(opts), _dtype_code(y), _stream(dev)))
     return qk_norm, g_beta
 
 
 def gdn_delta_varlen_ex(y, qk_norm, g_beta, offsets, state_init, *, H, HQ, K, V, opts, scale=0.0,
                         out=None, state_fin=None):
-    """gdn_delta_varlen with GDN_OPT_* options (GDN_OPT_NO_RETRIEVE acts here)."""
+    """gdn_delta_varlen with GDN_OPT_* options (GDN_OPT_NO_RETRIEVE and
+    GDN_OPT_GATE_PER_CHANNEL act here; the latter reads g_beta as g [N, H, K]
+    followed by beta [N, H])."""
     lib = load_library()
     N = y.shape[0]
     B = offsets.numel() - 1
@@ -455,8 +463,9 @@ def gdn_delta_varlen_ex(y, qk_norm, g_beta, offsets, state_init, *, H, HQ, K, V,
     out = torch.empty((N, H, V), dtype=y.dtype, device=dev) if out is None else out
     state_fin = torch.empty((B, H, V, K), dtype=f32, device=dev) if state_fin is None else state_fin
     W = 2 * HQ * K + H * V
+    gshape = (N * H * (K + 1),) if int(opts) & GDN_OPT_GATE_PER_CHANNEL else (2, N, H)
     args = [_ptr(y, "y", None, (N, W), dev), _ptr(qk_norm, "qk_norm", f32, (2, N, HQ, K), dev),
-            _ptr(g_beta, "g_beta", f32, (2, N, H), dev),
+            _ptr(g_beta, "g_beta", f32, gshape, dev),
             _ptr(offsets, "offsets", torch.int32, (B + 1,), dev),
             _ptr(state_init, "state_init", f32, (B, H, V, K), dev),
             _ptr(out, "out", y.dtype, (N, H, V), dev),
@@ -498,8 +507,9 @@ def gdn_layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, 
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     hp, keep = _host_offsets(offsets_host)
+    ashape = (N, H, K) if int(opts) & GDN_OPT_GATE_PER_CHANNEL else (N, H)
     args = [_ptr(qkv, "qkv", T, (N, W), dev), _ptr(w, "w", T, (W, Kc), dev),
-            _ptr(bias, "bias", T, (W,), dev), _ptr(a, "a", f32, (N, H), dev),
+            _ptr(bias, "bias", T, (W,), dev), _ptr(a, "a", f32, ashape, dev),
             _ptr(b, "b", f32, (N, H), dev), _ptr(A_log, "A_log", f32, (H,), dev),
             _ptr(dt_bias, "dt_bias", f32, (H,), dev),
             _ptr(offsets, "offsets", torch.int32, (B + 1,), dev), hp,

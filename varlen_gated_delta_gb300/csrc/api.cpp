@@ -384,6 +384,8 @@ static int prepare_impl(const void *y, const float *a, const float *b, const flo
     if (N > 0 && (!y || !qk_norm || !g_beta)) return fail(GDN_ERR_NULL, "prepare: a required pointer is NULL");
     rc = check_opts(opts, N, a, b, A_log, dt_bias, "prepare");
     if (rc) return rc;
+    if ((opts & GDN_OPT_GATE_PER_CHANNEL) && (long)N * H * (K + 1) > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "prepare: N*H*(K+1) gates exceed int32");
     if ((long)N * H > INT_MAX / 2 || (long)N * HQ * 32 > INT_MAX) return fail(GDN_ERR_OVERFLOW, "prepare dispatch exceeds int32");
     PrepParams p{};
     p.y = y; p.a = a; p.bl = b; p.A_log = A_log; p.dt_bias = dt_bias; p.qk = qk_norm; p.gb = g_beta;
@@ -422,6 +424,8 @@ static int delta_impl(const void *y, const float *qk_norm, const float *g_beta,
         return fail(GDN_ERR_NULL, "delta: a required pointer is NULL");
     if ((long)B * H * V * 32 > INT_MAX) return fail(GDN_ERR_OVERFLOW, "delta dispatch B*H*V*32 exceeds int32");
     if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
+    if ((opts & GDN_OPT_GATE_PER_CHANNEL) && cap)
+        return fail(GDN_ERR_UNSUPPORTED, "delta: state-update capture with the per-channel gate");
     DeltaParams p{};
     p.y = y; p.qk = qk_norm; p.gb = g_beta; p.offsets = offsets; p.state_init = state_init;
     p.out = out; p.state_fin = state_fin; p.B = B; p.N = N; p.H = H; p.HQ = HQ; p.K = K; p.V = V;
@@ -430,6 +434,12 @@ static int delta_impl(const void *y, const float *qk_norm, const float *g_beta,
     p.max_len = INT_MAX;
     p.conv_fin = nullptr;
     p.opts = opts;
+    if (opts & GDN_OPT_GATE_PER_CHANNEL) {  // g_beta = g [N, H, K] then beta [N, H]
+        if ((long)N * H * K > INT_MAX) return fail(GDN_ERR_OVERFLOW, "delta: N*H*K gates exceed int32");
+        p.gpc = g_beta;
+        p.gpc_logits = 0;
+        p.beta_base = g_beta + (size_t)N * H * K;
+    }
     if (cap) {
         p.cap = cap->cap; p.counts = cap->counts; p.active = cap->active; p.capsule = cap->capsule;
     }
@@ -519,6 +529,13 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         return fail(GDN_ERR_NULL, "layer: a required pointer is NULL");
     rc = check_opts(opts, N, a, b, A_log, dt_bias, "layer");
     if (rc) return rc;
+    // without decay a per-channel gate is g = 1 in every channel: the plain rule
+    if (opts & GDN_OPT_NO_DECAY) opts &= ~GDN_OPT_GATE_PER_CHANNEL;
+    const bool per_channel = (opts & GDN_OPT_GATE_PER_CHANNEL) != 0;
+    if (per_channel && cap)
+        return fail(GDN_ERR_UNSUPPORTED, "layer: state-update capture with the per-channel gate");
+    if (per_channel && (long)N * H * K > INT_MAX)
+        return fail(GDN_ERR_OVERFLOW, "layer: N*H*K decay logits exceed int32");
     if ((long)B * H * V * 32 > INT_MAX || (long)B * width > INT_MAX)
         return fail(GDN_ERR_OVERFLOW, "layer dispatch size exceeds int32");
     if (!std::isfinite(scale)) return fail(GDN_ERR_SHAPE, "scale is not finite");
@@ -532,7 +549,8 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         if (rc) return rc;
     }
     // path choice per sequence: at least `thr` tokens -> chunked kernel
-    const bool chunk_ok = chunked_supported(dtype, K, V, (int)width);
+    // (the per-channel gate has no chunked form: every sequence is token-serial)
+    const bool chunk_ok = chunked_supported(dtype, K, V, (int)width) && !per_channel;
     const int thr = chunk_min_len();
     const int serial_max = chunk_ok ? thr : INT_MAX;
     bool run_chunked = chunk_ok && N >= thr;
@@ -562,9 +580,16 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-
-
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws + lay.header);
+    const float eff_scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
+    int max_len = INT_MAX;  // unknown without host offsets
+    if (offsets_host) {
+        max_len = 0;
+        for (int i = 0; i < B; ++i) {
+            const int len = offsets_host[i + 1] - offsets_host[i];
+            max_len = len > max_len ? len : max_len;
+        }
+    }
     void *y = ws + lay.y;
     float *qk = reinterpret_cast<float *>(ws + lay.qk);
     float *gb = reinterpret_cast<float *>(ws + lay.gb);
@@ -592,7 +617,6 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         e = launch_prepare(pp, dtype, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
-    const float eff_scale = scale == 0.f ? 1.f / std::sqrt((float)K) : scale;
     auto launch_chunked = [&]() -> int {
         ChunkLaunch cl{};
         cl.y = y; cl.a = a; cl.bl = b; cl.A_log = A_log; cl.dt_bias = dt_bias;
@@ -624,21 +648,20 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     dp.out = out; dp.state_fin = state_fin; dp.B = B; dp.N = N; dp.H = H; dp.HQ = HQ; dp.K = K; dp.V = V;
     dp.scale = eff_scale;
     dp.serial_max_len = serial_max;
-    dp.max_len = INT_MAX;  // unknown without host offsets
-    if (offsets_host) {
-        int m = 0;
-        for (int i = 0; i < B; ++i) {
-            const int len = offsets_host[i + 1] - offsets_host[i];
-            m = len > m ? len : m;
-        }
-        dp.max_len = m;
-    }
+    dp.max_len = max_len;
     // the recurrence kernel also writes the final conv state (after the conv
     // kernel has finished reading the initial one) and overlaps, through
     // programmatic dependent launch, its state loads with the conv kernel
     dp.conv_x = qkv; dp.conv_init = conv_init; dp.conv_fin = L > 0 ? conv_fin : nullptr;
     dp.conv_L = (int)L;
     dp.opts = opts;
+    if (per_channel) {  // gates from the per-channel logits; beta from the prepare step
+        dp.gpc = a;
+        dp.gpc_logits = 1;
+        dp.A_log = A_log;
+        dp.dt_bias = dt_bias;
+        dp.beta_base = gb + (size_t)N * H;
+    }
     if (cap) {
         dp.cap = cap->cap; dp.counts = cap->counts; dp.active = cap->active;
         dp.conv_updates = cap->conv_updates; dp.capsule = cap->capsule;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace gdn {
@@ -43,6 +45,21 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// SiLU z sigmoid(z) = z (1 + tanh(z/2)) / 2 of a conv output stored in T: for
+// bf16 with the special-function unit's tanh (relative error about 2^-11,
+// below the output's rounding step), for fp32 with the fast exponential and
+// division (a few fp32 ulp).
+template <typename T>
+__device__ __forceinline__ float silu_for(float z) {
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+        float h;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(h) : "f"(0.5f * z));
+        return 0.5f * z * (1.f + h);
+    } else {
+        return __fdividef(z, 1.f + __expf(-z));
+    }
 }
 
 // Full-warp xor reduction over groups of `W` consecutive lanes (W a power of 2).
@@ -111,8 +128,8 @@ __device__ __forceinline__ void gates_opt(const float *a, const float *b, size_t
         decay_and_rate(__ldg(a + i), __ldg(dt_bias + h), __ldg(A_log + h), __ldg(b + i), g, beta);
         return;
     }
-    g = 1.f;
-    if (!(opts & GDN_OPT_NO_DECAY)) {
+    g = 1.f;  // (with the per-channel gate the gates come from gate_of_logit)
+    if (!(opts & (GDN_OPT_NO_DECAY | GDN_OPT_GATE_PER_CHANNEL))) {
         float x = __ldg(a + i);
         if (!(opts & GDN_OPT_GATE_EXP)) {
             x += __ldg(dt_bias + h);
@@ -126,6 +143,19 @@ __device__ __forceinline__ void gates_opt(const float *a, const float *b, size_t
         beta = __ldg(b + i);
         if (!(opts & GDN_OPT_BETA_RAW)) beta = 1.f / (1.f + expf(-beta));
     }
+}
+
+// Gate of one key channel from its decay logit x (GDN_OPT_GATE_PER_CHANNEL):
+// the scalar gate's activation applied to the channel's logit -- 1 without
+// decay, exp(x) for the exp gate, else exp(-exp(A_log) softplus(x + dt_bias)).
+__device__ __forceinline__ float gate_of_logit(float x, float dt_bias, float A_log, int opts) {
+    if (opts & GDN_OPT_NO_DECAY) return 1.f;
+    if (!(opts & GDN_OPT_GATE_EXP)) {
+        x += dt_bias;
+        const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+        x = -expf(A_log) * softplus;
+    }
+    return expf(x);
 }
 
 // log(g) for the same (token, value head), kept in the log domain.

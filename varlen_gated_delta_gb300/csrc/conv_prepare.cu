@@ -101,21 +101,6 @@ __device__ __forceinline__ void store_pair(Vec16<T> &v, int q, float a, float b)
     }
 }
 
-// SiLU z sigmoid(z) = z (1 + tanh(z/2)) / 2 of a conv output stored in T: for
-// bf16 with the special-function unit's tanh (relative error about 2^-11,
-// below the output's rounding step), for fp32 with the fast exponential and
-// division (a few fp32 ulp).
-template <typename T>
-__device__ __forceinline__ float silu_for(float z) {
-    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
-        float h;
-        asm("tanh.approx.f32 %0, %1;" : "=f"(h) : "f"(0.5f * z));
-        return 0.5f * z * (1.f + h);
-    } else {
-        return __fdividef(z, 1.f + __expf(-z));
-    }
-}
-
 __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, float &g,
                                            float &beta) {
     gates_opt(p.a, p.bl, (size_t)t * p.H + h, p.A_log, p.dt_bias, h, p.opts, g, beta);
@@ -752,8 +737,19 @@ __global__ void __launch_bounds__(256) prepare_kernel(const PrepParams p, const 
         const int h = (int)(i % p.H);
         float g, beta;
         gates_opt(p.a, p.bl, (size_t)i, p.A_log, p.dt_bias, h, p.opts, g, beta);
-        p.gb[i] = g;
-        p.gb[(size_t)p.N * p.H + i] = beta;
+        if (p.opts & GDN_OPT_GATE_PER_CHANNEL) {  // g [N, H, K], then beta [N, H]
+            const bool soft = !(p.opts & (GDN_OPT_NO_DECAY | GDN_OPT_GATE_EXP));
+            const float dtb = soft ? __ldg(p.dt_bias + h) : 0.f;
+            const float alog = soft ? __ldg(p.A_log + h) : 0.f;
+            const bool decay = !(p.opts & GDN_OPT_NO_DECAY);
+            for (int c = 0; c < p.K; ++c)
+                p.gb[(size_t)i * p.K + c] =
+                    gate_of_logit(decay ? __ldg(p.a + (size_t)i * p.K + c) : 0.f, dtb, alog, p.opts);
+            p.gb[(size_t)p.N * p.H * p.K + i] = beta;
+        } else {
+            p.gb[i] = g;
+            p.gb[(size_t)p.N * p.H + i] = beta;
+        }
     }
 }
 

@@ -98,7 +98,15 @@ struct DeltaParams {
     const int32_t *active;
     void *conv_updates;
     float *capsule;
-    int opts;  // GDN_OPT_* (GDN_OPT_NO_RETRIEVE acts here)
+    int opts;  // GDN_OPT_* (GDN_OPT_NO_RETRIEVE and GDN_OPT_GATE_PER_CHANNEL act here)
+    // per-key-channel gate (GDN_OPT_GATE_PER_CHANNEL): gpc [N, H, K] holds the
+    // gates (gpc_logits == 0) or the decay logits, activated here with the
+    // head's A_log / dt_bias (gpc_logits != 0: the layer); beta of token t,
+    // head h is beta_base[t * H + h]
+    const float *gpc;
+    int gpc_logits;
+    const float *A_log, *dt_bias;
+    const float *beta_base;
 };
 
 // Launch `kernel` on `s`; with pdl the launch may overlap the previous kernel
