@@ -760,11 +760,12 @@ int gdn_gated_delta_dense(const void *q, const void *k, const void *v, const flo
                         gate_per_channel, scale, dtype, stream);
 }
 
-// Workspace of the dense call's chunked route: header, order, offsets, packed
-// rows y [B S, 3 H n] bf16, log gates [B S, H], a zero initial state and a
-// final-state scratch [B, H, n, n] (for NULL state_init / state_fin).
+// Workspace of the dense call's chunked route: header, order, offsets, the
+// three operand maps (q, k, v read in place), log gates [B S, H], a zero
+// initial state and a final-state scratch [B, H, n, n] (for NULL state_init /
+// state_fin).
 struct DenseWs {
-    size_t header, order, offsets, y, a, zero, fin, total;
+    size_t header, order, offsets, maps, a, zero, fin, total;
 };
 static DenseWs dense_ws_layout(int B, int S, int H, int n) {
     DenseWs l;
@@ -773,7 +774,7 @@ static DenseWs dense_ws_layout(int B, int S, int H, int n) {
     l.header = off; off += align256(sizeof(WsHeader));
     l.order = off; off += align256((size_t)B * 4);
     l.offsets = off; off += align256((size_t)(B + 1) * 4);
-    l.y = off; off += align256(N * 3 * H * n * 2);
+    l.maps = off; off += align256(3 * sizeof(CUtensorMap));
     l.a = off; off += align256(N * H * 4);
     l.zero = off; off += align256(st);
     l.fin = off; off += align256(st);
@@ -817,16 +818,24 @@ int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const 
     }
     float *sf = state_fin ? state_fin : reinterpret_cast<float *>(ws + lay.fin);
     DensePack pk{};
-    pk.q = q; pk.k = k; pk.v = v; pk.g = g;
-    pk.y = ws + lay.y; pk.a = reinterpret_cast<float *>(ws + lay.a);
+    pk.g = g;
+    pk.a = reinterpret_cast<float *>(ws + lay.a);
     pk.offsets = reinterpret_cast<int32_t *>(ws + lay.offsets);
     pk.order = reinterpret_cast<int32_t *>(ws + lay.order);
     pk.header = reinterpret_cast<WsHeader *>(ws + lay.header);
     pk.B = B; pk.S = S; pk.H = H; pk.n = n;
+    // q, k, v are read in place by the chunked kernel: one operand map each
+    const long N = (long)B * S;
+    if (!encode_operand_map(&pk.maps[0], q, N, (long)H * n) ||
+        !encode_operand_map(&pk.maps[1], k, N, (long)H * n) ||
+        !encode_operand_map(&pk.maps[2], v, N, (long)H * n))
+        return fail(GDN_ERR_CUDA, "dense: encoding the q, k, v tensor maps failed");
+    pk.maps_dst = ws + lay.maps;
     cudaError_t e = launch_dense_pack(pk, st);
     if (e != cudaSuccess) return cuda_fail(e, "dense pack kernel launch");
     ChunkLaunch cl{};
-    cl.y = pk.y; cl.a = pk.a; cl.bl = beta; cl.A_log = nullptr; cl.dt_bias = nullptr;
+    cl.y = nullptr; cl.gmaps = ws + lay.maps;
+    cl.a = pk.a; cl.bl = beta; cl.A_log = nullptr; cl.dt_bias = nullptr;
     cl.offsets = pk.offsets; cl.seq_order = pk.order; cl.header = pk.header;
     cl.state_init = s0; cl.state_fin = sf; cl.out = out;
     cl.B = B; cl.N = B * S; cl.H = H; cl.HQ = H; cl.V = n; cl.W = 3 * H * n;

@@ -108,6 +108,9 @@ struct ChunkParams {
     unsigned int *counter;        // work counter of this launch
     float *seg_M, *seg_L;  // [phase-1 segment][H][128][128], [phase-1 segment][H][V][128]
     const float *seg_S;    // [segment][H][V][128]: start states of the segments
+    // Dense layout (DENSE3 kernels): three tensor maps in global memory over
+    // q, k and v [B S, H n] (written by the packing kernel); key head = value head.
+    const CUtensorMap *gmaps;
 };
 
 // Segment length of a sequence of len tokens cut into at most nseg segments
@@ -247,6 +250,10 @@ __device__ __forceinline__ void store_tw_tb(unsigned char *tw, unsigned char *tb
     *reinterpret_cast<uint32_t *>(tb + sw128_offset(r0 + 8, c)) = pack_bf16(d[2] * be.x, d[3] * be.y);
 }
 
+// DENSE3: the q, k, v tiles come from three tensor maps in global memory
+// (p.gmaps) over the dense layout's separate q, k, v tensors instead of the
+// packed conv output (ymap).
+template <bool DENSE3>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     chunked_delta_kernel(const __grid_constant__ CUtensorMap ymap,
                          const __grid_constant__ CUtensorMap omap, const ChunkParams p) {
@@ -295,6 +302,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     // everything below reads what the conv kernel wrote
     pdl_wait_primary();
+    if constexpr (DENSE3) {
+        if (tid == 0)
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                tensormap_acquire(p.gmaps + m);
+                tma_prefetch_desc(p.gmaps + m);
+            }
+    }
 
     const int H = p.H, HQ = p.HQ, V = p.V;
     const int G = H / HQ;
@@ -364,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
             }
         }
-        int s, e;
-        if (!seq_bounds(p.offsets, p.B, p.N, seq, s, e)) {
+        int s = p.offsets[seq], e = p.offsets[seq + 1];
+        if (s < 0 || e < s || e > p.N) {
             // malformed offsets (the schedule lists no unit then; this guard
             // keeps every load and store inside [0, N) regardless)
             __syncthreads();  // every thread has read s_unit before thread 0 rewrites it
@@ -424,12 +439,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             unsigned char *base = sm + kOffStage;
             const int t0 = s + n * kC;
             mbar_arrive_expect_tx(&bar_full[0], kStageBytes);
-            tma_load_2d(base + 0, &ymap, &bar_full[0], kcol, t0);
-            tma_load_2d(base + 8192, &ymap, &bar_full[0], qcol, t0);
-            tma_load_2d(base + 16384, &ymap, &bar_full[0], kcol + 64, t0);
-            tma_load_2d(base + 24576, &ymap, &bar_full[0], qcol + 64, t0);
-            tma_load_2d(base + 32768, &ymap, &bar_full[0], vcol, t0);
-            tma_load_2d(base + 40960, &ymap, &bar_full[0], vcol + 64, t0);
+            if constexpr (DENSE3) {  // q, k, v [B S, H n] with n = 128: head h at column 128 h
+                const CUtensorMap *qm = p.gmaps, *km = p.gmaps + 1, *vm = p.gmaps + 2;
+                const int c = h * 128;
+                tma_load_2d(base + 0, km, &bar_full[0], c, t0);
+                tma_load_2d(base + 8192, qm, &bar_full[0], c, t0);
+                tma_load_2d(base + 16384, km, &bar_full[0], c + 64, t0);
+                tma_load_2d(base + 24576, qm, &bar_full[0], c + 64, t0);
+                tma_load_2d(base + 32768, vm, &bar_full[0], c, t0);
+                tma_load_2d(base + 40960, vm, &bar_full[0], c + 64, t0);
+            } else {
+                tma_load_2d(base + 0, &ymap, &bar_full[0], kcol, t0);
+                tma_load_2d(base + 8192, &ymap, &bar_full[0], qcol, t0);
+                tma_load_2d(base + 16384, &ymap, &bar_full[0], kcol + 64, t0);
+                tma_load_2d(base + 24576, &ymap, &bar_full[0], qcol + 64, t0);
+                tma_load_2d(base + 32768, &ymap, &bar_full[0], vcol, t0);
+                tma_load_2d(base + 40960, &ymap, &bar_full[0], vcol + 64, t0);
+            }
         };
         if (tid == 0) issue_tma(0);
         // gates of chunk 0 (threads 0..63); later chunks' gates are computed
@@ -903,17 +929,33 @@ bool chunked_supported(int dtype, int K, int V, int W) {
 
 namespace {
 
+}  // namespace
+
+// Operand map of a bf16 row-major matrix [rows, cols] read in [64 x 64]
+// tiles with the 128-byte swizzle the chunked kernel's MMA descriptors expect.
+bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 // Tensor maps and kernel parameters of a chunked launch.
 cudaError_t chunk_setup(const ChunkLaunch &c, CUtensorMap &map, CUtensorMap &omap, ChunkParams &p) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)c.W, (cuuint64_t)(c.N > 0 ? c.N : 1)};
-    const cuuint64_t strides[1] = {(cuuint64_t)c.W * 2};
-    const cuuint32_t box[2] = {64, 64};
     const cuuint32_t es[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(c.y), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    // the packed conv output [N, W]; with the dense layout (c.gmaps) the kernel
+    // reads its three maps from global memory and this parameter is unused
+    if (c.gmaps == nullptr ? !encode_operand_map(&map, c.y, c.N, c.W)
+                           : !encode_operand_map(&map, c.out, c.N, (long)c.H * c.V))
         return cudaErrorInvalidValue;
     // output tiles [64 t][128 vi] of out viewed as [N, H V] (no swizzle)
     int tma_store = 0;
@@ -936,10 +978,14 @@ cudaError_t chunk_setup(const ChunkLaunch &c, CUtensorMap &map, CUtensorMap &oma
     p.tma_store = tma_store;
     p.opts = c.opts;
     p.counter = &c.header->next_unit;
+    p.gmaps = static_cast<const CUtensorMap *>(c.gmaps);
     static std::atomic<uint64_t> attr_set{0};
     return once_per_device(attr_set, [] {
-        return cudaFuncSetAttribute(chunked_delta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(chunked_delta_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(chunked_delta_kernel<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     });
 }
 
@@ -948,8 +994,11 @@ cudaError_t chunk_launch(const CUtensorMap &map, const CUtensorMap &omap, const 
     const long slots = (long)sm_count() * kCtasPerSm;
     const int grid = (int)(units < slots ? units : slots);
     if (grid <= 0) return cudaSuccess;
-    cudaError_t e = launch_kernel(chunked_delta_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s,
-                                  true, map, omap, p);
+    cudaError_t e = p.gmaps != nullptr
+                        ? launch_kernel(chunked_delta_kernel<true>, dim3(grid), dim3(kThreads),
+                                        kSmemBytes, s, true, map, omap, p)
+                        : launch_kernel(chunked_delta_kernel<false>, dim3(grid), dim3(kThreads),
+                                        kSmemBytes, s, true, map, omap, p);
     note_launch();
     return e;
 }

@@ -14,6 +14,7 @@
 // in registers for the whole sequence (16 fp32 per lane, n/16 lanes a row);
 // the two dot products of a token are reduced by one xor-shuffle tree.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace gdn {
 
@@ -172,21 +173,20 @@ cudaError_t launch_dense_t(const DenseParams &p, cudaStream_t s) {
     return launch_dense_kp<T, 256, 4>(p, s);
 }
 
-// Packs the dense layout for the chunked kernel (see DensePack): 16-byte
-// copies of the q, k, v rows, the log gates, and block 0 writes the schedule.
-__global__ void __launch_bounds__(256) dense_pack_kernel(const DensePack p) {
+// Prepares the dense layout for the chunked kernel (see DensePack): the log
+// gates, and block 0 copies the three operand maps to global memory and writes
+// the schedule.
+__global__ void __launch_bounds__(256) dense_pack_kernel(const __grid_constant__ DensePack p) {
     const long N = (long)p.B * p.S;
-    const long seg = (long)p.H * p.n / 8;  // 16-byte vectors per q, k or v row
     const long stride = (long)gridDim.x * blockDim.x;
     const long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    for (long i = i0; i < N * 3 * seg; i += stride) {
-        const long t = i / (3 * seg), j = i % (3 * seg);
-        const int part = (int)(j / seg);
-        const uint4 *src = static_cast<const uint4 *>(part == 0 ? p.q : part == 1 ? p.k : p.v);
-        static_cast<uint4 *>(p.y)[t * 3 * seg + j] = __ldg(src + t * seg + j % seg);
-    }
     for (long i = i0; i < N * p.H; i += stride) p.a[i] = logf(fmaxf(__ldg(p.g + i), 1e-30f));
     if (blockIdx.x == 0) {
+        // 3 maps x 128 bytes as 8-byte words
+        const uint64_t *src = reinterpret_cast<const uint64_t *>(p.maps);
+        uint64_t *dst = static_cast<uint64_t *>(p.maps_dst);
+        if (threadIdx.x < 3 * sizeof(CUtensorMap) / 8) dst[threadIdx.x] = src[threadIdx.x];
+        sm100::tensormap_release();
         for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.offsets[i] = i * p.S;
         for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.order[i] = i;
         if (threadIdx.x == 0) {
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(256) dense_pack_kernel(const DensePack p) {
 }  // namespace
 
 cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s) {
-    const long work = (long)p.B * p.S * 3 * p.H * p.n / 8;
+    const long work = (long)p.B * p.S * p.H;
     long blocks = (work + 255) / 256;
     blocks = blocks < 1 ? 1 : (blocks > 4L * 152 * 8 ? 4L * 152 * 8 : blocks);
     dense_pack_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);

@@ -2,6 +2,7 @@
 // kernel launchers (*.cu).  Not installed; the public ABI is include/gdn.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -162,7 +163,13 @@ struct ChunkLaunch {
     int nseq_seg;
     int seg_seq[kMaxSegSeqs], seg_m0[kMaxSegSeqs + 1], seg_s0[kMaxSegSeqs + 1];
     float *seg_M, *seg_L, *seg_S;
+    // dense layout: three CUtensorMaps (q, k, v [N, H V], bf16, see
+    // encode_operand_map) in global memory, 64-byte aligned; y is unused then
+    const void *gmaps = nullptr;
 };
+// Tensor map of a bf16 row-major [rows, cols] operand in the chunked kernel's
+// tile format (64 x 64 boxes, 128-byte swizzle); false if encoding fails.
+bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols);
 // Segment buffers: up to kMaxSegments segments of up to kMaxSegSeqs sequences.
 inline size_t segment_m_floats(int H) { return (size_t)(kMaxSegments - 1) * H * 128 * 128; }
 inline size_t segment_l_floats(int H, int V) { return (size_t)(kMaxSegments - 1) * H * V * 128; }
@@ -184,18 +191,20 @@ struct DenseParams {
 };
 cudaError_t launch_delta_dense(const DenseParams &p, int dtype, cudaStream_t s);
 
-// Dense layout -> the chunked kernel's packed inputs (bf16, scalar gate): the
-// rows [q | k | v] of every token into y [B S, 3 H n], a = ln(max(g, 1e-30))
-// [B S, H] (the kernel's exp gate), offsets i S, the sequence order and the
-// workspace header for B H (n / 128) units.
+// Dense layout -> the chunked kernel's inputs (bf16, scalar gate, n = 128): the
+// kernel reads q, k and v in place through three tensor maps that this step
+// copies to global memory; it also writes a = ln(max(g, 1e-30)) [B S, H] (the
+// kernel's exp gate), offsets i S, the sequence order and the workspace header
+// for B H (n / 128) units.
 struct DensePack {
-    const void *q, *k, *v;
     const float *g;
-    void *y;
     float *a;
     int32_t *offsets, *order;
     WsHeader *header;
     int B, S, H, n;
+    // the q, k, v operand maps, copied to maps_dst (global, 64-byte aligned)
+    CUtensorMap maps[3];
+    void *maps_dst;
 };
 cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
 

@@ -88,6 +88,18 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Before a tensor map that an earlier kernel wrote to global memory with
+// ordinary stores is used by TMA: make those stores visible to the tensor-map
+// proxy (the writer's kernel has completed).
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                     reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+__device__ __forceinline__ void tensormap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
