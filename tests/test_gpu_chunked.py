@@ -185,3 +185,27 @@ def test_segment_parallel_in_place_carry(lens):
     torch.cuda.synchronize()
     assert sfin.data_ptr() == st.data_ptr()
     assert rel_l2(cpu64(out), ref[0]) <= TOL and rel_l2(cpu64(sfin), ref[2]) <= TOL
+
+
+@pytest.mark.parametrize("B", [1000, 4096])
+def test_device_schedule_lists_chunked_sequences_longest_first(B):
+    """The conv pass's block 0 orders the chunked sequences longest first (ties by
+    index) with a bitonic sort, for up to 4096 of them, from the device offsets
+    alone; the order sits in the workspace right after its 256-byte header.  The
+    results match the token-serial route."""
+    g = torch.Generator().manual_seed(B)
+    lens = torch.randint(1, 141, (B,), generator=g).tolist()
+    wl, d = _case(tuple(lens), HQ=1, H=2)
+    ws = torch.zeros(gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D),
+                     dtype=torch.uint8, device=DEV)
+    out, cfin, sfin = run_layer(wl, d, workspace=ws)
+    status, counts = gdn.gdn_workspace_status(ws)
+    chunked = [b for b in range(B) if lens[b] >= gdn.gdn_chunk_min_len()]
+    assert status == 0 and counts[1] == len(chunked) and counts[2] == len(chunked) * wl.H
+    order = ws[256:256 + 4 * len(chunked)].view(torch.int32).cpu().tolist()
+    assert order == sorted(chunked, key=lambda b: (-lens[b], b))
+    with chunk_threshold(SERIAL_ONLY):
+        o2, c2, s2 = run_layer(wl, d)
+    torch.cuda.synchronize()
+    assert torch.equal(cfin, c2)
+    assert rel_l2(cpu64(out), cpu64(o2)) <= TOL and rel_l2(cpu64(sfin), cpu64(s2)) <= TOL

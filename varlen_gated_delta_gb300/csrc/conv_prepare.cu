@@ -109,11 +109,14 @@ __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, fl
 // Block 0 of the conv launch checks the whole offsets array, records the
 // status and the serial / chunked sequence counts in the workspace header
 // and, when asked, schedules the chunked work: the sequences of at least
-// chunk_min_len tokens are listed longest first (by rank, for up to 1024
-// sequences; in index order beyond that) and the work counter is reset.
-__device__ void schedule_block(const ConvParams &p) {
+// chunk_min_len tokens are listed longest first (ties by index) and the work
+// counter is reset.  The order comes from a bitonic sort of the keys
+// (~len << 32 | index) in `keys`, the first kSortKeys * 8 bytes of the
+// block's dynamic shared memory (used before the block's own conv work); with
+// more chunked sequences than that they are listed in index order.
+constexpr int kSortKeys = 4096;
+__device__ void schedule_block(const ConvParams &p, unsigned long long *keys) {
     __shared__ int s_bad, s_serial, s_chunked, s_base;
-    __shared__ int s_lens[1024];
     __shared__ int s_warp[kConvThreads / 32];
     const int B = p.B;
     if (threadIdx.x == 0) {
@@ -129,28 +132,61 @@ __device__ void schedule_block(const ConvParams &p) {
         if (len < 0) bad = 1;
         else if (len >= p.chunk_min_len) ++nc;
         else ++ns;
-        if (B <= 1024) s_lens[b] = len;
     }
     if (bad) atomicOr(&s_bad, 1);
     atomicAdd(&s_serial, ns);
     atomicAdd(&s_chunked, nc);
     __syncthreads();
     const bool ok = !s_bad;
+    const int nchunked = s_chunked;
     if (p.seq_order != nullptr && ok) {
         const int thr = p.chunk_min_len;
-        if (B <= 1024) {
-            for (int b = threadIdx.x; b < B; b += blockDim.x) {
-                const int len = s_lens[b];
-                if (len < thr) continue;
-                int rank = 0;
-                for (int o = 0; o < B; ++o) {
-                    const int lo = s_lens[o];
-                    rank += (lo >= thr) && (lo > len || (lo == len && o < b));
-                }
-                p.seq_order[rank] = b;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        if (nchunked <= kSortKeys) {
+            // keys of the chunked sequences, padded to a power of two with the
+            // largest key (they sort last and are not listed)
+            int P = 1;
+            while (P < nchunked) P <<= 1;
+            for (int i = threadIdx.x; i < P; i += blockDim.x) keys[i] = ~0ull;
+            __syncthreads();
+            if (threadIdx.x == 0) s_base = 0;
+            __syncthreads();
+            for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+                const int b = b0 + threadIdx.x;
+                const int len = b < B ? __ldg(p.offsets + b + 1) - __ldg(p.offsets + b) : 0;
+                const bool take = b < B && len >= thr;
+                const unsigned m = __ballot_sync(0xffffffffu, take);
+                if (lane == 0) s_warp[warp] = __popc(m);
+                __syncthreads();
+                int before = s_base;
+                for (int w = 0; w < warp; ++w) before += s_warp[w];
+                if (take)
+                    keys[before + __popc(m & ((1u << lane) - 1u))] =
+                        ((unsigned long long)(~(unsigned)len) << 32) | (unsigned)b;
+                __syncthreads();
+                if (threadIdx.x == 0)
+                    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s_base += s_warp[w];
+                __syncthreads();
             }
+            // bitonic sort, ascending: longest first, then lower index
+            for (int k = 2; k <= P; k <<= 1) {
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+                        const int l = i ^ j;
+                        if (l > i) {
+                            const unsigned long long x = keys[i], y = keys[l];
+                            if (((i & k) == 0) == (x > y)) {
+                                keys[i] = y;
+                                keys[l] = x;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            for (int i = threadIdx.x; i < nchunked; i += blockDim.x)
+                p.seq_order[i] = (int)(keys[i] & 0xffffffffu);
         } else {
-            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
             for (int b0 = 0; b0 < B; b0 += blockDim.x) {
                 const int b = b0 + threadIdx.x;
                 const bool take = b < B && (__ldg(p.offsets + b + 1) - __ldg(p.offsets + b)) >= thr;
@@ -170,12 +206,13 @@ __device__ void schedule_block(const ConvParams &p) {
     if (threadIdx.x == 0) {
         p.header->status = ok ? 0 : 4 /* GDN_ERR_OFFSETS */;
         p.header->n_serial = ok ? s_serial : 0;
-        p.header->n_chunked = ok ? s_chunked : 0;
-        p.header->n_units = (ok && p.seq_order != nullptr) ? s_chunked * p.H * p.VT : 0;
+        p.header->n_chunked = ok ? nchunked : 0;
+        p.header->n_units = (ok && p.seq_order != nullptr) ? nchunked * p.H * p.VT : 0;
         p.header->next_unit = 0;
         p.header->seg_next[0] = 0;
         p.header->seg_next[1] = 0;
     }
+    __syncthreads();  // the keys' shared memory is the block's conv scratch next
 }
 
 // Dynamic shared memory: [Kc][CT] f32 weights (KC == 0 only) | [TT+L][CT] T
@@ -206,7 +243,8 @@ __global__ void __launch_bounds__(kConvThreads)
     // The dependent kernel (recurrence / final state) may start streaming its
     // own inputs now; it waits for this grid before reading what it writes.
     pdl_launch_dependents();
-    if (p.header != nullptr && blockIdx.x == 0) schedule_block(p);
+    if (p.header != nullptr && blockIdx.x == 0)
+        schedule_block(p, reinterpret_cast<unsigned long long *>(smem));
 
     // 1. token -> sequence (or -1 when the token's sequence is malformed); the
     //    search runs in shared memory when the offsets fit there
@@ -396,6 +434,8 @@ __global__ void __launch_bounds__(kConvThreads)
 // the window is refilled from that sequence's initial conv state.
 constexpr int kRing = 8;
 constexpr int kRingBytes = (kConvThreads / 32) * kRing * 512;  // 32 lanes x 16 bytes per row
+static_assert(kRingBytes >= kSortKeys * (int)sizeof(unsigned long long),
+              "block 0 sorts the schedule keys in the ring's shared memory");
 
 template <typename T, int VEC, bool PREP, int KC, int D>
 __global__ void __launch_bounds__(kConvThreads, 2)
@@ -410,7 +450,8 @@ __global__ void __launch_bounds__(kConvThreads, 2)
     int *s_offs = reinterpret_cast<int *>(conv_dsm + kRingBytes);
 
     pdl_launch_dependents();
-    if (p.header != nullptr && blockIdx.x == 0) schedule_block(p);
+    if (p.header != nullptr && blockIdx.x == 0)
+        schedule_block(p, reinterpret_cast<unsigned long long *>(conv_dsm));
 
     const int B = p.B, N = p.N, C = p.C;
     const bool cache_offs = B + 1 <= kOffsetsCache;
@@ -766,7 +807,10 @@ cudaError_t launch_conv_kc(const ConvParams &p, cudaStream_t s) {
     const size_t window = (size_t)(TT + p.L) * CT * sizeof(T);
     const bool stage = window <= 64 * 1024;
     const size_t offs_bytes = p.B + 1 <= kOffsetsCache ? sizeof(int) * (p.B + 1) : 0;
-    const size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT + offs_bytes;
+    size_t smem = wbytes + (stage ? window : 0) + 3 * sizeof(int) * TT + offs_bytes;
+    // block 0 sorts the chunked sequences in the same shared memory first
+    if (p.header != nullptr && p.seq_order != nullptr && smem < kSortKeys * sizeof(unsigned long long))
+        smem = kSortKeys * sizeof(unsigned long long);
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     auto kern = stage ? conv_prepare_kernel<T, VEC, PREP, true, KC>
                       : conv_prepare_kernel<T, VEC, PREP, false, KC>;
