@@ -209,3 +209,50 @@ def test_device_schedule_lists_chunked_sequences_longest_first(B):
     torch.cuda.synchronize()
     assert torch.equal(cfin, c2)
     assert rel_l2(cpu64(out), cpu64(o2)) <= TOL and rel_l2(cpu64(sfin), cpu64(s2)) <= TOL
+
+
+def _mixed_case():
+    # two chunked sequences (8 units) beside short token-serial ones: free CTA
+    # slots, so the token-serial kernel runs beside the chunked kernel
+    lens = (700, 5, 1, 0, 1300, 33, 17, 1, 63, 2)
+    return _case(lens, HQ=2, H=4)
+
+
+def test_token_serial_beside_chunked_equals_the_sequential_route():
+    """With host offsets the token-serial kernel runs on a side stream beside the
+    chunked kernel; without them it runs after it.  Same kernels, disjoint
+    outputs: the results are bit-identical, and match the oracle."""
+    wl, d = _mixed_case()
+    beside = run_layer(wl, d, offsets_host=d["offsets_list"])
+    after = run_layer(wl, d)
+    torch.cuda.synchronize()
+    for x, y in zip(beside, after):
+        assert torch.equal(x, y)
+    _check(wl, d, *beside)
+
+
+def test_token_serial_beside_chunked_in_place_and_in_a_cuda_graph():
+    wl, d = _mixed_case()
+    ref = run_layer(wl, d)
+    st, cs = d["state_init"].clone(), d["conv_init"].clone()
+    out = torch.empty_like(ref[0])
+    ws = torch.empty(gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D),
+                     dtype=torch.uint8, device=DEV)
+    args = dict(offsets_host=d["offsets_list"], out=out, state_fin=st, conv_fin=cs, workspace=ws)
+    dd = dict(d, state_init=st, conv_init=cs)
+    run_layer(wl, dd, **args)                       # eager, in place
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref[0]) and torch.equal(st, ref[2]) and torch.equal(cs, ref[1])
+    # the same call captured once and replayed from the initial states
+    st.copy_(d["state_init"])
+    cs.copy_(d["conv_init"])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_layer(wl, dd, **args)
+    st.copy_(d["state_init"])
+    cs.copy_(d["conv_init"])
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref[0]) and torch.equal(st, ref[2]) and torch.equal(cs, ref[1])

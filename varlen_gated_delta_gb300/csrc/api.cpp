@@ -13,6 +13,7 @@
 
 #include <atomic>
 #include <climits>
+#include <mutex>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -100,6 +101,38 @@ static int sm_count_host() {
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Side stream on which the token-serial kernel runs beside the chunked kernel
+// of the same layer call, and the two events that fork it from and join it
+// to the caller's stream.  One set per device, created by the first call that
+// forks (make that call before any stream capture); calls from several host
+// threads take turns on it under a mutex, so each call's dependencies stay
+// exact (a wait on an event takes the record enqueued just before it).
+struct ForkSet {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+static std::mutex g_fork_mu;
+static ForkSet g_fork[64];
+
+static cudaError_t fork_set(ForkSet **out) {  // g_fork_mu held
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    ForkSet &f = g_fork[dev];
+    if (f.side == nullptr) {
+        e = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            f = ForkSet{};
+            return e;
+        }
+    }
+    *out = &f;
+    return cudaSuccess;
+}
 
 static bool dtype_ok(int dtype) { return dtype == GDN_F32 || dtype == GDN_BF16; }
 static size_t dsize(int dtype) { return dtype == GDN_BF16 ? 2 : 4; }
@@ -670,6 +703,36 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     // of chunked sequences from their initial state, so it runs before the
     // chunked kernel (which may overwrite that state in place).
     const bool serial_first = capsule && run_chunked;
+    // With CTA slots left free by the chunked units, the token-serial kernel
+    // (short sequences, and the final conv state of all) runs beside the
+    // chunked kernel on a side stream: both read only what the conv pass wrote
+    // and write disjoint outputs.
+    int n_serial_host = 0;
+    if (offsets_host)
+        for (int i = 0; i < B; ++i) {
+            const int len = offsets_host[i + 1] - offsets_host[i];
+            n_serial_host += len > 0 && len < serial_max;
+        }
+    if (run_chunked && !serial_first && seg.n == 0 && n_serial_host > 0 &&
+        max_units < 2L * sm_count_host()) {
+        std::lock_guard<std::mutex> lock(g_fork_mu);
+        ForkSet *f = nullptr;
+        e = fork_set(&f);
+        if (e == cudaSuccess) e = cudaEventRecord(f->fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(f->side, f->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "forking the token-serial kernel");
+        mark_before(GDN_KERNEL_SERIAL, f->side);
+        e = launch_delta_serial(dp, dtype, f->side, /*pdl=*/false);
+        mark_after(GDN_KERNEL_SERIAL, f->side);
+        if (e != cudaSuccess) return cuda_fail(e, "delta kernel launch");
+        e = cudaEventRecord(f->join, f->side);
+        if (e != cudaSuccess) return cuda_fail(e, "joining the token-serial kernel");
+        rc = launch_chunked();
+        e = cudaStreamWaitEvent(s, f->join, 0);  // joined even if the chunked launch failed
+        if (rc) return rc;
+        if (e != cudaSuccess) return cuda_fail(e, "joining the token-serial kernel");
+        return GDN_OK;
+    }
     if (run_chunked && !serial_first) {
         rc = launch_chunked();
         if (rc) return rc;
