@@ -187,7 +187,7 @@ GDN_API int gdn_workspace_status(const void *workspace, int *counts, void *strea
 /*
  * Length threshold (tokens) from which a sequence takes the chunked kernel.
  * gdn_set_chunk_min_len(n): n > 0 sets it, n == 0 restores the default
- * (environment variable GDN_CHUNK_MIN_LEN if set, else 64); a very large n
+ * (environment variable GDN_CHUNK_MIN_LEN if set, else 8); a very large n
  * keeps every sequence on the token-serial kernel.  Process-wide setting.
  */
 GDN_API int gdn_set_chunk_min_len(int n);

@@ -310,11 +310,13 @@ def test_segment_plan_invariants_on_random_batches():
     """Random batches: every plan fits one wave of CTA slots in both passes,
     gives no sequence more than 8 segments, cuts every segmented sequence into
     exactly its count of non-empty whole-chunk segments, and only segments
-    when every chunked sequence is long and there are at most four."""
+    when every sequence of at least one chunk (64 tokens, or the chunk
+    threshold if larger) is long and there are at most four; shorter
+    sequences beside segmented ones run token-serially."""
     import random
     rng = random.Random(20261203)
     plan = gdn.gdn_segment_plan
-    chunk_min = gdn.gdn_chunk_min_len()
+    chunk_min = max(gdn.gdn_chunk_min_len(), 64)
     for trial in range(300):
         min_len = rng.choice([64, 256, 1000, 4096])
         gdn.gdn_set_segment_min_len(min_len)

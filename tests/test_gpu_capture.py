@@ -85,7 +85,7 @@ def test_capture_tiny_fp32_matches_oracle_and_leaves_outputs_unchanged():
 
 @pytest.mark.parametrize("in_place", [False, True])
 def test_capture_with_chunked_sequences_bf16(in_place):
-    """Sequences of >= 64 tokens take the chunked kernel; their capsule comes
+    """Sequences of >= gdn_chunk_min_len() tokens take the chunked kernel; their capsule comes
     from a token-serial replay of the captured prefix, which must see the
     initial state even when the state is carried in place."""
     lens = (70, 5, 130, 1, 0, 64)

@@ -125,7 +125,7 @@ def test_dense_workspace_call_falls_back_to_the_serial_kernel(case):
     """Per-channel gates, sequences under the chunk threshold and n != 128 run
     the token-serial kernel even with a workspace, bit for bit as without."""
     n = 64 if case == "n64" else 128
-    S = 20 if case == "short" else 90
+    S = max(1, gdn.gdn_chunk_min_len() // 2) if case == "short" else 90
     B, H = 2, 2
     q, k, v, gate, gate_c, beta, state = _inputs(B, S, H, n, torch.bfloat16, 41)
     gg, pc = (gate_c, True) if case == "per_channel" else (gate, False)

@@ -228,21 +228,39 @@ def test_in_place_carry_equals_out_of_place():
     assert torch.equal(out, out2) and torch.equal(cfin, ci) and torch.equal(sfin, si)
 
 
-def test_split_sequence_resume_equals_one_call():
-    wl, d = _bf16_case(lens=(50,))
-    out, cfin, sfin = run_layer(wl, d)
-    cut = 23
+def _split_resume(wl, d, n, cut):
     part = lambda t, a, b: t[a:b].contiguous()
     d1 = dict(d, qkv=part(d["qkv"], 0, cut), a=part(d["a"], 0, cut), b=part(d["b"], 0, cut),
               offsets=torch.tensor([0, cut], dtype=torch.int32, device=DEV))
     o1, c1, s1 = run_layer(wl, d1)
-    d2 = dict(d, qkv=part(d["qkv"], cut, 50), a=part(d["a"], cut, 50), b=part(d["b"], cut, 50),
-              offsets=torch.tensor([0, 50 - cut], dtype=torch.int32, device=DEV),
+    d2 = dict(d, qkv=part(d["qkv"], cut, n), a=part(d["a"], cut, n), b=part(d["b"], cut, n),
+              offsets=torch.tensor([0, n - cut], dtype=torch.int32, device=DEV),
               conv_init=c1, state_init=s1)
     o2, c2, s2 = run_layer(wl, d2)
     torch.cuda.synchronize()
-    assert torch.equal(torch.cat([o1, o2]), out)
+    return torch.cat([o1, o2]), c2, s2
+
+
+def test_split_sequence_resume_equals_one_call():
+    """Token-serial: bit for bit (the same per-token arithmetic either way)."""
+    wl, d = _bf16_case(lens=(50,))
+    with chunk_threshold(SERIAL_ONLY):
+        out, cfin, sfin = run_layer(wl, d)
+        o, c2, s2 = _split_resume(wl, d, 50, 23)
+    assert torch.equal(o, out)
     assert torch.equal(c2, cfin) and torch.equal(s2, sfin)
+
+
+def test_split_sequence_resume_on_the_chunked_kernel():
+    """Chunked: the conv state carries bit for bit; the chunk boundaries move, so
+    outputs and states agree to the bf16 tolerance (and with the oracle)."""
+    wl, d = _bf16_case(lens=(300,))
+    out, cfin, sfin = run_layer(wl, d)
+    o, c2, s2 = _split_resume(wl, d, 300, 101)
+    assert torch.equal(c2, cfin)
+    assert rel_l2(cpu64(o), cpu64(out)) <= TOL["bf16"]
+    assert rel_l2(cpu64(s2), cpu64(sfin)) <= TOL["bf16"]
+    check_layer(wl, d, o, c2, s2)
 
 
 def test_packed_equals_each_sequence_alone_bitwise():

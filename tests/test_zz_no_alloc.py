@@ -78,10 +78,10 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
 
 def test_noalloc_chunked_batch_after_decode(lib):
     """A batch with a 300-token sequence (the chunked tensor-core kernel, its
-    work counters and schedule live in the static array) and a 40-token one
+    work counters and schedule live in the static array) and a 5-token one
     (token-serial), after the decode calls above: under the 16 MiB limit at
     the decode head geometry."""
-    wl = W.scaled(W.WORKLOADS["decode"], (40, 300), name="noalloc-chunked")
+    wl = W.scaled(W.WORKLOADS["decode"], (5, 300), name="noalloc-chunked")
     need = gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D)
     assert need <= 16 * 1024 * 1024
     _compare_two_calls(lib, wl, W.make_inputs(wl, DEV))
