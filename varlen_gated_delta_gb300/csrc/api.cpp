@@ -112,9 +112,10 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Side stream on which the token-serial kernel runs beside the chunked kernel
 // of the same layer call, and the two events that fork it from and join it
 // to the caller's stream.  One set per device, created by the first call that
-// forks (make that call before any stream capture); calls from several host
-// threads take turns on it under a mutex, so each call's dependencies stay
-// exact (a wait on an event takes the record enqueued just before it).
+// would fork outside a stream capture (captured calls before that run the two
+// kernels one after the other); calls from several host threads take turns on
+// it under a mutex, so each call's dependencies stay exact (a wait on an event
+// takes the record enqueued just before it).
 struct ForkSet {
     cudaStream_t side = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
@@ -122,13 +123,18 @@ struct ForkSet {
 static std::mutex g_fork_mu;
 static ForkSet g_fork[64];
 
-static cudaError_t fork_set(ForkSet **out) {  // g_fork_mu held
+// The set of the current device (g_fork_mu held); created on first use, but
+// not while `s` is being captured (then cudaErrorNotReady: no fork).
+static cudaError_t fork_set(ForkSet **out, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     ForkSet &f = g_fork[dev];
     if (f.side == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return cudaErrorNotReady;
         e = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming);
@@ -557,7 +563,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
                       void *conv_fin, const float *state_init, void *out, float *state_fin,
                       int B, int N, int H, int HQ, int K, int V, int Kc, int D, int act,
                       float scale, int dtype, void *workspace, size_t ws_bytes, void *stream,
-                      const Capture *cap, int opts = 0) {
+                      const Capture *cap, int opts = 0, bool allow_fork = true) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
     if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return fail(GDN_ERR_UNSUPPORTED, "activation %d not supported", act);
     long width;
@@ -727,12 +733,18 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
             const int len = offsets_host[i + 1] - offsets_host[i];
             n_serial_host += len > 0 && len < serial_max;
         }
-    if (run_chunked && !serial_first && seg.n == 0 && n_serial_host > 0 &&
+    ForkSet *f = nullptr;
+    std::unique_lock<std::mutex> fork_lock(g_fork_mu, std::defer_lock);
+    if (allow_fork && run_chunked && !serial_first && seg.n == 0 && n_serial_host > 0 &&
         max_units < 2L * sm_count_host()) {
-        std::lock_guard<std::mutex> lock(g_fork_mu);
-        ForkSet *f = nullptr;
-        e = fork_set(&f);
-        if (e == cudaSuccess) e = cudaEventRecord(f->fork, s);
+        fork_lock.lock();
+        if (fork_set(&f, s) != cudaSuccess) {  // not available: one after the other
+            f = nullptr;
+            fork_lock.unlock();
+        }
+    }
+    if (f != nullptr) {
+        e = cudaEventRecord(f->fork, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(f->side, f->fork, 0);
         if (e != cudaSuccess) return cuda_fail(e, "forking the token-serial kernel");
         mark_before(GDN_KERNEL_SERIAL, f->side);
@@ -761,6 +773,26 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     }
     return GDN_OK;
 }
+
+}  // extern "C"
+
+namespace gdn {
+// The layer call without the side-stream fork (creates no stream or event).
+int layer_varlen_nofork(const void *qkv, const void *w, const void *bias, const float *a,
+                        const float *b, const float *A_log, const float *dt_bias,
+                        const int32_t *offsets, const int32_t *offsets_host,
+                        const void *conv_init, void *conv_fin, const float *state_init,
+                        void *out, float *state_fin, int B, int N, int H, int HQ, int K, int V,
+                        int Kc, int D, int act, float scale, int dtype, void *workspace,
+                        size_t ws_bytes, void *stream) {
+    g_err[0] = 0;
+    return layer_impl(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
+                      conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act, scale,
+                      dtype, workspace, ws_bytes, stream, nullptr, 0, /*allow_fork=*/false);
+}
+}  // namespace gdn
+
+extern "C" {
 
 int gdn_layer_varlen(const void *qkv, const void *w, const void *bias, const float *a,
                      const float *b, const float *A_log, const float *dt_bias,

@@ -70,9 +70,9 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
 // The plain one-token (decode) variant with K = 128 is held to 80 registers so
 // that six CTAs share an SM: more state loads in flight per SM (measured on the
 // decode batch: 51.2 us a step against 52.8 us at five CTAs and 53.7 us at
-// seven, where spills grow).
+// seven, where spills grow); its per-channel-gate twin is held to four.
 template <typename T, int KP, int RG, bool VEC4, bool PF, bool CAPT, bool PC = false>
-__global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && !PC && KP == 128) ? 6 : 1)
+__global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? (PC ? 4 : 6) : 1)
     delta_serial_kernel(const DeltaParams p) {
     constexpr int EPL = 16;          // state values per lane per row
     constexpr int LPR = KP / EPL;    // lanes per row
@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && !PC && KP == 
     float gcv[EPL];  // per-channel gates of the lane's columns (PC)
     const float pc_dtb = PC && p.gpc_logits && p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
     const float pc_alog = PC && p.gpc_logits && p.A_log ? __ldg(p.A_log + h) : 0.f;
+    // PC with decay logits: the CTA activates each key column's gate once per
+    // token into shared memory (double-buffered by token parity) instead of
+    // every lane that holds the column doing it; every thread of the CTA walks
+    // the same tokens, so the barrier is uniform.
+    __shared__ __align__(16) float s_gate[PC ? 2 * KP : 4];
     auto fetch = [&](int t, float *q, float *k, float *v, float &g, float &beta, float *gv) {
         const float *qrow = p.qk + ((size_t)t * HQ + kh) * K;
         const float *krow = p.qk + (((size_t)N + t) * HQ + kh) * K;
@@ -198,11 +203,23 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && !PC && KP == 
         }
         if constexpr (PC) {
             const float *grow = p.gpc + ((size_t)t * H + h) * K;
+            if (p.gpc_logits) {
+                float *sg = s_gate + (t & 1) * KP;
+                for (int i = threadIdx.x; i < KP; i += blockDim.x)
+                    sg[i] = i < K ? gate_of_logit(__ldg(grow + i), pc_dtb, pc_alog, p.opts) : 0.f;
+                __syncthreads();
 #pragma unroll
-            for (int m = 0; m < 4; ++m) load4(grow, kidx[m], &gv[4 * m]);
-            if (p.gpc_logits)
+                for (int m = 0; m < 4; ++m) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(sg + kidx[m]);
+                    gv[4 * m] = g4.x;
+                    gv[4 * m + 1] = g4.y;
+                    gv[4 * m + 2] = g4.z;
+                    gv[4 * m + 3] = g4.w;
+                }
+            } else {
 #pragma unroll
-                for (int u = 0; u < EPL; ++u) gv[u] = gate_of_logit(gv[u], pc_dtb, pc_alog, p.opts);
+                for (int m = 0; m < 4; ++m) load4(grow, kidx[m], &gv[4 * m]);
+            }
             g = 1.f;
             beta = __ldg(p.beta_base + (size_t)t * H + h);
         } else {

@@ -217,6 +217,16 @@ bool conv_can_fuse_prepare(int dtype, int C, int K, const void *const *ptrs, int
 
 void note_launch(unsigned n = 1);
 
+// gdn_layer_varlen without running the token-serial kernel on a side stream
+// (so it creates no stream or event); same arguments and errors.
+int layer_varlen_nofork(const void *qkv, const void *w, const void *bias, const float *a,
+                        const float *b, const float *A_log, const float *dt_bias,
+                        const int32_t *offsets, const int32_t *offsets_host,
+                        const void *conv_init, void *conv_fin, const float *state_init,
+                        void *out, float *state_fin, int B, int N, int H, int HQ, int K, int V,
+                        int Kc, int D, int act, float scale, int dtype, void *workspace,
+                        size_t ws_bytes, void *stream);
+
 // Record a message for gdn_last_error() on this thread and return `code`.
 int set_error(int code, const char *fmt, ...);
 

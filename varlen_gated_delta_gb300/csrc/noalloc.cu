@@ -84,7 +84,9 @@ extern "C" int gdn_layer_varlen_noalloc(
     if (e != cudaSuccess)
         return gdn::set_error(GDN_ERR_CUDA, "clearing the static scratch header: %s",
                               cudaGetErrorString(e));
-    return gdn_layer_varlen(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host, conv_init,
-                            conv_fin, state_init, out, state_fin, B, N, H, HQ, K, V, Kc, D, act,
-                            scale, dtype, scratch, GDN_NOALLOC_SCRATCH_BYTES, stream);
+    // (the regular layer path, without its side stream: this call creates nothing)
+    return gdn::layer_varlen_nofork(qkv, w, bias, a, b, A_log, dt_bias, offsets, offsets_host,
+                                    conv_init, conv_fin, state_init, out, state_fin, B, N, H, HQ,
+                                    K, V, Kc, D, act, scale, dtype, scratch,
+                                    GDN_NOALLOC_SCRATCH_BYTES, stream);
 }
