@@ -256,3 +256,48 @@ def test_token_serial_beside_chunked_in_place_and_in_a_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref[0]) and torch.equal(st, ref[2]) and torch.equal(cs, ref[1])
+
+
+_FIRST_CALL_CAPTURED = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+import varlen_gated_delta_gb300 as gdn
+from varlen_gated_delta_gb300 import build, workloads as W
+build.build()
+gdn.load_library()
+lens = (700, 5, 1, 0, 1300, 33, 17, 1, 63, 2)
+wl = W.scaled(W.WORKLOADS["decode"], lens, name="first-captured", HQ=2, H=4)
+d = W.make_inputs(wl, "cuda:0")
+def run(out, st, cs, host):
+    return gdn.gdn_layer_varlen(d["qkv"], d["w"], d["bias"], d["a"], d["b"], d["A_log"],
+        d["dt_bias"], d["offsets"], d["conv_init"], d["state_init"], H=wl.H, HQ=wl.HQ, K=wl.K,
+        V=wl.V, Kc=wl.Kc, D=wl.D, scale=d["scale"], offsets_host=d["offsets_list"] if host else None,
+        out=out, state_fin=st, conv_fin=cs, workspace=ws)
+ws = torch.empty(gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D),
+                 dtype=torch.uint8, device="cuda:0")
+out = torch.empty((wl.N, wl.H, wl.V), dtype=torch.bfloat16, device="cuda:0")
+st = torch.empty_like(d["state_init"]); cs = torch.empty_like(d["conv_init"])
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g):          # the process's first call that would fork
+    run(out, st, cs, True)
+g.replay()
+torch.cuda.synchronize()
+ref = [t.clone() for t in run(torch.empty_like(out), torch.empty_like(st), torch.empty_like(cs), False)]
+torch.cuda.synchronize()
+ok = torch.equal(out, ref[0]) and torch.equal(cs, ref[1]) and torch.equal(st, ref[2])
+print("OK" if ok else "MISMATCH")
+"""
+
+
+def test_first_forking_call_inside_a_stream_capture_runs_sequentially():
+    """In a fresh process the first call that would run the token-serial kernel
+    on the side stream is made inside a CUDA-graph capture: the side stream is
+    not created there, the two kernels run one after the other, and the
+    replayed graph gives the same bits as an eager call."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_CAPTURED.format(root=root)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout + r.stderr
