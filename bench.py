@@ -50,13 +50,17 @@ def _args():
                     help="update rule (delta: no decay; gated: no retrieval; linear: neither)")
     ap.add_argument("--gate", default="scalar", choices=["scalar", "per_channel"],
                     help="per_channel: the layer with one decay logit per key channel, "
-                         "a [N, H, K] (GDN_OPT_GATE_PER_CHANNEL; token-serial kernel)")
+                         "a [N, H, K] (GDN_OPT_GATE_PER_CHANNEL)")
     ap.add_argument("--dense", default=None, choices=["scalar", "per_channel"],
                     help="time the dense-layout call (q, k, v [B, S, H, n]) on the workload's "
                          "batch and head geometry (equal lengths), scalar or per-channel gate")
     ap.add_argument("--capture", type=int, default=0,
                     help="state-update capture capacity (1..8): time gdn_layer_varlen_capture "
                          "with every sequence asking for that many tokens")
+    ap.add_argument("--chunk-min-len", type=int, default=None,
+                    help="sequences of at least this many tokens take a chunked kernel "
+                         "(gdn_set_chunk_min_len; a large value keeps every sequence "
+                         "token-serial)")
     ap.add_argument("--lens", default=None,
                     help="comma-separated sequence lengths replacing the workload's "
                          "(same head geometry and distributions; for small profiling cases)")
@@ -578,7 +582,9 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
                    "parallelism": f"replicas x{world}",
                    **({"capture": cap} if cap else {}),
                    **({"rule": args.rule} if args.rule != "gated_delta" else {}),
-                   **({"gate": "per_channel"} if args.gate == "per_channel" else {})},
+                   **({"gate": "per_channel"} if args.gate == "per_channel" else {}),
+                   **({"chunk_min_len": args.chunk_min_len}
+                      if args.chunk_min_len is not None else {})},
         "layer_gbs": algorithmic_bytes_layer(wl, N, B) / (ms * 1e-3 / args.steps) / 1e9,
         "roofline": roof,
         "e2e": {"value": _job_tokens_per_s(world, N, args.steps, e2e_ms), "unit": "tokens/s",
@@ -619,11 +625,13 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     gdn.load_library()
+    if args.chunk_min_len is not None:
+        gdn.gdn_set_chunk_min_len(args.chunk_min_len)
 
     line = _measure(args, wl, dev, world, rank, local, gdn, W)
     extras = {}
     plain = not (args.lens or args.capture or args.rule != "gated_delta"
-                 or args.gate != "scalar")
+                 or args.gate != "scalar" or args.chunk_min_len is not None)
     if plain and wl.name == "decode" and not args.no_extra:
         for name in EXTRA_WORKLOADS:
             torch.cuda.empty_cache()

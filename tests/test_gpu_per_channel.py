@@ -3,7 +3,10 @@
 gate_per_channel): decay logits a [N, H, K], one gate per key channel, state
 columns decayed separately.  Checked against the fp64 oracle (its pins are in
 test_oracle_pins.py) through the layer, the standalone prepare and the
-standalone recurrence; every sequence runs on the token-serial kernel.
+standalone recurrence.  In the layer, bf16 sequences with K = 128, V a
+multiple of 128 and at least the chunk threshold of tokens take the
+per-channel chunked tensor-core kernel (16-token chunks); the rest, and every
+sequence of the standalone recurrence, the token-serial kernel.
 """
 import numpy as np
 import pytest
@@ -13,6 +16,8 @@ import oracle
 import varlen_gated_delta_gb300 as gdn
 from varlen_gated_delta_gb300 import workloads as W
 from gdn_testlib import cpu64, max_abs, rel_l2
+from test_gpu_parity import SERIAL_ONLY, chunk_threshold
+from test_gpu_canary import Guarded
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -105,7 +110,8 @@ def test_per_channel_standalone_prepare_and_delta():
 
 def test_per_channel_layer_equals_composed_calls_bitwise():
     wl, d = _case("decode", (3, 17, 0, 1, 90), seed_shift=3, H=4, HQ=2)
-    out, cfin, sfin = _layer(wl, d)
+    with chunk_threshold(SERIAL_ONLY):   # the composed route is the token-serial kernel
+        out, cfin, sfin = _layer(wl, d)
     y, c2 = gdn.gdn_conv1d_varlen(d["qkv"], d["w"], d["bias"], d["offsets"], d["conv_init"],
                                   Kc=wl.Kc, D=wl.D)
     qk, gb = gdn.gdn_prepare_ex(y, d["a"], d["b"], d["A_log"], d["dt_bias"], H=wl.H, HQ=wl.HQ,
@@ -132,3 +138,85 @@ def test_per_channel_with_capture_is_rejected():
     with pytest.raises(gdn.GdnError) as ei:
         _layer(wl, d, cap=2, counts=counts)
     assert ei.value.status == 5
+
+
+# ---- the per-channel chunked kernel (16-token chunks on tcgen05) ----
+
+CHUNKED = [
+    # one full chunk, a lone token, ragged tails, the threshold itself and one below it
+    ("ragged", "decode", (16, 1, 300, 47, 8, 7, 0, 33), dict(H=4, HQ=2)),
+    ("v256-d2", "long", (200, 33), dict(H=4, HQ=2)),
+    ("one-long", "decode", (1500,), dict(H=2, HQ=1)),
+    ("gqa-4", "decode", (64, 129), dict(H=8, HQ=2)),
+]
+
+
+@pytest.mark.parametrize("host_offsets", [True, False])
+@pytest.mark.parametrize("geom", CHUNKED, ids=[g[0] for g in CHUNKED])
+def test_per_channel_chunked_matches_oracle(geom, host_offsets):
+    _, base, lens, over = geom
+    wl, d = _case(base, lens, seed_shift=10, **over)
+    kw = dict(offsets_host=d["offsets_list"]) if host_offsets else {}
+    out, cfin, sfin = _layer(wl, d, **kw)
+    with chunk_threshold(SERIAL_ONLY):
+        o_s, _, s_s = _layer(wl, d, **kw)
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cpu64(cfin), c_ref)
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], (
+        f"out {eo:.3e} (max-abs {max_abs(cpu64(out), o_ref):.3e}) state {es:.3e}")
+    # a different kernel ran for the long sequences than on the token-serial route
+    assert not torch.equal(out, o_s)
+    assert rel_l2(cpu64(o_s), o_ref) <= TOL["bf16"] and rel_l2(cpu64(s_s), s_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("scale_logits", [0.0, 8.0])
+def test_per_channel_chunked_extreme_decays(scale_logits):
+    """All gates 1 (logits far below the softplus knee and A_log = -inf-like),
+    and gates that fall to ~e^-40 within a chunk: no factor overflows."""
+    wl, d = _case("decode", (100, 37), seed_shift=11, H=2, HQ=1)
+    if scale_logits == 0.0:
+        d["a"] = torch.full_like(d["a"], -60.0)      # softplus ~ 0: g = 1
+    else:
+        d["a"] = d["a"] * scale_logits + 4.0         # steep, channel-dependent decays
+    out, cfin, sfin = _layer(wl, d, offsets_host=d["offsets_list"])
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(sfin).all()
+    assert rel_l2(cpu64(out), o_ref) <= TOL["bf16"] and rel_l2(cpu64(sfin), s_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("extra", [gdn.GDN_OPT_GATE_EXP, gdn.RULE_OPTS["gated"],
+                                   gdn.GDN_OPT_BETA_RAW, gdn.GDN_OPT_NO_BETA,
+                                   gdn.GDN_OPT_NO_QK_NORM])
+def test_per_channel_chunked_with_rule_options(extra):
+    wl, d = _case("decode", (90, 21, 5), seed_shift=12, H=4, HQ=2)
+    if extra & gdn.GDN_OPT_GATE_EXP:
+        d["a"] = -torch.nn.functional.softplus(d["a"]) * 0.5
+    if extra & gdn.GDN_OPT_BETA_RAW:
+        d["b"] = torch.sigmoid(d["b"])
+    if extra & gdn.GDN_OPT_NO_QK_NORM:
+        d["qkv"] = (d["qkv"].float() / 8.0).to(d["qkv"].dtype)  # keep S k bounded
+    opts = PC | extra
+    out, cfin, sfin = _layer(wl, d, opts=opts, offsets_host=d["offsets_list"])
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d, opts=opts)
+    torch.cuda.synchronize()
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], f"out {eo:.3e} state {es:.3e}"
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_per_channel_chunked_outputs_stay_inside_their_tensors(in_place):
+    wl, d = _case("decode", (130, 5, 47), seed_shift=13, H=4, HQ=2)
+    N, B = wl.N, wl.B
+    out = Guarded((N, wl.H, wl.V), torch.bfloat16)
+    cfin = Guarded((B, wl.width, wl.L), torch.bfloat16, fill=d["conv_init"] if in_place else None)
+    sfin = Guarded((B, wl.H, wl.V, wl.K), torch.float32, fill=d["state_init"] if in_place else None)
+    ws_n = gdn.gdn_workspace_bytes(B, N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D, gdn.GDN_BF16)
+    ws = Guarded((ws_n,), torch.uint8)
+    if in_place:
+        d = dict(d, conv_init=cfin.t, state_init=sfin.t)
+    _layer(wl, d, out=out.t, conv_fin=cfin.t, state_fin=sfin.t, workspace=ws.t,
+           offsets_host=d["offsets_list"])
+    assert [g.guards_intact() for g in (out, cfin, sfin, ws)] == [True] * 4

@@ -600,13 +600,16 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         if (rc) return rc;
     }
     // path choice per sequence: at least `thr` tokens -> chunked kernel
-    // (the per-channel gate has no chunked form: every sequence is token-serial)
-    const bool chunk_ok = chunked_supported(dtype, K, V, (int)width) && !per_channel;
+    // (the per-channel gate has its own chunked kernel; it reads a [N, H, K] as
+    // 16-byte vectors)
+    const bool chunk_ok = chunked_supported(dtype, K, V, (int)width) &&
+                          (!per_channel || (((uintptr_t)a & 15) == 0 && ((uintptr_t)state_init & 15) == 0 &&
+                                            ((uintptr_t)state_fin & 15) == 0));
     int thr = chunk_min_len();
     // Long chunked sequences that leave most of the GPU idle are cut into
     // segments run in parallel (two chunked launches and a combine step).
     // Sequences shorter than one chunk beside them run token-serially then.
-    const SegmentPlan seg = chunk_ok && offsets_host && lay.seg != 0
+    const SegmentPlan seg = chunk_ok && !per_channel && offsets_host && lay.seg != 0
                                 ? plan_segments(offsets_host, B, H, V, segment_plan_thr(thr),
                                                 lay.seg_seqs, sm_count_host())
                                 : SegmentPlan{};
@@ -671,6 +674,22 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
     auto launch_chunked = [&]() -> int {
+        if (per_channel) {  // the per-key-channel chunked kernel
+            const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
+            PcParams pp{};
+            pp.qb = yb; pp.kb = yb + (size_t)HQ * K; pp.vb = yb + 2 * (size_t)HQ * K; pp.rs = width;
+            pp.g = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias;
+            pp.offsets = offsets; pp.seq_order = order; pp.header = hdr;
+            pp.state_init = state_init; pp.state_fin = state_fin;
+            pp.out = static_cast<__nv_bfloat16 *>(out); pp.ors = (long)H * V;
+            pp.B = B; pp.N = N; pp.H = H; pp.HQ = HQ; pp.V = V; pp.VT = V / 128;
+            pp.scale = eff_scale; pp.opts = opts; pp.gate_factor = 0;
+            mark_before(GDN_KERNEL_CHUNKED, s);
+            cudaError_t ce = launch_delta_chunked_pc(pp, max_units, s);
+            mark_after(GDN_KERNEL_CHUNKED, s);
+            if (ce != cudaSuccess) return cuda_fail(ce, "per-channel chunked kernel launch");
+            return GDN_OK;
+        }
         ChunkLaunch cl{};
         cl.y = y; cl.a = a; cl.bl = b; cl.A_log = A_log; cl.dt_bias = dt_bias;
         cl.offsets = offsets; cl.seq_order = order; cl.header = hdr;

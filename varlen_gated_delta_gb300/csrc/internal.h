@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -207,6 +208,29 @@ struct DensePack {
     void *maps_dst;
 };
 cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
+
+// Chunked recurrence with a per-key-channel gate (bf16, K = 128, V a multiple
+// of 128): q, k, v rows of token t at qb / kb / vb + t * rs (bf16, the first
+// key / value head's columns; key head kh adds kh * 128, value head h and V
+// tile vt add h * V + vt * 128); g [N, H, 128] holds the decay logits, or the
+// gate factors when gate_factor; out [N, ors] (head h at column h * V).
+// Units and their order come from the workspace header and seq_order.
+struct PcParams {
+    const __nv_bfloat16 *qb, *kb, *vb;
+    long rs;
+    const float *g, *bl, *A_log, *dt_bias;
+    const int32_t *offsets, *seq_order;
+    WsHeader *header;
+    const float *state_init;
+    float *state_fin;
+    __nv_bfloat16 *out;
+    long ors;
+    int B, N, H, HQ, V, VT;
+    float scale;
+    int opts;         // GDN_OPT_* (rule and activation options)
+    int gate_factor;  // g holds gate factors, not logits
+};
+cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStream_t s);
 
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
