@@ -130,6 +130,20 @@ def algorithmic_bytes_delta(wl, N, B, cap=0, per_channel=False):
     return state + qk + gb + v + out + conv_state + pc + capture_bytes(wl, B, cap)
 
 
+def algorithmic_bytes_delta_pc(wl, N, B):
+    """Bytes the per-channel chunked recurrence (prepare + scan kernels) must
+    move per launch pair: the conv output's q, k and v columns, the decay
+    logits a [N, H, K] and beta logits, the output and the fp32 state in and
+    out.  The chunk images the prepare kernel writes and the scan kernel reads
+    back are the design's own traffic, not counted."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    state = 2 * B * wl.H * wl.V * wl.K * 4
+    qkv = N * (2 * wl.HQ * wl.K + wl.H * wl.V) * esz
+    logits = N * wl.H * (wl.K + 1) * 4
+    out = N * wl.H * wl.V * esz
+    return state + qkv + logits + out
+
+
 def algorithmic_bytes_layer(wl, N, B):
     """Bytes the whole layer must move per step (inputs read once, outputs written once)."""
     esz = 2 if wl.dtype == "bf16" else 4
@@ -342,9 +356,6 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
     offs = d["offsets_list"]
     N, B = offs[-1], len(offs) - 1
     act = gdn.GDN_ACT_SILU if wl.silu else gdn.GDN_ACT_NONE
-    ws = torch.empty(gdn.gdn_workspace_bytes(B, N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D,
-                                             gdn.GDN_BF16 if wl.dtype == "bf16" else gdn.GDN_F32),
-                     dtype=torch.uint8, device=dev)
     out = torch.empty((N, wl.H, wl.V), dtype=wl.torch_dtype, device=dev)
     conv_states = [d["conv_init"], d["conv_init"].clone()]
     states = [d["state_init"], d["state_init"].clone()]
@@ -360,6 +371,12 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
         opts |= gdn.GDN_OPT_GATE_PER_CHANNEL
         gpc = torch.Generator(device=dev).manual_seed(wl.seed + 500)
         d["a"] = torch.randn((N, wl.H, wl.K), generator=gpc, device=dev) * wl.a_std + wl.a_mean
+    # (with the per-channel gate the workspace also holds the chunk images of
+    # its chunked form)
+    ws = torch.empty(gdn.gdn_workspace_bytes_ex(B, N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D,
+                                                gdn.GDN_BF16 if wl.dtype == "bf16" else gdn.GDN_F32,
+                                                opts),
+                     dtype=torch.uint8, device=dev)
 
     def call(qkv, a, b, offsets, sset, out_t=None, capsule_t=None):
         # decode-style carry: the final states overwrite the initial ones in place
@@ -559,6 +576,13 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
         roof = {"kernel": "delta_serial_kernel", "bound": "hbm", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": None if cap else _profile_traffic("delta_serial", wl.name),
+                "algorithmic_bytes": kbytes, "kernel_ms": kavg,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    elif args.gate == "per_channel":
+        kbytes = algorithmic_bytes_delta_pc(wl, N, B)
+        achieved = kbytes / (kavg * 1e-3) / 1e9
+        roof = {"kernel": "pc_prep_kernel + pc_scan_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                 "algorithmic_bytes": kbytes, "kernel_ms": kavg,
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:

@@ -335,8 +335,13 @@ GDN_API int gdn_layer_varlen_noalloc(const void *qkv, const void *w, const void 
  *     (N*H*(K+1) floats); gdn_delta_varlen_ex reads that layout.
  *   The recurrence decays column i of every state row of head h by g[t, h, i]:
  *     S_t = S_{t-1} diag(g_t) + beta_t (v_t - S_{t-1} diag(g_t) k_t) k_t^T.
- *   Every sequence runs on the token-serial kernel (no chunked form).  Not
- *   combinable with state-update capture (GDN_ERR_UNSUPPORTED).
+ *   In gdn_layer_varlen_ex, sequences of at least gdn_chunk_min_len() tokens
+ *   run on a chunked tensor-core form (16-token chunks: a prepare kernel over
+ *   all chunks, then a scan kernel carrying the state) when the geometry
+ *   allows it (bf16, K == 128, V % 128 == 0, a, state_init and state_fin
+ *   16-byte aligned) and the workspace holds gdn_workspace_bytes_ex(...,
+ *   opts) bytes; otherwise, and in gdn_delta_varlen_ex, on the token-serial
+ *   kernel.  Not combinable with state-update capture (GDN_ERR_UNSUPPORTED).
  */
 #define GDN_OPT_GATE_PER_CHANNEL 64
 #define GDN_OPT_ALL 127
@@ -358,6 +363,18 @@ GDN_API int gdn_delta_varlen_ex(const void *y, const float *qk_norm, const float
                                 const int32_t *offsets, const float *state_init, void *out,
                                 float *state_fin, int B, int N, int H, int HQ, int K, int V,
                                 float scale, int opts, int dtype, void *stream);
+
+/*
+ * Workspace bytes gdn_layer_varlen_ex needs for this geometry and these
+ * options (0 on bad input).  Equal to gdn_workspace_bytes() unless opts has
+ * GDN_OPT_GATE_PER_CHANNEL and the geometry has the per-channel chunked form;
+ * then it adds the chunk images of that form:
+ *   ((N + 15) / 16 + B) * H * 14848 bytes (rounded up to 256).
+ * A smaller workspace (at least gdn_workspace_bytes()) is accepted: the
+ * per-channel sequences then run on the token-serial kernel.
+ */
+GDN_API size_t gdn_workspace_bytes_ex(int B, int N, int H, int HQ, int K, int V, int Kc, int D,
+                                      int dtype, int opts);
 
 GDN_API int gdn_layer_varlen_ex(const void *qkv, const void *w, const void *bias, const float *a,
                                 const float *b, const float *A_log, const float *dt_bias,

@@ -124,6 +124,27 @@ def test_workspace_bytes(lib):
     assert big > small
 
 
+def test_workspace_bytes_ex_adds_the_per_channel_chunk_images(lib):
+    PC = gdn.GDN_OPT_GATE_PER_CHANNEL
+    for geo in [(8, 32768, 32, 16, 128, 128, 4, 1), (3, 1000, 4, 2, 128, 256, 4, 2)]:
+        B, N, H, HQ, K, V, Kc, D = geo
+        base = lib.gdn_workspace_bytes(*geo, 1)
+        assert lib.gdn_workspace_bytes_ex(*geo, 1, 0) == base
+        assert lib.gdn_workspace_bytes_ex(*geo, 1, gdn.GDN_OPT_GATE_EXP) == base
+        # without decay the per-channel bit is the plain rule: no images
+        assert lib.gdn_workspace_bytes_ex(*geo, 1, PC | gdn.GDN_OPT_NO_DECAY) == base
+        # images: ((N + 15) / 16 + B) slots x H heads x 14848 bytes
+        img = ((N + 15) // 16 + B) * H * 14848
+        ex = lib.gdn_workspace_bytes_ex(*geo, 1, PC)
+        assert ex == base + (img + 255) // 256 * 256
+        # fp32 (no chunked form) and K != 128: no images
+        assert lib.gdn_workspace_bytes_ex(*geo, 0, PC) == lib.gdn_workspace_bytes(*geo, 0)
+    assert lib.gdn_workspace_bytes_ex(2, 64, 4, 2, 64, 128, 4, 1, 1, PC) == \
+        lib.gdn_workspace_bytes(2, 64, 4, 2, 64, 128, 4, 1, 1)
+    assert lib.gdn_workspace_bytes_ex(2, 64, 4, 2, 128, 128, 4, 1, 1, 128) == 0
+    assert lib.gdn_workspace_bytes_ex(2, 64, 3, 2, 128, 128, 4, 1, 1, PC) == 0
+
+
 def test_chunk_threshold_setting(lib):
     default = lib.gdn_chunk_min_len()
     assert default > 0

@@ -32,7 +32,7 @@ __all__ = [
     "GDN_OPT_BETA_RAW", "GDN_OPT_NO_QK_NORM", "GDN_OPT_GATE_PER_CHANNEL", "RULE_OPTS",
     "gdn_gated_delta_dense",
     "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
-    "gdn_selftest_wait_timeout", "gdn_dense_workspace_bytes",
+    "gdn_selftest_wait_timeout", "gdn_dense_workspace_bytes", "gdn_workspace_bytes_ex",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -84,6 +84,8 @@ def load_library():
     lib.gdn_layer_varlen_noalloc.restype = i
     lib.gdn_workspace_bytes.restype = sz
     lib.gdn_workspace_bytes.argtypes = [i] * 9
+    lib.gdn_workspace_bytes_ex.restype = sz
+    lib.gdn_workspace_bytes_ex.argtypes = [i] * 10
     lib.gdn_workspace_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     lib.gdn_set_chunk_min_len.argtypes = [i]
     lib.gdn_chunk_min_len.restype = i
@@ -252,6 +254,12 @@ def gdn_delta_varlen(y, qk_norm, g_beta, offsets, state_init, *, H, HQ, K, V, sc
 
 def gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dtype=GDN_BF16) -> int:
     return int(load_library().gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dtype))
+
+
+def gdn_workspace_bytes_ex(B, N, H, HQ, K, V, Kc, D, dtype=GDN_BF16, opts=0) -> int:
+    """Workspace of gdn_layer_varlen_ex with these options (adds the chunk
+    images of the per-channel chunked form when it applies)."""
+    return int(load_library().gdn_workspace_bytes_ex(B, N, H, HQ, K, V, Kc, D, dtype, int(opts)))
 
 
 def gdn_workspace_status(workspace: torch.Tensor):
@@ -503,7 +511,7 @@ def gdn_layer_varlen_ex(qkv, w, bias, a, b, A_log, dt_bias, offsets, conv_init, 
         conv_updates = (torch.empty((B, cap, W), dtype=T, device=dev) if conv_updates is None
                         else conv_updates)
         capsule = torch.empty((B, width), dtype=f32, device=dev) if capsule is None else capsule
-    need = gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dcode)
+    need = gdn_workspace_bytes_ex(B, N, H, HQ, K, V, Kc, D, dcode, opts)
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
     hp, keep = _host_offsets(offsets_host)

@@ -539,6 +539,16 @@ size_t gdn_workspace_bytes(int B, int N, int H, int HQ, int K, int V, int Kc, in
     return ws_layout(B, N, H, HQ, K, V, dtype).total;
 }
 
+size_t gdn_workspace_bytes_ex(int B, int N, int H, int HQ, int K, int V, int Kc, int D, int dtype,
+                              int opts) {
+    const size_t base = gdn_workspace_bytes(B, N, H, HQ, K, V, Kc, D, dtype);
+    if (base == 0 || (opts & ~GDN_OPT_ALL) != 0) return 0;
+    if (!(opts & GDN_OPT_GATE_PER_CHANNEL) || (opts & GDN_OPT_NO_DECAY)) return base;
+    const int width = 2 * HQ * K + H * V;
+    if (!chunked_supported(dtype, K, V, width)) return base;
+    return base + align256(pc_slots(B, N) * H * pc_img_bytes());
+}
+
 int gdn_workspace_status(const void *workspace, int *counts, void *stream) {
     g_err[0] = 0;
     if (!workspace) return fail(GDN_ERR_NULL, "workspace is NULL");
@@ -602,9 +612,11 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     // path choice per sequence: at least `thr` tokens -> chunked kernel
     // (the per-channel gate has its own chunked kernel; it reads a [N, H, K] as
     // 16-byte vectors)
+    const size_t pc_img = per_channel ? pc_slots(B, N) * H * pc_img_bytes() : 0;
     const bool chunk_ok = chunked_supported(dtype, K, V, (int)width) &&
                           (!per_channel || (((uintptr_t)a & 15) == 0 && ((uintptr_t)state_init & 15) == 0 &&
-                                            ((uintptr_t)state_fin & 15) == 0));
+                                            ((uintptr_t)state_fin & 15) == 0 &&
+                                            ws_bytes >= lay.total + pc_img));
     int thr = chunk_min_len();
     // Long chunked sequences that leave most of the GPU idle are cut into
     // segments run in parallel (two chunked launches and a combine step).
@@ -684,6 +696,13 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
             pp.out = static_cast<__nv_bfloat16 *>(out); pp.ors = (long)H * V;
             pp.B = B; pp.N = N; pp.H = H; pp.HQ = HQ; pp.V = V; pp.VT = V / 128;
             pp.scale = eff_scale; pp.opts = opts; pp.gate_factor = 0;
+            pp.thr = thr;
+            pp.img = reinterpret_cast<unsigned char *>(ws + lay.total);  // after the plain layout
+            pp.img_bytes = (long)pc_img_bytes();
+            // the v rows, read by the scan kernel in [64 x 16] boxes of the conv output
+            if (!encode_operand_map(&pp.vmap, y, N, width, 16))
+                return fail(GDN_ERR_CUDA, "encoding the per-channel v tensor map failed");
+            pp.vcol0 = 2 * HQ * K;
             mark_before(GDN_KERNEL_CHUNKED, s);
             cudaError_t ce = launch_delta_chunked_pc(pp, max_units, s);
             mark_after(GDN_KERNEL_CHUNKED, s);

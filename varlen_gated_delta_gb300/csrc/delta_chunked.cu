@@ -931,14 +931,15 @@ namespace {
 
 }  // namespace
 
-// Operand map of a bf16 row-major matrix [rows, cols] read in [64 x 64]
+// Operand map of a bf16 row-major matrix [rows, cols] read in [64 x box_rows]
 // tiles with the 128-byte swizzle the chunked kernel's MMA descriptors expect.
-bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols) {
+// (box_rows: rows of the box, 64 by default.)
+bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols, int box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -20,10 +20,16 @@
 // last token of i's block, two factors of at most 1 each; inside a block they
 // are taken pair by pair.  No factor can overflow, whatever the gates.
 //
-// Per chunk and (sequence, value head, 128-row V tile) unit, on CUDA cores:
-// the gates, norms, KK / QK, T, W, U and the scaled operands; on tcgen05
-// (M = 128 state rows, bf16 operands, fp32 accumulators in tensor memory):
-//   Dd = S0 W^T,  Do = S0 Qt^T   (S0 = bf16 copy of the state, N = 16)
+// Everything but Delta, O and S_C is independent of the state, so it is
+// computed for all chunks at once by pc_prep_kernel (CUDA cores; one CTA per
+// chunk and value head) and written out as a chunk image laid out exactly as
+// the scan kernel's shared-memory operands.  pc_scan_kernel then walks each
+// (sequence, value head, V tile) unit's chunks in order, copying each image in
+// with a bulk copy and the chunk's v rows with a tensor copy (two chunks
+// ahead), and runs on tcgen05 (M = 128 state rows, bf16 operands, fp32
+// accumulators in tensor memory):
+//   Delta^T = V^T (T diag(beta))^T - S0 W^T,  Do = S0 Qt^T
+//                                 (S0 = bf16 copy of the state, N = 16)
 //   Do += Delta^T P^T             (P = scale tril(QK), K = 16)
 //   S  += Delta^T Kp              (S first scaled by e^{b_C} per column, N = 128)
 #include <cuda.h>
@@ -38,100 +44,412 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kPc = 16;            // chunk length
-constexpr int kPcThreads = 256;    // 8 warps; thread 0 issues the MMAs
+constexpr int kPc = 16;                        // chunk length
 constexpr uint64_t kPcWaitNs = 2000000000ull;  // bounded waits: 2 s
 
-// Shared memory (offsets from a 1024-aligned base).  SW128 = rows of 128 bytes
-// in the 128-byte swizzle the MMA descriptors read.
-constexpr uint32_t kOS0 = 0;              // S0 bf16 [128 vi][128 kk]: two SW128 blocks of 16 KB
-constexpr uint32_t kODt = 32768;          // Delta^T bf16 [128 vi][16 t] in an SW128 [128][64] tile
-constexpr uint32_t kOW = 49152;           // W bf16 [16 t][128 kk]: two SW128 blocks of 2 KB
-constexpr uint32_t kOQt = kOW + 4096;     // Qt bf16 [16 t][128 kk], same layout
-constexpr uint32_t kOKp = kOQt + 4096;    // Kp bf16 [16 t][128 kk], same layout (MN-major B)
-constexpr uint32_t kOP = kOKp + 4096;     // P bf16 [16 t][16 i] in an SW128 [16][64] tile
-constexpr uint32_t kORawK = kOP + 2048;   // raw k rows bf16 [16][128]
-constexpr uint32_t kORawQ = kORawK + 4096;
-constexpr uint32_t kORawV = kORawQ + 4096;
-constexpr uint32_t kOB = kORawV + 4096;   // logits, then cumulative log decays, fp32 [16][128]
-constexpr uint32_t kOKt = kOB + 8192;     // Kt fp32 [16][128] (norm folded in)
-constexpr uint32_t kOU = kOKt + 8192;     // U fp32 [16][128]
-constexpr uint32_t kOKK = kOU + 8192;     // KK fp32 [16][16]
-constexpr uint32_t kOQK = kOKK + 1024;    // QK fp32 [16][16]
-constexpr uint32_t kOT = kOQK + 1024;     // T fp32 [16][16]
-constexpr uint32_t kOVec = kOT + 1024;    // beta[16], rk[16], rq[16], colscale[128]
-constexpr uint32_t kVecN = 16 * 3 + 128;
-constexpr uint32_t kOBar = kOVec + kVecN * 4;
-constexpr uint32_t kPcSmem = kOBar + 64 + 1024;  // + alignment slack
-static_assert(kOBar % 8 == 0, "mbarrier alignment");
-static_assert(kPcSmem <= 113 * 1024, "two CTAs per SM");
-
-// TMEM: the state in columns [0, 128); Dd in [128, 144), Do in [144, 160).
-constexpr uint32_t kPcTmemCols = 256;
-constexpr uint32_t kColS = 0, kColDd = 128, kColDo = 144;
+// chunk image offsets (bytes); P and T diag(beta) share one SW128 tile
+constexpr uint32_t kImW = 0, kImQt = 4096, kImKp = 8192, kImPT = 12288, kImCs = 14336;
+static_assert(kImCs + 512 == kPcImgHead, "image head layout");
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
-__device__ __forceinline__ void st8(unsigned char *tile, int row, int c8, const float *v) {
-    uint4 q;
-    q.x = pack2(v[0], v[1]);
-    q.y = pack2(v[2], v[3]);
-    q.z = pack2(v[4], v[5]);
-    q.w = pack2(v[6], v[7]);
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = q;
+__device__ __forceinline__ uint4 pack8(const float *v) {
+    return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
-// element (row, col) of a [rows][128] bf16 operand kept as two SW128 blocks
-// of [rows][64] that are `block` bytes apart
-__device__ __forceinline__ void st_el(unsigned char *tile, uint32_t block, int row, int col, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(tile + (col >> 6) * block + sw128_offset(row, col & 63)) =
-        __float2bfloat16_rn(v);
+// byte offset of element (row, col) of a [rows][128] bf16 operand kept as two
+// SW128 blocks of [rows][64], 2048 bytes apart (rows < 16)
+__device__ __forceinline__ uint32_t op_offset(int row, int col) {
+    return (uint32_t)(col >> 6) * 2048u + sw128_offset(row, col & 63);
+}
+__device__ __forceinline__ void st_bf16(unsigned char *p, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
 }
 
-// Natural-log gate of one key channel from its input under the options:
-// logits through the softplus gate (-exp(A_log) softplus(x + dt_bias)), the
-// exp gate (x), or (gate_factor) the gate factor itself, log(max(x, 1e-30)).
-__device__ __forceinline__ float log_gate(float x, float dtb, float alog, int opts, int gate_factor) {
-    if (opts & GDN_OPT_NO_DECAY) return 0.f;
-    if (gate_factor) return logf(fmaxf(x, 1e-30f));
-    if (opts & GDN_OPT_GATE_EXP) return x;
+// ------------------------------------------------------------------ prepare
+// One CTA per (image slot, value head): finds the slot's sequence and chunk,
+// and writes the chunk image.  Slots with no chunk (short sequences, the end
+// of a sequence's slot range) return at once.
+//
+// Every decay factor is a product of per-token gates g_j = e^{log g_j} (each
+// at most 1): with P_t = prod_{j<=t} g_j, Kt = k P_t, Qt = q P_t and
+// Kp = k prod_{j>t} g_j.  For KK / QK the 16 tokens form four blocks of 4;
+// for t in block TB and i in an earlier block, with r = 4 TB - 1,
+//   e^{b_t - b_i} = X_TB[t] Z_TB[i],  X_TB[t] = prod_{r<j<=t} g_j,
+//   Z_TB[i] = prod_{i<j<=r} g_j,
+// so those entries are dot products of the rows k_t X_TB[t] (or q_t X_TB[t])
+// and k_i Z_TB[i]; inside a block the factor of (t, i) is formed from the
+// gates between them.  q/k norms are applied to the finished dot products.
+constexpr int kPrepThreads = 256;
+
+// dynamic shared memory of the prepare kernel, in floats
+constexpr int kFK = 0;             // raw k [16][128]
+constexpr int kFQ = kFK + 2048;    // raw q [16][128]
+constexpr int kFG = kFQ + 2048;    // gate inputs, then gate factors [16][128]
+constexpr int kFKt = kFG + 2048;   // k P_t [16][128]
+constexpr int kFA = kFKt + 2048;   // k X_TB rows of blocks 1..3 [12][128]
+constexpr int kFAQ = kFA + 1536;   // q X_TB rows [12][128]
+constexpr int kFZ = kFAQ + 1536;   // k Z_TB rows: block 1 [4], 2 [8], 3 [12] -> [24][128]
+constexpr int kFAm = kFZ + 3072;   // A[t][i] = fr beta_t rk_t rk_i KK [16][16]
+constexpr int kFTb = kFAm + 256;   // T diag(beta rk) [16][16], for W
+constexpr int kFVec = kFTb + 256;  // beta[16], rk[16], rq[16]
+constexpr int kPrepFloats = kFVec + 48;
+constexpr size_t kPrepSmem = (size_t)kPrepFloats * 4;
+
+// gate factor of one key channel from its input under the options
+__device__ __forceinline__ float gate_factor_of(float x, float dtb, float neg_a, int opts, int factor) {
+    if (opts & GDN_OPT_NO_DECAY) return 1.f;
+    if (factor) return fmaxf(x, 0.f);
+    if (opts & GDN_OPT_GATE_EXP) return __expf(x);
     x += dtb;
-    const float softplus = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
-    return -expf(alog) * softplus;
+    const float softplus = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+    return __expf(neg_a * softplus);
 }
 
-__global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_constant__ PcParams p) {
+    // Every CTA waits for the conv kernel before it exits, slots without a
+    // chunk included: the scan kernel's wait on this grid then also covers
+    // the conv kernel's output (the schedule in the workspace header).
+    pdl_wait_primary();
+
+    const int q = blockIdx.x, h = blockIdx.y;
+    // the sequence i of slot q: the last with (offsets[i] >> 4) + i <= q
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((__ldg(p.offsets + mid) >> 4) + mid <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = __ldg(p.offsets + lo), e = __ldg(p.offsets + lo + 1);
+    if (s < 0 || e < s || e > p.N || e - s < p.thr) return;
+    const int n = q - ((s >> 4) + lo);
+    if (n < 0 || n >= (e - s + kPc - 1) / kPc) return;
+    const int t0 = s + n * kPc, Cn = min(kPc, e - t0);
+
+    extern __shared__ __align__(16) float fs[];
+    float *sK = fs + kFK, *sQ = fs + kFQ, *sG = fs + kFG, *sKt = fs + kFKt;
+    float *sA = fs + kFA, *sAQ = fs + kFAQ, *sZ = fs + kFZ, *sAm = fs + kFAm, *sTb = fs + kFTb;
+    float *v_beta = fs + kFVec, *v_rk = v_beta + 16, *v_rq = v_rk + 16;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, opts = p.opts;
+    const int kh = h / (H / p.HQ);
+    const __nv_bfloat16 *qsrc = p.qb + (size_t)kh * 128;
+    const __nv_bfloat16 *ksrc = p.kb + (size_t)kh * 128;
+    const bool soft = !(opts & (GDN_OPT_NO_DECAY | GDN_OPT_GATE_EXP)) && !p.gate_factor;
+    const float dtb = soft ? __ldg(p.dt_bias + h) : 0.f;
+    const float neg_a = soft ? -expf(__ldg(p.A_log + h)) : 0.f;
+    const float fr = (opts & GDN_OPT_NO_RETRIEVE) ? 0.f : 1.f;
+    unsigned char *img = p.img + ((size_t)q * H + h) * (size_t)p.img_bytes;
+
+    // ---- L: raw k, q rows as fp32 (rows past the sequence are 0), the gate
+    // inputs and beta
+    for (int i = tid; i < 2 * kPc * 16; i += kPrepThreads) {
+        const int tile = i >> 8, r = (i >> 4) & 15, c8 = (i & 15) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < Cn)
+            v = __ldg(reinterpret_cast<const uint4 *>((tile == 0 ? ksrc : qsrc) + (size_t)(t0 + r) * p.rs + c8));
+        const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&v);
+        float *dst = (tile == 0 ? sK : sQ) + r * 128 + c8;
+        *reinterpret_cast<float4 *>(dst) = make_float4(__bfloat162float(x[0]), __bfloat162float(x[1]),
+                                                       __bfloat162float(x[2]), __bfloat162float(x[3]));
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(__bfloat162float(x[4]), __bfloat162float(x[5]),
+                                                           __bfloat162float(x[6]), __bfloat162float(x[7]));
+    }
+    const bool decay = !(opts & GDN_OPT_NO_DECAY);
+    for (int i = tid; i < kPc * 32; i += kPrepThreads) {
+        const int r = i >> 5, c4 = i & 31;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < Cn && decay)
+            v = __ldg(reinterpret_cast<const float4 *>(p.g + ((size_t)(t0 + r) * H + h) * 128) + c4);
+        *reinterpret_cast<float4 *>(sG + r * 128 + c4 * 4) = v;
+    }
+    if (tid < kPc) {
+        float be = 0.f;
+        if (tid < Cn) {
+            be = 1.f;
+            if (!(opts & GDN_OPT_NO_BETA)) {
+                be = __ldg(p.bl + (size_t)(t0 + tid) * H + h);
+                if (!(opts & GDN_OPT_BETA_RAW)) be = 1.f / (1.f + expf(-be));
+            }
+        }
+        v_beta[tid] = be;
+    }
+    __syncthreads();
+
+    // ---- G: gate factors (1 past the sequence); q/k norms, 8 threads per
+    // (token, q|k)
+    for (int i = tid; i < kPc * 128; i += kPrepThreads)
+        sG[i] = (i >> 7) < Cn ? gate_factor_of(sG[i], dtb, neg_a, opts, p.gate_factor) : 1.f;
+    {
+        const int red = tid >> 3, part = tid & 7;
+        const int t = red & 15;
+        const float *src = ((red >> 4) ? sQ : sK) + t * 128 + part * 16;
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + j);
+            ss = dot4(x, x, ss);
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        if (part == 0) {
+            const float rn = (opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(ss + 1e-12f);
+            ((red >> 4) ? v_rq : v_rk)[t] = rn;
+        }
+    }
+    __syncthreads();
+
+    // ---- R: per key channel c, the decay products and scaled rows.
+    // Threads 0..127: P_t, Kt, Qt (image), e^{b_C} (image), the k X / q X rows;
+    // threads 128..255: the suffix products, Kp (image), the k Z rows.
+    {
+        const int c = tid & 127;
+        float g[kPc], k[kPc];
+#pragma unroll
+        for (int t = 0; t < kPc; ++t) {
+            g[t] = sG[t * 128 + c];
+            k[t] = sK[t * 128 + c];
+        }
+        if (tid < 128) {
+            float P = 1.f;
+            const float qs = p.scale;
+#pragma unroll
+            for (int t = 0; t < kPc; ++t) {
+                P *= g[t];
+                sKt[t * 128 + c] = k[t] * P;
+                st_bf16(img + kImQt + op_offset(t, c), sQ[t * 128 + c] * v_rq[t] * qs * P);
+            }
+            reinterpret_cast<float *>(img + kImCs)[c] = P;
+#pragma unroll
+            for (int TB = 1; TB < 4; ++TB) {
+                float X = 1.f;
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const int t = 4 * TB + a, row = 4 * (TB - 1) + a;
+                    X *= g[t];
+                    sA[row * 128 + c] = k[t] * X;
+                    sAQ[row * 128 + c] = sQ[t * 128 + c] * X;
+                }
+            }
+        } else {
+            float Qs = 1.f;
+#pragma unroll
+            for (int t = kPc - 1; t >= 0; --t) {
+                st_bf16(img + kImKp + op_offset(t, c), k[t] * v_rk[t] * Qs);
+                Qs *= g[t];
+            }
+#pragma unroll
+            for (int TB = 1; TB < 4; ++TB) {
+                const int base = TB == 1 ? 0 : TB == 2 ? 4 : 12;
+                float Z = 1.f;
+#pragma unroll
+                for (int i = 4 * TB - 1; i >= 0; --i) {
+                    sZ[(base + i) * 128 + c] = k[i] * Z;
+                    Z *= g[i];
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- D: KK and QK in 4x4-token blocks, a half-warp per block pair and a
+    // lane per 8 channels (two groups of 4, 64 apart), summed over the
+    // half-warp.  Threads 0..95: the six pairs of a later block TB with an
+    // earlier block IB (rows k X_TB, q X_TB against k Z_TB); threads 96..159:
+    // the four blocks with themselves (factors from the gates in between).
+    // KK lands as A[t,i] = fr beta_t rk_t rk_i KK (i < t), QK as
+    // P[t,i] = scale rq_t rk_i QK (i <= t) in the image.
+    if (tid < 160) {
+        const int bp = tid >> 4, cg = tid & 15;
+        float kk[4][4], qk[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
+        int TB, IB;
+        if (bp < 6) {
+            TB = bp < 1 ? 1 : bp < 3 ? 2 : 3;
+            IB = bp - (TB * (TB - 1)) / 2;
+            const int zb = (TB == 1 ? 0 : TB == 2 ? 4 : 12) + 4 * IB;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = cg * 4 + j * 64;
+                float4 x[4], xq[4], y[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    x[a] = *reinterpret_cast<const float4 *>(sA + (4 * (TB - 1) + a) * 128 + c);
+                    xq[a] = *reinterpret_cast<const float4 *>(sAQ + (4 * (TB - 1) + a) * 128 + c);
+                    y[a] = *reinterpret_cast<const float4 *>(sZ + (zb + a) * 128 + c);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        kk[a][b] = dot4(x[a], y[b], kk[a][b]);
+                        qk[a][b] = dot4(xq[a], y[b], qk[a][b]);
+                    }
+            }
+        } else {
+            TB = IB = bp - 6;
+            const int t0b = 4 * TB;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = cg * 4 + j * 64;
+                float4 kr[4], qr[4], gr[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    kr[a] = *reinterpret_cast<const float4 *>(sK + (t0b + a) * 128 + c);
+                    qr[a] = *reinterpret_cast<const float4 *>(sQ + (t0b + a) * 128 + c);
+                    gr[a] = *reinterpret_cast<const float4 *>(sG + (t0b + a) * 128 + c);
+                }
+                // column b: f = prod of the gates of tokens b+1 .. a of the block
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float4 f = kr[b];
+                    qk[b][b] = dot4(qr[b], f, qk[b][b]);
+#pragma unroll
+                    for (int a = b + 1; a < 4; ++a) {
+                        f.x *= gr[a].x; f.y *= gr[a].y; f.z *= gr[a].z; f.w *= gr[a].w;
+                        kk[a][b] = dot4(kr[a], f, kk[a][b]);
+                        qk[a][b] = dot4(qr[a], f, qk[a][b]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    kk[a][b] += __shfl_xor_sync(0xffffffffu, kk[a][b], o);
+                    qk[a][b] += __shfl_xor_sync(0xffffffffu, qk[a][b], o);
+                }
+        if (cg == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int t = 4 * TB + a, i = 4 * IB + b;
+                    if (TB > IB || b < a) sAm[t * 16 + i] = fr * v_beta[t] * v_rk[t] * v_rk[i] * kk[a][b];
+                    if (TB > IB || b <= a)
+                        st_bf16(img + kImPT + sw128_offset(t, i), p.scale * v_rq[t] * v_rk[i] * qk[a][b]);
+                }
+        }
+    }
+    // the zero upper triangle of P (i > t)
+    {
+        const int t = tid >> 4, i = tid & 15;
+        if (i > t) st_bf16(img + kImPT + sw128_offset(t, i), 0.f);
+    }
+    __syncthreads();
+
+    // ---- T = (I + A)^-1 (A strictly lower): forward substitution, one column
+    // per lane of warp 0.  Stored as T diag(beta) (bf16, image columns 16..31
+    // of the P tile) and T diag(beta rk) (fp32, for W).
+    if (warp == 0 && lane < 16) {
+        const int c = lane;
+        float pr[16], tc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) pr[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            tc[i] = (i == c) ? 1.f : (i > c ? -pr[i] : 0.f);
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) pr[r] = fmaf(sAm[r * 16 + i], tc[i], pr[r]);
+        }
+        const float bc = v_beta[c], bk = bc * v_rk[c];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            st_bf16(img + kImPT + sw128_offset(r, 16 + c), tc[r] * bc);
+            sTb[r * 16 + c] = tc[r] * bk;
+        }
+    }
+    __syncthreads();
+
+    // ---- W = T diag(beta rk) (k P_t): two rows and four columns per thread
+    {
+        const int tp = tid >> 5, c = (tid & 31) * 4;
+        const int ta = 2 * tp, tb = ta + 1;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        float ra[kPc], rb[kPc];
+#pragma unroll
+        for (int s4 = 0; s4 < kPc; s4 += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(sTb + ta * 16 + s4);
+            const float4 y = *reinterpret_cast<const float4 *>(sTb + tb * 16 + s4);
+            ra[s4] = x.x; ra[s4 + 1] = x.y; ra[s4 + 2] = x.z; ra[s4 + 3] = x.w;
+            rb[s4] = y.x; rb[s4 + 1] = y.y; rb[s4 + 2] = y.z; rb[s4 + 3] = y.w;
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kPc; ++s2) {
+            const float wa = ra[s2], wb = rb[s2];
+            const float4 f = *reinterpret_cast<const float4 *>(sKt + s2 * 128 + c);
+            a0[0] = fmaf(wa, f.x, a0[0]); a0[1] = fmaf(wa, f.y, a0[1]);
+            a0[2] = fmaf(wa, f.z, a0[2]); a0[3] = fmaf(wa, f.w, a0[3]);
+            a1[0] = fmaf(wb, f.x, a1[0]); a1[1] = fmaf(wb, f.y, a1[1]);
+            a1[2] = fmaf(wb, f.z, a1[2]); a1[3] = fmaf(wb, f.w, a1[3]);
+        }
+        *reinterpret_cast<uint2 *>(img + kImW + op_offset(ta, c)) =
+            make_uint2(pack2(fr * a0[0], fr * a0[1]), pack2(fr * a0[2], fr * a0[3]));
+        *reinterpret_cast<uint2 *>(img + kImW + op_offset(tb, c)) =
+            make_uint2(pack2(fr * a1[0], fr * a1[1]), pack2(fr * a1[2], fr * a1[3]));
+    }
+}
+
+// --------------------------------------------------------------------- scan
+constexpr int kScanThreads = 256;   // 8 warps; thread 0 issues copies and MMAs
+constexpr int kStages = 3;          // chunk images in flight (two ahead)
+// stage: the chunk's v rows of one V tile (two SW128 blocks [16 t][64 vi],
+// loaded through vmap), then the image head
+constexpr uint32_t kStV = 0, kStImg = 4096;
+constexpr uint32_t kStageBytes = 19456;  // rounded to 1 KB
+static_assert(kStImg + kPcImgHead <= kStageBytes, "stage size");
+
+// Shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t kOS0 = 0;          // S0 bf16 [128 vi][128 kk]: two SW128 blocks of 16 KB
+constexpr uint32_t kODt = 32768;      // Delta^T bf16 [128 vi][16 t] in an SW128 [128][64] tile
+constexpr uint32_t kOStage = 49152;   // kStages chunk images
+constexpr uint32_t kOBar = kOStage + kStages * kStageBytes;
+constexpr uint32_t kScanSmem = kOBar + 64 + 1024;  // + alignment slack
+static_assert(kScanSmem <= 112 * 1024, "two CTAs per SM");
+
+// TMEM: the state in columns [0, 128); Dd in [128, 144); Do in [144, 160) and
+// [160, 176) for even and odd chunks.
+constexpr uint32_t kScanTmemCols = 256;
+constexpr uint32_t kColS = 0, kColDd = 128, kColDo = 144;
+
+__device__ __forceinline__ void st8(unsigned char *tile, int row, int c8, const float *v) {
+    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = pack8(v);
+}
+
+__global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_constant__ PcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *v_beta = reinterpret_cast<float *>(sm + kOVec);
-    float *v_rk = v_beta + 16, *v_rq = v_rk + 16, *v_cs = v_rq + 16;
-    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(sm + kOBar);
+    uint64_t *bar_full = reinterpret_cast<uint64_t *>(sm + kOBar);  // [kStages]
+    uint64_t *bar_mma = bar_full + kStages;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar_mma + 1);
-    int *s_unit = reinterpret_cast<int *>(bar_mma + 2);
+    int *s_unit = reinterpret_cast<int *>(s_tmem + 1);
     int *s_abort = s_unit + 1;
-    float *sB = reinterpret_cast<float *>(sm + kOB);
-    float *sKt = reinterpret_cast<float *>(sm + kOKt);
-    float *sU = reinterpret_cast<float *>(sm + kOU);
-    float *sKK = reinterpret_cast<float *>(sm + kOKK);
-    float *sQK = reinterpret_cast<float *>(sm + kOQK);
-    float *sT = reinterpret_cast<float *>(sm + kOT);
-    __nv_bfloat16 *rawK = reinterpret_cast<__nv_bfloat16 *>(sm + kORawK);
-    __nv_bfloat16 *rawQ = reinterpret_cast<__nv_bfloat16 *>(sm + kORawQ);
-    __nv_bfloat16 *rawV = reinterpret_cast<__nv_bfloat16 *>(sm + kORawV);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hc = warp >> 2;
     const int row = quad * 32 + lane;  // this thread's TMEM lane (state row)
 
     if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(bar_full + i, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         *s_abort = 0;
     }
     if (warp == 0) {
-        tmem_alloc(s_tmem, kPcTmemCols);
+        tmem_alloc(s_tmem, kScanTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -140,14 +458,12 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
 
-    pdl_wait_primary();  // everything below reads what the conv kernel wrote
+    pdl_wait_primary();  // the chunk images are the prepare kernel's output
 
-    const int H = p.H, HQ = p.HQ, V = p.V, VT = p.VT;
-    const int G = H / HQ;
+    const int H = p.H, V = p.V, VT = p.VT;
     const int n_units = p.header->n_units;
-    const int opts = p.opts;
-    const float fr = (opts & GDN_OPT_NO_RETRIEVE) ? 0.f : 1.f;
     uint32_t mma_phase = 0;
+    uint32_t gc = 0;  // chunks this CTA has consumed: the stage ring position
 
     auto wait_mma = [&]() {
         const bool ok = mbar_wait(bar_mma, mma_phase & 1, kPcWaitNs);
@@ -159,6 +475,16 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+    };
+    // output rows t < rows of the chunk starting at token t0, from Do buffer `buf`
+    auto store_out = [&](int buf, int t0, int rows, int h, int vt) {
+        uint32_t r[16];
+        tmem_ld16(lane_base + kColDo + 16 * buf, r);
+        tmem_wait_ld();
+        __nv_bfloat16 *o = p.out + (size_t)t0 * p.ors + (size_t)h * V + (size_t)vt * 128 + row;
+#pragma unroll
+        for (int t = 0; t < kPc; ++t)
+            if (t < rows) o[(size_t)t * p.ors] = __float2bfloat16_rn(__uint_as_float(r[t]));
     };
 
     while (true) {
@@ -173,13 +499,23 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
             __syncthreads();
             continue;
         }
-        const int kh = h / G;
-        const __nv_bfloat16 *qsrc = p.qb + (size_t)kh * 128;
-        const __nv_bfloat16 *ksrc = p.kb + (size_t)kh * 128;
-        const __nv_bfloat16 *vsrc = p.vb + (size_t)h * V + (size_t)vt * 128;
-        const bool soft = !(opts & (GDN_OPT_NO_DECAY | GDN_OPT_GATE_EXP)) && !p.gate_factor;
-        const float dtb = soft ? __ldg(p.dt_bias + h) : 0.f;
-        const float alog = soft ? __ldg(p.A_log + h) : 0.f;
+        const int nch = (e - s + kPc - 1) / kPc;
+        const size_t chunk_stride = (size_t)H * p.img_bytes;
+        const unsigned char *img0 = p.img + ((size_t)((s >> 4) + seq) * H + h) * p.img_bytes;
+        const int vcol = p.vcol0 + h * V + vt * 128;
+        auto issue = [&](int n) {  // thread 0: chunk n's image head and v rows
+            const uint32_t st = (gc + n) % kStages;
+            unsigned char *dst = sm + kOStage + st * kStageBytes;
+            uint64_t *bar = bar_full + st;
+            mbar_arrive_expect_tx(bar, kPcImgHead + 4096);
+            bulk_load(dst + kStImg, img0 + (size_t)n * chunk_stride, kPcImgHead, bar);
+            tma_load_2d(dst + kStV, &p.vmap, bar, vcol, s + n * kPc);
+            tma_load_2d(dst + kStV + 2048, &p.vmap, bar, vcol + 64, s + n * kPc);
+        };
+        if (tid == 0) {
+            if (nch > 0) issue(0);
+            if (nch > 1) issue(1);
+        }
         const size_t state_row = ((size_t)seq * H + h) * V + (size_t)vt * 128 + row;
 
         // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
@@ -201,209 +537,17 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
             tmem_wait_st();
         }
 
-        const int nchunks = (e - s + kPc - 1) / kPc;
 #pragma unroll 1
-        for (int n = 0; n < nchunks; ++n) {
-            const int t0 = s + n * kPc;
-            const int Cn = min(kPc, e - t0);
+        for (int n = 0; n < nch; ++n) {
+            const uint32_t st = (gc + n) % kStages;
+            unsigned char *stage = sm + kOStage + st * kStageBytes;
+            if (!mbar_wait(bar_full + st, ((gc + n) / kStages) & 1, kPcWaitNs)) atomicExch(s_abort, 1);
 
-            // ---- L: raw k, q, v rows (16-byte vectors) and the gate inputs
-            for (int i = tid; i < 3 * kPc * 16; i += kPcThreads) {
-                const int tile = i >> 8, r = (i >> 4) & 15, c16 = i & 15;
-                const __nv_bfloat16 *src = tile == 0 ? ksrc : tile == 1 ? qsrc : vsrc;
-                __nv_bfloat16 *dst = tile == 0 ? rawK : tile == 1 ? rawQ : rawV;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (r < Cn) v = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)(t0 + r) * p.rs) + c16);
-                *reinterpret_cast<uint4 *>(dst + r * 128 + c16 * 8) = v;
-            }
-            const bool decay = !(opts & GDN_OPT_NO_DECAY);
-            for (int i = tid; i < kPc * 32; i += kPcThreads) {
-                const int r = i >> 5, c4 = i & 31;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r < Cn && decay)
-                    v = __ldg(reinterpret_cast<const float4 *>(p.g + ((size_t)(t0 + r) * H + h) * 128) + c4);
-                *reinterpret_cast<float4 *>(sB + r * 128 + c4 * 4) = v;
-            }
-            if (tid < kPc) {
-                float be = 0.f;
-                if (tid < Cn) {
-                    be = 1.f;
-                    if (!(opts & GDN_OPT_NO_BETA)) {
-                        be = __ldg(p.bl + (size_t)(t0 + tid) * H + h);
-                        if (!(opts & GDN_OPT_BETA_RAW)) be = 1.f / (1.f + expf(-be));
-                    }
-                }
-                v_beta[tid] = be;
-            }
-            __syncthreads();
-
-            // ---- G: cumulative log decays per channel (threads 0..127) and the
-            // q/k norms (threads 128..255: 4 threads per (token, q|k))
-            if (tid < 128) {
-                float acc = 0.f;
-#pragma unroll 4
-                for (int t = 0; t < kPc; ++t) {
-                    const float lg = t < Cn ? log_gate(sB[t * 128 + tid], dtb, alog, opts, p.gate_factor) : 0.f;
-                    acc += lg;
-                    sB[t * 128 + tid] = acc;
-                }
-                v_cs[tid] = expf(acc);  // e^{b_C}: the state's column decay over the chunk
-            } else {
-                const int idx = tid - 128, red = idx >> 2, part = idx & 3;
-                const int t = red & 15;
-                const __nv_bfloat16 *src = (red >> 4) ? rawQ : rawK;
-                float ss = 0.f;
-#pragma unroll 8
-                for (int c = part * 32; c < part * 32 + 32; ++c) {
-                    const float x = __bfloat162float(src[t * 128 + c]);
-                    ss = fmaf(x, x, ss);
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                if (part == 0) {
-                    const float rn = (opts & GDN_OPT_NO_QK_NORM) ? 1.f : rsqrtf(ss + 1e-12f);
-                    ((red >> 4) ? v_rq : v_rk)[t] = rn;
-                }
-            }
-            __syncthreads();
-
-            // ---- AP: KK and QK in 4x4-token blocks (threads 0..159: a half-warp
-            // per block pair, a lane per 8 channels); the scaled operands
-            // Kt, Qt, Kp (threads 160..255)
-            if (tid < 160) {
-                const int bp = tid >> 4, cg = tid & 15;
-                // block pairs (T, I), I <= T
-                const int TB = bp < 1 ? 0 : bp < 3 ? 1 : bp < 6 ? 2 : 3;
-                const int IB = bp - (TB * (TB + 1)) / 2;
-                float kk[4][4], qk[4][4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
-#pragma unroll 2
-                for (int j = 0; j < 8; ++j) {
-                    const int c = cg * 8 + j;
-                    float kt[4], qt[4], ki[4], bt[4], bi[4];
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) {
-                        kt[a] = __bfloat162float(rawK[(4 * TB + a) * 128 + c]);
-                        qt[a] = __bfloat162float(rawQ[(4 * TB + a) * 128 + c]);
-                        ki[a] = __bfloat162float(rawK[(4 * IB + a) * 128 + c]);
-                        bt[a] = sB[(4 * TB + a) * 128 + c];
-                        bi[a] = sB[(4 * IB + a) * 128 + c];
-                    }
-                    if (TB > IB) {
-                        const float ref = bi[3];
-                        float xk[4], xq[4], y[4];
-#pragma unroll
-                        for (int a = 0; a < 4; ++a) {
-                            const float ft = __expf(bt[a] - ref);
-                            xk[a] = kt[a] * ft;
-                            xq[a] = qt[a] * ft;
-                            y[a] = ki[a] * __expf(ref - bi[a]);
-                        }
-#pragma unroll
-                        for (int a = 0; a < 4; ++a)
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) {
-                                kk[a][b] = fmaf(xk[a], y[b], kk[a][b]);
-                                qk[a][b] = fmaf(xq[a], y[b], qk[a][b]);
-                            }
-                    } else {
-#pragma unroll
-                        for (int a = 0; a < 4; ++a)
-#pragma unroll
-                            for (int b = 0; b <= a; ++b) {
-                                const float y = ki[b] * __expf(bt[a] - bi[b]);
-                                if (b < a) kk[a][b] = fmaf(kt[a], y, kk[a][b]);
-                                qk[a][b] = fmaf(qt[a], y, qk[a][b]);
-                            }
-                    }
-                }
-                // sum over the 16 channel groups of the half-warp
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-#pragma unroll
-                        for (int o = 8; o > 0; o >>= 1) {
-                            kk[a][b] += __shfl_xor_sync(0xffffffffu, kk[a][b], o);
-                            qk[a][b] += __shfl_xor_sync(0xffffffffu, qk[a][b], o);
-                        }
-                if (cg == 0) {
-#pragma unroll
-                    for (int a = 0; a < 4; ++a)
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const int t = 4 * TB + a, i = 4 * IB + b;
-                            sKK[t * 16 + i] = kk[a][b];
-                            sQK[t * 16 + i] = qk[a][b];
-                        }
-                }
-            } else {
-                for (int idx = tid - 160; idx < kPc * 128; idx += kPcThreads - 160) {
-                    const int t = idx >> 7, c = idx & 127;
-                    const float bt = sB[t * 128 + c], bC = sB[(kPc - 1) * 128 + c];
-                    const float kr = __bfloat162float(rawK[t * 128 + c]) * v_rk[t];
-                    const float qr = __bfloat162float(rawQ[t * 128 + c]) * v_rq[t] * p.scale;
-                    const float et = __expf(bt);
-                    sKt[t * 128 + c] = kr * et;
-                    st_el(sm + kOQt, 2048, t, c, qr * et);
-                    st_el(sm + kOKp, 2048, t, c, kr * __expf(bC - bt));
-                }
-            }
-            __syncthreads();
-
-            // ---- T = (I + A)^-1 with A[t,i] = beta_t rk_t rk_i KK[t,i] (i < t):
-            // forward substitution, one column per lane (warp 0); the other
-            // warps write P[t,i] = scale rq_t rk_i QK[t,i] (i <= t) as bf16
-            if (warp == 0) {
-                if (lane < 16) {
-                    const int c = lane;
-                    float pr[16], tc[16];
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) pr[r] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        tc[i] = (i == c) ? 1.f : (i > c ? -pr[i] : 0.f);
-#pragma unroll
-                        for (int r = i + 1; r < 16; ++r)
-                            pr[r] = fmaf(fr * v_beta[r] * v_rk[r] * v_rk[i] * sKK[r * 16 + i], tc[i], pr[r]);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) sT[r * 16 + c] = tc[r];
-                }
-            } else if (tid < 32 + kPc * 2) {
-                // row t = (tid - 32) >> 1, eight columns per thread
-                const int q = tid - 32, t = q >> 1, c8 = q & 1;
-                float v8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = c8 * 8 + j;
-                    v8[j] = i <= t ? p.scale * v_rq[t] * v_rk[i] * sQK[t * 16 + i] : 0.f;
-                }
-                st8(sm + kOP, t, c8, v8);
-            }
-            __syncthreads();
-
-            // ---- W = T diag(beta) Kt (bf16 operand), U = T diag(beta) V (fp32);
-            // then the state's bf16 copy S0 and its column decay S *= e^{b_C}
-            for (int idx = tid; idx < 2 * kPc * 128; idx += kPcThreads) {
-                const int which = idx >> 11, t = (idx >> 7) & 15, c = idx & 127;
-                float acc = 0.f;
-                if (which == 0) {
-#pragma unroll
-                    for (int s2 = 0; s2 < kPc; ++s2)
-                        acc = fmaf(sT[t * 16 + s2] * v_beta[s2], sKt[s2 * 128 + c], acc);
-                    st_el(sm + kOW, 2048, t, c, fr * acc);
-                } else {
-#pragma unroll
-                    for (int s2 = 0; s2 < kPc; ++s2)
-                        acc = fmaf(sT[t * 16 + s2] * v_beta[s2], __bfloat162float(rawV[s2 * 128 + c]), acc);
-                    sU[t * 128 + c] = acc;
-                }
-            }
+            // ---- E1: the previous chunk's output rows (warps 0..3); the state's
+            // bf16 copy S0 and its column decay S *= e^{b_C} (all warps)
+            if (hc == 0 && n > 0) store_out((n - 1) & 1, s + (n - 1) * kPc, kPc, h, vt);
             {
+                const float *cs = reinterpret_cast<const float *>(stage + kStImg + kImCs);
                 unsigned char *s0 = sm + kOS0 + hc * 16384;  // this half is one K-block
 #pragma unroll 1
                 for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -416,8 +560,7 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) st8(s0, row, (c0 >> 3) + c8, v + c8 * 8);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = __float_as_uint(v[j] * v_cs[hc * 64 + c0 + j]);
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j] * cs[hc * 64 + c0 + j]);
                     tmem_st32(lane_base + kColS + hc * 64 + c0, r);
                 }
                 tmem_wait_st();
@@ -425,32 +568,42 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
             fence_async_smem();
             sync_all();
 
-            // ---- Dd = S0 W^T, Do = S0 Qt^T (M = 128, N = 16, K = 128)
+            // ---- Delta^T = V^T (T diag(beta))^T - S0 W^T and Do = S0 Qt^T
+            // (M = 128, N = 16; K = 128 for S0, 16 for V^T); the image two
+            // chunks ahead goes into the stage chunk n - 1 used
+            const uint32_t dbuf = kColDo + 16 * (n & 1);
             if (tid == 0) {
-                const uint32_t s0 = smem_u32(sm + kOS0), w = smem_u32(sm + kOW);
-                const uint32_t qt = smem_u32(sm + kOQt);
+                if (n + 2 < nch) issue(n + 2);
+                const uint32_t s0 = smem_u32(sm + kOS0), w = smem_u32(stage + kStImg + kImW);
+                const uint32_t qt = smem_u32(stage + kStImg + kImQt);
                 const uint32_t id = idesc_bf16(128, 16, false, false);
+                const uint32_t idn = idesc_bf16(128, 16, false, false, true);  // -S0
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
                     const uint32_t bo = (ks >> 2) * 2048 + (ks & 3) * 32;
                     mma_bf16(tmem + kColDd, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(w + bo, 16, 1024),
-                             id, ks > 0);
-                    mma_bf16(tmem + kColDo, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(qt + bo, 16, 1024),
+                             idn, ks > 0);
+                    mma_bf16(tmem + dbuf, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(qt + bo, 16, 1024),
                              id, ks > 0);
                 }
+                // V^T: MN-major A (two 64-row blocks 2048 bytes apart); T diag(beta):
+                // columns 16..31 of the P tile
+                mma_bf16(tmem + kColDd, sdesc_sw128(smem_u32(stage + kStV), 2048, 1024),
+                         sdesc_sw128(smem_u32(stage + kStImg + kImPT) + 32, 16, 1024),
+                         idesc_bf16(128, 16, true, false), 1);
                 mma_commit(bar_mma);
             }
             wait_mma();
 
-            // ---- Delta^T[vi, t] = U[t, vi] - Dd[vi, t] -> bf16 A operand (warps 0..3)
+            // ---- Delta^T -> bf16 A operand (warps 0..3)
             if (hc == 0) {
                 uint32_t r[16];
                 tmem_ld16(lane_base + kColDd, r);
                 tmem_wait_ld();
                 float d[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) d[t] = sU[t * 128 + row] - __uint_as_float(r[t]);
+                for (int t = 0; t < 16; ++t) d[t] = __uint_as_float(r[t]);
                 st8(sm + kODt, row, 0, d);
                 st8(sm + kODt, row, 1, d + 8);
             }
@@ -459,31 +612,23 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
 
             // ---- Do += Delta^T P^T (K = 16);  S += Delta^T Kp (N = 128, K = 16)
             if (tid == 0) {
-                const uint32_t dt = smem_u32(sm + kODt), pp = smem_u32(sm + kOP);
-                const uint32_t kp = smem_u32(sm + kOKp);
-                mma_bf16(tmem + kColDo, sdesc_sw128(dt, 16, 1024), sdesc_sw128(pp, 16, 1024),
+                const uint32_t dt = smem_u32(sm + kODt), pp = smem_u32(stage + kStImg + kImPT);
+                const uint32_t kp = smem_u32(stage + kStImg + kImKp);
+                mma_bf16(tmem + dbuf, sdesc_sw128(dt, 16, 1024), sdesc_sw128(pp, 16, 1024),
                          idesc_bf16(128, 16, false, false), 1);
                 mma_bf16(tmem + kColS, sdesc_sw128(dt, 16, 1024), sdesc_sw128(kp, 2048, 1024),
                          idesc_bf16(128, 128, false, true), 1);
                 mma_commit(bar_mma);
             }
             wait_mma();
-
-            // ---- output rows t < Cn (warps 0..3; a warp writes 32 consecutive values of a row)
-            if (hc == 0) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + kColDo, r);
-                tmem_wait_ld();
-                __nv_bfloat16 *obase = p.out + (size_t)t0 * p.ors + (size_t)h * V + (size_t)vt * 128 + row;
-                for (int t = 0; t < Cn; ++t)
-                    obase[(size_t)t * p.ors] = __float2bfloat16_rn(__uint_as_float(r[t]));
-            }
-            sync_all();
             if (*s_abort) break;
         }
+        gc += nch;
         if (*s_abort) break;
 
-        // final state row `row`, columns [64 hc, 64 hc + 64) -> global
+        // the last chunk's output rows; the final state row `row`, columns
+        // [64 hc, 64 hc + 64) -> global
+        if (hc == 0 && nch > 0) store_out((nch - 1) & 1, s + (nch - 1) * kPc, e - s - (nch - 1) * kPc, h, vt);
         {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
 #pragma unroll
@@ -502,15 +647,15 @@ __global__ void __launch_bounds__(kPcThreads, 2) chunked_pc_kernel(const PcParam
     }
 
     if (*s_abort && tid == 0) {
-        // a bounded wait gave up: record it and give MMAs still in flight time
-        // to land before the tensor memory is released
+        // a bounded wait gave up: record it and give copies and MMAs still in
+        // flight time to land before the shared and tensor memory are released
         atomicExch(&p.header->status, 7 /* GDN_ERR_TIMEOUT */);
         const uint64_t ts = global_timer_ns();
         while (global_timer_ns() - ts < 10000000ull) {  // 10 ms
         }
     }
     sync_all();
-    if (warp == 0) tmem_dealloc(tmem, kPcTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kScanTmemCols);
 }
 
 int pc_sm_count() {
@@ -525,14 +670,23 @@ int pc_sm_count() {
 cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStream_t s) {
     static std::atomic<uint64_t> attr_set{0};
     cudaError_t e = once_per_device(attr_set, [] {
-        return cudaFuncSetAttribute(chunked_pc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kPcSmem);
+        cudaError_t e2 = cudaFuncSetAttribute(pc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kPrepSmem);
+        if (e2 != cudaSuccess) return e2;
+        return cudaFuncSetAttribute(pc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kScanSmem);
     });
     if (e != cudaSuccess) return e;
-    const long slots = (long)pc_sm_count() * 2;
-    const int grid = (int)(max_units < slots ? max_units : slots);
-    if (grid <= 0) return cudaSuccess;
-    e = launch_kernel(chunked_pc_kernel, dim3(grid), dim3(kPcThreads), kPcSmem, s, true, p);
+    if (max_units <= 0) return cudaSuccess;
+    const size_t slots = pc_slots(p.B, p.N);
+    if (slots > 0x7fffffffull || p.H > 65535) return cudaErrorInvalidValue;
+    e = launch_kernel(pc_prep_kernel, dim3((unsigned)slots, (unsigned)p.H), dim3(kPrepThreads),
+                      kPrepSmem, s, true, p);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    const long ctas = (long)pc_sm_count() * 2;
+    const int grid = (int)(max_units < ctas ? max_units : ctas);
+    e = launch_kernel(pc_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
     note_launch();
     return e;
 }

@@ -170,7 +170,8 @@ struct ChunkLaunch {
 };
 // Tensor map of a bf16 row-major [rows, cols] operand in the chunked kernel's
 // tile format (64 x 64 boxes, 128-byte swizzle); false if encoding fails.
-bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols);
+bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols,
+                        int box_rows = 64);
 // Segment buffers: up to kMaxSegments segments of up to kMaxSegSeqs sequences.
 inline size_t segment_m_floats(int H) { return (size_t)(kMaxSegments - 1) * H * 128 * 128; }
 inline size_t segment_l_floats(int H, int V) { return (size_t)(kMaxSegments - 1) * H * V * 128; }
@@ -210,12 +211,36 @@ struct DensePack {
 cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
 
 // Chunked recurrence with a per-key-channel gate (bf16, K = 128, V a multiple
-// of 128): q, k, v rows of token t at qb / kb / vb + t * rs (bf16, the first
-// key / value head's columns; key head kh adds kh * 128, value head h and V
-// tile vt add h * V + vt * 128); g [N, H, 128] holds the decay logits, or the
-// gate factors when gate_factor; out [N, ors] (head h at column h * V).
-// Units and their order come from the workspace header and seq_order.
+// of 128), in two launches:
+//  - a prepare kernel, one CTA per (16-token chunk, value head), parallel over
+//    every chunk: it writes the chunk's state-independent operands (the chunk
+//    image below) to the workspace;
+//  - a scan kernel, persistent over (sequence, value head, V tile) units, that
+//    carries the fp32 state in tensor memory and streams the images in.
+// q, k, v rows of token t at qb / kb / vb + t * rs (bf16, the first key /
+// value head's columns; key head kh adds kh * 128, value head h and V tile vt
+// add h * V + vt * 128); g [N, H, 128] holds the decay logits, or the gate
+// factors when gate_factor; out [N, ors] (head h at column h * V).  Only
+// sequences of at least `thr` tokens are processed.  Units and their order
+// come from the workspace header and seq_order.
+//
+// Chunk n of sequence i (start s_i) has image slot (s_i >> 4) + i + n; slots
+// of a valid offsets array never collide and number below pc_slots(B, N).
+// The image of (slot, value head h) sits at img + (slot * H + h) * img_bytes:
+//   [0, 4096)       W  = T diag(beta) Kt, bf16 [16 t][128 c], two SW128 blocks
+//   [4096, 8192)    Qt = scale q e^{b_t}, same layout
+//   [8192, 12288)   Kp = k e^{b_C - b_t}, same layout
+//   [12288, 14336)  an SW128 [16][64] bf16 tile: columns 0..15 hold
+//                   P = scale tril(QK) [t][i], columns 16..31 T diag(beta) [t][s]
+//   [14336, 14848)  e^{b_C}, fp32 [128]
+// The scan kernel reads the chunk's v rows itself, through vmap (a [64 x 16]
+// box map of the matrix whose row t holds token t's v; value head h, V tile
+// vt at column vcol0 + h * V + vt * 128).
+constexpr uint32_t kPcImgHead = 14848;
+inline size_t pc_img_bytes() { return kPcImgHead; }
+inline size_t pc_slots(int B, int N) { return ((size_t)N + 15) / 16 + (size_t)B; }
 struct PcParams {
+    CUtensorMap vmap;  // (first: the map type carries its own alignment)
     const __nv_bfloat16 *qb, *kb, *vb;
     long rs;
     const float *g, *bl, *A_log, *dt_bias;
@@ -226,9 +251,13 @@ struct PcParams {
     __nv_bfloat16 *out;
     long ors;
     int B, N, H, HQ, V, VT;
+    int vcol0;
     float scale;
     int opts;         // GDN_OPT_* (rule and activation options)
     int gate_factor;  // g holds gate factors, not logits
+    int thr;          // chunked sequences have at least thr tokens
+    unsigned char *img;  // chunk images, pc_slots(B, N) * H * pc_img_bytes() bytes
+    long img_bytes;      // pc_img_bytes()
 };
 cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStream_t s);
 

@@ -66,6 +66,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar` as transaction
+// bytes.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+        "r"(smem_u32(bar))
+        : "memory");
+}
 // Store a 2D box from shared memory to global memory (bulk async group of the
 // issuing thread; the source must not change until bulk_wait_read()).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int x,
