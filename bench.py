@@ -710,10 +710,12 @@ def run_dense(args, wl):
     beta = torch.sigmoid(r(B, S, H))
     state = r(B, H, n, n) * 0.05
     out = torch.empty((B, S, H, n), dtype=T, device=dev)
-    # long bf16 sequences with a scalar gate take the chunked kernel through the
-    # workspace entry point (packing kernel + chunked kernel)
-    ws_bytes = gdn.gdn_dense_workspace_bytes(B, S, H, n, gdn.GDN_BF16) if T == torch.bfloat16 else 0
-    chunked = ws_bytes > 0 and not perch and S >= gdn.gdn_chunk_min_len()
+    # long bf16 sequences take a chunked route through the workspace entry
+    # point: packing kernel + chunked kernel (scalar gate), or packing +
+    # prepare + scan kernels (per-channel gate, workspace with chunk images)
+    ws_bytes = (gdn.gdn_dense_workspace_bytes_ex(B, S, H, n, gdn.GDN_BF16, perch)
+                if T == torch.bfloat16 else 0)
+    chunked = ws_bytes > 0 and S >= gdn.gdn_chunk_min_len()
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if chunked else None
 
     def step():
@@ -770,7 +772,14 @@ def run_dense(args, wl):
             "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
             "algorithmic_bytes": kbytes, "kernel_ms": ms,
             "peak_source": f"hbm_gbs of {peak_src}"}
-    if chunked:
+    if chunked and perch:  # prepare + scan against the bytes they must move
+        kb = (2 * B * H * n * n * 4 + 4 * N * H * n * esz + N * H * 4 + N * H * n * 4)
+        ach = kb / (kern_ms * 1e-3) / 1e9
+        roof = {"kernel": "pc_prep_kernel + pc_scan_kernel", "bound": "hbm", "achieved": ach,
+                "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                "algorithmic_bytes": kb, "kernel_ms": kern_ms,
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    elif chunked:
         kflops = N * H * (2 * 64 * (3 * n + 2 * n) + 6 * n * n)
         ach = kflops / (kern_ms * 1e-3) / 1e12
         roof = {"kernel": "chunked_delta_kernel", "bound": "tensor", "achieved": ach, "peak": tf,
@@ -784,7 +793,8 @@ def run_dense(args, wl):
         "config": {"workload": f"{wl.name}-dense", "B": B, "S": S, "H": H, "n": n,
                    "gate": args.dense, "state_carry": "in place"},
         "roofline": roof,
-        "route": "packing kernel + chunked kernel" if chunked else "token-serial dense kernel",
+        "route": ("packing + per-channel prepare + scan kernels" if chunked and perch else
+                  "packing kernel + chunked kernel" if chunked else "token-serial dense kernel"),
         "timing": "CUDA graph replay of one gdn_gated_delta_dense%s call per step"
                   % ("_ws" if chunked else ""),
         "clocks": clocks,

@@ -485,10 +485,20 @@ GDN_API int gdn_gated_delta_dense(const void *q, const void *k, const void *v, c
  * workspace.
  *   workspace  device, 256-byte aligned, gdn_dense_workspace_bytes() bytes
  *              (0 from that query: no chunked route for this geometry)
+ * With gate_per_channel (g [B, S, H, n] gate factors, 16-byte aligned) the
+ * chunked route is the per-key-channel one (16-token chunks: a prepare kernel
+ * over all chunks, then a scan kernel carrying the state; the factors are used
+ * as they are); it needs gdn_dense_workspace_bytes_ex(..., 1) bytes, and with
+ * a smaller workspace the call runs on the token-serial kernel.
  * Errors: as gdn_gated_delta_dense, plus GDN_ERR_WORKSPACE when the chunked
  * route applies and the workspace is missing, misaligned or too small.
  */
 GDN_API size_t gdn_dense_workspace_bytes(int B, int S, int H, int n, int dtype);
+/* Workspace of gdn_gated_delta_dense_ws for this gate kind (0: no chunked
+ * route): gdn_dense_workspace_bytes() plus, with gate_per_channel, the chunk
+ * images ((B S + 15) / 16 + B) * H * 14848 bytes (rounded up to 256). */
+GDN_API size_t gdn_dense_workspace_bytes_ex(int B, int S, int H, int n, int dtype,
+                                            int gate_per_channel);
 GDN_API int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const float *g,
                                      const float *beta, const float *state_init, void *out,
                                      float *state_fin, int B, int S, int H, int n,

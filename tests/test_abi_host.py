@@ -145,6 +145,16 @@ def test_workspace_bytes_ex_adds_the_per_channel_chunk_images(lib):
     assert lib.gdn_workspace_bytes_ex(2, 64, 3, 2, 128, 128, 4, 1, 1, PC) == 0
 
 
+def test_dense_workspace_bytes_ex_adds_the_per_channel_chunk_images(lib):
+    B, S, H, n = 8, 4096, 32, 128
+    base = lib.gdn_dense_workspace_bytes(B, S, H, n, 1)
+    assert base > 0 and lib.gdn_dense_workspace_bytes_ex(B, S, H, n, 1, 0) == base
+    img = ((B * S + 15) // 16 + B) * H * 14848
+    assert lib.gdn_dense_workspace_bytes_ex(B, S, H, n, 1, 1) == base + (img + 255) // 256 * 256
+    assert lib.gdn_dense_workspace_bytes_ex(B, S, H, 64, 1, 1) == 0   # no chunked route
+    assert lib.gdn_dense_workspace_bytes_ex(B, S, H, n, 0, 1) == 0
+
+
 def test_chunk_threshold_setting(lib):
     default = lib.gdn_chunk_min_len()
     assert default > 0

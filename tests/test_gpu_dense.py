@@ -120,19 +120,63 @@ def test_dense_chunked_route_from_a_zero_state_without_state_out():
     assert rel_l2(cpu64(out), o_ref) <= 2e-2
 
 
-@pytest.mark.parametrize("case", ["per_channel", "short", "n64"])
+@pytest.mark.parametrize("case", ["per_channel_without_images", "short", "n64"])
 def test_dense_workspace_call_falls_back_to_the_serial_kernel(case):
-    """Per-channel gates, sequences under the chunk threshold and n != 128 run
-    the token-serial kernel even with a workspace, bit for bit as without."""
+    """Per-channel gates with a workspace too small for the chunk images,
+    sequences under the chunk threshold and n != 128 run the token-serial
+    kernel even with a workspace, bit for bit as without."""
     n = 64 if case == "n64" else 128
     S = max(1, gdn.gdn_chunk_min_len() // 2) if case == "short" else 90
     B, H = 2, 2
     q, k, v, gate, gate_c, beta, state = _inputs(B, S, H, n, torch.bfloat16, 41)
-    gg, pc = (gate_c, True) if case == "per_channel" else (gate, False)
+    pc = case.startswith("per_channel")
+    gg = gate_c if pc else gate
+    ws = True
+    if pc:  # the scalar route's workspace: no room for the per-channel images
+        ws = torch.empty(gdn.gdn_dense_workspace_bytes(B, S, H, n), dtype=torch.uint8, device=DEV)
     s1, s2 = state.clone(), state.clone()
     n0 = gdn.gdn_launch_count()
-    o1, _ = gdn.gdn_gated_delta_dense(q, k, v, gg, beta, s1, gate_per_channel=pc, workspace=True)
+    o1, _ = gdn.gdn_gated_delta_dense(q, k, v, gg, beta, s1, gate_per_channel=pc, workspace=ws)
     assert gdn.gdn_launch_count() - n0 == 1
     o2, _ = gdn.gdn_gated_delta_dense(q, k, v, gg, beta, s2, gate_per_channel=pc)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("S", [16, 300])
+def test_dense_per_channel_chunked_route_matches_oracle_and_the_serial_route(S):
+    """bf16, n = 128, per-key-channel gate factors: with a workspace holding
+    the chunk images the call runs the prepare and scan kernels (16-token
+    chunks; a ragged last chunk for S = 300), state carried in place."""
+    B, H, n = 2, 4, 128
+    q, k, v, _, gate_c, beta, state = _inputs(B, S, H, n, torch.bfloat16, 300 + S)
+    keep = state.clone()
+    ws = torch.empty(gdn.gdn_dense_workspace_bytes_ex(B, S, H, n, gdn.GDN_BF16, True),
+                     dtype=torch.uint8, device=DEV)
+    assert ws.numel() > gdn.gdn_dense_workspace_bytes(B, S, H, n)
+    n0 = gdn.gdn_launch_count()
+    out, fin = gdn.gdn_gated_delta_dense(q, k, v, gate_c, beta, state, gate_per_channel=True,
+                                         scale=0.5, workspace=ws)
+    assert gdn.gdn_launch_count() - n0 == 3  # packing, prepare and scan kernels
+    serial = keep.clone()
+    o_s, f_s = gdn.gdn_gated_delta_dense(q, k, v, gate_c, beta, serial, gate_per_channel=True,
+                                         scale=0.5)
+    o_ref, s_ref = oracle.dense_delta(cpu64(q), cpu64(k), cpu64(v), cpu64(gate_c), cpu64(beta),
+                                      cpu64(keep), per_channel=True, scale=0.5)
+    torch.cuda.synchronize()
+    assert fin.data_ptr() == state.data_ptr()
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(fin), s_ref)
+    assert eo <= 2e-2 and es <= 2e-2, f"out {eo:.3e} (max-abs {max_abs(cpu64(out), o_ref):.3e}), state {es:.3e}"
+    assert rel_l2(cpu64(out), cpu64(o_s)) <= 2e-2 and rel_l2(cpu64(fin), cpu64(f_s)) <= 2e-2
+
+
+def test_dense_per_channel_chunked_route_from_a_zero_state_without_state_out():
+    B, S, H, n = 1, 200, 2, 128
+    q, k, v, _, gate_c, beta, _ = _inputs(B, S, H, n, torch.bfloat16, 32)
+    out, fin = gdn.gdn_gated_delta_dense(q, k, v, gate_c, beta, gate_per_channel=True,
+                                         workspace=True)
+    o_ref, _ = oracle.dense_delta(cpu64(q), cpu64(k), cpu64(v), cpu64(gate_c), cpu64(beta), None,
+                                  per_channel=True, want_state=False)
+    torch.cuda.synchronize()
+    assert fin is None
+    assert rel_l2(cpu64(out), o_ref) <= 2e-2

@@ -33,6 +33,7 @@ __all__ = [
     "gdn_gated_delta_dense",
     "gdn_set_segment_min_len", "gdn_segment_min_len", "gdn_segment_plan",
     "gdn_selftest_wait_timeout", "gdn_dense_workspace_bytes", "gdn_workspace_bytes_ex",
+    "gdn_dense_workspace_bytes_ex",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -108,6 +109,8 @@ def load_library():
     lib.gdn_gated_delta_dense_ws.restype = i
     lib.gdn_dense_workspace_bytes.argtypes = [i] * 5
     lib.gdn_dense_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_dense_workspace_bytes_ex.argtypes = [i] * 6
+    lib.gdn_dense_workspace_bytes_ex.restype = ctypes.c_size_t
     lib.gdn_set_kernel_events.argtypes = [i, vp, vp]
     lib.gdn_set_kernel_events.restype = i
     for name in ("gdn_conv1d_varlen", "gdn_prepare", "gdn_delta_varlen", "gdn_layer_varlen",
@@ -545,6 +548,14 @@ def gdn_dense_workspace_bytes(B: int, S: int, H: int, n: int, dtype: int = GDN_B
     return int(load_library().gdn_dense_workspace_bytes(B, S, H, n, dtype))
 
 
+def gdn_dense_workspace_bytes_ex(B: int, S: int, H: int, n: int, dtype: int = GDN_BF16,
+                                 gate_per_channel: bool = False) -> int:
+    """Workspace of the dense call for this gate kind (with gate_per_channel
+    it adds the chunk images of the per-channel chunked route)."""
+    return int(load_library().gdn_dense_workspace_bytes_ex(B, S, H, n, dtype,
+                                                           int(bool(gate_per_channel))))
+
+
 def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=False, scale=0.0,
                           out=None, state_fin=None, carry_state=None, workspace=None):
     """Recurrence on dense q, k, v [B, S, H, n] (g [B,S,H] or [B,S,H,n], beta [B,S,H]).
@@ -578,7 +589,7 @@ def gdn_gated_delta_dense(q, k, v, g, beta, state=None, *, gate_per_channel=Fals
                                          float(scale), _dtype_code(q), _stream(dev)))
         return out, state_fin
     if workspace is True:
-        nb = gdn_dense_workspace_bytes(B, S, H, n, _dtype_code(q))
+        nb = gdn_dense_workspace_bytes_ex(B, S, H, n, _dtype_code(q), gate_per_channel)
         workspace = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
     if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
         raise GdnError(2, "workspace must be a contiguous uint8 tensor on the inputs' device")

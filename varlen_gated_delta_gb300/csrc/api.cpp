@@ -935,6 +935,59 @@ size_t gdn_dense_workspace_bytes(int B, int S, int H, int n, int dtype) {
     return dense_ws_layout(B, S, H, n).total;
 }
 
+size_t gdn_dense_workspace_bytes_ex(int B, int S, int H, int n, int dtype, int gate_per_channel) {
+    const size_t base = gdn_dense_workspace_bytes(B, S, H, n, dtype);
+    if (base == 0 || !gate_per_channel) return base;
+    return base + align256(pc_slots(B, B * S) * H * pc_img_bytes());
+}
+
+// The dense call's per-key-channel route: the two-kernel chunked form on q,
+// k, v read in place, the gate factors as given, raw beta, no q/k norm.
+static int dense_per_channel_chunked(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const float *state_init, void *out,
+                                     float *state_fin, int B, int S, int H, int n, float scale,
+                                     char *ws, cudaStream_t st) {
+    const DenseWs lay = dense_ws_layout(B, S, H, n);
+    const float *s0 = state_init;
+    if (!s0) {
+        cudaError_t e = cudaMemsetAsync(ws + lay.zero, 0, (size_t)B * H * n * n * 4, st);
+        if (e != cudaSuccess) return cuda_fail(e, "dense: zero initial state");
+        s0 = reinterpret_cast<const float *>(ws + lay.zero);
+    }
+    float *sf = state_fin ? state_fin : reinterpret_cast<float *>(ws + lay.fin);
+    DensePack pk{};  // offsets, order and header only
+    pk.offsets = reinterpret_cast<int32_t *>(ws + lay.offsets);
+    pk.order = reinterpret_cast<int32_t *>(ws + lay.order);
+    pk.header = reinterpret_cast<WsHeader *>(ws + lay.header);
+    pk.B = B; pk.S = S; pk.H = H; pk.n = n;
+    cudaError_t e = launch_dense_pack(pk, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dense pack kernel launch");
+    const long N = (long)B * S;
+    PcParams pp{};
+    if (!encode_operand_map(&pp.vmap, v, N, (long)H * n, 16))
+        return fail(GDN_ERR_CUDA, "dense: encoding the v tensor map failed");
+    pp.qb = static_cast<const __nv_bfloat16 *>(q);
+    pp.kb = static_cast<const __nv_bfloat16 *>(k);
+    pp.vb = static_cast<const __nv_bfloat16 *>(v);
+    pp.rs = (long)H * n;
+    pp.g = g; pp.bl = beta; pp.A_log = nullptr; pp.dt_bias = nullptr;
+    pp.offsets = pk.offsets; pp.seq_order = pk.order; pp.header = pk.header;
+    pp.state_init = s0; pp.state_fin = sf;
+    pp.out = static_cast<__nv_bfloat16 *>(out); pp.ors = (long)H * n;
+    pp.B = B; pp.N = (int)N; pp.H = H; pp.HQ = H; pp.V = n; pp.VT = n / 128; pp.vcol0 = 0;
+    pp.scale = scale == 0.f ? 1.f / std::sqrt((float)n) : scale;
+    pp.opts = GDN_OPT_BETA_RAW | GDN_OPT_NO_QK_NORM;
+    pp.gate_factor = 1;
+    pp.thr = 1;
+    pp.img = reinterpret_cast<unsigned char *>(ws + lay.total);
+    pp.img_bytes = (long)pc_img_bytes();
+    mark_before(GDN_KERNEL_CHUNKED, st);
+    e = launch_delta_chunked_pc(pp, (long)B * H * (n / 128), st);
+    mark_after(GDN_KERNEL_CHUNKED, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dense: per-channel chunked kernel launch");
+    return GDN_OK;
+}
+
 int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const float *g,
                              const float *beta, const float *state_init, void *out,
                              float *state_fin, int B, int S, int H, int n, int gate_per_channel,
@@ -946,6 +999,18 @@ int gdn_gated_delta_dense_ws(const void *q, const void *k, const void *v, const 
     const bool aligned = ((uintptr_t)q & 15) == 0 && ((uintptr_t)k & 15) == 0 &&
                          ((uintptr_t)v & 15) == 0 && ((uintptr_t)out & 15) == 0;
     const size_t need = gdn_dense_workspace_bytes(B, S, H, n, dtype);
+    if (gate_per_channel) {
+        // the per-channel chunked route when the workspace holds its chunk images
+        const size_t need_pc = gdn_dense_workspace_bytes_ex(B, S, H, n, dtype, 1);
+        const bool pc = need > 0 && S >= chunk_min_len() && aligned &&
+                        chunked_supported(dtype, n, n, 3 * H * n) && ((uintptr_t)g & 15) == 0 &&
+                        ((uintptr_t)state_init & 15) == 0 && ((uintptr_t)state_fin & 15) == 0 &&
+                        workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && ws_bytes >= need_pc;
+        if (pc)
+            return dense_per_channel_chunked(q, k, v, g, beta, state_init, out, state_fin, B, S, H,
+                                             n, scale, static_cast<char *>(workspace),
+                                             static_cast<cudaStream_t>(stream));
+    }
     const bool chunked = need > 0 && !gate_per_channel && S >= chunk_min_len() && aligned &&
                          chunked_supported(dtype, n, n, 3 * H * n);
     if (!chunked)

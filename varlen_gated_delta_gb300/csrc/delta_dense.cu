@@ -180,13 +180,16 @@ __global__ void __launch_bounds__(256) dense_pack_kernel(const __grid_constant__
     const long N = (long)p.B * p.S;
     const long stride = (long)gridDim.x * blockDim.x;
     const long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    for (long i = i0; i < N * p.H; i += stride) p.a[i] = logf(fmaxf(__ldg(p.g + i), 1e-30f));
+    if (p.a != nullptr)  // (the per-channel route reads the gate factors itself)
+        for (long i = i0; i < N * p.H; i += stride) p.a[i] = logf(fmaxf(__ldg(p.g + i), 1e-30f));
     if (blockIdx.x == 0) {
-        // 3 maps x 128 bytes as 8-byte words
-        const uint64_t *src = reinterpret_cast<const uint64_t *>(p.maps);
-        uint64_t *dst = static_cast<uint64_t *>(p.maps_dst);
-        if (threadIdx.x < 3 * sizeof(CUtensorMap) / 8) dst[threadIdx.x] = src[threadIdx.x];
-        sm100::tensormap_release();
+        if (p.maps_dst != nullptr) {
+            // 3 maps x 128 bytes as 8-byte words
+            const uint64_t *src = reinterpret_cast<const uint64_t *>(p.maps);
+            uint64_t *dst = static_cast<uint64_t *>(p.maps_dst);
+            if (threadIdx.x < 3 * sizeof(CUtensorMap) / 8) dst[threadIdx.x] = src[threadIdx.x];
+            sm100::tensormap_release();
+        }
         for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.offsets[i] = i * p.S;
         for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.order[i] = i;
         if (threadIdx.x == 0) {
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(256) dense_pack_kernel(const __grid_constant__
 }  // namespace
 
 cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s) {
-    const long work = (long)p.B * p.S * p.H;
+    const long work = p.a != nullptr ? (long)p.B * p.S * p.H : 1;
     long blocks = (work + 255) / 256;
     blocks = blocks < 1 ? 1 : (blocks > 4L * 152 * 8 ? 4L * 152 * 8 : blocks);
     dense_pack_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
