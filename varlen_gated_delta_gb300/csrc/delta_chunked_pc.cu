@@ -72,8 +72,9 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
 
 // ------------------------------------------------------------------ prepare
 // One CTA per (image slot, value head): finds the slot's sequence and chunk,
-// and writes the chunk image.  Slots with no chunk (short sequences, the end
-// of a sequence's slot range) return at once.
+// and writes the chunk image (the P / T diag(beta) tile is built in shared
+// memory, an operand of the W MMA, and copied out at the end).  Slots with no chunk (short sequences, the end of a sequence's slot range)
+// return at once.
 //
 // Every decay factor is a product of per-token gates g_j = e^{log g_j} (each
 // at most 1): with P_t = prod_{j<=t} g_j, Kt = k P_t, Qt = q P_t and
@@ -82,23 +83,29 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
 //   e^{b_t - b_i} = X_TB[t] Z_TB[i],  X_TB[t] = prod_{r<j<=t} g_j,
 //   Z_TB[i] = prod_{i<j<=r} g_j,
 // so those entries are dot products of the rows k_t X_TB[t] (or q_t X_TB[t])
-// and k_i Z_TB[i]; inside a block the factor of (t, i) is formed from the
-// gates between them.  q/k norms are applied to the finished dot products.
+// and k_i Z_TB[i]: one tcgen05 MMA of the 24 Z rows (M, padded to 128: the
+// rows past 24 are whatever shared memory follows them, and their results are
+// never read) with the 24 X rows (N = 32).  Inside a block the factor of
+// (t, i) is formed from the gates between them, on CUDA cores.  q/k norms
+// are applied to the finished dot products.  W^T = Kt^T (T diag(beta rk))^T
+// is a second MMA (M = 128 channels, N = 16, K = 16).
 constexpr int kPrepThreads = 256;
 
-// dynamic shared memory of the prepare kernel, in floats
-constexpr int kFK = 0;             // raw k [16][128]
-constexpr int kFQ = kFK + 2048;    // raw q [16][128]
-constexpr int kFG = kFQ + 2048;    // gate inputs, then gate factors [16][128]
-constexpr int kFKt = kFG + 2048;   // k P_t [16][128]
-constexpr int kFA = kFKt + 2048;   // k X_TB rows of blocks 1..3 [12][128]
-constexpr int kFAQ = kFA + 1536;   // q X_TB rows [12][128]
-constexpr int kFZ = kFAQ + 1536;   // k Z_TB rows: block 1 [4], 2 [8], 3 [12] -> [24][128]
-constexpr int kFAm = kFZ + 3072;   // A[t][i] = fr beta_t rk_t rk_i KK [16][16]
-constexpr int kFTb = kFAm + 256;   // T diag(beta rk) [16][16], for W
-constexpr int kFVec = kFTb + 256;  // beta[16], rk[16], rq[16]
-constexpr int kPrepFloats = kFVec + 48;
-constexpr size_t kPrepSmem = (size_t)kPrepFloats * 4;
+// shared memory of the prepare kernel (bytes from a 1024-aligned base)
+constexpr uint32_t kPZ0 = 0;          // Z rows, channels 0..63: SW128 rows 0..23 of a [128][64] span
+constexpr uint32_t kPK = 3072;        // raw k, fp32 [16][128]
+constexpr uint32_t kPAm = 11264;      // A[t][i] = fr beta_t rk_t rk_i KK, fp32 [16][16]
+constexpr uint32_t kPVec = 12288;     // beta[16], rk[16], rq[16]; barrier, TMEM address, flag
+constexpr uint32_t kPZ1 = 16384;      // Z rows, channels 64..127 (second half of the span)
+constexpr uint32_t kPQ = 19456;       // raw q, fp32 [16][128]
+constexpr uint32_t kPL = 28672;       // X rows (k X: 0..11, q X: 12..23): two SW128 blocks [32][64]
+constexpr uint32_t kPG = 36864;       // gate inputs, then gate factors, fp32 [16][128]
+constexpr uint32_t kPKt = 45056;      // Kt = k P_t, bf16: two SW128 blocks [16][64]
+constexpr uint32_t kPPT = 49152;      // the image's P / T diag(beta) tile (SW128 [16][64])
+constexpr uint32_t kPrepSmem = kPPT + 2048 + 1024;  // + alignment slack: four CTAs per SM
+static_assert(kPK >= 24 * 128 && kPQ >= kPZ1 + 24 * 128 && kPL >= kPQ + 8192, "prepare layout");
+static_assert(kPVec + 256 <= kPZ1 && kPPT % 1024 == 0, "prepare layout");
+constexpr uint32_t kPrepTmemCols = 64;  // KK / QK products in [0, 32), W^T in [32, 48)
 
 // gate factor of one key channel from its input under the options
 __device__ __forceinline__ float gate_factor_of(float x, float dtb, float neg_a, int opts, int factor) {
@@ -110,7 +117,7 @@ __device__ __forceinline__ float gate_factor_of(float x, float dtb, float neg_a,
     return __expf(neg_a * softplus);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_constant__ PcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_constant__ PcParams p) {
     // Every CTA waits for the conv kernel before it exits, slots without a
     // chunk included: the scan kernel's wait on this grid then also covers
     // the conv kernel's output (the schedule in the workspace header).
@@ -130,10 +137,17 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
     if (n < 0 || n >= (e - s + kPc - 1) / kPc) return;
     const int t0 = s + n * kPc, Cn = min(kPc, e - t0);
 
-    extern __shared__ __align__(16) float fs[];
-    float *sK = fs + kFK, *sQ = fs + kFQ, *sG = fs + kFG, *sKt = fs + kFKt;
-    float *sA = fs + kFA, *sAQ = fs + kFAQ, *sZ = fs + kFZ, *sAm = fs + kFAm, *sTb = fs + kFTb;
-    float *v_beta = fs + kFVec, *v_rk = v_beta + 16, *v_rq = v_rk + 16;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *sK = reinterpret_cast<float *>(sm + kPK), *sQ = reinterpret_cast<float *>(sm + kPQ);
+    float *sG = reinterpret_cast<float *>(sm + kPG), *sAm = reinterpret_cast<float *>(sm + kPAm);
+    float *v_beta = reinterpret_cast<float *>(sm + kPVec), *v_rk = v_beta + 16, *v_rq = v_rk + 16;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kPVec + 192);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bar + 1);
+    int *s_bad = reinterpret_cast<int *>(s_tmem + 1);
+    unsigned char *pt = sm + kPPT;  // the P / T diag(beta) tile
+    unsigned char *img = p.img + ((size_t)q * p.H + h) * (size_t)p.img_bytes;  // global
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H, opts = p.opts;
@@ -144,7 +158,16 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
     const float dtb = soft ? __ldg(p.dt_bias + h) : 0.f;
     const float neg_a = soft ? -expf(__ldg(p.A_log + h)) : 0.f;
     const float fr = (opts & GDN_OPT_NO_RETRIEVE) ? 0.f : 1.f;
-    unsigned char *img = p.img + ((size_t)q * H + h) * (size_t)p.img_bytes;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        *s_bad = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kPrepTmemCols);
+        tmem_relinquish();
+    }
 
     // ---- L: raw k, q rows as fp32 (rows past the sequence are 0), the gate
     // inputs and beta
@@ -179,7 +202,10 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
         }
         v_beta[tid] = be;
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
 
     // ---- G: gate factors (1 past the sequence); q/k norms, 8 threads per
     // (token, q|k)
@@ -205,11 +231,13 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
     }
     __syncthreads();
 
-    // ---- R: per key channel c, the decay products and scaled rows.
-    // Threads 0..127: P_t, Kt, Qt (image), e^{b_C} (image), the k X / q X rows;
-    // threads 128..255: the suffix products, Kp (image), the k Z rows.
+    // ---- R: per key channel c, the decay products and the bf16 operands.
+    // Threads 0..127: P_t, Kt = rk k P_t (MMA operand), Qt (image), e^{b_C} (image), the
+    // X rows (MMA operand); threads 128..255: the suffix products, Kp (image),
+    // the Z rows (MMA operand).
     {
         const int c = tid & 127;
+        const uint32_t cb = (uint32_t)(c & 63);
         float g[kPc], k[kPc];
 #pragma unroll
         for (int t = 0; t < kPc; ++t) {
@@ -222,10 +250,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
 #pragma unroll
             for (int t = 0; t < kPc; ++t) {
                 P *= g[t];
-                sKt[t * 128 + c] = k[t] * P;
+                st_bf16(sm + kPKt + op_offset(t, c), k[t] * v_rk[t] * P);
                 st_bf16(img + kImQt + op_offset(t, c), sQ[t * 128 + c] * v_rq[t] * qs * P);
             }
             reinterpret_cast<float *>(img + kImCs)[c] = P;
+            unsigned char *L = sm + kPL + (c >> 6) * 4096;
 #pragma unroll
             for (int TB = 1; TB < 4; ++TB) {
                 float X = 1.f;
@@ -233,8 +262,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
                 for (int a = 0; a < 4; ++a) {
                     const int t = 4 * TB + a, row = 4 * (TB - 1) + a;
                     X *= g[t];
-                    sA[row * 128 + c] = k[t] * X;
-                    sAQ[row * 128 + c] = sQ[t * 128 + c] * X;
+                    st_bf16(L + sw128_offset(row, cb), k[t] * X);
+                    st_bf16(L + sw128_offset(12 + row, cb), sQ[t * 128 + c] * X);
                 }
             }
         } else {
@@ -244,115 +273,119 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
                 st_bf16(img + kImKp + op_offset(t, c), k[t] * v_rk[t] * Qs);
                 Qs *= g[t];
             }
+            unsigned char *Zt = sm + ((c >> 6) ? kPZ1 : kPZ0);
 #pragma unroll
             for (int TB = 1; TB < 4; ++TB) {
                 const int base = TB == 1 ? 0 : TB == 2 ? 4 : 12;
                 float Z = 1.f;
 #pragma unroll
                 for (int i = 4 * TB - 1; i >= 0; --i) {
-                    sZ[(base + i) * 128 + c] = k[i] * Z;
+                    st_bf16(Zt + sw128_offset(base + i, cb), k[i] * Z);
                     Z *= g[i];
                 }
             }
         }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
-    // ---- D: KK and QK in 4x4-token blocks, a half-warp per block pair and a
-    // lane per 8 channels (two groups of 4, 64 apart), summed over the
-    // half-warp.  Threads 0..95: the six pairs of a later block TB with an
-    // earlier block IB (rows k X_TB, q X_TB against k Z_TB); threads 96..159:
-    // the four blocks with themselves (factors from the gates in between).
-    // KK lands as A[t,i] = fr beta_t rk_t rk_i KK (i < t), QK as
-    // P[t,i] = scale rq_t rk_i QK (i <= t) in the image.
-    if (tid < 160) {
-        const int bp = tid >> 4, cg = tid & 15;
+    // ---- D: KK and QK.  Later-block entries: one MMA, D[m][j] = Z_m . X_j
+    // (TMEM columns 0..31), issued by thread 0 and read by warp 0.  A block
+    // with itself: a half-warp per block (warps 4, 5), a lane per 8 channels,
+    // summed over the half-warp.  KK lands as A[t,i] = fr beta_t rk_t rk_i KK
+    // (i < t), QK as P[t,i] = scale rq_t rk_i QK (i <= t) in the image.
+    if (tid == 0) {
+        const uint32_t za = smem_u32(sm + kPZ0), xb = smem_u32(sm + kPL);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * 4096 + (ks & 3) * 32;
+            mma_bf16(tmem, sdesc_sw128(za + ao, 16, 1024), sdesc_sw128(xb + bo, 16, 1024),
+                     idesc_bf16(128, 32, false, false), ks > 0);
+        }
+        mma_commit(bar);
+    }
+    if (warp == 4 || warp == 5) {
+        const int TB = (tid - 128) >> 4, cg = tid & 15;
+        const int t0b = 4 * TB;
         float kk[4][4], qk[4][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
-        int TB, IB;
-        if (bp < 6) {
-            TB = bp < 1 ? 1 : bp < 3 ? 2 : 3;
-            IB = bp - (TB * (TB - 1)) / 2;
-            const int zb = (TB == 1 ? 0 : TB == 2 ? 4 : 12) + 4 * IB;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = cg * 4 + j * 64;
-                float4 x[4], xq[4], y[4];
+        for (int j = 0; j < 2; ++j) {
+            const int c = cg * 4 + j * 64;
+            float4 kr[4], qr[4], gr[4];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    x[a] = *reinterpret_cast<const float4 *>(sA + (4 * (TB - 1) + a) * 128 + c);
-                    xq[a] = *reinterpret_cast<const float4 *>(sAQ + (4 * (TB - 1) + a) * 128 + c);
-                    y[a] = *reinterpret_cast<const float4 *>(sZ + (zb + a) * 128 + c);
-                }
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        kk[a][b] = dot4(x[a], y[b], kk[a][b]);
-                        qk[a][b] = dot4(xq[a], y[b], qk[a][b]);
-                    }
+            for (int a = 0; a < 4; ++a) {
+                kr[a] = *reinterpret_cast<const float4 *>(sK + (t0b + a) * 128 + c);
+                qr[a] = *reinterpret_cast<const float4 *>(sQ + (t0b + a) * 128 + c);
+                gr[a] = *reinterpret_cast<const float4 *>(sG + (t0b + a) * 128 + c);
             }
-        } else {
-            TB = IB = bp - 6;
-            const int t0b = 4 * TB;
+            // column b: f = k_b times the gates of tokens b+1 .. a of the block
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = cg * 4 + j * 64;
-                float4 kr[4], qr[4], gr[4];
+            for (int b = 0; b < 4; ++b) {
+                float4 f = kr[b];
+                qk[b][b] = dot4(qr[b], f, qk[b][b]);
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    kr[a] = *reinterpret_cast<const float4 *>(sK + (t0b + a) * 128 + c);
-                    qr[a] = *reinterpret_cast<const float4 *>(sQ + (t0b + a) * 128 + c);
-                    gr[a] = *reinterpret_cast<const float4 *>(sG + (t0b + a) * 128 + c);
-                }
-                // column b: f = prod of the gates of tokens b+1 .. a of the block
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    float4 f = kr[b];
-                    qk[b][b] = dot4(qr[b], f, qk[b][b]);
-#pragma unroll
-                    for (int a = b + 1; a < 4; ++a) {
-                        f.x *= gr[a].x; f.y *= gr[a].y; f.z *= gr[a].z; f.w *= gr[a].w;
-                        kk[a][b] = dot4(kr[a], f, kk[a][b]);
-                        qk[a][b] = dot4(qr[a], f, qk[a][b]);
-                    }
+                for (int a = b + 1; a < 4; ++a) {
+                    f.x *= gr[a].x; f.y *= gr[a].y; f.z *= gr[a].z; f.w *= gr[a].w;
+                    kk[a][b] = dot4(kr[a], f, kk[a][b]);
+                    qk[a][b] = dot4(qr[a], f, qk[a][b]);
                 }
             }
         }
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int b = 0; b <= a; ++b)
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) {
-                    kk[a][b] += __shfl_xor_sync(0xffffffffu, kk[a][b], o);
+                    if (b < a) kk[a][b] += __shfl_xor_sync(0xffffffffu, kk[a][b], o);
                     qk[a][b] += __shfl_xor_sync(0xffffffffu, qk[a][b], o);
                 }
         if (cg == 0) {
 #pragma unroll
             for (int a = 0; a < 4; ++a)
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int t = 4 * TB + a, i = 4 * IB + b;
-                    if (TB > IB || b < a) sAm[t * 16 + i] = fr * v_beta[t] * v_rk[t] * v_rk[i] * kk[a][b];
-                    if (TB > IB || b <= a)
-                        st_bf16(img + kImPT + sw128_offset(t, i), p.scale * v_rq[t] * v_rk[i] * qk[a][b]);
+                for (int b = 0; b <= a; ++b) {
+                    const int t = t0b + a, i = t0b + b;
+                    if (b < a) sAm[t * 16 + i] = fr * v_beta[t] * v_rk[t] * v_rk[i] * kk[a][b];
+                    st_bf16(pt + sw128_offset(t, i), p.scale * v_rq[t] * v_rk[i] * qk[a][b]);
                 }
         }
     }
-    // the zero upper triangle of P (i > t)
-    {
+    {  // the zero upper triangle of P (i > t)
         const int t = tid >> 4, i = tid & 15;
-        if (i > t) st_bf16(img + kImPT + sw128_offset(t, i), 0.f);
+        if (i > t) st_bf16(pt + sw128_offset(t, i), 0.f);
+    }
+    if (warp == 0) {
+        if (!mbar_wait(bar, 0, kPcWaitNs)) atomicExch(s_bad, 1);
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(tmem, r);  // lanes 0..31 = Z rows
+        tmem_wait_ld();
+        if (lane < 24) {
+            const int TB = lane < 4 ? 1 : lane < 12 ? 2 : 3;
+            const int i = lane - (TB == 1 ? 0 : TB == 2 ? 4 : 12);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const uint32_t kx = TB == 1 ? r[a] : TB == 2 ? r[4 + a] : r[8 + a];
+                const uint32_t qx = TB == 1 ? r[12 + a] : TB == 2 ? r[16 + a] : r[20 + a];
+                const int t = 4 * TB + a;
+                sAm[t * 16 + i] = fr * v_beta[t] * v_rk[t] * v_rk[i] * __uint_as_float(kx);
+                st_bf16(pt + sw128_offset(t, i), p.scale * v_rq[t] * v_rk[i] * __uint_as_float(qx));
+            }
+        }
     }
     __syncthreads();
 
     // ---- T = (I + A)^-1 (A strictly lower): forward substitution, one column
-    // per lane of warp 0.  Stored as T diag(beta) (bf16, image columns 16..31
-    // of the P tile) and T diag(beta rk) (fp32, for W).
+    // per lane of warp 0, stored as T diag(beta) (image columns 16..31 of the
+    // P tile: the B operand of the scan's V^T MMA and of the W MMA below)
     if (warp == 0 && lane < 16) {
         const int c = lane;
         float pr[16], tc[16];
@@ -364,42 +397,47 @@ __global__ void __launch_bounds__(kPrepThreads, 3) pc_prep_kernel(const __grid_c
 #pragma unroll
             for (int r = i + 1; r < 16; ++r) pr[r] = fmaf(sAm[r * 16 + i], tc[i], pr[r]);
         }
-        const float bc = v_beta[c], bk = bc * v_rk[c];
+        const float bc = v_beta[c];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            st_bf16(img + kImPT + sw128_offset(r, 16 + c), tc[r] * bc);
-            sTb[r * 16 + c] = tc[r] * bk;
+        for (int r = 0; r < 16; ++r) st_bf16(pt + sw128_offset(r, 16 + c), tc[r] * bc);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- W^T[c][t] = sum_s Kt[s][c] (T diag(beta))[t][s] (M = 128 channels,
+    // N = 16, K = 16; A is Kt, MN-major); warps 0..3 write W (times fr)
+    if (tid == 0) {
+        mma_bf16(tmem + 32, sdesc_sw128(smem_u32(sm + kPKt), 2048, 1024),
+                 sdesc_sw128(smem_u32(pt) + 32, 16, 1024), idesc_bf16(128, 16, true, false), 0);
+        mma_commit(bar);
+    }
+    if (warp < 4) {
+        if (!mbar_wait(bar, 1, kPcWaitNs)) atomicExch(s_bad, 1);
+        tc_fence_after();
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 32, r);
+        tmem_wait_ld();
+        const int c = warp * 32 + lane;
+#pragma unroll
+        for (int t = 0; t < kPc; ++t) st_bf16(img + kImW + op_offset(t, c), fr * __uint_as_float(r[t]));
+    } else {  // warps 4..7: the P / T diag(beta) tile to the image
+        const int i = tid - 128;
+        reinterpret_cast<uint4 *>(img + kImPT)[i] = reinterpret_cast<const uint4 *>(pt)[i];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (tid == 0 && *s_bad) {
+        atomicExch(&p.header->status, 7 /* GDN_ERR_TIMEOUT */);
+        const uint64_t ts = global_timer_ns();  // let a late MMA land before the
+        while (global_timer_ns() - ts < 10000000ull) {  // tensor memory is released
         }
     }
     __syncthreads();
-
-    // ---- W = T diag(beta rk) (k P_t): two rows and four columns per thread
-    {
-        const int tp = tid >> 5, c = (tid & 31) * 4;
-        const int ta = 2 * tp, tb = ta + 1;
-        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-        float ra[kPc], rb[kPc];
-#pragma unroll
-        for (int s4 = 0; s4 < kPc; s4 += 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(sTb + ta * 16 + s4);
-            const float4 y = *reinterpret_cast<const float4 *>(sTb + tb * 16 + s4);
-            ra[s4] = x.x; ra[s4 + 1] = x.y; ra[s4 + 2] = x.z; ra[s4 + 3] = x.w;
-            rb[s4] = y.x; rb[s4 + 1] = y.y; rb[s4 + 2] = y.z; rb[s4 + 3] = y.w;
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < kPc; ++s2) {
-            const float wa = ra[s2], wb = rb[s2];
-            const float4 f = *reinterpret_cast<const float4 *>(sKt + s2 * 128 + c);
-            a0[0] = fmaf(wa, f.x, a0[0]); a0[1] = fmaf(wa, f.y, a0[1]);
-            a0[2] = fmaf(wa, f.z, a0[2]); a0[3] = fmaf(wa, f.w, a0[3]);
-            a1[0] = fmaf(wb, f.x, a1[0]); a1[1] = fmaf(wb, f.y, a1[1]);
-            a1[2] = fmaf(wb, f.z, a1[2]); a1[3] = fmaf(wb, f.w, a1[3]);
-        }
-        *reinterpret_cast<uint2 *>(img + kImW + op_offset(ta, c)) =
-            make_uint2(pack2(fr * a0[0], fr * a0[1]), pack2(fr * a0[2], fr * a0[3]));
-        *reinterpret_cast<uint2 *>(img + kImW + op_offset(tb, c)) =
-            make_uint2(pack2(fr * a1[0], fr * a1[1]), pack2(fr * a1[2], fr * a1[3]));
-    }
+    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
 // --------------------------------------------------------------------- scan

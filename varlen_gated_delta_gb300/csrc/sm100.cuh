@@ -77,6 +77,15 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint3
         "r"(smem_u32(bar))
         : "memory");
 }
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from shared to global memory, in the issuing thread's bulk async
+// group (see bulk_commit / bulk_wait_all).
+__device__ __forceinline__ void bulk_store(void *dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
 // Store a 2D box from shared memory to global memory (bulk async group of the
 // issuing thread; the source must not change until bulk_wait_read()).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int x,
