@@ -703,6 +703,10 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
             if (!encode_operand_map(&pp.vmap, y, N, width, 16))
                 return fail(GDN_ERR_CUDA, "encoding the per-channel v tensor map failed");
             pp.vcol0 = 2 * HQ * K;
+            // a (chunk, sequence, head) grid unless most of its CTAs would be empty
+            const long gchunks = offsets_host && B <= 65535 ? (max_len + 15) / 16 : 0;
+            pp.grid_chunks = gchunks * B * 4 <= (long)pc_slots(B, N) * 5 ? (int)gchunks : 0;
+            pp.uniform_len = 0;
             mark_before(GDN_KERNEL_CHUNKED, s);
             cudaError_t ce = launch_delta_chunked_pc(pp, max_units, s);
             mark_after(GDN_KERNEL_CHUNKED, s);
@@ -981,6 +985,8 @@ static int dense_per_channel_chunked(const void *q, const void *k, const void *v
     pp.thr = 1;
     pp.img = reinterpret_cast<unsigned char *>(ws + lay.total);
     pp.img_bytes = (long)pc_img_bytes();
+    pp.grid_chunks = B <= 65535 ? (S + 15) / 16 : 0;
+    pp.uniform_len = S;
     mark_before(GDN_KERNEL_CHUNKED, st);
     e = launch_delta_chunked_pc(pp, (long)B * H * (n / 128), st);
     mark_after(GDN_KERNEL_CHUNKED, st);

@@ -28,8 +28,8 @@
 // with a bulk copy and the chunk's v rows with a tensor copy (two chunks
 // ahead), and runs on tcgen05 (M = 128 state rows, bf16 operands, fp32
 // accumulators in tensor memory):
-//   Delta^T = V^T (T diag(beta))^T - S0 W^T,  Do = S0 Qt^T
-//                                 (S0 = bf16 copy of the state, N = 16)
+//   [Delta^T | Do] = S0 [-W ; Qt]^T + [V^T (T diag(beta))^T | 0]
+//                                 (S0 = bf16 copy of the state, N = 32 and 16)
 //   Do += Delta^T P^T             (P = scale tril(QK), K = 16)
 //   S  += Delta^T Kp              (S first scaled by e^{b_C} per column, N = 128)
 #include <cuda.h>
@@ -48,7 +48,9 @@ constexpr int kPc = 16;                        // chunk length
 constexpr uint64_t kPcWaitNs = 2000000000ull;  // bounded waits: 2 s
 
 // chunk image offsets (bytes); P and T diag(beta) share one SW128 tile
-constexpr uint32_t kImW = 0, kImQt = 4096, kImKp = 8192, kImPT = 12288, kImCs = 14336;
+// [-W ; Qt] is one [32][128] operand: two SW128 blocks of [32][64], 4096 bytes
+// apart, rows 0..15 = -W and 16..31 = Qt
+constexpr uint32_t kImWQ = 0, kImKp = 8192, kImPT = 12288, kImCs = 14336;
 static_assert(kImCs + 512 == kPcImgHead, "image head layout");
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -62,6 +64,10 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
 // SW128 blocks of [rows][64], 2048 bytes apart (rows < 16)
 __device__ __forceinline__ uint32_t op_offset(int row, int col) {
     return (uint32_t)(col >> 6) * 2048u + sw128_offset(row, col & 63);
+}
+// the same for the [32][128] operand [-W ; Qt] (blocks 4096 bytes apart)
+__device__ __forceinline__ uint32_t wq_offset(int row, int col) {
+    return (uint32_t)(col >> 6) * 4096u + sw128_offset(row, col & 63);
 }
 __device__ __forceinline__ void st_bf16(unsigned char *p, float v) {
     *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
@@ -123,18 +129,38 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
     // the conv kernel's output (the schedule in the workspace header).
     pdl_wait_primary();
 
-    const int q = blockIdx.x, h = blockIdx.y;
-    // the sequence i of slot q: the last with (offsets[i] >> 4) + i <= q
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((__ldg(p.offsets + mid) >> 4) + mid <= q) lo = mid;
-        else hi = mid - 1;
+    // the CTA's sequence lo, chunk n and value head h: from a (chunk, sequence,
+    // head) grid, or from the image slot q (a (slot, head) grid): the last
+    // sequence with (offsets[i] >> 4) + i <= q
+    int lo, n, h, s, e;
+    if (p.grid_chunks > 0) {
+        n = blockIdx.x;
+        lo = blockIdx.y;
+        h = blockIdx.z;
+        if (p.uniform_len > 0) {
+            s = lo * p.uniform_len;
+            e = s + p.uniform_len;
+        } else {
+            s = __ldg(p.offsets + lo);
+            e = __ldg(p.offsets + lo + 1);
+        }
+    } else {
+        const int slot = blockIdx.x;
+        h = blockIdx.y;
+        lo = 0;
+        int hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((__ldg(p.offsets + mid) >> 4) + mid <= slot) lo = mid;
+            else hi = mid - 1;
+        }
+        s = __ldg(p.offsets + lo);
+        e = __ldg(p.offsets + lo + 1);
+        n = slot - ((s >> 4) + lo);
     }
-    const int s = __ldg(p.offsets + lo), e = __ldg(p.offsets + lo + 1);
     if (s < 0 || e < s || e > p.N || e - s < p.thr) return;
-    const int n = q - ((s >> 4) + lo);
     if (n < 0 || n >= (e - s + kPc - 1) / kPc) return;
+    const int q = (s >> 4) + lo + n;  // the image slot
     const int t0 = s + n * kPc, Cn = min(kPc, e - t0);
 
     extern __shared__ unsigned char smem_raw[];
@@ -170,37 +196,44 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
     }
 
     // ---- L: raw k, q rows as fp32 (rows past the sequence are 0), the gate
-    // inputs and beta
-    for (int i = tid; i < 2 * kPc * 16; i += kPrepThreads) {
-        const int tile = i >> 8, r = (i >> 4) & 15, c8 = (i & 15) * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < Cn)
-            v = __ldg(reinterpret_cast<const uint4 *>((tile == 0 ? ksrc : qsrc) + (size_t)(t0 + r) * p.rs + c8));
-        const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&v);
-        float *dst = (tile == 0 ? sK : sQ) + r * 128 + c8;
-        *reinterpret_cast<float4 *>(dst) = make_float4(__bfloat162float(x[0]), __bfloat162float(x[1]),
-                                                       __bfloat162float(x[2]), __bfloat162float(x[3]));
-        *reinterpret_cast<float4 *>(dst + 4) = make_float4(__bfloat162float(x[4]), __bfloat162float(x[5]),
-                                                           __bfloat162float(x[6]), __bfloat162float(x[7]));
-    }
-    const bool decay = !(opts & GDN_OPT_NO_DECAY);
-    for (int i = tid; i < kPc * 32; i += kPrepThreads) {
-        const int r = i >> 5, c4 = i & 31;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < Cn && decay)
-            v = __ldg(reinterpret_cast<const float4 *>(p.g + ((size_t)(t0 + r) * H + h) * 128) + c4);
-        *reinterpret_cast<float4 *>(sG + r * 128 + c4 * 4) = v;
-    }
-    if (tid < kPc) {
+    // inputs and beta; every load is issued before the first is used
+    {
+        const bool decay = !(opts & GDN_OPT_NO_DECAY);
+        uint4 kq[2];
+        float4 lg[2];
         float be = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = tid + j * kPrepThreads;
+            const int tile = i >> 8, r = (i >> 4) & 15, c8 = (i & 15) * 8;
+            kq[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < Cn)
+                kq[j] = __ldg(reinterpret_cast<const uint4 *>((tile == 0 ? ksrc : qsrc) + (size_t)(t0 + r) * p.rs + c8));
+            const int r2 = i >> 5, c4 = i & 31;
+            lg[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r2 < Cn && decay)
+                lg[j] = __ldg(reinterpret_cast<const float4 *>(p.g + ((size_t)(t0 + r2) * H + h) * 128) + c4);
+        }
         if (tid < Cn) {
             be = 1.f;
-            if (!(opts & GDN_OPT_NO_BETA)) {
-                be = __ldg(p.bl + (size_t)(t0 + tid) * H + h);
-                if (!(opts & GDN_OPT_BETA_RAW)) be = 1.f / (1.f + expf(-be));
-            }
+            if (!(opts & GDN_OPT_NO_BETA)) be = __ldg(p.bl + (size_t)(t0 + tid) * H + h);
         }
-        v_beta[tid] = be;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = tid + j * kPrepThreads;
+            const int tile = i >> 8, r = (i >> 4) & 15, c8 = (i & 15) * 8;
+            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&kq[j]);
+            float *dst = (tile == 0 ? sK : sQ) + r * 128 + c8;
+            *reinterpret_cast<float4 *>(dst) = make_float4(__bfloat162float(x[0]), __bfloat162float(x[1]),
+                                                           __bfloat162float(x[2]), __bfloat162float(x[3]));
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(__bfloat162float(x[4]), __bfloat162float(x[5]),
+                                                               __bfloat162float(x[6]), __bfloat162float(x[7]));
+            reinterpret_cast<float4 *>(sG)[i] = lg[j];
+        }
+        if (tid < kPc) {
+            if (tid < Cn && !(opts & (GDN_OPT_NO_BETA | GDN_OPT_BETA_RAW))) be = 1.f / (1.f + expf(-be));
+            v_beta[tid] = be;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -251,7 +284,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
             for (int t = 0; t < kPc; ++t) {
                 P *= g[t];
                 st_bf16(sm + kPKt + op_offset(t, c), k[t] * v_rk[t] * P);
-                st_bf16(img + kImQt + op_offset(t, c), sQ[t * 128 + c] * v_rq[t] * qs * P);
+                st_bf16(img + kImWQ + wq_offset(16 + t, c), sQ[t * 128 + c] * v_rq[t] * qs * P);
             }
             reinterpret_cast<float *>(img + kImCs)[c] = P;
             unsigned char *L = sm + kPL + (c >> 6) * 4096;
@@ -421,7 +454,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
         tmem_wait_ld();
         const int c = warp * 32 + lane;
 #pragma unroll
-        for (int t = 0; t < kPc; ++t) st_bf16(img + kImW + op_offset(t, c), fr * __uint_as_float(r[t]));
+        for (int t = 0; t < kPc; ++t) st_bf16(img + kImWQ + wq_offset(t, c), -fr * __uint_as_float(r[t]));
     } else {  // warps 4..7: the P / T diag(beta) tile to the image
         const int i = tid - 128;
         reinterpret_cast<uint4 *>(img + kImPT)[i] = reinterpret_cast<const uint4 *>(pt)[i];
@@ -457,10 +490,10 @@ constexpr uint32_t kOBar = kOStage + kStages * kStageBytes;
 constexpr uint32_t kScanSmem = kOBar + 64 + 1024;  // + alignment slack
 static_assert(kScanSmem <= 112 * 1024, "two CTAs per SM");
 
-// TMEM: the state in columns [0, 128); Dd in [128, 144); Do in [144, 160) and
-// [160, 176) for even and odd chunks.
+// TMEM: the state in columns [0, 128); then per chunk parity a 32-column
+// block [Dd | Do] at 128 (even chunks) or 160 (odd chunks).
 constexpr uint32_t kScanTmemCols = 256;
-constexpr uint32_t kColS = 0, kColDd = 128, kColDo = 144;
+constexpr uint32_t kColS = 0, kColD = 128;
 
 __device__ __forceinline__ void st8(unsigned char *tile, int row, int c8, const float *v) {
     *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = pack8(v);
@@ -517,7 +550,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
     // output rows t < rows of the chunk starting at token t0, from Do buffer `buf`
     auto store_out = [&](int buf, int t0, int rows, int h, int vt) {
         uint32_t r[16];
-        tmem_ld16(lane_base + kColDo + 16 * buf, r);
+        tmem_ld16(lane_base + kColD + 32 * buf + 16, r);
         tmem_wait_ld();
         __nv_bfloat16 *o = p.out + (size_t)t0 * p.ors + (size_t)h * V + (size_t)vt * 128 + row;
 #pragma unroll
@@ -598,7 +631,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) st8(s0, row, (c0 >> 3) + c8, v + c8 * 8);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j] * cs[hc * 64 + c0 + j]);
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(cs + hc * 64 + c0 + j);
+                        r[j] = __float_as_uint(v[j] * f.x);
+                        r[j + 1] = __float_as_uint(v[j + 1] * f.y);
+                        r[j + 2] = __float_as_uint(v[j + 2] * f.z);
+                        r[j + 3] = __float_as_uint(v[j + 3] * f.w);
+                    }
                     tmem_st32(lane_base + kColS + hc * 64 + c0, r);
                 }
                 tmem_wait_st();
@@ -606,28 +645,23 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
             fence_async_smem();
             sync_all();
 
-            // ---- Delta^T = V^T (T diag(beta))^T - S0 W^T and Do = S0 Qt^T
-            // (M = 128, N = 16; K = 128 for S0, 16 for V^T); the image two
-            // chunks ahead goes into the stage chunk n - 1 used
-            const uint32_t dbuf = kColDo + 16 * (n & 1);
+            // ---- [Dd | Do] = S0 [-W ; Qt]^T (M = 128, N = 32, K = 128), then
+            // Dd += V^T (T diag(beta))^T (N = 16, K = 16): Dd = Delta^T, Do = S0 Qt^T.
+            // The image two chunks ahead goes into the stage chunk n - 1 used.
+            const uint32_t dbuf = kColD + 32 * (n & 1);  // [Dd | Do] of this chunk
             if (tid == 0) {
                 if (n + 2 < nch) issue(n + 2);
-                const uint32_t s0 = smem_u32(sm + kOS0), w = smem_u32(stage + kStImg + kImW);
-                const uint32_t qt = smem_u32(stage + kStImg + kImQt);
-                const uint32_t id = idesc_bf16(128, 16, false, false);
-                const uint32_t idn = idesc_bf16(128, 16, false, false, true);  // -S0
+                const uint32_t s0 = smem_u32(sm + kOS0), wq = smem_u32(stage + kStImg + kImWQ);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    const uint32_t bo = (ks >> 2) * 2048 + (ks & 3) * 32;
-                    mma_bf16(tmem + kColDd, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(w + bo, 16, 1024),
-                             idn, ks > 0);
-                    mma_bf16(tmem + dbuf, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(qt + bo, 16, 1024),
-                             id, ks > 0);
+                    const uint32_t bo = (ks >> 2) * 4096 + (ks & 3) * 32;
+                    mma_bf16(tmem + dbuf, sdesc_sw128(s0 + ao, 16, 1024), sdesc_sw128(wq + bo, 16, 1024),
+                             idesc_bf16(128, 32, false, false), ks > 0);
                 }
                 // V^T: MN-major A (two 64-row blocks 2048 bytes apart); T diag(beta):
                 // columns 16..31 of the P tile
-                mma_bf16(tmem + kColDd, sdesc_sw128(smem_u32(stage + kStV), 2048, 1024),
+                mma_bf16(tmem + dbuf, sdesc_sw128(smem_u32(stage + kStV), 2048, 1024),
                          sdesc_sw128(smem_u32(stage + kStImg + kImPT) + 32, 16, 1024),
                          idesc_bf16(128, 16, true, false), 1);
                 mma_commit(bar_mma);
@@ -637,7 +671,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
             // ---- Delta^T -> bf16 A operand (warps 0..3)
             if (hc == 0) {
                 uint32_t r[16];
-                tmem_ld16(lane_base + kColDd, r);
+                tmem_ld16(lane_base + dbuf, r);
                 tmem_wait_ld();
                 float d[16];
 #pragma unroll
@@ -652,7 +686,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
             if (tid == 0) {
                 const uint32_t dt = smem_u32(sm + kODt), pp = smem_u32(stage + kStImg + kImPT);
                 const uint32_t kp = smem_u32(stage + kStImg + kImKp);
-                mma_bf16(tmem + dbuf, sdesc_sw128(dt, 16, 1024), sdesc_sw128(pp, 16, 1024),
+                mma_bf16(tmem + dbuf + 16, sdesc_sw128(dt, 16, 1024), sdesc_sw128(pp, 16, 1024),
                          idesc_bf16(128, 16, false, false), 1);
                 mma_bf16(tmem + kColS, sdesc_sw128(dt, 16, 1024), sdesc_sw128(kp, 2048, 1024),
                          idesc_bf16(128, 128, false, true), 1);
@@ -718,8 +752,11 @@ cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStrea
     if (max_units <= 0) return cudaSuccess;
     const size_t slots = pc_slots(p.B, p.N);
     if (slots > 0x7fffffffull || p.H > 65535) return cudaErrorInvalidValue;
-    e = launch_kernel(pc_prep_kernel, dim3((unsigned)slots, (unsigned)p.H), dim3(kPrepThreads),
-                      kPrepSmem, s, true, p);
+    // a (chunk, sequence, head) grid when the longest sequence is known, else
+    // one CTA per (image slot, head) that searches the offsets for its sequence
+    const dim3 pgrid = p.grid_chunks > 0 ? dim3((unsigned)p.grid_chunks, (unsigned)p.B, (unsigned)p.H)
+                                         : dim3((unsigned)slots, (unsigned)p.H);
+    e = launch_kernel(pc_prep_kernel, pgrid, dim3(kPrepThreads), kPrepSmem, s, true, p);
     note_launch();
     if (e != cudaSuccess) return e;
     const long ctas = (long)pc_sm_count() * 2;

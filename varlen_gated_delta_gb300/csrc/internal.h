@@ -227,9 +227,9 @@ cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
 // Chunk n of sequence i (start s_i) has image slot (s_i >> 4) + i + n; slots
 // of a valid offsets array never collide and number below pc_slots(B, N).
 // The image of (slot, value head h) sits at img + (slot * H + h) * img_bytes:
-//   [0, 4096)       W  = T diag(beta) Kt, bf16 [16 t][128 c], two SW128 blocks
-//   [4096, 8192)    Qt = scale q e^{b_t}, same layout
-//   [8192, 12288)   Kp = k e^{b_C - b_t}, same layout
+//   [0, 8192)       [-W ; Qt], bf16 [32][128] as two SW128 blocks of [32][64]:
+//                   rows 0..15 -W = -T diag(beta) Kt, rows 16..31 Qt = scale q e^{b_t}
+//   [8192, 12288)   Kp = k e^{b_C - b_t}, bf16 [16 t][128 c], two SW128 blocks
 //   [12288, 14336)  an SW128 [16][64] bf16 tile: columns 0..15 hold
 //                   P = scale tril(QK) [t][i], columns 16..31 T diag(beta) [t][s]
 //   [14336, 14848)  e^{b_C}, fp32 [128]
@@ -258,6 +258,12 @@ struct PcParams {
     int thr;          // chunked sequences have at least thr tokens
     unsigned char *img;  // chunk images, pc_slots(B, N) * H * pc_img_bytes() bytes
     long img_bytes;      // pc_img_bytes()
+    // prepare grid: grid_chunks > 0 (at least the chunks of the longest
+    // sequence; B <= 65535) runs a (chunk, sequence, head) grid, 0 a (slot,
+    // head) grid; uniform_len > 0: sequence i is [i L, i L + L) (offsets are
+    // then read by the scan kernel only)
+    int grid_chunks;
+    int uniform_len;
 };
 cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStream_t s);
 
