@@ -220,3 +220,26 @@ def test_per_channel_chunked_outputs_stay_inside_their_tensors(in_place):
     _layer(wl, d, out=out.t, conv_fin=cfin.t, state_fin=sfin.t, workspace=ws.t,
            offsets_host=d["offsets_list"])
     assert [g.guards_intact() for g in (out, cfin, sfin, ws)] == [True] * 4
+
+
+@pytest.mark.parametrize("offs", [[0, 4, 8, 10], [0, 70, 140, 170], [0, 100, 90, 160]])
+def test_per_channel_malformed_device_offsets_write_nothing_outside(offs):
+    """Offsets checked on the device only (no host copy): malformed batches make
+    the call report GDN_ERR_OFFSETS through the workspace status and no kernel
+    writes outside its tensors, the per-channel prepare kernel included."""
+    N = 160 if offs[-1] != 10 else 12
+    wl, d = _case("decode", (N,), seed_shift=14, H=2, HQ=1)
+    B = len(offs) - 1
+    d = dict(d, offsets=torch.tensor(offs, dtype=torch.int32, device=DEV),
+             conv_init=torch.zeros((B, wl.width, wl.L), dtype=torch.bfloat16, device=DEV),
+             state_init=torch.zeros((B, wl.H, wl.V, wl.K), dtype=torch.float32, device=DEV))
+    out = Guarded((N, wl.H, wl.V), torch.bfloat16)
+    cfin = Guarded((B, wl.width, wl.L), torch.bfloat16)
+    sfin = Guarded((B, wl.H, wl.V, wl.K), torch.float32)
+    ws_n = gdn.gdn_workspace_bytes_ex(B, N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D, gdn.GDN_BF16, PC)
+    ws = Guarded((ws_n,), torch.uint8)
+    _layer(wl, d, out=out.t, conv_fin=cfin.t, state_fin=sfin.t, workspace=ws.t)
+    assert [g.guards_intact() for g in (out, cfin, sfin, ws)] == [True] * 4
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.gdn_workspace_status(ws.t)
+    assert ei.value.status == 4
