@@ -18,6 +18,7 @@ from varlen_gated_delta_gb300 import workloads as W
 from gdn_testlib import cpu64, max_abs, rel_l2
 from test_gpu_parity import SERIAL_ONLY, chunk_threshold
 from test_gpu_canary import Guarded
+from test_gpu_chunked import segment_threshold
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -243,3 +244,50 @@ def test_per_channel_malformed_device_offsets_write_nothing_outside(offs):
     with pytest.raises(gdn.GdnError) as ei:
         gdn.gdn_workspace_status(ws.t)
     assert ei.value.status == 4
+
+
+# ---- segment-parallel scan (few long per-channel sequences)
+
+SEG_CASES = [
+    ("one-long", "decode", (1000,), dict(H=8, HQ=4)),
+    ("among-serial", "decode", (5, 1500, 40, 1), dict(H=8, HQ=4)),
+    ("long-geometry", "long", (1100,), dict(H=4, HQ=2)),
+    ("two-long", "decode", (900, 1300), dict(H=8, HQ=4)),
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES, ids=[c[0] for c in SEG_CASES])
+def test_per_channel_segment_parallel_matches_oracle_and_the_unsegmented_path(case):
+    """Segments (the segment threshold lowered to 256 tokens): the prepare
+    kernel, scan pass 1 (transitions and local states from zero), the
+    combine step and scan pass 2 against the oracle and the one-pass scan."""
+    _, base, lens, over = case
+    wl, d = _case(base, lens, seed_shift=20, **over)
+    with segment_threshold(1 << 30):
+        n0 = gdn.gdn_launch_count()
+        plain = _layer(wl, d, offsets_host=d["offsets_list"])
+        n_plain = gdn.gdn_launch_count() - n0
+    with segment_threshold(256):
+        n0 = gdn.gdn_launch_count()
+        out, cfin, sfin = _layer(wl, d, offsets_host=d["offsets_list"])
+        n_seg = gdn.gdn_launch_count() - n0
+    assert n_seg == n_plain + 2  # pass 1 and the combine step beside pass 2
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cpu64(cfin), c_ref)
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], f"out {eo:.3e} state {es:.3e}"
+    assert rel_l2(cpu64(out), cpu64(plain[0])) <= TOL["bf16"]
+    assert rel_l2(cpu64(sfin), cpu64(plain[2])) <= TOL["bf16"]
+
+
+def test_per_channel_segment_parallel_in_place_carry():
+    wl, d = _case("decode", (600, 1000), seed_shift=21, H=8, HQ=4)
+    o_ref, _, s_ref = _oracle_layer(wl, d)
+    st, cs = d["state_init"].clone(), d["conv_init"].clone()
+    with segment_threshold(256):
+        out, cfin, sfin = _layer(wl, dict(d, state_init=st, conv_init=cs),
+                                 offsets_host=d["offsets_list"], state_fin=st, conv_fin=cs)
+    torch.cuda.synchronize()
+    assert sfin.data_ptr() == st.data_ptr()
+    assert rel_l2(cpu64(out), o_ref) <= TOL["bf16"] and rel_l2(cpu64(sfin), s_ref) <= TOL["bf16"]

@@ -621,7 +621,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     // Long chunked sequences that leave most of the GPU idle are cut into
     // segments run in parallel (two chunked launches and a combine step).
     // Sequences shorter than one chunk beside them run token-serially then.
-    const SegmentPlan seg = chunk_ok && !per_channel && offsets_host && lay.seg != 0
+    const SegmentPlan seg = chunk_ok && offsets_host && lay.seg != 0
                                 ? plan_segments(offsets_host, B, H, V, segment_plan_thr(thr),
                                                 lay.seg_seqs, sm_count_host())
                                 : SegmentPlan{};
@@ -685,8 +685,24 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         e = launch_prepare(pp, dtype, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "prepare kernel launch");
     }
+    // segment-parallel buffers and plan (both chunked forms)
+    ChunkLaunch segl{};
+    if (seg.n > 0) {
+        float *segb = reinterpret_cast<float *>(ws + lay.seg);
+        segl.nseq_seg = seg.n;
+        for (int i = 0; i < kMaxSegSeqs; ++i) segl.seg_seq[i] = seg.seq[i];
+        for (int i = 0; i <= kMaxSegSeqs; ++i) {
+            segl.seg_m0[i] = seg.m0[i];
+            segl.seg_s0[i] = seg.s0[i];
+        }
+        segl.seg_M = segb;
+        segl.seg_L = segl.seg_M + (size_t)lay.seg_seqs * segment_m_floats(H);
+        segl.seg_S = segl.seg_L + (size_t)lay.seg_seqs * segment_l_floats(H, V);
+        segl.offsets = offsets; segl.state_init = state_init; segl.header = hdr;
+        segl.H = H; segl.V = V;
+    }
     auto launch_chunked = [&]() -> int {
-        if (per_channel) {  // the per-key-channel chunked kernel
+        if (per_channel) {  // the per-key-channel chunked kernels
             const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
             PcParams pp{};
             pp.qb = yb; pp.kb = yb + (size_t)HQ * K; pp.vb = yb + 2 * (size_t)HQ * K; pp.rs = width;
@@ -708,7 +724,8 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
             pp.grid_chunks = gchunks * B * 4 <= (long)pc_slots(B, N) * 5 ? (int)gchunks : 0;
             pp.uniform_len = 0;
             mark_before(GDN_KERNEL_CHUNKED, s);
-            cudaError_t ce = launch_delta_chunked_pc(pp, max_units, s);
+            cudaError_t ce = seg.n > 0 ? launch_delta_chunked_pc_segmented(pp, segl, s)
+                                       : launch_delta_chunked_pc(pp, max_units, s);
             mark_after(GDN_KERNEL_CHUNKED, s);
             if (ce != cudaSuccess) return cuda_fail(ce, "per-channel chunked kernel launch");
             return GDN_OK;
@@ -720,16 +737,15 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         cl.B = B; cl.N = N; cl.H = H; cl.HQ = HQ; cl.V = V; cl.W = (int)width;
         cl.scale = eff_scale; cl.max_units = max_units; cl.opts = opts;
         if (seg.n > 0) {
-            float *segb = reinterpret_cast<float *>(ws + lay.seg);
             cl.nseq_seg = seg.n;
             for (int i = 0; i < kMaxSegSeqs; ++i) cl.seg_seq[i] = seg.seq[i];
             for (int i = 0; i <= kMaxSegSeqs; ++i) {
                 cl.seg_m0[i] = seg.m0[i];
                 cl.seg_s0[i] = seg.s0[i];
             }
-            cl.seg_M = segb;
-            cl.seg_L = cl.seg_M + (size_t)lay.seg_seqs * segment_m_floats(H);
-            cl.seg_S = cl.seg_L + (size_t)lay.seg_seqs * segment_l_floats(H, V);
+            cl.seg_M = segl.seg_M;
+            cl.seg_L = segl.seg_L;
+            cl.seg_S = segl.seg_S;
         }
         mark_before(GDN_KERNEL_CHUNKED, s);
         cudaError_t ce = seg.n > 0 ? launch_delta_chunked_segmented(cl, s) : launch_delta_chunked(cl, s);

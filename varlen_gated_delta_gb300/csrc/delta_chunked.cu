@@ -116,8 +116,8 @@ struct ChunkParams {
 // Segment length of a sequence of len tokens cut into at most nseg segments
 // (a multiple of the chunk) and the number of non-empty segments.
 __device__ __forceinline__ void segments_of(int len, int nseg, int &seg_len, int &count) {
-    seg_len = ((len + nseg - 1) / nseg + kC - 1) / kC * kC;
-    count = seg_len > 0 ? (len + seg_len - 1) / seg_len : 0;
+    static_assert(kC == 64, "segment_split rounds segments to the 64-token chunk");
+    segment_split(len, nseg, seg_len, count);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -1057,6 +1057,28 @@ cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s) {
     cudaError_t e = chunk_setup(c, map, omap, p);
     if (e != cudaSuccess) return e;
     return chunk_launch(map, omap, p, c.max_units, s);
+}
+
+cudaError_t launch_segment_combine(const ChunkLaunch &c, cudaStream_t s) {
+    if (c.nseq_seg < 1 || c.nseq_seg > kMaxSegSeqs) return cudaErrorInvalidValue;
+    ChunkParams p{};
+    p.offsets = c.offsets;
+    p.state_init = c.state_init;
+    p.H = c.H;
+    p.V = c.V;
+    p.nseq_seg = c.nseq_seg;
+    for (int i = 0; i < kMaxSegSeqs; ++i) p.seg_seq[i] = c.seg_seq[i];
+    for (int i = 0; i <= kMaxSegSeqs; ++i) {
+        p.seg_m0[i] = c.seg_m0[i];
+        p.seg_s0[i] = c.seg_s0[i];
+    }
+    p.seg_M = c.seg_M;
+    p.seg_L = c.seg_L;
+    p.seg_S = c.seg_S;
+    cudaError_t e = launch_kernel(segment_combine_kernel, dim3((unsigned)(c.nseq_seg * c.H * (c.V / 32))),
+                                  dim3(128), 0, s, true, p);
+    note_launch();
+    return e;
 }
 
 // c.nseq_seg long chunked sequences (c.seg_seq), sequence i cut into up to

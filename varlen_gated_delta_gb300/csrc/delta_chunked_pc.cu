@@ -532,7 +532,8 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
     pdl_wait_primary();  // the chunk images are the prepare kernel's output
 
     const int H = p.H, V = p.V, VT = p.VT;
-    const int n_units = p.header->n_units;
+    const int n_units = p.seg_mode ? p.seg_units : p.header->n_units;
+    unsigned int *counter = p.seg_mode ? p.counter : &p.header->next_unit;
     uint32_t mma_phase = 0;
     uint32_t gc = 0;  // chunks this CTA has consumed: the stage ring position
 
@@ -559,20 +560,60 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
     };
 
     while (true) {
-        if (tid == 0) *s_unit = (int)atomicAdd(&p.header->next_unit, 1u);
+        if (tid == 0) *s_unit = (int)atomicAdd(counter, 1u);
         __syncthreads();
         const int u = *s_unit;
         if (u >= n_units || *s_abort) break;
-        const int seq = p.seq_order[u / (H * VT)];
-        const int h = (u / VT) % H, vt = u % VT;
-        const int s = p.offsets[seq], e = p.offsets[seq + 1];
+        int seq, h, vt, q = 0, seg = 0, nseg_here = 1;
+        bool mtile = false;  // the transition tile of a segment (seg_mode 1)
+        if (p.seg_mode == 0) {
+            seq = p.seq_order[u / (H * VT)];
+            h = (u / VT) % H;
+            vt = u % VT;
+        } else {
+            // q: the segment's index among this pass's segments (numbering the M /
+            // L or start-state buffers); constant indices into the tables only
+            const int tiles = VT + (p.seg_mode == 1);
+            q = u / (H * tiles);
+            h = (u / tiles) % H;
+            const int tile = u % tiles;
+            mtile = tile == VT;
+            vt = mtile ? 0 : tile;
+            seq = p.seg_seq[0];
+            seg = q;
+            nseg_here = p.seg_s0[1];
+#pragma unroll
+            for (int i = 1; i < kMaxSegSeqs; ++i) {
+                const int f = p.seg_mode == 1 ? p.seg_m0[i] : p.seg_s0[i];
+                if (i < p.nseq_seg && q >= f) {
+                    seq = p.seg_seq[i];
+                    seg = q - f;
+                    nseg_here = p.seg_s0[i + 1] - p.seg_s0[i];
+                }
+            }
+        }
+        const int s_seq = p.offsets[seq];
+        int s = s_seq, e = p.offsets[seq + 1];
         if (s < 0 || e < s || e > p.N) {  // malformed offsets: nothing is read or written
             __syncthreads();
             continue;
         }
+        if (p.seg_mode) {  // this segment's tokens (a multiple of 64 from the sequence start)
+            int seg_len;
+            segment_split(e - s, nseg_here, seg_len, nseg_here);
+            if (seg >= (p.seg_mode == 1 ? nseg_here - 1 : nseg_here)) {
+                __syncthreads();
+                continue;
+            }
+            s += seg * seg_len;
+            e = min(e, s + seg_len);
+        }
+        const bool write_out = p.seg_mode != 1;
         const int nch = (e - s + kPc - 1) / kPc;
         const size_t chunk_stride = (size_t)H * p.img_bytes;
-        const unsigned char *img0 = p.img + ((size_t)((s >> 4) + seq) * H + h) * p.img_bytes;
+        // the image of the unit's first chunk: chunk (s - s_seq) / 16 of its sequence
+        const unsigned char *img0 =
+            p.img + ((size_t)((s_seq >> 4) + seq + (s - s_seq) / kPc) * H + h) * p.img_bytes;
         const int vcol = p.vcol0 + h * V + vt * 128;
         auto issue = [&](int n) {  // thread 0: chunk n's image head and v rows
             const uint32_t st = (gc + n) % kStages;
@@ -589,19 +630,28 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
         }
         const size_t state_row = ((size_t)seq * H + h) * V + (size_t)vt * 128 + row;
 
-        // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM
+        // state row `row`, columns [64 hc, 64 hc + 64) -> TMEM: the initial
+        // state, a segment's start state, zero, or the identity (transition tile)
         {
             const float *src = p.state_init + state_row * 128 + hc * 64;
+            if (p.seg_mode == 2)
+                src = p.seg_S + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
+                if (p.seg_mode == 1) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(src + c0 + j);
-                    r[j] = __float_as_uint(f.x);
-                    r[j + 1] = __float_as_uint(f.y);
-                    r[j + 2] = __float_as_uint(f.z);
-                    r[j + 3] = __float_as_uint(f.w);
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(mtile && row == hc * 64 + c0 + j ? 1.f : 0.f);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(src + c0 + j);
+                        r[j] = __float_as_uint(f.x);
+                        r[j + 1] = __float_as_uint(f.y);
+                        r[j + 2] = __float_as_uint(f.z);
+                        r[j + 3] = __float_as_uint(f.w);
+                    }
                 }
                 tmem_st32(lane_base + kColS + hc * 64 + c0, r);
             }
@@ -616,7 +666,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
 
             // ---- E1: the previous chunk's output rows (warps 0..3); the state's
             // bf16 copy S0 and its column decay S *= e^{b_C} (all warps)
-            if (hc == 0 && n > 0) store_out((n - 1) & 1, s + (n - 1) * kPc, kPc, h, vt);
+            if (hc == 0 && n > 0 && write_out) store_out((n - 1) & 1, s + (n - 1) * kPc, kPc, h, vt);
             {
                 const float *cs = reinterpret_cast<const float *>(stage + kStImg + kImCs);
                 unsigned char *s0 = sm + kOS0 + hc * 16384;  // this half is one K-block
@@ -660,10 +710,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
                              idesc_bf16(128, 32, false, false), ks > 0);
                 }
                 // V^T: MN-major A (two 64-row blocks 2048 bytes apart); T diag(beta):
-                // columns 16..31 of the P tile
-                mma_bf16(tmem + dbuf, sdesc_sw128(smem_u32(stage + kStV), 2048, 1024),
-                         sdesc_sw128(smem_u32(stage + kStImg + kImPT) + 32, 16, 1024),
-                         idesc_bf16(128, 16, true, false), 1);
+                // columns 16..31 of the P tile (v = 0 for a transition tile)
+                if (!mtile)
+                    mma_bf16(tmem + dbuf, sdesc_sw128(smem_u32(stage + kStV), 2048, 1024),
+                             sdesc_sw128(smem_u32(stage + kStImg + kImPT) + 32, 16, 1024),
+                             idesc_bf16(128, 16, true, false), 1);
                 mma_commit(bar_mma);
             }
             wait_mma();
@@ -700,9 +751,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
 
         // the last chunk's output rows; the final state row `row`, columns
         // [64 hc, 64 hc + 64) -> global
-        if (hc == 0 && nch > 0) store_out((nch - 1) & 1, s + (nch - 1) * kPc, e - s - (nch - 1) * kPc, h, vt);
-        {
+        if (hc == 0 && nch > 0 && write_out)
+            store_out((nch - 1) & 1, s + (nch - 1) * kPc, e - s - (nch - 1) * kPc, h, vt);
+        if (p.seg_mode != 2 || seg == nseg_here - 1) {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
+            if (p.seg_mode == 1)
+                dst = mtile ? p.seg_M + ((((size_t)q * H + h) * 128 + row) * 128 + hc * 64)
+                            : p.seg_L + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
@@ -749,7 +804,6 @@ cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStrea
                                     (int)kScanSmem);
     });
     if (e != cudaSuccess) return e;
-    if (max_units <= 0) return cudaSuccess;
     const size_t slots = pc_slots(p.B, p.N);
     if (slots > 0x7fffffffull || p.H > 65535) return cudaErrorInvalidValue;
     // a (chunk, sequence, head) grid when the longest sequence is known, else
@@ -761,6 +815,40 @@ cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStrea
     if (e != cudaSuccess) return e;
     const long ctas = (long)pc_sm_count() * 2;
     const int grid = (int)(max_units < ctas ? max_units : ctas);
+    if (grid <= 0) return cudaSuccess;  // (the prepare kernel ran: a segment pass may follow)
+    e = launch_kernel(pc_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_delta_chunked_pc_segmented(const PcParams &p0, const ChunkLaunch &c, cudaStream_t s) {
+    if (c.nseq_seg < 1 || c.nseq_seg > kMaxSegSeqs) return cudaErrorInvalidValue;
+    PcParams p = p0;
+    p.nseq_seg = c.nseq_seg;
+    for (int i = 0; i < kMaxSegSeqs; ++i) p.seg_seq[i] = c.seg_seq[i];
+    for (int i = 0; i <= kMaxSegSeqs; ++i) {
+        p.seg_m0[i] = c.seg_m0[i];
+        p.seg_s0[i] = c.seg_s0[i];
+    }
+    p.seg_M = c.seg_M;
+    p.seg_L = c.seg_L;
+    p.seg_S = c.seg_S;
+    // the prepare kernel (images of every chunk) and pass 1 (transitions and
+    // local states of every segment but the last, from zero)
+    p.seg_mode = 1;
+    p.seg_units = c.seg_m0[c.nseq_seg] * p.H * (p.VT + 1);
+    p.counter = &c.header->seg_next[0];
+    cudaError_t e = launch_delta_chunked_pc(p, p.seg_units, s);
+    if (e != cudaSuccess) return e;
+    e = launch_segment_combine(c, s);
+    if (e != cudaSuccess) return e;
+    // pass 2: every segment from its start state, outputs and final states
+    p.seg_mode = 2;
+    p.seg_units = c.seg_s0[c.nseq_seg] * p.H * p.VT;
+    p.counter = &c.header->seg_next[1];
+    const long ctas = (long)pc_sm_count() * 2;
+    const int grid = (int)(p.seg_units < ctas ? p.seg_units : ctas);
+    if (grid <= 0) return cudaSuccess;
     e = launch_kernel(pc_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
     note_launch();
     return e;

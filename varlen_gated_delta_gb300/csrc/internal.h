@@ -172,6 +172,17 @@ struct ChunkLaunch {
 // tile format (64 x 64 boxes, 128-byte swizzle); false if encoding fails.
 bool encode_operand_map(CUtensorMap *map, const void *base, long rows, long cols,
                         int box_rows = 64);
+// Segments of a segmented sequence of `len` tokens cut into at most `nseg`:
+// seg_len tokens each (a multiple of 64, so also of every chunk length),
+// `count` segments in all.
+__host__ __device__ inline void segment_split(int len, int nseg, int &seg_len, int &count) {
+    seg_len = ((len + nseg - 1) / nseg + 63) / 64 * 64;
+    count = seg_len > 0 ? (len + seg_len - 1) / seg_len : 0;
+}
+// Start states of the segments of c's segmented sequences from the phase-1
+// transitions and local states (S_0 = state_init, S_{j+1} = S_j M_j + L_j),
+// written to c.seg_S; launched with programmatic dependent launch.
+cudaError_t launch_segment_combine(const ChunkLaunch &c, cudaStream_t s);
 // Segment buffers: up to kMaxSegments segments of up to kMaxSegSeqs sequences.
 inline size_t segment_m_floats(int H) { return (size_t)(kMaxSegments - 1) * H * 128 * 128; }
 inline size_t segment_l_floats(int H, int V) { return (size_t)(kMaxSegments - 1) * H * V * 128; }
@@ -264,8 +275,20 @@ struct PcParams {
     // then read by the scan kernel only)
     int grid_chunks;
     int uniform_len;
+    // segment-parallel scan (seg_mode 1 / 2, as in ChunkLaunch; 0: one pass)
+    int seg_mode, nseq_seg, seg_units;
+    int seg_seq[kMaxSegSeqs], seg_m0[kMaxSegSeqs + 1], seg_s0[kMaxSegSeqs + 1];
+    unsigned int *counter;  // work counter of a segment pass
+    float *seg_M, *seg_L;
+    const float *seg_S;
 };
 cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStream_t s);
+// The same with the scan segment-parallel for the sequences of `seg` (its
+// nseq_seg, seg_seq, seg_m0, seg_s0 and seg buffers; p's seg fields are set here):
+// prepare kernel, scan pass 1 (transitions M and local states L), segment
+// combine, scan pass 2 (outputs and final states).
+cudaError_t launch_delta_chunked_pc_segmented(const PcParams &p, const ChunkLaunch &seg,
+                                              cudaStream_t s);
 
 bool chunked_supported(int dtype, int K, int V, int W);
 cudaError_t launch_delta_chunked(const ChunkLaunch &c, cudaStream_t s);
