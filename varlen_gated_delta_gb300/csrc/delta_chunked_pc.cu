@@ -499,7 +499,11 @@ __device__ __forceinline__ void st8(unsigned char *tile, int row, int c8, const 
     *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c8 * 8)) = pack8(v);
 }
 
+// SEG: the segment passes (p.seg_mode 1 or 2); the one-pass instance carries
+// none of their code.
+template <bool SEG>
 __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_constant__ PcParams p) {
+    const int seg_mode = SEG ? p.seg_mode : 0;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -532,8 +536,8 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
     pdl_wait_primary();  // the chunk images are the prepare kernel's output
 
     const int H = p.H, V = p.V, VT = p.VT;
-    const int n_units = p.seg_mode ? p.seg_units : p.header->n_units;
-    unsigned int *counter = p.seg_mode ? p.counter : &p.header->next_unit;
+    const int n_units = seg_mode ? p.seg_units : p.header->n_units;
+    unsigned int *counter = seg_mode ? p.counter : &p.header->next_unit;
     uint32_t mma_phase = 0;
     uint32_t gc = 0;  // chunks this CTA has consumed: the stage ring position
 
@@ -566,14 +570,14 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
         if (u >= n_units || *s_abort) break;
         int seq, h, vt, q = 0, seg = 0, nseg_here = 1;
         bool mtile = false;  // the transition tile of a segment (seg_mode 1)
-        if (p.seg_mode == 0) {
+        if (seg_mode == 0) {
             seq = p.seq_order[u / (H * VT)];
             h = (u / VT) % H;
             vt = u % VT;
         } else {
             // q: the segment's index among this pass's segments (numbering the M /
             // L or start-state buffers); constant indices into the tables only
-            const int tiles = VT + (p.seg_mode == 1);
+            const int tiles = VT + (seg_mode == 1);
             q = u / (H * tiles);
             h = (u / tiles) % H;
             const int tile = u % tiles;
@@ -584,7 +588,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
             nseg_here = p.seg_s0[1];
 #pragma unroll
             for (int i = 1; i < kMaxSegSeqs; ++i) {
-                const int f = p.seg_mode == 1 ? p.seg_m0[i] : p.seg_s0[i];
+                const int f = seg_mode == 1 ? p.seg_m0[i] : p.seg_s0[i];
                 if (i < p.nseq_seg && q >= f) {
                     seq = p.seg_seq[i];
                     seg = q - f;
@@ -598,17 +602,17 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
             __syncthreads();
             continue;
         }
-        if (p.seg_mode) {  // this segment's tokens (a multiple of 64 from the sequence start)
+        if (seg_mode) {  // this segment's tokens (a multiple of 64 from the sequence start)
             int seg_len;
             segment_split(e - s, nseg_here, seg_len, nseg_here);
-            if (seg >= (p.seg_mode == 1 ? nseg_here - 1 : nseg_here)) {
+            if (seg >= (seg_mode == 1 ? nseg_here - 1 : nseg_here)) {
                 __syncthreads();
                 continue;
             }
             s += seg * seg_len;
             e = min(e, s + seg_len);
         }
-        const bool write_out = p.seg_mode != 1;
+        const bool write_out = seg_mode != 1;
         const int nch = (e - s + kPc - 1) / kPc;
         const size_t chunk_stride = (size_t)H * p.img_bytes;
         // the image of the unit's first chunk: chunk (s - s_seq) / 16 of its sequence
@@ -634,12 +638,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
         // state, a segment's start state, zero, or the identity (transition tile)
         {
             const float *src = p.state_init + state_row * 128 + hc * 64;
-            if (p.seg_mode == 2)
+            if (seg_mode == 2)
                 src = p.seg_S + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r[32];
-                if (p.seg_mode == 1) {
+                if (seg_mode == 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         r[j] = __float_as_uint(mtile && row == hc * 64 + c0 + j ? 1.f : 0.f);
@@ -753,9 +757,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) pc_scan_kernel(const __grid_c
         // [64 hc, 64 hc + 64) -> global
         if (hc == 0 && nch > 0 && write_out)
             store_out((nch - 1) & 1, s + (nch - 1) * kPc, e - s - (nch - 1) * kPc, h, vt);
-        if (p.seg_mode != 2 || seg == nseg_here - 1) {
+        if (seg_mode != 2 || seg == nseg_here - 1) {
             float *dst = p.state_fin + state_row * 128 + hc * 64;
-            if (p.seg_mode == 1)
+            if (seg_mode == 1)
                 dst = mtile ? p.seg_M + ((((size_t)q * H + h) * 128 + row) * 128 + hc * 64)
                             : p.seg_L + ((((size_t)q * H + h) * V + vt * 128 + row) * 128 + hc * 64);
 #pragma unroll
@@ -799,8 +803,11 @@ cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStrea
     cudaError_t e = once_per_device(attr_set, [] {
         cudaError_t e2 = cudaFuncSetAttribute(pc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)kPrepSmem);
+        if (e2 == cudaSuccess)
+            e2 = cudaFuncSetAttribute(pc_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kScanSmem);
         if (e2 != cudaSuccess) return e2;
-        return cudaFuncSetAttribute(pc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(pc_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kScanSmem);
     });
     if (e != cudaSuccess) return e;
@@ -816,7 +823,8 @@ cudaError_t launch_delta_chunked_pc(const PcParams &p, long max_units, cudaStrea
     const long ctas = (long)pc_sm_count() * 2;
     const int grid = (int)(max_units < ctas ? max_units : ctas);
     if (grid <= 0) return cudaSuccess;  // (the prepare kernel ran: a segment pass may follow)
-    e = launch_kernel(pc_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
+    e = p.seg_mode ? launch_kernel(pc_scan_kernel<true>, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p)
+                   : launch_kernel(pc_scan_kernel<false>, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
     note_launch();
     return e;
 }
@@ -849,7 +857,7 @@ cudaError_t launch_delta_chunked_pc_segmented(const PcParams &p0, const ChunkLau
     const long ctas = (long)pc_sm_count() * 2;
     const int grid = (int)(p.seg_units < ctas ? p.seg_units : ctas);
     if (grid <= 0) return cudaSuccess;
-    e = launch_kernel(pc_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
+    e = launch_kernel(pc_scan_kernel<true>, dim3(grid), dim3(kScanThreads), kScanSmem, s, true, p);
     note_launch();
     return e;
 }
