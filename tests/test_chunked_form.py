@@ -174,3 +174,128 @@ def test_per_channel_chunked_form_equals_the_dense_recurrence(T, n):
                                       per_channel=True, scale=0.7)
     np.testing.assert_allclose(out, o_ref[0, :, 0], rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(S, s_ref[0, 0], rtol=1e-9, atol=1e-11)
+
+
+def chunk_forward_products(S0, q, k, v, g, beta, scale, mistake=None):
+    """The per-key-channel chunked form as the prepare and scan kernels compute
+    it (16-token chunks, values as given): every decay factor is a product of
+    gates, never a quotient.  With P_t = prod_{j<=t} g_j (per channel, inside the
+    chunk), Kt = k P_t, Qt = scale q P_t, Kp_t = k_t prod_{j>t} g_j, and for t in
+    4-token block TB > IB (the block of i), r = 4 TB - 1,
+    e^{b_t - b_i} = X_TB[t] Z_TB[i], X_TB[t] = prod_{r<j<=t} g_j, Z_TB[i] = prod_{i<j<=r} g_j;
+    inside a block the factor of (t, i) is the product of the gates i < j <= t.
+      A = diag(beta) strict-lower(KK), T = (I + A)^-1 (forward substitution),
+      Delta = T diag(beta) V - (T diag(beta) Kt) S_0^T,
+      O = Qt S_0^T + scale tril(QK) Delta,  S_C = S_0 diag(P_15) + Delta^T Kp.
+    Rows past a ragged chunk's end are zero with gate 1 and beta 0."""
+    Cp = 16
+    T, K = k.shape
+    S = S0.copy()
+    out = np.zeros((T, S0.shape[0]))
+    for t0 in range(0, T, Cp):
+        n = min(Cp, T - t0)
+        qc, kc, vc = np.zeros((Cp, K)), np.zeros((Cp, K)), np.zeros((Cp, v.shape[1]))
+        gc, bc = np.ones((Cp, K)), np.zeros(Cp)
+        qc[:n], kc[:n], vc[:n], gc[:n], bc[:n] = q[t0:t0 + n], k[t0:t0 + n], v[t0:t0 + n], g[t0:t0 + n], beta[t0:t0 + n]
+        P = np.cumprod(gc, axis=0)
+        suffix = np.ones((Cp, K))
+        for t in range(Cp - 2, -1, -1):
+            suffix[t] = suffix[t + 1] * gc[t + 1]
+        if mistake == "kp_prefix":
+            suffix = P
+        KK, QK = np.zeros((Cp, Cp)), np.zeros((Cp, Cp))
+        for TB in range(4):
+            for IB in range(TB + 1):
+                for a in range(4):
+                    for b in range(4):
+                        t, i = 4 * TB + a, 4 * IB + b
+                        if i > t:
+                            continue
+                        if TB > IB:
+                            r = 4 * TB - 1
+                            X = np.prod(gc[r + 1:t + 1], axis=0)
+                            lo = i if mistake == "z_inclusive" else i + 1
+                            Z = np.prod(gc[lo:r + 1], axis=0)
+                            f = X * Z
+                        else:
+                            f = np.prod(gc[i + 1:t + 1], axis=0)
+                        if i < t:
+                            KK[t, i] = np.dot(kc[t] * f, kc[i])
+                        if i < t or mistake != "no_qk_diagonal":
+                            QK[t, i] = np.dot(qc[t] * f, kc[i])
+        A = bc[:, None] * KK
+        Tm = np.zeros((Cp, Cp))
+        for c in range(Cp):  # forward substitution, column by column
+            col = np.zeros(Cp)
+            col[c] = 1.0
+            for r in range(c + 1, Cp):
+                col[r] = -np.dot(A[r, :r], col[:r])
+            Tm[:, c] = col
+        Tb = Tm * bc[None, :]
+        W = Tb @ (kc * P)
+        Delta = Tb @ vc - W @ S.T
+        out[t0:t0 + n] = ((scale * qc * P) @ S.T + scale * QK @ Delta)[:n]
+        S = S * P[-1][None, :] + Delta.T @ (kc * suffix)
+    return out, S
+
+
+def _per_channel_case(T, n, lo, seed):
+    rng = np.random.default_rng(seed)
+    q, k, v = rng.normal(size=(T, n)), rng.normal(size=(T, n)) / np.sqrt(n), rng.normal(size=(T, n))
+    g = rng.uniform(lo, 1.0, size=(T, n))
+    beta = rng.uniform(0.0, 1.0, T)
+    S0 = rng.normal(scale=0.2, size=(n, n))
+    o_ref, s_ref = oracle.dense_delta(q[None, :, None], k[None, :, None], v[None, :, None],
+                                      g[None, :, None], beta[None, :, None], S0[None, None],
+                                      per_channel=True, scale=0.7)
+    return (S0, q, k, v, g, beta), o_ref[0, :, 0], s_ref[0, 0]
+
+
+@pytest.mark.parametrize("T,n,lo", [(16, 8, 0.6), (47, 16, 0.6), (70, 12, 0.05)])
+def test_per_channel_gate_product_form_equals_the_dense_recurrence(T, n, lo):
+    """The prepare / scan kernels' algebra (gate products, 4-token blocks, a
+    ragged last chunk) against the fp64 oracle, including gates down to 0.05
+    whose 16-token products reach ~1e-21."""
+    args, o_ref, s_ref = _per_channel_case(T, n, lo, T * n)
+    out, S = chunk_forward_products(*args, 0.7)
+    np.testing.assert_allclose(out, o_ref, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, s_ref, rtol=1e-9, atol=1e-11)
+
+
+def test_per_channel_gate_products_stay_finite_under_extreme_decay():
+    """Gates of 1e-30: the quotient form would divide by products below the
+    fp64 range inside a chunk; the product form stays finite and exact."""
+    args, o_ref, s_ref = _per_channel_case(40, 8, 0.5, 7)
+    S0, q, k, v, g, beta = args
+    g = g.copy()
+    g[5:9] = 1e-30
+    o_ref, s_ref = oracle.dense_delta(q[None, :, None], k[None, :, None], v[None, :, None],
+                                      g[None, :, None], beta[None, :, None], S0[None, None],
+                                      per_channel=True, scale=0.7)
+    out, S = chunk_forward_products(S0, q, k, v, g, beta, 0.7)
+    assert np.isfinite(out).all() and np.isfinite(S).all()
+    np.testing.assert_allclose(out, o_ref[0, :, 0], rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, s_ref[0, 0], rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("mistake", ["kp_prefix", "z_inclusive", "no_qk_diagonal"])
+def test_per_channel_planted_mistakes_break_the_match(mistake):
+    args, o_ref, s_ref = _per_channel_case(40, 8, 0.6, 11)
+    out, S = chunk_forward_products(*args, 0.7, mistake=mistake)
+    assert not (np.allclose(out, o_ref, rtol=1e-6, atol=1e-8) and np.allclose(S, s_ref, rtol=1e-6, atol=1e-8))
+
+
+def test_chunk_image_slots_are_distinct_and_bounded():
+    """The per-channel prepare kernel stores chunk n of sequence i (start s_i)
+    at image slot (s_i >> 4) + i + n: for valid offsets no two chunks share a
+    slot and every slot is below (N + 15) / 16 + B, the images the workspace
+    holds (pc_slots)."""
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        B = int(rng.integers(1, 40))
+        lens = rng.integers(0, 90, size=B) * (rng.random(B) < 0.9)
+        offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        N = int(offs[-1])
+        slots = [(int(offs[i]) >> 4) + i + n for i in range(B) for n in range((int(lens[i]) + 15) // 16)]
+        assert len(slots) == len(set(slots))
+        assert all(0 <= q < (N + 15) // 16 + B for q in slots)
