@@ -72,7 +72,7 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
 // decode batch: 51.2 us a step against 52.8 us at five CTAs and 53.7 us at
 // seven, where spills grow); its per-channel-gate twin is held to four.
 template <typename T, int KP, int RG, bool VEC4, bool PF, bool CAPT, bool PC = false>
-__global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? (PC ? 4 : 6) : 1)
+__global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? (PC ? 5 : 6) : 1)
     delta_serial_kernel(const DeltaParams p) {
     constexpr int EPL = 16;          // state values per lane per row
     constexpr int LPR = KP / EPL;    // lanes per row
@@ -238,14 +238,13 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
         if constexpr (PF) {
             if (t + 1 < t_end) fetch(t + 1, qn, kn, vn, gn, bn, gvn);
         }
-        // per-channel gate: read-out and retrieval use the decayed directions
-        float gq[EPL], gk[EPL];
+        // per-channel gate: the state's key columns are decayed first, each by
+        // its own gate; retrieval and read-out then use the decayed state
         if constexpr (PC) {
 #pragma unroll
-            for (int u = 0; u < EPL; ++u) {
-                gk[u] = gcv[u] * kc[u];
-                gq[u] = gcv[u] * qc[u];
-            }
+            for (int r = 0; r < RG; ++r)
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) S[r][u] *= gcv[u];
         }
 
         float kq = 0.f;
@@ -259,8 +258,8 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int u = 0; u < EPL; ++u) {
-                a0 = fmaf(S[r][u], PC ? gk[u] : kc[u], a0);
-                a1 = fmaf(S[r][u], PC ? gq[u] : qc[u], a1);
+                a0 = fmaf(S[r][u], kc[u], a0);
+                a1 = fmaf(S[r][u], qc[u], a1);
             }
             sk[r] = a0;
             sq[r] = a1;
@@ -289,11 +288,12 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
             // RETRIEVE (delta rules): subtract the decayed state's retrieval S k
-            // (with the per-channel gate gc = 1: sk, sq already hold the decay)
+            // (with the per-channel gate gc = 1: S is already decayed)
             const float delta = bc * (retrieve ? vc[r] - gc * sk[r] : vc[r]);
             const float o = gc * sq[r] + delta * kq;
 #pragma unroll
-            for (int u = 0; u < EPL; ++u) S[r][u] = fmaf(PC ? gcv[u] : gc, S[r][u], delta * kc[u]);
+            for (int u = 0; u < EPL; ++u)
+                S[r][u] = PC ? S[r][u] + delta * kc[u] : fmaf(gc, S[r][u], delta * kc[u]);
             if (sub == 0 && vi[r] < V) {
                 if (own) out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
                 if constexpr (CAPT) {
