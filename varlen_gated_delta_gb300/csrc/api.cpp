@@ -705,7 +705,7 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
         if (per_channel) {  // the per-key-channel chunked kernels
             const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
             PcParams pp{};
-            pp.qb = yb; pp.kb = yb + (size_t)HQ * K; pp.vb = yb + 2 * (size_t)HQ * K; pp.rs = width;
+            pp.qb = yb; pp.kb = yb + (size_t)HQ * K; pp.rs = width;
             pp.g = a; pp.bl = b; pp.A_log = A_log; pp.dt_bias = dt_bias;
             pp.offsets = offsets; pp.seq_order = order; pp.header = hdr;
             pp.state_init = state_init; pp.state_fin = state_fin;
@@ -988,7 +988,6 @@ static int dense_per_channel_chunked(const void *q, const void *k, const void *v
         return fail(GDN_ERR_CUDA, "dense: encoding the v tensor map failed");
     pp.qb = static_cast<const __nv_bfloat16 *>(q);
     pp.kb = static_cast<const __nv_bfloat16 *>(k);
-    pp.vb = static_cast<const __nv_bfloat16 *>(v);
     pp.rs = (long)H * n;
     pp.g = g; pp.bl = beta; pp.A_log = nullptr; pp.dt_bias = nullptr;
     pp.offsets = pk.offsets; pp.seq_order = pk.order; pp.header = pk.header;

@@ -228,9 +228,9 @@ cudaError_t launch_dense_pack(const DensePack &p, cudaStream_t s);
 //    image below) to the workspace;
 //  - a scan kernel, persistent over (sequence, value head, V tile) units, that
 //    carries the fp32 state in tensor memory and streams the images in.
-// q, k, v rows of token t at qb / kb / vb + t * rs (bf16, the first key /
-// value head's columns; key head kh adds kh * 128, value head h and V tile vt
-// add h * V + vt * 128); g [N, H, 128] holds the decay logits, or the gate
+// q, k rows of token t at qb / kb + t * rs (bf16, the first key head's
+// columns; key head kh adds kh * 128), v rows through vmap (below);
+// g [N, H, 128] holds the decay logits, or the gate
 // factors when gate_factor; out [N, ors] (head h at column h * V).  Only
 // sequences of at least `thr` tokens are processed.  Units and their order
 // come from the workspace header and seq_order.
@@ -252,7 +252,7 @@ inline size_t pc_img_bytes() { return kPcImgHead; }
 inline size_t pc_slots(int B, int N) { return ((size_t)N + 15) / 16 + (size_t)B; }
 struct PcParams {
     CUtensorMap vmap;  // (first: the map type carries its own alignment)
-    const __nv_bfloat16 *qb, *kb, *vb;
+    const __nv_bfloat16 *qb, *kb;
     long rs;
     const float *g, *bl, *A_log, *dt_bias;
     const int32_t *offsets, *seq_order;
