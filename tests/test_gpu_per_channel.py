@@ -149,6 +149,7 @@ CHUNKED = [
     ("v256-d2", "long", (200, 33), dict(H=4, HQ=2)),
     ("one-long", "decode", (1500,), dict(H=2, HQ=1)),
     ("gqa-4", "decode", (64, 129), dict(H=8, HQ=2)),
+    ("v384", "decode", (90, 20), dict(H=2, HQ=1, V=384)),
 ]
 
 
@@ -291,3 +292,17 @@ def test_per_channel_segment_parallel_in_place_carry():
     torch.cuda.synchronize()
     assert sfin.data_ptr() == st.data_ptr()
     assert rel_l2(cpu64(out), o_ref) <= TOL["bf16"] and rel_l2(cpu64(sfin), s_ref) <= TOL["bf16"]
+
+
+def test_per_channel_chunked_many_sequences():
+    """4100 chunked sequences (more than the device schedule sorts; the rest are
+    listed in index order) with device offsets only: the prepare kernel finds
+    each chunk's sequence by searching the offsets."""
+    lens = tuple(8 + (i * 7) % 9 for i in range(4100))
+    wl, d = _case("decode", lens, seed_shift=30, H=2, HQ=1)
+    out, cfin, sfin = _layer(wl, d)
+    o_ref, c_ref, s_ref = _oracle_layer(wl, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(cpu64(cfin), c_ref)
+    eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], f"out {eo:.3e} state {es:.3e}"
