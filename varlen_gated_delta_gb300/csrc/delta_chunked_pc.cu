@@ -264,57 +264,71 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
     }
     __syncthreads();
 
-    // ---- R: per key channel c, the decay products and the bf16 operands.
-    // Threads 0..127: P_t, Kt = rk k P_t (MMA operand), Qt (image), e^{b_C} (image), the
-    // X rows (MMA operand); threads 128..255: the suffix products, Kp (image),
-    // the Z rows (MMA operand).
+    // ---- R: per pair of key channels (c, c + 1), the decay products and the
+    // bf16 operands, written two channels at a time; four roles of 64 threads:
+    //   0: P_t, Kt = rk k P_t (MMA operand), Qt (image), e^{b_C} (image);
+    //   1: the X rows k X, q X (MMA operand);
+    //   2: the suffix products and Kp (image);
+    //   3: the Z rows (MMA operand).
     {
-        const int c = tid & 127;
+        const int role = tid >> 6, c = (tid & 63) * 2;
         const uint32_t cb = (uint32_t)(c & 63);
-        float g[kPc], k[kPc];
-#pragma unroll
-        for (int t = 0; t < kPc; ++t) {
-            g[t] = sG[t * 128 + c];
-            k[t] = sK[t * 128 + c];
-        }
-        if (tid < 128) {
-            float P = 1.f;
+        auto ld2 = [&](const float *base, int t) {
+            return *reinterpret_cast<const float2 *>(base + t * 128 + c);
+        };
+        auto st2 = [&](unsigned char *dst, float x, float y) {
+            *reinterpret_cast<uint32_t *>(dst) = pack2(x, y);
+        };
+        if (role == 0) {
+            float2 P = make_float2(1.f, 1.f);
             const float qs = p.scale;
 #pragma unroll
             for (int t = 0; t < kPc; ++t) {
-                P *= g[t];
-                st_bf16(sm + kPKt + op_offset(t, c), k[t] * v_rk[t] * P);
-                st_bf16(img + kImWQ + wq_offset(16 + t, c), sQ[t * 128 + c] * v_rq[t] * qs * P);
+                const float2 g = ld2(sG, t), k = ld2(sK, t), qv = ld2(sQ, t);
+                P.x *= g.x;
+                P.y *= g.y;
+                const float fk = v_rk[t], fq = v_rq[t] * qs;
+                st2(sm + kPKt + op_offset(t, c), k.x * fk * P.x, k.y * fk * P.y);
+                st2(img + kImWQ + wq_offset(16 + t, c), qv.x * fq * P.x, qv.y * fq * P.y);
             }
-            reinterpret_cast<float *>(img + kImCs)[c] = P;
+            *reinterpret_cast<float2 *>(img + kImCs + c * 4) = P;
+        } else if (role == 1) {
             unsigned char *L = sm + kPL + (c >> 6) * 4096;
 #pragma unroll
             for (int TB = 1; TB < 4; ++TB) {
-                float X = 1.f;
+                float2 X = make_float2(1.f, 1.f);
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
                     const int t = 4 * TB + a, row = 4 * (TB - 1) + a;
-                    X *= g[t];
-                    st_bf16(L + sw128_offset(row, cb), k[t] * X);
-                    st_bf16(L + sw128_offset(12 + row, cb), sQ[t * 128 + c] * X);
+                    const float2 g = ld2(sG, t), k = ld2(sK, t), qv = ld2(sQ, t);
+                    X.x *= g.x;
+                    X.y *= g.y;
+                    st2(L + sw128_offset(row, cb), k.x * X.x, k.y * X.y);
+                    st2(L + sw128_offset(12 + row, cb), qv.x * X.x, qv.y * X.y);
                 }
             }
-        } else {
-            float Qs = 1.f;
+        } else if (role == 2) {
+            float2 Qs = make_float2(1.f, 1.f);
 #pragma unroll
             for (int t = kPc - 1; t >= 0; --t) {
-                st_bf16(img + kImKp + op_offset(t, c), k[t] * v_rk[t] * Qs);
-                Qs *= g[t];
+                const float2 g = ld2(sG, t), k = ld2(sK, t);
+                const float fk = v_rk[t];
+                st2(img + kImKp + op_offset(t, c), k.x * fk * Qs.x, k.y * fk * Qs.y);
+                Qs.x *= g.x;
+                Qs.y *= g.y;
             }
+        } else {
             unsigned char *Zt = sm + ((c >> 6) ? kPZ1 : kPZ0);
 #pragma unroll
             for (int TB = 1; TB < 4; ++TB) {
                 const int base = TB == 1 ? 0 : TB == 2 ? 4 : 12;
-                float Z = 1.f;
+                float2 Z = make_float2(1.f, 1.f);
 #pragma unroll
                 for (int i = 4 * TB - 1; i >= 0; --i) {
-                    st_bf16(Zt + sw128_offset(base + i, cb), k[i] * Z);
-                    Z *= g[i];
+                    const float2 g = ld2(sG, i), k = ld2(sK, i);
+                    st2(Zt + sw128_offset(base + i, cb), k.x * Z.x, k.y * Z.y);
+                    Z.x *= g.x;
+                    Z.y *= g.y;
                 }
             }
         }
