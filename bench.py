@@ -667,6 +667,17 @@ def run_ours(args, wl):
                           "vs_baseline", "data", "metric", "unit"):
                     rec.pop(k, None)
                 extras[name] = rec
+        # the prefill batch with one decay logit per key channel (the
+        # per-channel chunked route: prepare and scan kernels)
+        pc_args = argparse.Namespace(**vars(args))
+        pc_args.gate = "per_channel"
+        torch.cuda.empty_cache()
+        rec = _measure(pc_args, W.WORKLOADS["prefill"], dev, world, rank, local, gdn, W)
+        if rank == 0:
+            for k in ("n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                      "vs_baseline", "data", "metric", "unit"):
+                rec.pop(k, None)
+            extras["prefill_per_channel"] = rec
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl)
