@@ -306,3 +306,33 @@ def test_per_channel_chunked_many_sequences():
     np.testing.assert_array_equal(cpu64(cfin), c_ref)
     eo, es = rel_l2(cpu64(out), o_ref), rel_l2(cpu64(sfin), s_ref)
     assert eo <= TOL["bf16"] and es <= TOL["bf16"], f"out {eo:.3e} state {es:.3e}"
+
+
+def test_per_channel_plain_sized_workspace_runs_token_serially():
+    """A workspace of gdn_workspace_bytes() (no room for the chunk images) keeps
+    per-channel sequences on the token-serial kernel: bit for bit the route
+    with the chunk threshold out of reach."""
+    wl, d = _case("decode", (40, 3, 100), seed_shift=40, H=4, HQ=2)
+    plain = torch.empty(gdn.gdn_workspace_bytes(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc, wl.D),
+                        dtype=torch.uint8, device=DEV)
+    assert plain.numel() < gdn.gdn_workspace_bytes_ex(wl.B, wl.N, wl.H, wl.HQ, wl.K, wl.V, wl.Kc,
+                                                      wl.D, gdn.GDN_BF16, PC)
+    o1, c1, s1 = _layer(wl, d, workspace=plain, offsets_host=d["offsets_list"])
+    with chunk_threshold(SERIAL_ONLY):
+        o2, c2, s2 = _layer(wl, d, offsets_host=d["offsets_list"])
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2) and torch.equal(c1, c2)
+
+
+def test_per_channel_more_sequences_than_a_grid_dimension():
+    """70000 chunked sequences with host offsets: more than a grid's y extent,
+    so the prepare kernel runs over image slots and searches the offsets; the
+    result equals the token-serial route within the bf16 tolerance."""
+    lens = (8,) * 70000
+    wl, d = _case("decode", lens, seed_shift=41, H=1, HQ=1)
+    out, _, sfin = _layer(wl, d, offsets_host=d["offsets_list"])
+    with chunk_threshold(SERIAL_ONLY):
+        o2, _, s2 = _layer(wl, d, offsets_host=d["offsets_list"])
+    torch.cuda.synchronize()
+    assert not torch.equal(out, o2)
+    assert rel_l2(cpu64(out), cpu64(o2)) <= TOL["bf16"] and rel_l2(cpu64(sfin), cpu64(s2)) <= TOL["bf16"]
