@@ -101,6 +101,21 @@ __device__ __forceinline__ void store_pair(Vec16<T> &v, int q, float a, float b)
     }
 }
 
+// silu_for on a pair of values; for bf16 the scale, add and product run as
+// packed fp32 operations with the scalar roundings.
+template <typename T>
+__device__ __forceinline__ float2 silu2_for(float2 z) {
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+        const float2 hz = __fmul2_rn(make_float2(0.5f, 0.5f), z);
+        float2 th;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(th.x) : "f"(hz.x));
+        asm("tanh.approx.f32 %0, %1;" : "=f"(th.y) : "f"(hz.y));
+        return __fmul2_rn(hz, __fadd2_rn(make_float2(1.f, 1.f), th));
+    } else {
+        return make_float2(silu_for<T>(z.x), silu_for<T>(z.y));
+    }
+}
+
 __device__ __forceinline__ void decay_rate(const ConvParams &p, int t, int h, float &g,
                                            float &beta) {
     gates_opt(p.a, p.bl, (size_t)t * p.H + h, p.A_log, p.dt_bias, h, p.opts, g, beta);
@@ -589,24 +604,21 @@ __global__ void __launch_bounds__(kConvThreads, 2)
                     }
                     T *yrow = yfirst + (size_t)r * xstep;
                     if (!seq_ok) return;
-                    float acc[VEC];
-#pragma unroll
-                    for (int q = 0; q < VEC; ++q) acc[q] = bias[q];
-#pragma unroll
-                    for (int j = 0; j < KC; ++j) {
-                        const float(&xs)[VEC] = win[(ph - (KC - 1 - j) + KC * 4) % KC];
-#pragma unroll
-                        for (int q = 0; q < VEC; ++q) acc[q] = fmaf(xs[q], wr[j][q], acc[q]);
-                    }
+                    // channel pairs on the packed fp32 pipe: each component of
+                    // __ffma2_rn / __fmul2_rn / __fadd2_rn rounds exactly as the
+                    // scalar operation, so the outputs are those of scalar code
                     Vec16<T> yo;
 #pragma unroll
                     for (int q = 0; q < VEC; q += 2) {
-                        float z0 = acc[q], z1 = acc[q + 1];
-                        if (p.silu) {
-                            z0 = silu_for<T>(z0);
-                            z1 = silu_for<T>(z1);
+                        float2 acc = make_float2(bias[q], bias[q + 1]);
+#pragma unroll
+                        for (int j = 0; j < KC; ++j) {
+                            const float(&xs)[VEC] = win[(ph - (KC - 1 - j) + KC * 4) % KC];
+                            acc = __ffma2_rn(make_float2(xs[q], xs[q + 1]),
+                                             make_float2(wr[j][q], wr[j][q + 1]), acc);
                         }
-                        store_pair<T>(yo, q, z0, z1);  // the conv output is stored in T
+                        if (p.silu) acc = silu2_for<T>(acc);
+                        store_pair<T>(yo, q, acc.x, acc.y);  // the conv output is stored in T
                     }
                     if (cvalid) *reinterpret_cast<uint4 *>(yrow) = yo.u;
                     if constexpr (PREP) {
