@@ -75,6 +75,17 @@ __device__ __forceinline__ void st_bf16(unsigned char *p, float v) {
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
 }
+// Packed fp32 (two lanes of one instruction; each component rounds exactly as
+// the scalar multiply / fused multiply-add).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+// dot4 of a and of b with the same f, two chains side by side: (a.f + acc.x, b.f + acc.y)
+__device__ __forceinline__ float2 dot4x2(float4 a, float4 b, float4 f, float2 acc) {
+    acc = __ffma2_rn(make_float2(a.x, b.x), splat2(f.x), acc);
+    acc = __ffma2_rn(make_float2(a.y, b.y), splat2(f.y), acc);
+    acc = __ffma2_rn(make_float2(a.z, b.z), splat2(f.z), acc);
+    return __ffma2_rn(make_float2(a.w, b.w), splat2(f.w), acc);
+}
 
 // ------------------------------------------------------------------ prepare
 // One CTA per (image slot, value head): finds the slot's sequence and chunk,
@@ -285,11 +296,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
 #pragma unroll
             for (int t = 0; t < kPc; ++t) {
                 const float2 g = ld2(sG, t), k = ld2(sK, t), qv = ld2(sQ, t);
-                P.x *= g.x;
-                P.y *= g.y;
+                P = mul2(P, g);
                 const float fk = v_rk[t], fq = v_rq[t] * qs;
-                st2(sm + kPKt + op_offset(t, c), k.x * fk * P.x, k.y * fk * P.y);
-                st2(img + kImWQ + wq_offset(16 + t, c), qv.x * fq * P.x, qv.y * fq * P.y);
+                const float2 kt = mul2(mul2(k, splat2(fk)), P), qt = mul2(mul2(qv, splat2(fq)), P);
+                st2(sm + kPKt + op_offset(t, c), kt.x, kt.y);
+                st2(img + kImWQ + wq_offset(16 + t, c), qt.x, qt.y);
             }
             *reinterpret_cast<float2 *>(img + kImCs + c * 4) = P;
         } else if (role == 1) {
@@ -301,10 +312,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
                 for (int a = 0; a < 4; ++a) {
                     const int t = 4 * TB + a, row = 4 * (TB - 1) + a;
                     const float2 g = ld2(sG, t), k = ld2(sK, t), qv = ld2(sQ, t);
-                    X.x *= g.x;
-                    X.y *= g.y;
-                    st2(L + sw128_offset(row, cb), k.x * X.x, k.y * X.y);
-                    st2(L + sw128_offset(12 + row, cb), qv.x * X.x, qv.y * X.y);
+                    X = mul2(X, g);
+                    const float2 kx = mul2(k, X), qx = mul2(qv, X);
+                    st2(L + sw128_offset(row, cb), kx.x, kx.y);
+                    st2(L + sw128_offset(12 + row, cb), qx.x, qx.y);
                 }
             }
         } else if (role == 2) {
@@ -313,9 +324,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
             for (int t = kPc - 1; t >= 0; --t) {
                 const float2 g = ld2(sG, t), k = ld2(sK, t);
                 const float fk = v_rk[t];
-                st2(img + kImKp + op_offset(t, c), k.x * fk * Qs.x, k.y * fk * Qs.y);
-                Qs.x *= g.x;
-                Qs.y *= g.y;
+                const float2 kp = mul2(mul2(k, splat2(fk)), Qs);
+                st2(img + kImKp + op_offset(t, c), kp.x, kp.y);
+                Qs = mul2(Qs, g);
             }
         } else {
             unsigned char *Zt = sm + ((c >> 6) ? kPZ1 : kPZ0);
@@ -326,9 +337,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
 #pragma unroll
                 for (int i = 4 * TB - 1; i >= 0; --i) {
                     const float2 g = ld2(sG, i), k = ld2(sK, i);
-                    st2(Zt + sw128_offset(base + i, cb), k.x * Z.x, k.y * Z.y);
-                    Z.x *= g.x;
-                    Z.y *= g.y;
+                    const float2 kz = mul2(k, Z);
+                    st2(Zt + sw128_offset(base + i, cb), kz.x, kz.y);
+                    Z = mul2(Z, g);
                 }
             }
         }
@@ -379,9 +390,13 @@ __global__ void __launch_bounds__(kPrepThreads, 4) pc_prep_kernel(const __grid_c
                 qk[b][b] = dot4(qr[b], f, qk[b][b]);
 #pragma unroll
                 for (int a = b + 1; a < 4; ++a) {
-                    f.x *= gr[a].x; f.y *= gr[a].y; f.z *= gr[a].z; f.w *= gr[a].w;
-                    kk[a][b] = dot4(kr[a], f, kk[a][b]);
-                    qk[a][b] = dot4(qr[a], f, qk[a][b]);
+                    const float2 fxy = mul2(make_float2(f.x, f.y), make_float2(gr[a].x, gr[a].y));
+                    const float2 fzw = mul2(make_float2(f.z, f.w), make_float2(gr[a].z, gr[a].w));
+                    f = make_float4(fxy.x, fxy.y, fzw.x, fzw.y);
+                    // the KK and QK chains of (a, b) side by side
+                    const float2 kq = dot4x2(kr[a], qr[a], f, make_float2(kk[a][b], qk[a][b]));
+                    kk[a][b] = kq.x;
+                    qk[a][b] = kq.y;
                 }
             }
         }
