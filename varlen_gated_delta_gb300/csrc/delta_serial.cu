@@ -240,11 +240,25 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
         }
         // per-channel gate: the state's key columns are decayed first, each by
         // its own gate; retrieval and read-out then use the decayed state
+        // With PF (runs of tokens) the column pairs below take the packed fp32
+        // pipe (each component rounds exactly as the scalar multiply / fused
+        // multiply-add): measured 10% faster there, and 4% slower on the
+        // one-token decode instances, which keep the scalar form.
         if constexpr (PC) {
 #pragma unroll
             for (int r = 0; r < RG; ++r)
 #pragma unroll
-                for (int u = 0; u < EPL; ++u) S[r][u] *= gcv[u];
+                for (int u = 0; u < EPL; u += 2) {
+                    if constexpr (PF) {
+                        const float2 d2 = __fmul2_rn(make_float2(S[r][u], S[r][u + 1]),
+                                                     make_float2(gcv[u], gcv[u + 1]));
+                        S[r][u] = d2.x;
+                        S[r][u + 1] = d2.y;
+                    } else {
+                        S[r][u] *= gcv[u];
+                        S[r][u + 1] *= gcv[u + 1];
+                    }
+                }
         }
 
         float kq = 0.f;
@@ -255,14 +269,23 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
         float sk[RG], sq[RG];
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
-            float a0 = 0.f, a1 = 0.f;
+            if constexpr (PF) {
+                float2 a = make_float2(0.f, 0.f);  // the S k and S q chains side by side
 #pragma unroll
-            for (int u = 0; u < EPL; ++u) {
-                a0 = fmaf(S[r][u], kc[u], a0);
-                a1 = fmaf(S[r][u], qc[u], a1);
+                for (int u = 0; u < EPL; ++u)
+                    a = __ffma2_rn(make_float2(S[r][u], S[r][u]), make_float2(kc[u], qc[u]), a);
+                sk[r] = a.x;
+                sq[r] = a.y;
+            } else {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) {
+                    a0 = fmaf(S[r][u], kc[u], a0);
+                    a1 = fmaf(S[r][u], qc[u], a1);
+                }
+                sk[r] = a0;
+                sq[r] = a1;
             }
-            sk[r] = a0;
-            sq[r] = a1;
         }
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) {
@@ -291,9 +314,21 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? 
             // (with the per-channel gate gc = 1: S is already decayed)
             const float delta = bc * (retrieve ? vc[r] - gc * sk[r] : vc[r]);
             const float o = gc * sq[r] + delta * kq;
+            if constexpr (PF) {
 #pragma unroll
-            for (int u = 0; u < EPL; ++u)
-                S[r][u] = PC ? S[r][u] + delta * kc[u] : fmaf(gc, S[r][u], delta * kc[u]);
+                for (int u = 0; u < EPL; u += 2) {
+                    const float2 s2 = make_float2(S[r][u], S[r][u + 1]), k2 = make_float2(kc[u], kc[u + 1]);
+                    const float2 d2 = make_float2(delta, delta);
+                    const float2 n2 = PC ? __ffma2_rn(d2, k2, s2)
+                                         : __ffma2_rn(make_float2(gc, gc), s2, __fmul2_rn(d2, k2));
+                    S[r][u] = n2.x;
+                    S[r][u + 1] = n2.y;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < EPL; ++u)
+                    S[r][u] = PC ? S[r][u] + delta * kc[u] : fmaf(gc, S[r][u], delta * kc[u]);
+            }
             if (sub == 0 && vi[r] < V) {
                 if (own) out[((size_t)t * H + h) * V + vi[r]] = from_f32<T>(o * scale);
                 if constexpr (CAPT) {
