@@ -464,6 +464,12 @@ __global__ void __launch_bounds__(kConvThreads, 2)
     T *s_ring = reinterpret_cast<T *>(conv_dsm);
     int *s_offs = reinterpret_cast<int *>(conv_dsm + kRingBytes);
 
+    // Launched as a dependent of the stream's previous kernel: nothing is read
+    // before that kernel has finished.  Only then may this kernel's own
+    // dependents start (the recurrence issues its state loads before it waits
+    // for this kernel, and a state carried in place from the previous call
+    // must be final by then).
+    pdl_wait_primary();
     pdl_launch_dependents();
     if (p.header != nullptr && blockIdx.x == 0)
         schedule_block(p, reinterpret_cast<unsigned long long *>(conv_dsm));
@@ -679,9 +685,10 @@ cudaError_t launch_conv_stream(const ConvParams &p, cudaStream_t s) {
                                     (int)(kRingBytes + sizeof(int) * kOffsetsCache));
     });
     if (e != cudaSuccess) return e;
-    conv_stream_kernel<T, VEC, PREP, KC, D><<<(unsigned)blocks, kConvThreads, smem, s>>>(p, (int)R, n_ctiles);
+    e = launch_kernel(conv_stream_kernel<T, VEC, PREP, KC, D>, dim3((unsigned)blocks), dim3(kConvThreads), smem, s,
+                      /*pdl=*/true, p, (int)R, n_ctiles);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 // Final conv state: fin[b,c,j] = x~(len - L + j).  One thread per (b, c) walks

@@ -70,10 +70,18 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
 // The plain one-token (decode) variant with K = 128 is held to 80 registers so
 // that six CTAs share an SM: more state loads in flight per SM (measured on the
 // decode batch: 51.2 us a step against 52.8 us at five CTAs and 53.7 us at
-// seven, where spills grow); its per-channel-gate twin is held to four.
+// seven, where spills grow); its per-channel-gate and capture twins are held to
+// five (96 registers; the capture twin unbounded took 144 registers, three
+// CTAs per SM, and ran the capture-8 decode batch at 84 us against 63.5 us).
+// The prefetching variants take the registers they want: held to three or four
+// CTAs per SM they ran 6-19% slower.
 template <typename T, int KP, int RG, bool VEC4, bool PF, bool CAPT, bool PC = false>
-__global__ void __launch_bounds__(kSerialThreads, (!PF && !CAPT && KP == 128) ? (PC ? 5 : 6) : 1)
+__global__ void __launch_bounds__(kSerialThreads, (!PF && KP == 128) ? (CAPT ? 5 : (PC ? 5 : 6)) : 1)
     delta_serial_kernel(const DeltaParams p) {
+    // the next kernel of the stream (the following call's conv pass, which
+    // waits for this grid before it reads anything) may be placed while this
+    // grid's last CTAs run
+    pdl_launch_dependents();
     constexpr int EPL = 16;          // state values per lane per row
     constexpr int LPR = KP / EPL;    // lanes per row
     constexpr int RPI = 32 / LPR;    // rows per warp per row group
