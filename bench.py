@@ -511,13 +511,14 @@ def _measure(args, wl, dev, world, rank, local, gdn, W):
         with torch.cuda.stream(h2d_s):
             if i >= 2:  # buffer j was last read by step i - 2 of this run
                 h2d_s.wait_event(in_free[j])
+                # step i - 2's output has left too: the compute stream then joins
+                # one other stream per step (this copy), off its critical path
+                h2d_s.wait_event(out_free[j])
             for k in host:
                 dev_in[j][k].copy_(host[k], non_blocking=True)
             dev_offs[j].copy_(host_offs, non_blocking=True)
             in_ready[j].record(h2d_s)
         comp.wait_event(in_ready[j])
-        if i >= 2:  # step i - 2's output has left
-            comp.wait_event(out_free[j])
         call(dev_in[j]["qkv"], dev_in[j]["a"], dev_in[j]["b"], dev_offs[j], j, out_t=outs[j],
              capsule_t=caps[j] if cap else None)
         in_free[j].record(comp)
