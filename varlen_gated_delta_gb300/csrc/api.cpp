@@ -798,12 +798,12 @@ static int layer_impl(const void *qkv, const void *w, const void *bias, const fl
     const bool conv_fin_written = L > 0 && conv_fin != nullptr;
     ForkSet *f = nullptr;
     std::unique_lock<std::mutex> fork_lock(g_fork_mu, std::defer_lock);
-    // (The persistent scalar chunked kernel holds its CTA slots from the start,
-    // so there the token-serial CTAs only take slots its last units leave:
-    // ragged 1542 -> 1526 us a step.  The per-channel prepare kernel is a
-    // plain grid that they would compete with: only with free slots there.)
+    // (Only with slots left free: with more units than slots the token-serial
+    // CTAs take the slots the last chunked units leave and share their SMs,
+    // which cost the ragged batch's chunked kernel 5% of its time for a 1%
+    // shorter step, and made the per-channel prepare kernel's grid 1.3% slower.)
     if (allow_fork && run_chunked && !serial_first && seg.n == 0 && (n_serial_host > 0 || conv_fin_written) &&
-        (!per_channel || max_units < 2L * sm_count_host())) {
+        max_units < 2L * sm_count_host()) {
         fork_lock.lock();
         if (fork_set(&f, s) != cudaSuccess) {  // not available: one after the other
             f = nullptr;
