@@ -29,7 +29,11 @@ constexpr int kSerialThreads = 128;
 // fin[b,c,j] = x~(len - L + j), and the conv capture rows when asked for.  One thread per channel walks j upward and
 // reads index len + j >= j of its own row before writing index j, so the
 // final state may alias the initial one.
-template <typename T>
+// BATCH: read all L values of a channel before writing any (L <= 8), so the
+// loads overlap (the per-channel and capture decode instances: 9% and 6%
+// faster; the plain decode instance, held to 80 registers, ran 3% slower
+// with it and keeps one value at a time).
+template <typename T, bool BATCH>
 __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int slice,
                                  int nslices, size_t C) {
     const int L = p.conv_L;
@@ -44,10 +48,22 @@ __device__ void conv_final_slice(const DeltaParams &p, int b, int s, int e, int 
         if (fin != nullptr) {
             const T *irow = init + ((size_t)b * C + c) * L;
             T *frow = fin + ((size_t)b * C + c) * L;
-            for (int j = 0; j < L; ++j) {
-                const int local = len - L + j;
-                const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
-                frow[j] = v;
+            if (BATCH && L <= 8) {  // all reads before the first write: the loads overlap
+                T v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int local = len - L + j;
+                    if (j < L) v[j] = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < L) frow[j] = v[j];
+            } else {
+                for (int j = 0; j < L; ++j) {
+                    const int local = len - L + j;
+                    const T v = local >= 0 ? x[(size_t)(s + local) * C + c] : irow[L + local];
+                    frow[j] = v;
+                }
             }
         }
         if (p.conv_updates != nullptr) {  // CONV_CAPTURE: first raw input rows, zero beyond
@@ -157,7 +173,7 @@ __global__ void __launch_bounds__(kSerialThreads, (!PF && KP == 128) ? (CAPT ? 5
     // conv/prepare kernel wrote (when launched as its PDL dependent).
     pdl_wait_primary();
     if (p.conv_fin != nullptr || p.conv_updates != nullptr)
-        conv_final_slice<T>(p, b, s, e, h * nrb + rb, H * nrb, W);
+        conv_final_slice<T, PC || CAPT>(p, b, s, e, h * nrb + rb, H * nrb, W);
 
     // capsule blocks of this sequence (CAPT): g [cap][H], k [cap][HQ][K], delta [cap][H][V]
     float *cap_g = nullptr, *cap_k = nullptr, *cap_d = nullptr;
