@@ -23,8 +23,13 @@ namespace {
 constexpr int kDenseThreads = 128;
 
 // VEC4: n % 4 == 0 and 16-byte aligned states (state rows move as float4).
+// The scalar-gate instance with n = 128 is held to six CTAs per SM (80
+// registers; it took 96 and ran five): dense decode 49.4 -> 47.2 us a step.
+// The per-channel instance takes 80 registers unbounded; bounded it spilled
+// and ran 47.2 -> 50.4 us.  (A minimum of 0 CTAs leaves the bound unset.)
 template <typename T, int KP, int RG, bool PERCH, bool VEC4>
-__global__ void __launch_bounds__(kDenseThreads) delta_dense_kernel(const DenseParams p) {
+__global__ void __launch_bounds__(kDenseThreads, (KP == 128 && !PERCH) ? 6 : 0)
+    delta_dense_kernel(const DenseParams p) {
     constexpr int EPL = 16;           // state values per lane per row
     constexpr int LPR = KP / EPL;     // lanes per row
     constexpr int RPI = 32 / LPR;     // rows per warp per row group
